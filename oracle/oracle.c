@@ -1,0 +1,264 @@
+/*
+ * Oracle for the paged-KV hot path.  TEST INFRASTRUCTURE ONLY: the CUDA
+ * library never links, includes or calls this file, and only the tests, the
+ * smoke check and the benchmark's CPU-baseline leg load it.
+ *
+ * Plain, slow, single-threaded, fp32 (the precision the problem statement
+ * fixes for the reference computation), written straight from the pages:
+ *
+ *   store   - "Inference engine: inside nano-vLLM", section "Attention in
+ *             nano-vLLM" (store_kvcache): token t's K and V rows go to cache
+ *             row slot_mapping[t]; a slot of -1 is skipped.
+ *   gather  - "nano-vLLM Part 2: Block Tables, KV Cache, and the Path to the
+ *             GPU", section 2.2: logical position j of a sequence lives in
+ *             physical row block_table[j / bs] * bs + j % bs.  Paging is
+ *             lossless ("How vLLM works", paged attention), so attention over
+ *             the gathered rows is attention over a contiguous cache.
+ *   decode  - softmax(scale * q K^T) V over the context_len gathered rows
+ *             (context_len counts the token stored this step; page 1 section
+ *             3.1).  Two passes: max, then exp-sum; d and j ascending.
+ *   prefill - per sequence, Lq = cu_q[i+1]-cu_q[i] new queries over
+ *             Lk = cu_k[i+1]-cu_k[i] keys; prefix P = Lk - Lq; query r sees
+ *             keys 0..P+r (bottom-right causal; page 1 sections 2.5 and 4.1,
+ *             page 4 section 8.1).  Keys j < P come from the pages, keys
+ *             j >= P are this step's packed k/v rows.
+ *
+ * GQA: q head h reads kv head h / (H_q / H_kv) (contiguous groups).
+ * Inputs are raw 16-bit words (fp16 or bf16); outputs are fp32.
+ * Every function returns 0 on success and a negative code on invalid input
+ * (nothing is written to the output in that case).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_F16 0
+#define OR_BF16 1
+
+static float bf16_bits_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* IEEE 754 binary16 -> binary32, exact (every half is a float). */
+static float f16_bits_to_float(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)m, -24);              /* zero or subnormal */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(m + 1024), e - 25);  /* 1.m * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+static float to_float(uint16_t h, int dtype)
+{
+    return dtype == OR_BF16 ? bf16_bits_to_float(h) : f16_bits_to_float(h);
+}
+
+float oracle_half_to_float(uint16_t bits, int dtype) { return to_float(bits, dtype); }
+
+/* ---------------------------------------------------------------- store */
+
+int oracle_store_kv(const uint16_t *k, const uint16_t *v, int64_t k_row_stride, int64_t v_row_stride,
+                    uint16_t *k_cache, uint16_t *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;   /* elements of one token's K (or V) */
+    const int64_t rows = (int64_t)num_blocks * block_size;  /* slots in the pool */
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < -1 || s >= rows)
+            return -1;
+    }
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s == -1)
+            continue;
+        for (int64_t e = 0; e < row; ++e) {
+            k_cache[s * row + e] = k[t * k_row_stride + e];
+            v_cache[s * row + e] = v[t * v_row_stride + e];
+        }
+    }
+    return 0;
+}
+
+/* --------------------------------------------------------------- gather */
+
+/* Copies logical positions [0, n) of one sequence out of the pool into
+ * dense fp32 buffers kc/vc of shape [n, H_kv, D]. */
+static int gather(const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *table,
+                  int32_t table_len, int32_t n, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t num_blocks, int32_t block_size, int dtype, float *kc, float *vc)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int32_t j = 0; j < n; ++j) {
+        int32_t logical = j / block_size;
+        if (logical >= table_len)
+            return -2;
+        int32_t page = table[logical];
+        if (page < 0 || page >= num_blocks)
+            return -2;
+        int64_t r = (int64_t)page * block_size + j % block_size;
+        for (int64_t e = 0; e < row; ++e) {
+            kc[j * row + e] = to_float(k_cache[r * row + e], dtype);
+            vc[j * row + e] = to_float(v_cache[r * row + e], dtype);
+        }
+    }
+    return 0;
+}
+
+/* softmax(scale * q . K_j) V over rows j in [0, n) of kv head g of the dense
+ * buffers; q is one head's D values; result in out[D]. */
+static void attend(const float *q, const float *kc, const float *vc, int32_t n, int32_t g,
+                   int32_t num_kv_heads, int32_t head_dim, float scale, float *s, float *out)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (n == 0) {
+        for (int32_t d = 0; d < head_dim; ++d)
+            out[d] = 0.0f;
+        return;
+    }
+    float m = -INFINITY;
+    for (int32_t j = 0; j < n; ++j) {
+        const float *kj = kc + j * row + (int64_t)g * head_dim;
+        float dot = 0.0f;
+        for (int32_t d = 0; d < head_dim; ++d)
+            dot += q[d] * kj[d];
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+    }
+    float l = 0.0f;
+    for (int32_t j = 0; j < n; ++j) {
+        s[j] = expf(s[j] - m);
+        l += s[j];
+    }
+    for (int32_t d = 0; d < head_dim; ++d)
+        out[d] = 0.0f;
+    for (int32_t j = 0; j < n; ++j) {
+        const float *vj = vc + j * row + (int64_t)g * head_dim;
+        for (int32_t d = 0; d < head_dim; ++d)
+            out[d] += s[j] * vj[d];
+    }
+    for (int32_t d = 0; d < head_dim; ++d)
+        out[d] /= l;
+}
+
+static int check_heads(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim)
+{
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_q_heads % num_kv_heads)
+        return -3;
+    return 0;
+}
+
+/* --------------------------------------------------------------- decode */
+
+int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                  int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t num_blocks, int32_t block_size, float scale, int dtype, float *out)
+{
+    if (check_heads(num_q_heads, num_kv_heads, head_dim))
+        return -3;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    int32_t max_len = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (context_lens[b] < 0)
+            return -4;
+        if (context_lens[b] > max_len)
+            max_len = context_lens[b];
+    }
+    float *kc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
+    float *vc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
+    float *s = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1));
+    float *qh = malloc(sizeof(float) * (size_t)head_dim);
+    float *res = malloc(sizeof(float) * (size_t)batch * num_q_heads * head_dim + 1);
+    int rc = (kc && vc && s && qh && res) ? 0 : -5;
+    for (int32_t b = 0; b < batch && !rc; ++b) {
+        int32_t n = context_lens[b];
+        rc = gather(k_cache, v_cache, block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
+                    n, num_kv_heads, head_dim, num_blocks, block_size, dtype, kc, vc);
+        for (int32_t h = 0; h < num_q_heads && !rc; ++h) {
+            const uint16_t *qb = q + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                qh[d] = to_float(qb[d], dtype);
+            attend(qh, kc, vc, n, h / group, num_kv_heads, head_dim, scale, s,
+                   res + ((int64_t)b * num_q_heads + h) * head_dim);
+        }
+    }
+    if (!rc)
+        memcpy(out, res, sizeof(float) * (size_t)batch * num_q_heads * head_dim);
+    free(kc); free(vc); free(s); free(qh); free(res);
+    return rc;
+}
+
+/* -------------------------------------------------------------- prefill */
+
+int oracle_prefill_paged(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t num_blocks, int32_t block_size, float scale, int dtype, float *out)
+{
+    if (check_heads(num_q_heads, num_kv_heads, head_dim))
+        return -3;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    const int64_t total_q = cu_seqlens_q[num_seqs];
+    int32_t max_k = 0;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        int32_t lq = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+        int32_t lk = cu_seqlens_k[i + 1] - cu_seqlens_k[i];
+        if (lq < 0 || lk < lq)
+            return -4;
+        if (!block_tables && lk != lq)
+            return -4;   /* without a block table there is no cached prefix to read */
+        if (lk > max_k)
+            max_k = lk;
+    }
+    float *kc = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1) * row);
+    float *vc = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1) * row);
+    float *s = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1));
+    float *qh = malloc(sizeof(float) * (size_t)head_dim);
+    float *res = malloc(sizeof(float) * (size_t)total_q * num_q_heads * head_dim + 1);
+    int rc = (kc && vc && s && qh && res) ? 0 : -5;
+    for (int32_t i = 0; i < num_seqs && !rc; ++i) {
+        const int32_t q0 = cu_seqlens_q[i];
+        const int32_t lq = cu_seqlens_q[i + 1] - q0;
+        const int32_t lk = cu_seqlens_k[i + 1] - cu_seqlens_k[i];
+        const int32_t prefix = lk - lq;
+        if (prefix > 0)
+            rc = gather(k_cache, v_cache, block_tables + (int64_t)i * max_blocks_per_seq,
+                        max_blocks_per_seq, prefix, num_kv_heads, head_dim, num_blocks, block_size,
+                        dtype, kc, vc);
+        for (int32_t r = 0; r < lq && !rc; ++r)   /* this step's keys follow the prefix */
+            for (int64_t e = 0; e < row; ++e) {
+                kc[(prefix + r) * row + e] = to_float(k[(q0 + r) * row + e], dtype);
+                vc[(prefix + r) * row + e] = to_float(v[(q0 + r) * row + e], dtype);
+            }
+        for (int32_t r = 0; r < lq && !rc; ++r)
+            for (int32_t h = 0; h < num_q_heads; ++h) {
+                const uint16_t *qr = q + ((int64_t)(q0 + r) * num_q_heads + h) * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    qh[d] = to_float(qr[d], dtype);
+                attend(qh, kc, vc, prefix + r + 1, h / group, num_kv_heads, head_dim, scale, s,
+                       res + ((int64_t)(q0 + r) * num_q_heads + h) * head_dim);
+            }
+    }
+    if (!rc)
+        memcpy(out, res, sizeof(float) * (size_t)total_q * num_q_heads * head_dim);
+    free(kc); free(vc); free(s); free(qh); free(res);
+    return rc;
+}
