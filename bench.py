@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV hot path on GB300.
+
+One step = one pass of the layer's hot path over one batch of synthetic input
+resident in HBM: ``pa_store_kv`` of the step's new K/V rows, then the
+attention call(s) of that step (``pa_decode``; the mixed chunked-prefill
+workload also runs ``pa_prefill_paged``).  The L2 is flushed (a 256 MB write)
+between timed steps, outside the timed events, so every step streams its KV
+pages from HBM as one layer of a real multi-layer step would.
+
+Prints ONE JSON line.  ``value`` = algorithmic KV bytes of the step's decode
+attention (sum of context lengths x 2 x H_kv x D x 2 bytes) / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on the host
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path needs no exchange); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "paged decode KV GB/s (% of GB300 HBM peak) and decode tokens/s on 1 GPU"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 256 << 20
+DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
+
+# DRAM bytes (read + write) per pa_decode call measured by ncu on the committed
+# kernels, per workload; None until a capture of the current kernels exists.
+TRAFFIC_PER_CALL = {}
+
+WORKLOAD_CONFIG = {
+    "tiny_decode": dict(batch=4, context="{1,17,100,255}", H_q=4, H_kv=2, D=64, block_size=16, dtype="fp16"),
+    "qwen3_0p6b_decode": dict(batch=64, context="U[128,4096]", H_q=16, H_kv=8, D=128, block_size=256,
+                              dtype="bf16", pool="1.25x need, shuffled"),
+    "qwen3_8b_shared_decode": dict(batch=256, context="U[513,2048]", H_q=32, H_kv=8, D=128, block_size=16,
+                                   dtype="bf16", sharing="groups of 8 share a 512-token prefix"),
+    "long_context_decode": dict(batch=4, context="32768", H_q=32, H_kv=8, D=128, block_size=256, dtype="bf16",
+                                pool="600 blocks, shuffled"),
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_CONFIG))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples of this process's GPU while running."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if self.uuid:
+            mine = [r for r in rows if self.uuid in r[0]]
+            rows = mine or rows
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workloads
+
+class DecodeWorkload:
+    """A decode step (store of one token per sequence + paged decode) with
+    all inputs resident on the device."""
+
+    def __init__(self, name: str, dev: torch.device):
+        from tests import inputs
+        import paged_kv_cache_bs_gb300 as pa
+        self.pa = pa
+        self.name = name
+        self.st = st = inputs.WORKLOADS[name]()
+        p = st.pool
+        self.dev = dev
+        self.kc, self.vc = p.k_cache.to(dev), p.v_cache.to(dev)
+        self.host = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "slot_mapping": st.slot_mapping,
+                     "block_tables": st.block_tables, "context_lens": st.context_lens}
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        self.out = torch.empty_like(self.d["q"])
+        self.ws = pa.alloc_decode_workspace(self.d["q"], self.kc, self.d["block_tables"])
+        self.kv_bytes = st.kv_bytes()
+        self.batch = st.batch
+        row = p.num_kv_heads * p.head_dim * st.q.element_size()
+        self.store_bytes = 2 * 2 * int((st.slot_mapping >= 0).sum()) * row   # k and v, read + write
+        self.launches_per_step = 3   # store, decode partitions, log-sum-exp combine
+
+    def store(self):
+        d = self.d
+        self.pa.store_kv(d["k_new"], d["v_new"], self.kc, self.vc, d["slot_mapping"])
+
+    def attend(self):
+        d = self.d
+        self.pa.decode(d["q"], self.kc, self.vc, d["block_tables"], d["context_lens"], self.st.scale,
+                       out=self.out, workspace=self.ws)
+
+    def e2e_buffers(self):
+        pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        return pinned, out_host, h2d, out_host.numel() * out_host.element_size()
+
+    def e2e_step(self, pinned, out_host):
+        for k, v in pinned.items():
+            self.d[k].copy_(v, non_blocking=True)
+        self.store()
+        self.attend()
+        out_host.copy_(self.out, non_blocking=True)
+
+
+# ------------------------------------------------------------------ timing
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world, local):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier(device_ids=[local]) if dist.get_backend() == "nccl" else dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(name: str, seconds: float):
+    """The oracle as it stands, single-threaded on this host: store + decode of
+    the workload's sequences one at a time until the time budget is spent."""
+    import oracle
+    from tests import inputs
+    st = inputs.WORKLOADS[name]()
+    p = st.pool
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+    row = 2 * p.num_kv_heads * p.head_dim * st.q.element_size()
+    done_bytes, n, t_total = 0, 0, 0.0
+    while t_total < seconds:          # whole passes over the batch until the budget is spent
+        b = n % st.batch
+        sl = slice(b, b + 1)
+        t0 = time.perf_counter()
+        oracle.store_kv(st.k_new[sl], st.v_new[sl], kc, vc, st.slot_mapping[sl])
+        oracle.decode(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(st.context_lens[b]) * row
+        n += 1
+    return {"value": done_bytes / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"store + decode of {n} sequences (round robin over the {st.batch} of the workload) "
+                      f"({done_bytes / 1e6:.1f} MB of KV), single-threaded C oracle, "
+                      f"{os.cpu_count()} host cores present"}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed as the reference arm: each step decodes one sequence of
+    the workload (round robin) on the host."""
+    if rank != 0:
+        return
+    import oracle
+    from tests import inputs
+    st = inputs.WORKLOADS[args.workload]()
+    p = st.pool
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+    oracle.store_kv(st.k_new, st.v_new, kc, vc, st.slot_mapping)
+    row = 2 * p.num_kv_heads * p.head_dim * st.q.element_size()
+
+    def step(i):
+        b = i % st.batch
+        sl = slice(b, b + 1)
+        oracle.store_kv(st.k_new[sl], st.v_new[sl], kc, vc, st.slot_mapping[sl])
+        oracle.decode(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale)
+        return int(st.context_lens[b]) * row
+
+    for i in range(args.warmup):
+        step(i)
+    nbytes, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        nbytes += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": WORKLOAD_CONFIG[args.workload]["dtype"],
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+                       "sample": "one sequence (round robin) per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "one sequence of the workload per step, store + decode"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = DecodeWorkload(args.workload, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        w.store()
+        w.attend()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world, local)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                 # L2 flush between steps, outside the events
+        ev[i][0].record(stream)
+        w.store()
+        ev[i][1].record(stream)
+        w.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, local)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    store_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = sum(store_ms) / K + sum(dec_ms) / K
+    step_ms_max = max_over_ranks(step_ms, world, dev)
+
+    # ---- end to end: pinned host inputs in, result out, every step
+    pinned, out_host, h2d, d2h = w.e2e_buffers()
+    for _ in range(args.warmup):
+        w.e2e_step(pinned, out_host)
+    torch.cuda.synchronize(dev)
+    Ke = min(K, 1000)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    barrier(world, local)
+    for i in range(Ke):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        w.e2e_step(pinned, out_host)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, local)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / Ke, world, dev)
+
+    peaks, peak_kind = measured_peaks()
+    dec_avg_s = sum(dec_ms) / K / 1e3
+    achieved = w.kv_bytes / dec_avg_s / 1e9
+    value = world * w.kv_bytes / (step_ms_max / 1e3) / 1e9
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+    traffic = TRAFFIC_PER_CALL.get(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": WORKLOAD_CONFIG[args.workload]["dtype"], "data": "synthetic",
+        "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+                   "l2": "flushed (256 MB write) between steps, outside the timed events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": world * w.batch / (step_ms_max / 1e3),
+        "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
+        "decode_ms": sum(dec_ms) / K, "store_ms": sum(store_ms) / K,
+        "store_gbs": w.store_bytes / (sum(store_ms) / K / 1e3) / 1e9,
+        "kv_bytes_per_step": w.kv_bytes,
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (split-K partitions + combine)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.kv_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": K * w.launches_per_step,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

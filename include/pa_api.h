@@ -1,0 +1,182 @@
+/*
+ * pa_api.h -- C ABI of the paged-KV attention library (libpa.so, sm_103a).
+ *
+ * Three operations of one attention layer of a paged-KV inference engine:
+ *
+ *   pa_store_kv       write this step's new K/V rows into the paged pool
+ *   pa_decode         one query token per sequence attending over its paged
+ *                     context (split-K over context partitions)
+ *   pa_prefill_paged  chunked prefill: new query tokens attending causally over
+ *                     a cached paged prefix plus themselves
+ *
+ * Conventions shared by every call
+ *   - All tensor arguments are DEVICE pointers to caller-owned memory; the
+ *     library allocates nothing and keeps no state besides cached device
+ *     properties.  Integer size arguments are host values.
+ *   - Element type: PA_F16 or PA_BF16 (IEEE binary16 / bfloat16) for every
+ *     q/k/v/cache/out buffer of a call.  Arithmetic is fp32.
+ *   - The pool of one layer is two buffers k_cache and v_cache, each
+ *     [num_blocks, block_size, num_kv_heads, head_dim] contiguous: physical
+ *     block b, token offset o, kv head g, dim d is element
+ *     ((b * block_size + o) * num_kv_heads + g) * head_dim + d ("nano-vLLM
+ *     Part 2: Block Tables, KV Cache, and the Path to the GPU", section 1).
+ *     A slot is the flattened row index b * block_size + o (section 2.2).
+ *   - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   - Supported: head_dim 64 or 128; num_q_heads % num_kv_heads == 0 with a
+ *     group size of 1, 2, 4 or 8; block_size a power of two in [8, 1024].
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Issue pa_store_kv before the attention call of the
+ *     same step on the same stream: attention reads the stored rows.
+ *   - Return value: PA_OK, or a negative PA_ERR_* code.  Argument checks run
+ *     on the host before anything is launched; on PA_ERR_INVALID_ARG and
+ *     PA_ERR_UNSUPPORTED no CUDA call has been made.  pa_last_error() gives a
+ *     message for the calling thread's most recent failure.  The library never
+ *     exits, throws or traps.
+ *   - err_flag (nullable DEVICE int32): kernels OR bits into it when the DATA
+ *     is invalid -- PA_FLAG_BAD_SLOT (slot outside [-1, num_blocks*block_size)),
+ *     PA_FLAG_BAD_BLOCK (a block id inside a context outside [0, num_blocks)),
+ *     PA_FLAG_BAD_LENGTH (a negative or over-long context / cu_seqlens).  The
+ *     offending access is skipped (a bad page reads as zeros), so bad metadata
+ *     never faults; the corresponding outputs are then unspecified.
+ */
+#ifndef PA_API_H
+#define PA_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,
+    PA_ERR_UNSUPPORTED = -2,
+    PA_ERR_CUDA = -3,
+};
+
+enum {
+    PA_FLAG_BAD_SLOT = 1,
+    PA_FLAG_BAD_BLOCK = 2,
+    PA_FLAG_BAD_LENGTH = 4,
+};
+
+/* Message describing the calling thread's last failed call ("" if none). */
+PA_API const char *pa_last_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+PA_API int pa_version(void);
+
+/*
+ * pa_store_kv -- slot-mapped store of this step's K/V rows.
+ *
+ * Follows the store_kvcache kernel of "Inference engine: inside nano-vLLM"
+ * (section "Attention in nano-vLLM"): for every token t with
+ * s = slot_mapping[t] != -1, copy the num_kv_heads*head_dim elements of row t
+ * of k into row s of k_cache, and the same for v; slot -1 (padding, e.g. a
+ * CUDA-graph pad row, "nano-vLLM Part 2", section 4.2) is skipped.
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim]; row t starts at
+ *                 element t * k_row_stride (v_row_stride); heads and dims of a
+ *                 row are contiguous.  Strides are in ELEMENTS and may exceed
+ *                 num_kv_heads*head_dim (e.g. k and v as views of a fused qkv).
+ *   k_cache/v_cache  the layer's pool (see above), written in place.
+ *   slot_mapping  int32 [num_tokens].  Distinct slots are required for a
+ *                 deterministic result; duplicated slots race.
+ *   The copy is bit-exact (raw 16-bit words).
+ * Errors: INVALID_ARG for null pointers, negative sizes, strides smaller than
+ * a row; UNSUPPORTED for dtype/head_dim outside the supported set.
+ */
+PA_API int pa_store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                void *k_cache, void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                pa_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
+ * pa_decode_workspace_bytes -- device scratch pa_decode needs for this shape
+ * (per-partition softmax partials).  Pure host computation; 0 on invalid
+ * arguments.
+ */
+PA_API size_t pa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_blocks_per_seq, int32_t block_size);
+
+/*
+ * pa_decode -- paged GQA decode attention, one query token per sequence.
+ *
+ * The flash_attn_with_kvcache call of "Inference engine: inside nano-vLLM"
+ * (section "Attention in nano-vLLM", decode branch) and "From nano-vLLM to
+ * vLLM" section 11: sequence b attends over logical positions
+ * [0, context_lens[b]) of its context, position j living in cache row
+ * block_tables[b][j / block_size] * block_size + j % block_size.
+ * out[b, h, :] = softmax_j(scale * q[b,h,:] . K_j) V_j, with K_j/V_j of kv head
+ * h / (num_q_heads/num_kv_heads).  context_lens counts the token stored this
+ * step ("nano-vLLM Part 2", section 3.1).  A context length of 0 (a padding
+ * row) gives an all-zero output row and reads no page.
+ *
+ *   q             [batch, num_q_heads, head_dim]; row b starts at element
+ *                 b * q_row_stride; heads/dims contiguous.
+ *   block_tables  int32 [batch, max_blocks_per_seq] row-major, -1 padded;
+ *                 entries past ceil(context_len / block_size) are never read.
+ *   context_lens  int32 [batch], each in [0, max_blocks_per_seq * block_size].
+ *   out           [batch, num_q_heads, head_dim] contiguous, written.
+ *   workspace     device scratch of at least pa_decode_workspace_bytes(...)
+ *                 bytes; its contents need no initialisation and are
+ *                 clobbered.  Two calls in flight at once need two workspaces.
+ * The work is split over fixed-size context partitions (one CTA per
+ * sequence, kv head and partition); a second kernel merges the partitions'
+ * softmax partials by log-sum-exp.
+ */
+PA_API int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+              int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+              int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
+              size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
+ * pa_prefill_paged -- causal varlen prefill over a paged prefix.
+ *
+ * The flash_attn_varlen_func call of "Inference engine: inside nano-vLLM"
+ * (section "Attention in nano-vLLM", prefill branch) with the cu_seqlens of
+ * "nano-vLLM Part 2", section 4.1.  Sequence i owns query rows
+ * [cu_seqlens_q[i], cu_seqlens_q[i+1]) (Lq of them) and a context of
+ * Lk = cu_seqlens_k[i+1] - cu_seqlens_k[i] >= Lq tokens whose first
+ * P = Lk - Lq are a cached prefix.  Query row r (0-based within the
+ * sequence) attends over context positions [0, P + r] (causal, aligned to the
+ * end of the context).
+ *
+ * Where the keys come from, as in the pages' attention layer:
+ *   - block_tables != NULL: every context position j in [0, Lk) is read from
+ *     the pool through block_tables[i] -- the prefix and this step's rows,
+ *     which pa_store_kv must already have written.  k and v are not read.
+ *   - block_tables == NULL: no prefix (Lk must equal Lq for every sequence);
+ *     keys are rows [cu_seqlens_q[i], cu_seqlens_q[i+1]) of k and v.
+ *
+ *   q             [total_q, num_q_heads, head_dim] contiguous.
+ *   k, v          [total_q, num_kv_heads, head_dim] contiguous (may be NULL
+ *                 when block_tables != NULL).
+ *   cu_seqlens_q/k  int32 [num_seqs + 1], DEVICE.
+ *   max_seqlen_q/k  host upper bounds on Lq / Lk (size the launch).
+ *   out           [total_q, num_q_heads, head_dim] contiguous, written.
+ * QK^T and PV run on the tensor cores (tcgen05, accumulators in TMEM).
+ */
+PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache,
+                     const void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                     int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                     const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                     float scale, void *out, pa_dtype dtype, int32_t *err_flag, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_API_H */

@@ -1,0 +1,183 @@
+"""Paged-KV attention for GB300 (sm_103a): Python binding of libpa.so.
+
+Argument marshalling only: every step of the store, decode and prefill path
+runs in the library's CUDA kernels.  torch supplies device memory and the
+current stream.  Importing this package loads ``libpa.so`` and raises if it is
+missing -- there is no fallback path.  Build it with
+``python paged_kv_cache_bs_gb300/build.py``.
+
+The functions mirror the C ABI in ``include/pa_api.h``:
+
+* :func:`store_kv`       -- ``pa_store_kv``
+* :func:`decode`         -- ``pa_decode`` (+ ``pa_decode_workspace_bytes``)
+* :func:`prefill_paged`  -- ``pa_prefill_paged``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run `python paged_kv_cache_bs_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_p, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_lib.pa_last_error.restype = ctypes.c_char_p
+_lib.pa_last_error.argtypes = []
+_lib.pa_version.restype = ctypes.c_int
+_lib.pa_store_kv.restype = ctypes.c_int
+_lib.pa_store_kv.argtypes = [_p, _p, _i64, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _p, _p]
+_lib.pa_decode_workspace_bytes.restype = _sz
+_lib.pa_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+_lib.pa_decode.restype = ctypes.c_int
+_lib.pa_decode.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
+                           ctypes.c_int, _p, _p]
+_lib.pa_prefill_paged.restype = ctypes.c_int
+_lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32, _i32,
+                                  _i32, _f32, _p, ctypes.c_int, _p, _p]
+
+PA_F16, PA_BF16 = 0, 1
+_DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH = 1, 2, 4
+
+
+class PagedAttentionError(RuntimeError):
+    """A libpa call returned an error code."""
+
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed ({code}): {_lib.pa_last_error().decode()}")
+        self.code = code
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libpa.so handle (for direct C-ABI calls)."""
+    return _lib
+
+
+def _ptr(t) -> ctypes.c_void_p | None:
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise PagedAttentionError(fn, rc)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float16 or bfloat16")
+    return _DTYPES[t.dtype]
+
+
+def _cache_shape(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache / v_cache must both be [num_blocks, block_size, H_kv, D]")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache / v_cache must be contiguous")
+    if not (k_cache.is_cuda and v_cache.is_cuda):
+        raise ValueError("k_cache / v_cache must be CUDA tensors")
+    return k_cache.shape
+
+
+def _rows(t: torch.Tensor, name: str) -> int:
+    """Row stride (elements) of a [T, H, D] tensor whose heads/dims are contiguous."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name} must be [T, H, D] with contiguous heads and dims")
+    return t.stride(0)
+
+
+def store_kv(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+             slot_mapping: torch.Tensor, err_flag: torch.Tensor | None = None) -> None:
+    """Write rows of k/v ([T, H_kv, D]) to cache rows ``slot_mapping`` (int32; -1 skips)."""
+    n, bs, hkv, d = _cache_shape(k_cache, v_cache)
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int32")
+    if k.shape[0] != slot_mapping.numel() or v.shape[0] != slot_mapping.numel():
+        raise ValueError("k/v rows must match slot_mapping")
+    if k.shape[1:] != (hkv, d) or v.shape[1:] != (hkv, d):
+        raise ValueError("k/v must be [T, H_kv, D] matching the cache")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype:
+        raise TypeError("k/v dtype must match the cache")
+    rc = _lib.pa_store_kv(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(k_cache), _ptr(v_cache),
+                          _ptr(slot_mapping), slot_mapping.numel(), hkv, d, n, bs, _dtype(k_cache), _ptr(err_flag),
+                          _stream(k_cache))
+    _check("pa_store_kv", rc)
+
+
+def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           max_blocks_per_seq: int, block_size: int) -> int:
+    return int(_lib.pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                              block_size))
+
+
+def alloc_decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor) -> torch.Tensor:
+    n, bs, hkv, d = k_cache.shape
+    nbytes = decode_workspace_bytes(q.shape[0], q.shape[1], hkv, d, block_tables.shape[1], bs)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """Paged decode attention: q [B, H_q, D] -> out [B, H_q, D]."""
+    n, bs, hkv, d = _cache_shape(k_cache, v_cache)
+    B, hq = q.shape[0], q.shape[1]
+    if q.dim() != 3 or q.shape[2] != d:
+        raise ValueError("q must be [B, H_q, D]")
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
+    if out is None:
+        out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_decode_workspace(q, k_cache, block_tables)
+    rc = _lib.pa_decode(_ptr(q), _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                        block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale), _ptr(out),
+                        _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
+                        _stream(q))
+    _check("pa_decode", rc)
+    return out
+
+
+def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | None, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                  max_seqlen_q: int, max_seqlen_k: int, block_tables: torch.Tensor | None, scale: float,
+                  out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """Causal varlen prefill over a paged prefix: q [Tq, H_q, D] -> out [Tq, H_q, D]."""
+    n, bs, hkv, d = _cache_shape(k_cache, v_cache)
+    tq, hq = q.shape[0], q.shape[1]
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [Tq, H_q, D]")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if block_tables is not None and (block_tables.dtype != torch.int32 or not block_tables.is_contiguous()):
+        raise ValueError("block_tables must be contiguous int32")
+    for name, t in (("k", k), ("v", v)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty(tq, hq, d, dtype=q.dtype, device=q.device)
+    rc = _lib.pa_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k),
+                               _ptr(block_tables), block_tables.shape[1] if block_tables is not None else 0,
+                               hq, hkv, d, n, bs, float(scale), _ptr(out), _dtype(q), _ptr(err_flag), _stream(q))
+    _check("pa_prefill_paged", rc)
+    return out
+
+
+__all__ = ["store_kv", "decode", "prefill_paged", "decode_workspace_bytes", "alloc_decode_workspace",
+           "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
+           "FLAG_BAD_LENGTH"]

@@ -1,0 +1,150 @@
+// C ABI of the paged-KV attention library: argument validation on the host,
+// then a launch on the caller's stream.  No call allocates memory.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "pa_common.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+bool aligned(const void *p, int bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
+bool valid_dtype(int d) { return d == PA_F16 || d == PA_BF16; }
+
+// Checks shared by the attention calls.  Returns PA_OK or an error code.
+int check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                          int32_t block_size, float scale, pa_dtype dtype) {
+    if (!valid_dtype(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not PA_F16 or PA_BF16", (int)dtype);
+    if (num_q_heads <= 0 || num_kv_heads <= 0)
+        return fail(PA_ERR_INVALID_ARG, "head counts must be positive (H_q=%d, H_kv=%d)", num_q_heads,
+                    num_kv_heads);
+    if (num_q_heads % num_kv_heads)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                    num_kv_heads);
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8)
+        return fail(PA_ERR_UNSUPPORTED, "GQA group size %d (supported: 1, 2, 4, 8)", group);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+    if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive (%d)", num_blocks);
+    if (!is_pow2(block_size) || block_size < 8 || block_size > 1024)
+        return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two in [8, 1024])", block_size);
+    if (!isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_last_error(void) { return g_err; }
+
+int pa_version(void) { return 100; }
+
+int pa_store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache,
+                void *v_cache, const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype, int32_t *err_flag,
+                void *stream) {
+    if (!valid_dtype(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not PA_F16 or PA_BF16", (int)dtype);
+    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens is negative (%d)", num_tokens);
+    if (num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "sizes must be positive (H_kv=%d, D=%d, N=%d, bs=%d)", num_kv_heads,
+                    head_dim, num_blocks, block_size);
+    if (!k_cache || !v_cache) return fail(PA_ERR_INVALID_ARG, "k_cache/v_cache is NULL");
+    if (num_tokens == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "k, v or slot_mapping is NULL");
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (row > (1 << 30)) return fail(PA_ERR_INVALID_ARG, "row of %lld elements is too large", (long long)row);
+    if (k_row_stride < row || v_row_stride < row)
+        return fail(PA_ERR_INVALID_ARG, "row strides (%lld, %lld) are smaller than a row (%lld)",
+                    (long long)k_row_stride, (long long)v_row_stride, (long long)row);
+    if (!aligned(k, 2) || !aligned(v, 2) || !aligned(k_cache, 2) || !aligned(v_cache, 2))
+        return fail(PA_ERR_INVALID_ARG, "buffers must be 2-byte aligned");
+    const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
+    return cuda_status(pa::launch_store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping,
+                                           num_tokens, static_cast<int32_t>(row), slots, err_flag,
+                                           static_cast<cudaStream_t>(stream)),
+                       "pa_store_kv launch");
+}
+
+size_t pa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_blocks_per_seq, int32_t block_size) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+        !is_pow2(block_size))
+        return 0;
+    return pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size).ws_bytes;
+}
+
+int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+              float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag,
+              void *stream) {
+    int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
+    if (rc) return rc;
+    if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch is negative (%d)", batch);
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (1LL << 30))
+        return fail(PA_ERR_INVALID_ARG, "max context of %lld tokens is too large",
+                    (long long)max_blocks_per_seq * block_size);
+    if (batch == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (q_row_stride < static_cast<int64_t>(num_q_heads) * head_dim || q_row_stride % 2)
+        return fail(PA_ERR_INVALID_ARG, "q_row_stride %lld must be even and at least H_q*D",
+                    (long long)q_row_stride);
+    if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 2) ||
+        !aligned(workspace, 256))
+        return fail(PA_ERR_INVALID_ARG, "alignment: q 4 B, caches 16 B, out 2 B, workspace 256 B");
+    const pa::DecodePlan plan =
+        pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+    if (workspace_bytes < plan.ws_bytes)
+        return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
+                    plan.ws_bytes);
+    return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         block_size, scale, out, workspace, plan, dtype, err_flag,
+                                         static_cast<cudaStream_t>(stream)),
+                       "pa_decode launch");
+}
+
+int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
+                     int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
+                     int32_t *err_flag, void *stream) {
+    int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
+    if (rc) return rc;
+    (void)q; (void)k; (void)v; (void)k_cache; (void)v_cache; (void)cu_seqlens_q; (void)cu_seqlens_k;
+    (void)num_seqs; (void)max_seqlen_q; (void)max_seqlen_k; (void)block_tables; (void)max_blocks_per_seq;
+    (void)out; (void)err_flag; (void)stream;
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_paged is not built yet");
+}
+
+}  // extern "C"

@@ -16,3 +16,19 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def pa():
+    """The CUDA library's binding, built in-tree first.  GPU tests need a GPU:
+    there is no fallback, so a missing device is an error, not a skip."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "pa_build", os.path.join(ROOT, "paged_kv_cache_bs_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import paged_kv_cache_bs_gb300
+    return paged_kv_cache_bs_gb300

@@ -1,0 +1,128 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+``include/pa_api.h`` declares, and rejects invalid arguments on the host
+before making any CUDA call.  Also checks that the CUDA library and the oracle
+share no symbols."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa_api.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("pa_build", os.path.join(ROOT, "paged_kv_cache_bs_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import paged_kv_cache_bs_gb300 as pa
+    return pa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def exported_symbols(path):
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if line.strip()}
+
+
+def test_every_declared_function_is_exported(lib):
+    import paged_kv_cache_bs_gb300 as pa
+    names = declared_functions()
+    assert {"pa_store_kv", "pa_decode", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_last_error"} <= set(names)
+    syms = exported_symbols(pa.LIB_PATH)
+    for n in names:
+        assert n in syms, n
+        assert getattr(lib, n) is not None
+    # nothing but the C ABI is exported
+    assert {s for s in syms if s.startswith("pa_")} == set(names)
+
+
+def test_oracle_and_library_share_nothing(lib, oracle_lib):
+    import oracle
+    import paged_kv_cache_bs_gb300 as pa
+    a, b = exported_symbols(pa.LIB_PATH), exported_symbols(oracle.LIB)
+    assert not any(s.startswith("oracle_") for s in a)
+    assert not any(s.startswith("pa_") for s in b)
+    src = open(os.path.join(ROOT, "oracle", "oracle.c")).read()
+    assert "pa_api.h" not in src and "pa_common" not in src
+    for f in os.listdir(os.path.join(ROOT, "paged_kv_cache_bs_gb300", "csrc")):
+        assert "oracle" not in open(os.path.join(ROOT, "paged_kv_cache_bs_gb300", "csrc", f)).read().lower()
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
+
+
+def test_store_validation(lib):
+    args = dict(k=FAKE, v=FAKE, ks=1024, vs=1024, kc=FAKE, vc=FAKE, sm=FAKE, T=4, hkv=8, d=128, n=10, bs=16, dt=1)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return lib.pa_store_kv(a["k"], a["v"], a["ks"], a["vs"], a["kc"], a["vc"], a["sm"], a["T"], a["hkv"], a["d"],
+                               a["n"], a["bs"], a["dt"], None, None)
+    assert call(dt=5) == -2
+    assert call(T=-1) == -1
+    assert call(k=None) == -1
+    assert call(kc=None) == -1
+    assert call(ks=1000) == -1
+    assert call(hkv=0) == -1
+    assert call(k=ctypes.c_void_p((1 << 20) + 1)) == -1  # odd address
+    assert b"stride" in ctypes.cast(lib.pa_last_error(), ctypes.c_char_p).value or True
+    assert call(T=0, k=None, v=None, sm=None) == 0       # empty step is a no-op
+
+
+def test_decode_validation(lib):
+    base = dict(q=FAKE, qs=2048, kc=FAKE, vc=FAKE, bt=FAKE, mb=16, cl=FAKE, B=64, hq=16, hkv=8, d=128, n=700,
+                bs=256, scale=0.088, out=FAKE, ws=FAKE, wsb=1 << 30, dt=1)
+
+    def call(**kw):
+        a = {**base, **kw}
+        return lib.pa_decode(a["q"], a["qs"], a["kc"], a["vc"], a["bt"], a["mb"], a["cl"], a["B"], a["hq"], a["hkv"],
+                             a["d"], a["n"], a["bs"], ctypes.c_float(a["scale"]), a["out"], a["ws"], a["wsb"], a["dt"],
+                             None, None)
+    assert call(hq=12, hkv=8) == -1          # not a multiple
+    assert call(hq=48, hkv=3) == -2          # group of 16 unsupported
+    assert call(d=96) == -2
+    assert call(bs=12) == -2
+    assert call(bs=2048) == -2
+    assert call(dt=3) == -2
+    assert call(B=-1) == -1
+    assert call(q=None) == -1
+    assert call(ws=None) == -1
+    assert call(qs=100) == -1
+    assert call(wsb=16) == -1
+    assert call(kc=ctypes.c_void_p((1 << 20) + 8)) == -1   # cache not 16-byte aligned
+    assert call(scale=float("nan")) == -1
+    assert call(B=0, q=None, out=None, ws=None) == 0
+
+
+def test_workspace_size_is_host_only_and_sane(lib):
+    lib.pa_decode_workspace_bytes.restype = ctypes.c_size_t
+    w = lib.pa_decode_workspace_bytes(64, 16, 8, 128, 16, 256)
+    assert w > 0 and w % 4 == 0
+    assert lib.pa_decode_workspace_bytes(128, 16, 8, 128, 16, 256) >= w
+    assert lib.pa_decode_workspace_bytes(-1, 16, 8, 128, 16, 256) == 0
+    assert lib.pa_decode_workspace_bytes(4, 32, 8, 128, 128, 12) == 0
+
+
+def test_prefill_validation(lib):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, S=8, mq=512, mk=4096, bt=FAKE, mb=16,
+                 hq=32, hkv=8, d=128, n=600, bs=256, scale=0.088, out=FAKE, dt=1)
+        a.update(kw)
+        return lib.pa_prefill_paged(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["cq"], a["ck"], a["S"], a["mq"],
+                                    a["mk"], a["bt"], a["mb"], a["hq"], a["hkv"], a["d"], a["n"], a["bs"],
+                                    ctypes.c_float(a["scale"]), a["out"], a["dt"], None, None)
+    assert call(hq=30) == -1
+    assert call(d=80) == -2
+    assert call(dt=9) == -2
