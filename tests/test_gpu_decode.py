@@ -108,8 +108,9 @@ def test_decode_identical_keys_mean_of_v(pa):
     p = st.pool
     kf = p.k_cache.view(-1, 1, 128)
     rows = [inputs.slot_of(p.tables[0], 16, j) for j in range(777)]
-    kf[rows] = kf[rows[0]]
-    st.k_new[:] = kf[rows[0]]
+    k0 = kf[rows[0]].clone()
+    kf[rows] = k0
+    st.k_new[:] = k0
     out, _, vc = run_decode_gpu(pa, st)
     mean = vc.view(-1, 1, 128)[torch.tensor(rows).cuda()].double().mean(0)[0]
     for h in range(4):
