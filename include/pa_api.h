@@ -142,6 +142,35 @@ PA_API int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, c
               size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag, void *stream);
 
 /*
+ * pa_decode_static_workspace -- pa_decode for callers that cannot allocate
+ * device memory.  The pages describe no such call: it has no counterpart there.
+ *
+ * Same arguments and result as pa_decode, minus the workspace.  The split-K
+ * partials go to scratch memory owned by the library itself: one static
+ * 8 MiB device array on every GPU the library is loaded on, held until the
+ * process exits.  It serves engines that gave (nearly) all free device memory
+ * to their KV pool at start-up, and plugins whose host framework owns every
+ * device allocation: neither can cudaMalloc a per-call workspace.  This call
+ * allocates nothing.
+ *   - A shape whose pa_decode_workspace_bytes(...) exceeds 8 MiB is rejected
+ *     with PA_ERR_UNSUPPORTED (see pa_last_error) before any CUDA call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents.  Each call writes every scratch element it later reads, so
+ *     nothing needs clearing.  Calls that overlap on the GPU (unordered
+ *     streams) race on the scratch: order them on one stream.
+ */
+PA_API int pa_decode_static_workspace(const void *q, int64_t q_row_stride, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                      float scale, void *out, pa_dtype dtype, int32_t *err_flag,
+                                      void *stream);
+
+/*
  * pa_prefill_paged -- causal varlen prefill over a paged prefix.
  *
  * The flash_attn_varlen_func call of "Inference engine: inside nano-vLLM"

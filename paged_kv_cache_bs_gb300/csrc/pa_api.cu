@@ -54,6 +54,11 @@ int check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t hea
 
 }  // namespace
 
+namespace pa {
+// Records `msg` as the calling thread's last error and returns `code`.
+int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace pa
+
 extern "C" {
 
 const char *pa_last_error(void) { return g_err; }
