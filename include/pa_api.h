@@ -35,8 +35,10 @@
  *   - err_flag (nullable DEVICE int32): kernels OR bits into it when the DATA
  *     is invalid -- PA_FLAG_BAD_SLOT (slot outside [-1, num_blocks*block_size)),
  *     PA_FLAG_BAD_BLOCK (a block id inside a context outside [0, num_blocks)),
- *     PA_FLAG_BAD_LENGTH (a negative or over-long context / cu_seqlens).  The
- *     offending access is skipped (a bad page reads as zeros), so bad metadata
+ *     PA_FLAG_BAD_LENGTH (a negative or over-long context / cu_seqlens),
+ *     PA_FLAG_TIMEOUT (a kernel's bounded wait on its own asynchronous copies
+ *     or tensor-core work gave up; the kernel drained and returned).  The
+ *     offending access is skipped or kept inside the pool, so bad metadata
  *     never faults; the corresponding outputs are then unspecified.
  */
 #ifndef PA_API_H
@@ -68,6 +70,7 @@ enum {
     PA_FLAG_BAD_SLOT = 1,
     PA_FLAG_BAD_BLOCK = 2,
     PA_FLAG_BAD_LENGTH = 4,
+    PA_FLAG_TIMEOUT = 8,
 };
 
 /* Message describing the calling thread's last failed call ("" if none). */
@@ -189,17 +192,21 @@ PA_API int pa_decode_static_workspace(const void *q, int64_t q_row_stride, const
  *   - block_tables == NULL: no prefix (Lk must equal Lq for every sequence);
  *     keys are rows [cu_seqlens_q[i], cu_seqlens_q[i+1]) of k and v.
  *
- *   q             [total_q, num_q_heads, head_dim] contiguous.
+ *   q             [total_q, num_q_heads, head_dim] contiguous; total_q (host) is
+ *                 its row count, and cu_seqlens_q[num_seqs] must not exceed it.
  *   k, v          [total_q, num_kv_heads, head_dim] contiguous (may be NULL
  *                 when block_tables != NULL).
  *   cu_seqlens_q/k  int32 [num_seqs + 1], DEVICE.
  *   max_seqlen_q/k  host upper bounds on Lq / Lk (size the launch).
  *   out           [total_q, num_q_heads, head_dim] contiguous, written.
- * QK^T and PV run on the tensor cores (tcgen05, accumulators in TMEM).
+ * Buffers q, k, v, k_cache, v_cache must be 16-byte aligned (TMA).
+ * QK^T and PV run on the tensor cores (tcgen05, accumulators in TMEM), one
+ * CTA per 128 query rows of one head; K/V tiles of 128 keys come through the
+ * block table by TMA.
  */
 PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache,
                      const void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                     int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                     int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
                      const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_q_heads,
                      int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                      float scale, void *out, pa_dtype dtype, int32_t *err_flag, void *stream);

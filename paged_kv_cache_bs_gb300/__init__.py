@@ -39,12 +39,12 @@ _lib.pa_decode.restype = ctypes.c_int
 _lib.pa_decode.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
                            ctypes.c_int, _p, _p]
 _lib.pa_prefill_paged.restype = ctypes.c_int
-_lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32, _i32,
-                                  _i32, _f32, _p, ctypes.c_int, _p, _p]
+_lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32,
+                                  _i32, _i32, _f32, _p, ctypes.c_int, _p, _p]
 
 PA_F16, PA_BF16 = 0, 1
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
-FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH = 1, 2, 4
+FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT = 1, 2, 4, 8
 
 
 class PagedAttentionError(RuntimeError):
@@ -171,7 +171,7 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     if out is None:
         out = torch.empty(tq, hq, d, dtype=q.dtype, device=q.device)
     rc = _lib.pa_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
-                               _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k),
+                               _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq, int(max_seqlen_q), int(max_seqlen_k),
                                _ptr(block_tables), block_tables.shape[1] if block_tables is not None else 0,
                                hq, hkv, d, n, bs, float(scale), _ptr(out), _dtype(q), _ptr(err_flag), _stream(q))
     _check("pa_prefill_paged", rc)
@@ -180,4 +180,4 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
 
 __all__ = ["store_kv", "decode", "prefill_paged", "decode_workspace_bytes", "alloc_decode_workspace",
            "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
-           "FLAG_BAD_LENGTH"]
+           "FLAG_BAD_LENGTH", "FLAG_TIMEOUT"]

@@ -139,17 +139,38 @@ int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const vo
 }
 
 int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
-                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
                      int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
                      int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                      int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
                      int32_t *err_flag, void *stream) {
     int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
     if (rc) return rc;
-    (void)q; (void)k; (void)v; (void)k_cache; (void)v_cache; (void)cu_seqlens_q; (void)cu_seqlens_k;
-    (void)num_seqs; (void)max_seqlen_q; (void)max_seqlen_k; (void)block_tables; (void)max_blocks_per_seq;
-    (void)out; (void)err_flag; (void)stream;
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_paged is not built yet");
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < max_seqlen_q)
+        return fail(PA_ERR_INVALID_ARG, "sizes: num_seqs %d, total_q %d, max_seqlen_q %d, max_seqlen_k %d", num_seqs,
+                    total_q, max_seqlen_q, max_seqlen_k);
+    if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !out)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!block_tables && (!k || !v)) return fail(PA_ERR_INVALID_ARG, "k and v are required without block_tables");
+    if (block_tables && max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive with block_tables");
+    if (block_tables && static_cast<int64_t>(max_blocks_per_seq) * block_size > (1LL << 30))
+        return fail(PA_ERR_INVALID_ARG, "max context of %lld tokens is too large",
+                    (long long)max_blocks_per_seq * block_size);
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        (!block_tables && (!aligned(k, 16) || !aligned(v, 16))))
+        return fail(PA_ERR_INVALID_ARG, "q, k, v, caches and out must be 16-byte aligned");
+    const char *why = nullptr;
+    const cudaError_t e = pa::launch_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs,
+                                             total_q, max_seqlen_q, block_tables, max_blocks_per_seq, num_q_heads,
+                                             num_kv_heads, head_dim, num_blocks, block_size, scale, out, dtype,
+                                             err_flag, static_cast<cudaStream_t>(stream), &why);
+    if (why) return fail(PA_ERR_CUDA, "pa_prefill_paged: %s", why);
+    return cuda_status(e, "pa_prefill_paged launch");
 }
 
 }  // extern "C"

@@ -117,12 +117,16 @@ def test_workspace_size_is_host_only_and_sane(lib):
 
 def test_prefill_validation(lib):
     def call(**kw):
-        a = dict(q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, S=8, mq=512, mk=4096, bt=FAKE, mb=16,
+        a = dict(q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, S=8, tq=4096, mq=512, mk=4096, bt=FAKE, mb=16,
                  hq=32, hkv=8, d=128, n=600, bs=256, scale=0.088, out=FAKE, dt=1)
         a.update(kw)
-        return lib.pa_prefill_paged(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["cq"], a["ck"], a["S"], a["mq"],
+        return lib.pa_prefill_paged(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["cq"], a["ck"], a["S"], a["tq"], a["mq"],
                                     a["mk"], a["bt"], a["mb"], a["hq"], a["hkv"], a["d"], a["n"], a["bs"],
                                     ctypes.c_float(a["scale"]), a["out"], a["dt"], None, None)
     assert call(hq=30) == -1
     assert call(d=80) == -2
     assert call(dt=9) == -2
+    assert call(mk=100) == -1                       # max_seqlen_k < max_seqlen_q
+    assert call(bt=None, k=None) == -1              # packed keys needed without a block table
+    assert call(q=ctypes.c_void_p((1 << 20) + 8)) == -1   # TMA needs 16-byte alignment
+    assert call(S=0) == 0 and call(tq=0) == 0

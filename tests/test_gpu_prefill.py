@@ -1,0 +1,142 @@
+"""GPU parity of pa_prefill_paged (after pa_store_kv) against the oracle.
+
+Small cases run whole; the mixed chunked-prefill workload (8 x 512-token
+chunks over prefixes up to 3584 tokens) runs at full size through the call
+bench.py times, and the oracle recomputes sampled row windows of every
+sequence (the whole step is ~137 GFLOP, too slow for a single-threaded CPU).
+"""
+
+import pytest
+import torch
+
+import oracle
+from tests import inputs
+from tests.gpu_cases import TOL, assert_bit_equal, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill_gpu(pa, st, use_table=True, err_flag=None):
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    kn, vn = st.k_new.cuda(), st.v_new.cuda()
+    pa.store_kv(kn, vn, kc, vc, st.slot_mapping.cuda(), err_flag=err_flag)
+    bt = st.block_tables.cuda() if use_table else None
+    out = pa.prefill_paged(st.q.cuda(), kn, vn, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(),
+                           st.max_seqlen_q, st.max_seqlen_k, bt, st.scale, err_flag=err_flag)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def oracle_after_store(st):
+    okc, ovc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+    oracle.store_kv(st.k_new, st.v_new, okc, ovc, st.slot_mapping)
+    return okc, ovc
+
+
+def check_prefill_full(pa, st, use_table=True):
+    out, kc, vc = run_prefill_gpu(pa, st, use_table)
+    okc, ovc = oracle_after_store(st)
+    assert_bit_equal(kc, okc, "k_cache after store")
+    ref = oracle.prefill_paged(st.q, st.k_new, st.v_new, okc, ovc, st.cu_seqlens_q, st.cu_seqlens_k,
+                               st.block_tables if use_table else None, st.scale)
+    err = max_err(out, ref)
+    assert err <= TOL[st.q.dtype], f"max |err| {err}"
+    return err
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("head_dim", [128, 64])
+@pytest.mark.parametrize("bs", [16, 256])
+def test_prefill_over_prefix_small(pa, dtype, head_dim, bs):
+    # prefixes on and off tile boundaries, chunks from 1 row to several 128-row tiles
+    prefix = [0, 5, 128, 300, 1000, 77]
+    chunk = [7, 128, 200, 1, 129, 300]
+    st, _ = inputs.make_prefill(prefix, chunk, num_q_heads=8, num_kv_heads=2, head_dim=head_dim, block_size=bs,
+                                dtype=dtype, seed=70 + bs + head_dim)
+    err = check_prefill_full(pa, st)
+    print(f"prefill {dtype} D{head_dim} bs{bs}: max|err| {err:.2e}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 1), (32, 8)])
+@pytest.mark.parametrize("bs", [8, 64, 1024])
+def test_prefill_group_sizes_and_block_sizes(pa, hq, hkv, bs):
+    st, _ = inputs.make_prefill([33, 0, 640], [100, 64, 257], num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                                block_size=bs, dtype=torch.bfloat16, seed=80 + hq + bs)
+    check_prefill_full(pa, st)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_prefill_without_block_table(pa, dtype):
+    # fresh prompts: no cached prefix, keys are the packed k/v rows
+    st, _ = inputs.make_prefill([0, 0, 0], [11, 300, 129], num_q_heads=8, num_kv_heads=4, head_dim=128,
+                                block_size=16, dtype=dtype, seed=90)
+    check_prefill_full(pa, st, use_table=False)
+
+
+def test_prefill_table_and_packed_agree_without_prefix(pa):
+    st, _ = inputs.make_prefill([0, 0], [200, 77], num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                                dtype=torch.bfloat16, seed=91)
+    a, _, _ = run_prefill_gpu(pa, st, use_table=True)
+    b, _, _ = run_prefill_gpu(pa, st, use_table=False)
+    assert_bit_equal(a, b, "paged vs packed keys")
+
+
+def test_prefill_single_query_matches_decode(pa):
+    st, _ = inputs.make_prefill([500, 31, 4000], [1, 1, 1], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                block_size=256, dtype=torch.bfloat16, seed=92)
+    out, kc, vc = run_prefill_gpu(pa, st)
+    ctx = (st.cu_seqlens_k[1:] - st.cu_seqlens_k[:-1]).to(torch.int32)
+    dec = pa.decode(st.q.cuda(), kc, vc, st.block_tables.cuda(), ctx.cuda(), st.scale)
+    torch.cuda.synchronize()
+    assert max_err(out, dec.cpu().float()) <= TOL[torch.bfloat16]
+
+
+def test_prefill_mixed_workload_sampled_rows(pa):
+    m = inputs.mixed_chunked_prefill()
+    st = m.prefill
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    pa.store_kv(m.k_new.cuda(), m.v_new.cuda(), kc, vc, m.slot_mapping.cuda())
+    out = pa.prefill_paged(st.q.cuda(), st.k_new.cuda(), st.v_new.cuda(), kc, vc, st.cu_seqlens_q.cuda(),
+                           st.cu_seqlens_k.cuda(), st.max_seqlen_q, st.max_seqlen_k, st.block_tables.cuda(),
+                           st.scale)
+    torch.cuda.synchronize()
+    okc, ovc = p.k_cache.clone(), p.v_cache.clone()
+    oracle.store_kv(m.k_new, m.v_new, okc, ovc, m.slot_mapping)
+    assert_bit_equal(kc, okc, "k_cache after the mixed store")
+    assert_bit_equal(vc, ovc, "v_cache after the mixed store")
+    cq, ck = st.cu_seqlens_q.tolist(), st.cu_seqlens_k.tolist()
+    worst = 0.0
+    for i in range(len(cq) - 1):
+        lq, lk = cq[i + 1] - cq[i], ck[i + 1] - ck[i]
+        P = lk - lq
+        for r0, r1 in ((0, 16), (120, 136), (lq - 16, lq)):
+            rows = slice(cq[i] + r0, cq[i] + r1)
+            ref = oracle.prefill_paged(st.q[rows], st.k_new[rows], st.v_new[rows], okc, ovc,
+                                       torch.tensor([0, r1 - r0], dtype=torch.int32),
+                                       torch.tensor([0, P + r1], dtype=torch.int32), st.block_tables[i:i + 1],
+                                       st.scale)
+            worst = max(worst, max_err(out[rows], ref))
+    assert worst <= TOL[torch.bfloat16], f"max |err| {worst}"
+    print(f"mixed workload prefill: max|err| over sampled rows {worst:.2e}")
+
+
+def test_prefill_bad_metadata_is_flagged_not_fatal(pa):
+    st, _ = inputs.make_prefill([40, 40], [30, 30], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
+                                dtype=torch.bfloat16, seed=93)
+    bt = st.block_tables.clone()
+    bt[0, 1] = -1
+    bt[1, 2] = st.pool.num_blocks + 3
+    kc, vc = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.prefill_paged(st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(),
+                     st.max_seqlen_q, st.max_seqlen_k, bt.cuda(), st.scale, err_flag=flag)
+    ck = st.cu_seqlens_k.clone()
+    ck[2] = ck[1] + 10                      # context shorter than the query chunk
+    pa.prefill_paged(st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), ck.cuda(),
+                     st.max_seqlen_q, st.max_seqlen_k, st.block_tables.cuda(), st.scale, err_flag=flag)
+    torch.cuda.synchronize()
+    f = int(flag.item())
+    assert f & pa.FLAG_BAD_BLOCK and f & pa.FLAG_BAD_LENGTH and not f & pa.FLAG_TIMEOUT
+    check_prefill_full(pa, st)
