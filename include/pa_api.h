@@ -37,7 +37,8 @@
  *     PA_FLAG_BAD_BLOCK (a block id inside a context outside [0, num_blocks)),
  *     PA_FLAG_BAD_LENGTH (a negative or over-long context / cu_seqlens),
  *     PA_FLAG_TIMEOUT (a kernel's bounded wait on its own asynchronous copies
- *     or tensor-core work gave up; the kernel drained and returned).  The
+ *     or tensor-core work gave up; the kernel drained and returned),
+ *     PA_FLAG_INTERNAL (an internal layout invariant did not hold).  The
  *     offending access is skipped or kept inside the pool, so bad metadata
  *     never faults; the corresponding outputs are then unspecified.
  */
@@ -71,6 +72,7 @@ enum {
     PA_FLAG_BAD_BLOCK = 2,
     PA_FLAG_BAD_LENGTH = 4,
     PA_FLAG_TIMEOUT = 8,
+    PA_FLAG_INTERNAL = 16,
 };
 
 /* Message describing the calling thread's last failed call ("" if none). */
@@ -199,7 +201,8 @@ PA_API int pa_decode_static_workspace(const void *q, int64_t q_row_stride, const
  *   cu_seqlens_q/k  int32 [num_seqs + 1], DEVICE.
  *   max_seqlen_q/k  host upper bounds on Lq / Lk (size the launch).
  *   out           [total_q, num_q_heads, head_dim] contiguous, written.
- * Buffers q, k, v, k_cache, v_cache must be 16-byte aligned (TMA).
+ * Buffers q, k, v, k_cache, v_cache must be 16-byte aligned (TMA); scale must
+ * be positive (the kernel takes the row maximum of the unscaled scores).
  * QK^T and PV run on the tensor cores (tcgen05, accumulators in TMEM), one
  * CTA per 128 query rows of one head; K/V tiles of 128 keys come through the
  * block table by TMA.

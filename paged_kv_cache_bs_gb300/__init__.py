@@ -44,7 +44,7 @@ _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, 
 
 PA_F16, PA_BF16 = 0, 1
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
-FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT = 1, 2, 4, 8
+FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_INTERNAL = 1, 2, 4, 8, 16
 
 
 class PagedAttentionError(RuntimeError):
@@ -180,4 +180,4 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
 
 __all__ = ["store_kv", "decode", "prefill_paged", "decode_workspace_bytes", "alloc_decode_workspace",
            "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
-           "FLAG_BAD_LENGTH", "FLAG_TIMEOUT"]
+           "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL"]

@@ -146,6 +146,7 @@ int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_
                      int32_t *err_flag, void *stream) {
     int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
     if (rc) return rc;
+    if (!(scale > 0.f)) return fail(PA_ERR_INVALID_ARG, "pa_prefill_paged needs scale > 0 (got %g)", scale);
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < max_seqlen_q)
         return fail(PA_ERR_INVALID_ARG, "sizes: num_seqs %d, total_q %d, max_seqlen_q %d, max_seqlen_k %d", num_seqs,
                     total_q, max_seqlen_q, max_seqlen_k);

@@ -10,7 +10,16 @@
 // rows pa_store_kv wrote this step, as the pages' layer does with
 // k, v = k_cache, v_cache); without one, keys are the packed k/v rows.
 //
-// One CTA = 128 query rows of one query head (TMEM lane r = query row r).
+// One CTA = the same 128 query rows of two query heads of one GQA group
+// (one head without GQA), so every K/V tile serves two 128-row Q tiles.
+// Warp-specialised: warp 8 issues every TMA load and tcgen05.mma (one
+// thread); warpgroups 0 and 1 each run the softmax of one Q tile (TMEM lane
+// r = query row r); they hand off through mbarriers.  K/V go through a
+// 4-stage ring.  Each group has two TMEM slots: S_kt lands in slot kt & 1, the
+// softmax overwrites it with P_kt, and PV_kt reads P straight from TMEM, so
+// S_{kt+1} is computed while S_kt is softmaxed; the exponentials of tile kt
+// are computed while PV_{kt-1} runs, and only the TMEM store of P_kt waits
+// for it.
 //   * Q (once) and each 128-key K/V tile arrive by TMA with the 128-byte
 //     swizzle the MMA descriptors expect; K/V tiles are double-buffered and
 //     fetched page by page through the block table (one box per page when a
@@ -20,10 +29,9 @@
 //     (causal, bottom-right aligned, and past the context), and exponentiates
 //     in the log2 domain against a running maximum that is only moved when a
 //     tile's maximum exceeds it by more than 2^8, so the TMEM accumulator O
-//     is rescaled rarely; P goes to shared memory as bf16/fp16 in the swizzled
-//     K-major layout.
-//   * O += P V: tcgen05.mma with V as an N-major (D-contiguous) operand,
-//     accumulating in TMEM.
+//     is rescaled rarely; P is written back to TMEM as bf16/fp16.
+//   * O += P V: tcgen05.mma with A = P in TMEM and V as an N-major
+//     (D-contiguous) shared-memory operand, accumulating in TMEM.
 //   * Every mbarrier wait is bounded; a wait that gives up flags
 //     PA_FLAG_TIMEOUT, drains what this CTA has in flight (bounded again),
 //     frees TMEM and returns.
@@ -34,16 +42,19 @@
 namespace pa {
 namespace {
 
-constexpr int kBM = 128;  // query rows per CTA
-constexpr int kBN = 128;  // keys per tile
-constexpr int kThreads = 128;
+constexpr int kBM = 128;  // query rows per Q tile
+constexpr int kBN = 64;   // keys per K/V tile
+constexpr int kStages = 4;  // K/V ring depth
+constexpr int kWgThreads = 128;  // one softmax warpgroup: thread = query row = TMEM lane
+constexpr int kProducerWarp = 8; // warps 0-3: Q tile A, warps 4-7: Q tile B, warp 8: TMA + MMA
+constexpr int kThreads = 2 * kWgThreads + 32;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct PrefillMaps {
-    CUtensorMap q;  // [total_q rows, H_q*D cols]
-    CUtensorMap k;  // pool [N*bs rows, H_kv*D cols] (or packed [total_q, H_kv*D])
+    CUtensorMap q;  // [total_q rows, H_q*D cols], 128-row boxes
+    CUtensorMap k;  // pool [N*bs rows, H_kv*D cols] (or packed [total_q, H_kv*D]), boxes of min(bs, 64) rows
     CUtensorMap v;
 };
 
@@ -54,9 +65,10 @@ struct PrefillArgs {
     int32_t max_blocks;
     int32_t num_blocks;
     int32_t log2_bs;
-    int32_t box_rows;  // rows per K/V TMA box: min(block_size, 128)
+    int32_t box_rows;  // rows per K/V TMA box: min(block_size, kBN)
     int32_t num_q_heads;
     int32_t group;
+    int32_t heads_per_cta;  // 2: two query heads of one GQA group share K/V; 1 without GQA
     int32_t total_q;
     int32_t qtiles;
     float scale_log2;
@@ -64,17 +76,23 @@ struct PrefillArgs {
     int32_t *err_flag;
 };
 
+// Shared memory, every tile 1024-byte aligned with the 128-byte swizzle and
+// stored as 64-column "halves" of 128-byte rows:
+//   Q tile A, Q tile B [128 x D] | 4 stages of (K, V) [64 x D] | barriers
+// 192 KB at D = 128: one CTA per SM, whose two warpgroups fill all 512 TMEM
+// columns.  Per group: S/P slots 0 and 1 (64 columns each: S_kt in fp32,
+// then P_kt packed to 16 bits in its first 32 columns), O (D columns).
 template <int D> struct PShape {
-    static constexpr int kHalfBytes = 128 * 128;          // 128 rows x 64 columns (128 B) of a tile
     static constexpr int kHalves = D / 64;
-    static constexpr int kTileBytes = kHalves * kHalfBytes;  // Q, K or V tile of 128 rows
-    static constexpr int kPBytes = 2 * kHalfBytes;           // 128 rows x 128 keys
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kTileBytes;                // stage s: K then V
-    static constexpr int kOffP = kOffKV + 4 * kTileBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
-    static constexpr int kSmem = kOffBar + 64 + 1024;       // barriers, TMEM slot, alignment slack
-    static constexpr uint32_t kTmemCols = 256;               // S: 128 columns, O: D columns
+    static constexpr int kQHalf = kBM * 128;
+    static constexpr int kKHalf = kBN * 128;
+    static constexpr int kQBytes = kHalves * kQHalf;
+    static constexpr int kKVBytes = kHalves * kKHalf;
+    static constexpr int kOffQ = 0;                        // + wg * kQBytes
+    static constexpr int kOffK = 2 * kQBytes;              // + stage * 2 * kKVBytes (V follows K)
+    static constexpr int kOffBar = kOffK + kStages * 2 * kKVBytes;
+    static constexpr int kSmem = kOffBar + 256;
+    static constexpr uint32_t kTmemCols = 512;
 };
 
 template <typename T> struct IsBf16 { static constexpr bool value = false; };
@@ -84,13 +102,12 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillMaps maps,
                                                               const PrefillArgs a) {
     using S = PShape<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t sb = (raw + 1023u) & ~1023u;  // 1024-byte aligned for the 128-byte swizzle atoms
-    uint8_t *sgen = smem_raw + (sb - raw);
-
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int seq = blockIdx.z, h = blockIdx.y;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sb = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seq = blockIdx.z;
+    const int h0 = blockIdx.y * a.heads_per_cta;  // first query head of this CTA
+    const int nwg = a.heads_per_cta;
     const int qt = a.qtiles - 1 - static_cast<int>(blockIdx.x);  // later (heavier) tiles start first
 
     const int q_start = a.cu_q[seq], q_end = a.cu_q[seq + 1];
@@ -100,280 +117,308 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const bool bad = Lq < 0 || P < 0 || q_start < 0 || q_end > a.total_q || (!paged && P != 0) ||
                      (paged && static_cast<int64_t>(Lk) > (static_cast<int64_t>(a.max_blocks) << a.log2_bs));
     if (bad) {
-        if (tid == 0 && blockIdx.x == 0 && h == 0) raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
+        if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
         return;
     }
-    if (tid == 0 && blockIdx.x == 0 && h == 0 && Lq > a.qtiles * kBM) raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && Lq > a.qtiles * kBM)
+        raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
     const int q0 = qt * kBM;
     if (q0 >= Lq) return;
+    if (sb & 1023u) {  // the swizzled tiles need 1024-byte alignment
+        if (tid == 0) raise_flag(a.err_flag, PA_FLAG_INTERNAL);
+        return;
+    }
 
-    const int g = h / a.group;
+    const int g = h0 / a.group;            // both heads of the CTA read kv head g
     const int hi = min(Lk, P + q0 + kBM);  // keys [0, hi) are visible to some row of this tile
     const int nkt = (hi + kBN - 1) / kBN;
 
-    const uint32_t sQ = sb + S::kOffQ;
-    const uint32_t sP = sb + S::kOffP;
-    const uint32_t bar_full = sb + S::kOffBar;  // + 8 * stage
-    const uint32_t bar_q = bar_full + 16, bar_s = bar_full + 24, bar_o = bar_full + 32;
-    const uint32_t tmem_slot = bar_full + 40;
-    __shared__ int s_abort;
+    // mbarriers (8 bytes each) after the tiles
+    const uint32_t bar_full = sb + S::kOffBar;  // [4] K and V of a stage landed
+    const uint32_t bar_q = bar_full + 32;        // Q tiles landed
+    // per warpgroup w (base + 32 * w): S slot ready [2], P written, PV done
+    auto bar_sf = [&](int w, int slot) { return bar_full + 40 + 32 * w + 8 * slot; };
+    auto bar_p = [&](int w) { return bar_full + 56 + 32 * w; };
+    auto bar_o = [&](int w) { return bar_full + 64 + 32 * w; };
+    const uint32_t tmem_slot = bar_full + 136;
+    volatile int *abort_word = reinterpret_cast<volatile int *>(smem + S::kOffBar + 140);
 
     if (tid == 0) {
-        tc::mbar_init(bar_full, 1);
-        tc::mbar_init(bar_full + 8, 1);
+        for (int i = 0; i < kStages; ++i) tc::mbar_init(bar_full + 8 * i, 1);
         tc::mbar_init(bar_q, 1);
-        tc::mbar_init(bar_s, 1);
-        tc::mbar_init(bar_o, 1);
+        for (int w = 0; w < 2; ++w) {
+            for (int sl = 0; sl < 2; ++sl) tc::mbar_init(bar_sf(w, sl), 1);
+            tc::mbar_init(bar_p(w), kWgThreads);
+            tc::mbar_init(bar_o(w), 1);
+        }
         tc::mbar_fence_init();
-        tc::prefetch_tmap(&maps.q);
-        tc::prefetch_tmap(&maps.k);
-        tc::prefetch_tmap(&maps.v);
-        s_abort = 0;
+        *abort_word = 0;
     }
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         tc::tmem_alloc(tmem_slot, S::kTmemCols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + S::kOffBar + 40);
-    const uint32_t tS = tmem, tO = tmem + 128;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
-
-    auto sK = [&](int st) { return sb + S::kOffKV + st * 2 * S::kTileBytes; };
-    auto sV = [&](int st) { return sK(st) + S::kTileBytes; };
-
-    // ---- producer: one K/V tile through the block table (thread 0 only)
-    auto load_kv = [&](int kt, int st) {
-        const uint32_t bar = bar_full + 8 * st;
-        const int j0 = kt * kBN;
-        const int x = g * D;
-        if (!paged) {
-            tc::mbar_arrive_expect_tx(bar, 2 * S::kTileBytes);
-            for (int hf = 0; hf < S::kHalves; ++hf) {
-                tc::tma_load_2d(sK(st) + hf * S::kHalfBytes, &maps.k, x + hf * 64, q_start + j0, bar);
-                tc::tma_load_2d(sV(st) + hf * S::kHalfBytes, &maps.v, x + hf * 64, q_start + j0, bar);
-            }
-            return;
-        }
-        const int rows = a.box_rows;
-        const int npg = kBN / rows;
-        const int pages_in_ctx = (Lk + (1 << a.log2_bs) - 1) >> a.log2_bs;
-        int n = 0;
-        for (int p = 0; p < npg; ++p)
-            if (((j0 + p * rows) >> a.log2_bs) < pages_in_ctx) ++n;
-        tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * rows * 128 * S::kHalves * 2));
-        for (int p = 0; p < npg; ++p) {
-            const int jp = j0 + p * rows;
-            const int lp = jp >> a.log2_bs;
-            if (lp >= pages_in_ctx) break;
-            int page = a.block_tables[static_cast<int64_t>(seq) * a.max_blocks + lp];
-            if (page < 0 || page >= a.num_blocks) {
-                raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
-                page = 0;  // stay inside the pool; the sequence's output is then unspecified
-            }
-            const int y = (page << a.log2_bs) + (jp & ((1 << a.log2_bs) - 1));
-            for (int hf = 0; hf < S::kHalves; ++hf) {
-                tc::tma_load_2d(sK(st) + hf * S::kHalfBytes + p * rows * 128, &maps.k, x + hf * 64, y, bar);
-                tc::tma_load_2d(sV(st) + hf * S::kHalfBytes + p * rows * 128, &maps.v, x + hf * 64, y, bar);
-            }
-        }
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kOffBar + 136);
+    auto tS = [&](int w, int slot) { return tmem + 256 * w + 64 * slot; };
+    auto tO = [&](int w) { return tmem + 256 * w + 128; };
+    auto sQ = [&](int w) { return sb + S::kOffQ + w * S::kQBytes; };
+    auto sK = [&](int st) { return sb + S::kOffK + st * 2 * S::kKVBytes; };
+    auto sV = [&](int st) { return sK(st) + S::kKVBytes; };
+    auto wait = [&](uint32_t bar, uint32_t phase) {
+        return tc::mbar_wait_or_abort(bar, phase, kWaitCycles, abort_word);
     };
 
-    // in-flight bookkeeping for the bounded-wait exit path (thread 0)
-    int loads_issued = 0;  // K/V tiles whose TMA was issued
-    if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_q, S::kTileBytes);
-        for (int hf = 0; hf < S::kHalves; ++hf)
-            tc::tma_load_2d(sQ + hf * S::kHalfBytes, &maps.q, h * D + hf * 64, q_start + q0, bar_q);
-        load_kv(0, 0);
-        loads_issued = 1;
-        if (nkt > 1) {
-            load_kv(1, 1);
-            loads_issued = 2;
-        }
-    }
+    if (warp == kProducerWarp) {
+        // ================= producer + MMA issuer: one thread =================
+        if (lane == 0) {
+            const int pages_in_ctx = (Lk + (1 << a.log2_bs) - 1) >> a.log2_bs;
+            // K and V of keys [kt*kBN, kt*kBN + kBN) into stage kt % kStages, one barrier
+            auto load_kv = [&](int kt) {
+                const int st = kt % kStages;
+                const uint32_t bar = bar_full + 8 * st;
+                const int j0 = kt * kBN;
+                const int x = g * D;
+                if (!paged) {
+                    tc::mbar_arrive_expect_tx(bar, 2 * S::kKVBytes);
+                    for (int hf = 0; hf < S::kHalves; ++hf) {
+                        tc::tma_load_2d(sK(st) + hf * S::kKHalf, &maps.k, x + hf * 64, q_start + j0, bar);
+                        tc::tma_load_2d(sV(st) + hf * S::kKHalf, &maps.v, x + hf * 64, q_start + j0, bar);
+                    }
+                    return;
+                }
+                const int rows = a.box_rows;
+                const int npg = kBN / rows;
+                int n = 0;
+                for (int p = 0; p < npg; ++p)
+                    if (((j0 + p * rows) >> a.log2_bs) < pages_in_ctx) ++n;
+                tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * n * rows * 128 * S::kHalves));
+                for (int p = 0; p < npg; ++p) {
+                    const int jp = j0 + p * rows;
+                    const int lp = jp >> a.log2_bs;
+                    if (lp >= pages_in_ctx) break;
+                    int page = a.block_tables[static_cast<int64_t>(seq) * a.max_blocks + lp];
+                    if (page < 0 || page >= a.num_blocks) {
+                        raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
+                        page = 0;  // stay inside the pool; the sequence's output is then unspecified
+                    }
+                    const int y = (page << a.log2_bs) + (jp & ((1 << a.log2_bs) - 1));
+                    for (int hf = 0; hf < S::kHalves; ++hf) {
+                        tc::tma_load_2d(sK(st) + hf * S::kKHalf + p * rows * 128, &maps.k, x + hf * 64, y, bar);
+                        tc::tma_load_2d(sV(st) + hf * S::kKHalf + p * rows * 128, &maps.v, x + hf * 64, y, bar);
+                    }
+                }
+            };
+            constexpr uint32_t kIdS = tc::idesc_f16(kBM, kBN, IsBf16<T>::value, false);
+            constexpr uint32_t kIdO = tc::idesc_f16(kBM, D, IsBf16<T>::value, true);
+            // Descriptors are built once; a k-step or stage moves only the start-address field
+            // (bits 0-13, in 16-byte units), so each MMA issue is a single 64-bit add.
+            const uint64_t dQ0 = tc::smem_desc_sw128(sQ(0), 16, 1024);
+            const uint64_t dK0 = tc::smem_desc_sw128(sK(0), 16, 1024);
+            const uint64_t dV0 = tc::smem_desc_sw128(sV(0), S::kKHalf, 1024);
+            auto issue_s = [&](int w, int kt) {  // S_w[kt & 1] = Q_w K_kt^T
+                const uint64_t dq = dQ0 + static_cast<uint64_t>((w * S::kQBytes) >> 4);
+                const uint64_t dk = dK0 + static_cast<uint64_t>(((kt % kStages) * 2 * S::kKVBytes) >> 4);
+                const uint32_t d = tS(w, kt & 1);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc::umma_f16(d, dq + (((ks / 4) * S::kQHalf + (ks % 4) * 32) >> 4),
+                                 dk + (((ks / 4) * S::kKHalf + (ks % 4) * 32) >> 4), kIdS, ks > 0);
+                tc::umma_commit(bar_sf(w, kt & 1));
+            };
+            auto issue_pv = [&](int w, int kt) {  // O_w += P_w V_kt, P_w from its TMEM slot
+                const uint64_t dv = dV0 + static_cast<uint64_t>(((kt % kStages) * 2 * S::kKVBytes) >> 4);
+                const uint32_t a = tS(w, kt & 1), d = tO(w);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    tc::umma_f16_ts(d, a + ks * 8, dv + ((ks * 16 * 128) >> 4), kIdO, (kt > 0 || ks > 0) ? 1u : 0u);
+                tc::umma_commit(bar_o(w));
+            };
 
-    constexpr uint32_t kIdS = tc::idesc_f16(kBM, kBN, IsBf16<T>::value, false);
-    constexpr uint32_t kIdO = tc::idesc_f16(kBM, D, IsBf16<T>::value, true);
-
-    const int row = tid;                 // TMEM lane and query row within the tile
-    const int limit = P + q0 + row;      // last visible context position of this row
-    float m_used = -INFINITY, l_sum = 0.f;
-    bool ok = true;
-    int waited_tiles = 0, s_commits = 0, o_commits = 0;
-
-    for (int kt = 0; kt < nkt; ++kt) {
-        const int st = kt & 1;
-        const uint32_t full_phase = (kt >> 1) & 1;
-        const int j0 = kt * kBN;
-        const int valid = min(kBN, Lk - j0);
-        if (tid == 0) {
-            ok = tc::mbar_wait(bar_full + 8 * st, full_phase, kWaitCycles);
-            if (kt == 0) ok = ok && tc::mbar_wait(bar_q, 0, kWaitCycles);
-        }
-        if (valid < kBN) {
-            // rows past the context may hold anything (NaN included): zero them so P*V stays finite
-            if (tid != 0) ok = tc::mbar_wait(bar_full + 8 * st, full_phase, kWaitCycles);
-            const int nchunks = (kBN - valid) * 8 * S::kHalves;
-            uint4 *vz = reinterpret_cast<uint4 *>(sgen + (sV(st) - sb));
-            for (int c = tid; c < nchunks; c += kThreads) {
-                const int hf = c / ((kBN - valid) * 8);
-                const int rem = c % ((kBN - valid) * 8);
-                vz[(hf * S::kHalfBytes + (valid + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+            int issued = 0, waited = 0, commits = 0;  // K/V tiles loaded / consumed; MMA commits
+            uint32_t last_bar = 0, last_phase = 0;
+            bool ok = true;
+            tc::prefetch_tmap(&maps.q);
+            tc::prefetch_tmap(&maps.k);
+            tc::prefetch_tmap(&maps.v);
+            tc::mbar_arrive_expect_tx(bar_q, nwg * S::kQBytes);
+            for (int w = 0; w < nwg; ++w)
+                for (int hf = 0; hf < S::kHalves; ++hf)
+                    tc::tma_load_2d(sQ(w) + hf * S::kQHalf, &maps.q, (h0 + w) * D + hf * 64, q_start + q0, bar_q);
+            for (int t = 0; t < kStages && t < nkt; ++t) {
+                load_kv(t);
+                issued = t + 1;
             }
-            tc::fence_async_smem();
+            ok = wait(bar_q, 0) && wait(bar_full, 0);
+            waited = 1;
+            if (ok) {
+                tc::fence_after_sync();
+                for (int w = 0; w < nwg; ++w) issue_s(w, 0);
+                ++commits, last_bar = bar_sf(nwg - 1, 0), last_phase = 0;
+            }
+            for (int kt = 0; kt < nkt && ok; ++kt) {
+                // S_{kt+1} for every group into the slot of S/P_{kt-1}: the softmax was done with
+                // that slot before PV_{kt-1} (issued last iteration) and MMAs run in issue order.
+                if (kt + 1 < nkt) {
+                    const int n = kt + 1;
+                    ok = wait(bar_full + 8 * (n % kStages), (n / kStages) & 1);
+                    waited = n + 1;
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    for (int w = 0; w < nwg; ++w) issue_s(w, n);
+                    ++commits, last_bar = bar_sf(nwg - 1, n & 1), last_phase = (n >> 1) & 1;
+                }
+                // refill the stage tile kt-1 used with tile kt+3 once PV_{kt-1} is done everywhere
+                if (kt >= 1 && kt + 3 < nkt) {
+                    for (int w = 0; w < nwg && ok; ++w) ok = wait(bar_o(w), (kt - 1) & 1);
+                    if (!ok) break;
+                    load_kv(kt + 3);
+                    issued = kt + 4;
+                }
+                // O_w += P_w V_kt as each group's P is ready
+                for (int w = 0; w < nwg && ok; ++w) {
+                    ok = wait(bar_p(w), kt & 1);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_pv(w, kt);
+                    ++commits, last_bar = bar_o(w), last_phase = kt & 1;
+                }
+            }
+            if (!ok) {
+                // drain what this CTA started (bounded, ignoring the abort word), then report
+                raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
+                *abort_word = 1;
+                tc::mbar_wait(bar_q, 0, kWaitCycles);
+                for (int t = waited; t < issued; ++t)
+                    tc::mbar_wait(bar_full + 8 * (t % kStages), (t / kStages) & 1, kWaitCycles);
+                if (commits) tc::mbar_wait(last_bar, last_phase, kWaitCycles);  // covers every earlier MMA
+            }
         }
-        if (__syncthreads_or(!ok)) goto abort;
-        waited_tiles = kt + 1;
-
-        // ---- S = Q K^T
-        if (tid == 0) {
+        __syncwarp();
+    } else if (warp / 4 < nwg) {
+        // ================= softmax: thread = query row = TMEM lane =================
+        // Scores stay raw (unscaled) until the single FFMA feeding the
+        // exponential: scale > 0 keeps the raw maximum the scaled maximum.
+        const int w = warp / 4;
+        const int row = tid & (kWgThreads - 1);
+        const int h = h0 + w;
+        const int limit = P + q0 + row;  // last visible context position of this row
+        const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const float c = a.scale_log2;
+        float m_used = -INFINITY, l_sum = 0.f;  // m_used in scaled log2 units
+        bool ok = true;
+        for (int kt = 0; kt < nkt && ok; ++kt) {
+            const int j0 = kt * kBN;
+            ok = __all_sync(0xffffffffu, wait(bar_sf(w, kt & 1), (kt >> 1) & 1));  // warp-uniform
+            if (!ok) break;
             tc::fence_after_sync();
+            uint32_t sr[kBN];
+            tc::tmem_ld64(tS(w, kt & 1) + lane_base, sr);
+            if ((j0 + kBN - 1 > P + q0) || (j0 + kBN > Lk)) {  // diagonal or last tile: mask
+                const int lim = min(limit, Lk - 1) - j0;          // last visible column of this row
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (ks / 4) * S::kHalfBytes + (ks % 4) * 32;
-                tc::umma_f16(tS, tc::smem_desc_sw128(sQ + off, 16, 1024), tc::smem_desc_sw128(sK(st) + off, 16, 1024),
-                             kIdS, ks > 0);
+                for (int e = 0; e < kBN; ++e)
+                    if (e > lim) sr[e] = __float_as_uint(-INFINITY);
             }
-            tc::umma_commit(bar_s);
-        }
-        s_commits = kt + 1;
-        ok = tc::mbar_wait(bar_s, kt & 1, kWaitCycles);
-        tc::fence_after_sync();
-        if (__syncthreads_or(!ok)) goto abort;
-
-        // ---- softmax, part 1: the row of S, masked and scaled, and its maximum
-        uint32_t sr[4][32];
-        float mx = -INFINITY;
-        const bool need_mask = (j0 + kBN - 1 > P + q0) || (j0 + kBN > Lk);
+            float m8[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            tc::tmem_ld32(tS + lane_base + 32 * c, sr[c]);
+            for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(sr[e]);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int j = j0 + 32 * c + e;
-                float s = __uint_as_float(sr[c][e]) * a.scale_log2;
-                if (need_mask && (j > limit || j >= Lk)) s = -INFINITY;
-                sr[c][e] = __float_as_uint(s);
-                mx = fmaxf(mx, s);
+            for (int e = 8; e < kBN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * c;
+            // running maximum, moved only when this tile exceeds it by more than 2^8
+            const float m_new = fmaxf(m_used, mx);
+            float alpha = 1.f;
+            bool rescale = false;
+            if (kt == 0) {
+                m_used = m_new;
+            } else if (m_new > m_used + kRescaleThreshold) {
+                alpha = tc::ex2_approx(m_used - m_new);
+                m_used = m_new;
+                rescale = true;
             }
+            // P = 2^(c*s - m), packed to 16 bits
+            const float neg_m = -m_used;
+            uint32_t pw[kBN / 2];
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < kBN; e += 2) {
+                const float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[e]), c, neg_m));
+                const float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[e + 1]), c, neg_m));
+                l4[(e >> 1) & 3] += p0 + p1;
+                pw[e >> 1] = Dt<T>::pack(p0, p1);
+            }
+            l_sum = l_sum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+            if (kt > 0) {
+                // PV_{kt-1} must be done before P_kt goes to TMEM: a tcgen05.st into this group's
+                // lanes while its previous PV (A read from TMEM) was still running corrupted the
+                // result on sm_103a.  It also makes O stable for the (rare) rescale.
+                ok = __all_sync(0xffffffffu, wait(bar_o(w), (kt - 1) & 1));
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tO(w) + lane_base + 32 * cc, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::tmem_st32(tO(w) + lane_base + 32 * cc, o);
+                    }
+                }
+            }
+            tc::tmem_st32(tS(w, kt & 1) + lane_base, pw);  // P_kt over S_kt, read by PV_kt
+            const int valid = min(kBN, Lk - j0);
+            if (w == 0 && valid < kBN) {
+                // V rows past the context may hold anything (NaN included): zero them so P V stays
+                // finite.  Group 0 does it; the other group's PV is issued after group 0's.
+                const int st = kt % kStages;
+                ok = __all_sync(0xffffffffu, wait(bar_full + 8 * st, (kt / kStages) & 1));
+                if (!ok) break;
+                const int per_half = (kBN - valid) * 8;
+                uint4 *vz = reinterpret_cast<uint4 *>(smem + S::kOffK + st * 2 * S::kKVBytes + S::kKVBytes);
+                for (int i = row; i < per_half * S::kHalves; i += kWgThreads) {
+                    const int hf = i / per_half, rem = i % per_half;
+                    vz[(hf * S::kKHalf + (valid + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+                }
+                tc::fence_async_smem();
+            }
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar_p(w));
         }
-
-        // ---- PV of the previous tile must be done: O is stable, P and its K/V stage are free
-        if (kt > 0) {
-            ok = tc::mbar_wait(bar_o, (kt - 1) & 1, kWaitCycles);
+        if (ok) ok = wait(bar_o(w), (nkt - 1) & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
             tc::fence_after_sync();
-        }
-        if (tid == 0 && ok && kt >= 1 && kt + 1 < nkt) {
-            load_kv(kt + 1, st ^ 1);
-            loads_issued = kt + 2;
-        }
-
-        // ---- softmax, part 2: running maximum, rare rescale of O, P to shared memory
-        const float m_new = fmaxf(m_used, mx);
-        const bool rescale = kt > 0 && m_new > m_used + kRescaleThreshold;
-        if (kt == 0) {
-            m_used = m_new;
-        } else if (__any_sync(0xffffffffu, rescale)) {
-            const float alpha = rescale ? exp2f(m_used - m_new) : 1.f;
+            const int qrow = q0 + row;
+            const float inv_l = 1.f / l_sum;
+            T *dst = static_cast<T *>(a.out) + (static_cast<int64_t>(q_start + qrow) * a.num_q_heads + h) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
-                tc::tmem_ld32(tO + lane_base + 32 * c, o);
+                tc::tmem_ld32(tO(w) + lane_base + 32 * cc, o);
+                if (qrow < Lq) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                tc::tmem_st32(tO + lane_base + 32 * c, o);
-            }
-            l_sum *= alpha;
-            if (rescale) m_used = m_new;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk
-                uint32_t w[4];
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const float p0 = exp2f(__uint_as_float(sr[c][q8 * 8 + 2 * e2]) - m_used);
-                    const float p1 = exp2f(__uint_as_float(sr[c][q8 * 8 + 2 * e2 + 1]) - m_used);
-                    l_sum += p0 + p1;
-                    w[e2] = Dt<T>::pack(p0, p1);
-                }
-                const int chunk = c * 4 + q8;  // 0..15 along the keys
-                const int hf = chunk >> 3, cc = chunk & 7;
-                const uint32_t addr = sP + hf * S::kHalfBytes + row * 128 + ((cc ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
-                             : "memory");
-            }
-        }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        if (__syncthreads_or(!ok)) goto abort;
-
-        // ---- O += P V
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks) {
-                const uint32_t aoff = (ks / 4) * S::kHalfBytes + (ks % 4) * 32;
-                tc::umma_f16(tO, tc::smem_desc_sw128(sP + aoff, 16, 1024),
-                             tc::smem_desc_sw128(sV(st) + ks * 16 * 128, S::kHalfBytes, 1024), kIdO,
-                             (kt > 0 || ks > 0) ? 1u : 0u);
-            }
-            tc::umma_commit(bar_o);
-        }
-        o_commits = kt + 1;
-    }
-
-    // ---- epilogue: O / l -> out
-    ok = tc::mbar_wait(bar_o, (nkt - 1) & 1, kWaitCycles);
-    tc::fence_after_sync();
-    if (__syncthreads_or(!ok)) goto abort;
-    {
-        const int qrow = q0 + row;
-        const float inv_l = 1.f / l_sum;
-        T *dst = static_cast<T *>(a.out) + (static_cast<int64_t>(q_start + qrow) * a.num_q_heads + h) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(tO + lane_base + 32 * c, o);
-            if (qrow < Lq) {
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    uint4 v;
-                    v.x = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 0]) * inv_l, __uint_as_float(o[q8 * 8 + 1]) * inv_l);
-                    v.y = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 2]) * inv_l, __uint_as_float(o[q8 * 8 + 3]) * inv_l);
-                    v.z = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 4]) * inv_l, __uint_as_float(o[q8 * 8 + 5]) * inv_l);
-                    v.w = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 6]) * inv_l, __uint_as_float(o[q8 * 8 + 7]) * inv_l);
-                    *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q8) = v;
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        uint4 v;
+                        v.x = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 0]) * inv_l, __uint_as_float(o[q8 * 8 + 1]) * inv_l);
+                        v.y = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 2]) * inv_l, __uint_as_float(o[q8 * 8 + 3]) * inv_l);
+                        v.z = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 4]) * inv_l, __uint_as_float(o[q8 * 8 + 5]) * inv_l);
+                        v.w = Dt<T>::pack(__uint_as_float(o[q8 * 8 + 6]) * inv_l, __uint_as_float(o[q8 * 8 + 7]) * inv_l);
+                        *reinterpret_cast<uint4 *>(dst + 32 * cc + 8 * q8) = v;
+                    }
                 }
             }
         }
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 0) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, S::kTmemCols);
-    }
-    return;
 
-abort:
-    // A wait gave up: flag it, let what this CTA started finish (bounded), free TMEM.
-    if (tid == 0) {
-        if (atomicExch(&s_abort, 1) == 0) raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
-        for (int t = waited_tiles; t < loads_issued; ++t)
-            tc::mbar_wait(bar_full + 8 * (t & 1), (t >> 1) & 1, kWaitCycles);
-        if (s_commits > 0) tc::mbar_wait(bar_s, (s_commits - 1) & 1, kWaitCycles);
-        if (o_commits > 0) tc::mbar_wait(bar_o, (o_commits - 1) & 1, kWaitCycles);
-        tc::mbar_wait(bar_q, 0, kWaitCycles);
-    }
+    // teardown: every role is done with TMEM (the producer drained on abort)
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, S::kTmemCols);
     }
@@ -424,7 +469,8 @@ cudaError_t run(const PrefillMaps &maps, const PrefillArgs &a, int num_seqs, cud
     using S = PShape<D>;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<T, D><<<dim3(a.qtiles, a.num_q_heads, num_seqs), kThreads, S::kSmem, stream>>>(maps, a);
+    prefill_kernel<T, D><<<dim3(a.qtiles, a.num_q_heads / a.heads_per_cta, num_seqs), kThreads, S::kSmem, stream>>>(
+        maps, a);
     return cudaGetLastError();
 }
 
@@ -448,7 +494,8 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
         ok = ok && make_map(&maps.k, k_cache, dtype, kv_cols, rows, box_rows) &&
              make_map(&maps.v, v_cache, dtype, kv_cols, rows, box_rows);
     } else {
-        ok = ok && make_map(&maps.k, k, dtype, kv_cols, total_q, kBN) && make_map(&maps.v, v, dtype, kv_cols, total_q, kBN);
+        ok = ok && make_map(&maps.k, k, dtype, kv_cols, total_q, kBN) &&
+             make_map(&maps.v, v, dtype, kv_cols, total_q, kBN);
     }
     if (!ok) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor too large)";
@@ -464,6 +511,7 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
     a.box_rows = box_rows;
     a.num_q_heads = num_q_heads;
     a.group = num_q_heads / num_kv_heads;
+    a.heads_per_cta = a.group >= 2 ? 2 : 1;
     a.total_q = total_q;
     a.qtiles = (max_seqlen_q + kBM - 1) / kBM;
     a.scale_log2 = scale * kLog2e;

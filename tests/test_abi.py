@@ -129,4 +129,5 @@ def test_prefill_validation(lib):
     assert call(mk=100) == -1                       # max_seqlen_k < max_seqlen_q
     assert call(bt=None, k=None) == -1              # packed keys needed without a block table
     assert call(q=ctypes.c_void_p((1 << 20) + 8)) == -1   # TMA needs 16-byte alignment
+    assert call(scale=0.0) == -1 and call(scale=-0.1) == -1
     assert call(S=0) == 0 and call(tq=0) == 0
