@@ -108,7 +108,8 @@ PA_API int pa_store_kv(const void *k, const void *v, int64_t k_row_stride, int64
 
 /*
  * pa_decode_workspace_bytes -- device scratch pa_decode needs for this shape
- * (per-partition softmax partials).  Pure host computation; 0 on invalid
+ * (per-partition softmax partials) on the current device: the split-K plan
+ * depends on its SM count, which is queried once per device.  0 on invalid
  * arguments.
  */
 PA_API size_t pa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,

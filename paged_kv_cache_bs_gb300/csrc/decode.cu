@@ -40,7 +40,7 @@ constexpr int kStages = 3;
 constexpr int kMaxTablePages = 257;  // block-table entries one partition may touch
 constexpr int kMaxPartition = 2048;
 constexpr int kMinPartition = 128;
-constexpr int kTargetCtas = 16 * 152;  // enough waves to absorb ragged contexts
+constexpr int kTargetCtas = 16 * 152;  // ragged batches: enough waves to absorb the length spread
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
@@ -349,19 +349,46 @@ int ilog2(int x) {
 
 }  // namespace
 
+// Resident decode CTAs the current device holds at once (2 per SM).
+static int resident_ctas() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2 * 148;
+    if (!cached[dev]) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+        cached[dev] = 2 * sms;
+    }
+    return cached[dev];
+}
+
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                        int32_t max_blocks_per_seq, int32_t block_size) {
     DecodePlan pl{};
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int64_t pairs = static_cast<int64_t>(batch) * num_kv_heads;
-    int part = kMaxPartition;
-    while (part > kMinPartition && pairs * ((cap + part - 1) / part) < kTargetCtas) part /= 2;
+    const int64_t slots = resident_ctas();
+    const int64_t tiles = (cap + kTile - 1) / kTile;
+    int64_t part;
+    if (pairs >= 2 * slots) {
+        part = tiles * kTile;  // (sequence, kv head) pairs alone fill two waves: no split
+    } else if (2 * pairs <= slots) {
+        // few (sequence, kv head) pairs: one wave of equal partitions, each CTA streaming as
+        // long as possible (the per-CTA start-up cost is paid once per SM slot)
+        const int64_t per = slots / pairs > 1 ? slots / pairs : 1;
+        part = ((tiles + per - 1) / per) * kTile;
+    } else {
+        // ragged batches: enough smaller partitions for the scheduler to even out lengths
+        part = kMaxPartition;
+        while (part > kMinPartition && pairs * ((cap + part - 1) / part) < kTargetCtas) part /= 2;
+    }
     if (const char *env = getenv("PA_DECODE_PARTITION")) {  // tuning override
         const int v = atoi(env);
-        if (v >= kTile && v % kTile == 0 && v <= 16384) part = v;
+        if (v >= kTile && v % kTile == 0 && v <= (1 << 20)) part = v;
     }
-    while (part / block_size > kMaxTablePages - 1) part /= 2;  // table slice must fit in shared memory
-    pl.partition = part;
+    while (part / block_size > kMaxTablePages - 1) part = (part / 2 + kTile - 1) / kTile * kTile;  // table slice fits
+    if (part < kTile) part = kTile;
+    pl.partition = static_cast<int>(part);
     pl.max_parts = static_cast<int>(cap > 0 ? (cap + part - 1) / part : 1);
     const size_t n = static_cast<size_t>(batch) * num_q_heads * pl.max_parts;
     const size_t ml_bytes = (n * sizeof(float2) + 255) / 256 * 256;

@@ -110,7 +110,10 @@ def test_workspace_size_is_host_only_and_sane(lib):
     lib.pa_decode_workspace_bytes.restype = ctypes.c_size_t
     w = lib.pa_decode_workspace_bytes(64, 16, 8, 128, 16, 256)
     assert w > 0 and w % 4 == 0
-    assert lib.pa_decode_workspace_bytes(128, 16, 8, 128, 16, 256) >= w
+    # the split-K plan depends on the shape: any valid shape needs a positive, 4-byte multiple
+    for shape in ((128, 16, 8, 128, 16, 256), (4, 32, 8, 128, 128, 256), (256, 32, 8, 128, 128, 16)):
+        v = lib.pa_decode_workspace_bytes(*shape)
+        assert v > 0 and v % 4 == 0
     assert lib.pa_decode_workspace_bytes(-1, 16, 8, 128, 16, 256) == 0
     assert lib.pa_decode_workspace_bytes(4, 32, 8, 128, 128, 12) == 0
 
