@@ -24,7 +24,8 @@
 //   * Warps merge through shared memory at the end of the partition; a
 //     sequence with one partition writes its output directly, otherwise the
 //     (max, sum, unnormalised O) partials go to the workspace and a second
-//     kernel merges them by log-sum-exp.
+//     kernel merges them by log-sum-exp; it is launched as a programmatic
+//     dependent of the first, so its launch overlaps the partition kernel.
 #include <math.h>
 #include <stdlib.h>
 
@@ -99,6 +100,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 
     const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // Launched as a programmatic dependent of the previous kernel on the stream (the store
+    // of this step): wait for it to finish before reading the cache, and let the merge
+    // kernel be launched right away (it waits for this grid itself).
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     int L = context_len(a, b);
     if (L < 0) {
@@ -324,6 +330,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
     const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    // launched early (programmatic dependent launch): wait until the partition grid has
+    // finished and its partials are visible
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int L = max(context_len(a, b), 0);
     const int np = (L + a.partition - 1) / a.partition;
     if (np <= 1) return;
@@ -436,8 +445,16 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
         if (a.max_parts > 1) {
-            kern_comb<<<dim3(a.num_q_heads, batch), d, 0, stream>>>(a);
-            err = cudaGetLastError();
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(a.num_q_heads, batch);
+            cfg.blockDim = dim3(d);
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&cfg, kern_comb, a);
         }
         return err;
     };

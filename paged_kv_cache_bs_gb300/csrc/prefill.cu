@@ -103,6 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                                               const PrefillArgs a) {
     using S = PShape<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
+    // launched as a programmatic dependent of the store of this step: wait for it first
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seq = blockIdx.z;
@@ -469,9 +471,17 @@ cudaError_t run(const PrefillMaps &maps, const PrefillArgs &a, int num_seqs, cud
     using S = PShape<D>;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<T, D><<<dim3(a.qtiles, a.num_q_heads / a.heads_per_cta, num_seqs), kThreads, S::kSmem, stream>>>(
-        maps, a);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.qtiles, a.num_q_heads / a.heads_per_cta, num_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = S::kSmem;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<T, D>, maps, a);
 }
 
 }  // namespace

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 store_kv_kernel(const V *__restrict__ k, const V *__restrict__ v, int64_t k_stride_v, int64_t v_stride_v,
                 V *__restrict__ k_cache, V *__restrict__ v_cache, const int32_t *__restrict__ slot_mapping,
                 int32_t num_tokens, int32_t row_v, int64_t num_slots, int32_t *err_flag) {
+    // the attention kernel of the same step may be launched now (it waits for this grid)
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int32_t t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= num_tokens) return;
