@@ -11,15 +11,14 @@
 // k, v = k_cache, v_cache); without one, keys are the packed k/v rows.
 //
 // One CTA = the same 128 query rows of two query heads of one GQA group
-// (one head without GQA), so every K/V tile serves two 128-row Q tiles.
-// Warp-specialised: warp 8 issues every TMA load and tcgen05.mma (one
-// thread); warpgroups 0 and 1 each run the softmax of one Q tile (TMEM lane
-// r = query row r); they hand off through mbarriers.  K/V go through a
-// 4-stage ring.  Each group has two TMEM slots: S_kt lands in slot kt & 1, the
-// softmax overwrites it with P_kt, and PV_kt reads P straight from TMEM, so
-// S_{kt+1} is computed while S_kt is softmaxed; the exponentials of tile kt
-// are computed while PV_{kt-1} runs, and only the TMEM store of P_kt waits
-// for it.
+// (one head without GQA), so every 128-key K/V tile serves two Q tiles.
+// Warp-specialised: warp 9 issues every TMA load, warp 8 every tcgen05.mma
+// (one thread each); warpgroups 0 and 1 run the softmax of heads A and B
+// (TMEM lane r = query row r); all hand-offs are mbarriers.  A single
+// tcgen05.mma issue takes ~100 cycles on this part, so S MMAs use N = 128
+// keys.  The heads ping-pong: while head A's softmax runs, the tensor core
+// does head B's PV and next S, and vice versa.  Each head's S tile is
+// overwritten in TMEM by its P, which the PV MMA reads from TMEM.
 //   * Q (once) and each 128-key K/V tile arrive by TMA with the 128-byte
 //     swizzle the MMA descriptors expect; K/V tiles are double-buffered and
 //     fetched page by page through the block table (one box per page when a
@@ -43,18 +42,18 @@ namespace pa {
 namespace {
 
 constexpr int kBM = 128;  // query rows per Q tile
-constexpr int kBN = 64;   // keys per K/V tile
-constexpr int kStages = 4;  // K/V ring depth
-constexpr int kWgThreads = 128;  // one softmax warpgroup: thread = query row = TMEM lane
-constexpr int kProducerWarp = 8; // warps 0-3: Q tile A, warps 4-7: Q tile B, warp 8: TMA + MMA
-constexpr int kThreads = 2 * kWgThreads + 32;
+constexpr int kBN = 128;  // keys per K/V tile (the N of every S MMA)
+constexpr int kWgThreads = 128;    // one softmax warpgroup: thread = query row = TMEM lane
+constexpr int kMmaWarp = 8;        // warps 0-3: head A softmax, 4-7: head B softmax
+constexpr int kTmaWarp = 9;        // warp 8: MMA issuer, warp 9: TMA producer
+constexpr int kThreads = 2 * kWgThreads + 64;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct PrefillMaps {
     CUtensorMap q;  // [total_q rows, H_q*D cols], 128-row boxes
-    CUtensorMap k;  // pool [N*bs rows, H_kv*D cols] (or packed [total_q, H_kv*D]), boxes of min(bs, 64) rows
+    CUtensorMap k;  // pool [N*bs rows, H_kv*D cols] (or packed [total_q, H_kv*D]), boxes of min(bs, 128) rows
     CUtensorMap v;
 };
 
@@ -78,19 +77,18 @@ struct PrefillArgs {
 
 // Shared memory, every tile 1024-byte aligned with the 128-byte swizzle and
 // stored as 64-column "halves" of 128-byte rows:
-//   Q tile A, Q tile B [128 x D] | 4 stages of (K, V) [64 x D] | barriers
-// 192 KB at D = 128: one CTA per SM, whose two warpgroups fill all 512 TMEM
-// columns.  Per group: S/P slots 0 and 1 (64 columns each: S_kt in fp32,
-// then P_kt packed to 16 bits in its first 32 columns), O (D columns).
+//   Q tile A, Q tile B [128 x D] | K slots 0, 1 [128 x D] | V slots 0, 1 [128 x D] | barriers
+// 192 KB at D = 128: one CTA per SM.  TMEM (512 columns): per head, S/P
+// [0, 128) (S_kt in fp32, then P_kt packed to 16 bits in its first 64
+// columns) and O [128, 128 + D).
 template <int D> struct PShape {
     static constexpr int kHalves = D / 64;
-    static constexpr int kQHalf = kBM * 128;
-    static constexpr int kKHalf = kBN * 128;
-    static constexpr int kQBytes = kHalves * kQHalf;
-    static constexpr int kKVBytes = kHalves * kKHalf;
-    static constexpr int kOffQ = 0;                        // + wg * kQBytes
-    static constexpr int kOffK = 2 * kQBytes;              // + stage * 2 * kKVBytes (V follows K)
-    static constexpr int kOffBar = kOffK + kStages * 2 * kKVBytes;
+    static constexpr int kHalf = 128 * 128;  // one 64-column half of a 128-row tile
+    static constexpr int kTile = kHalves * kHalf;
+    static constexpr int kOffQ = 0;                 // + head * kTile
+    static constexpr int kOffK = 2 * kTile;         // + slot * kTile
+    static constexpr int kOffV = 4 * kTile;         // + slot * kTile
+    static constexpr int kOffBar = 6 * kTile;
     static constexpr int kSmem = kOffBar + 256;
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -136,59 +134,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int nkt = (hi + kBN - 1) / kBN;
 
     // mbarriers (8 bytes each) after the tiles
-    const uint32_t bar_full = sb + S::kOffBar;  // [4] K and V of a stage landed
-    const uint32_t bar_q = bar_full + 32;        // Q tiles landed
-    // per warpgroup w (base + 32 * w): S slot ready [2], P written, PV done
-    auto bar_sf = [&](int w, int slot) { return bar_full + 40 + 32 * w + 8 * slot; };
-    auto bar_p = [&](int w) { return bar_full + 56 + 32 * w; };
-    auto bar_o = [&](int w) { return bar_full + 64 + 32 * w; };
-    const uint32_t tmem_slot = bar_full + 136;
-    volatile int *abort_word = reinterpret_cast<volatile int *>(smem + S::kOffBar + 140);
+    const uint32_t bar0 = sb + S::kOffBar;
+    const uint32_t bar_q = bar0;                                      // Q tiles landed
+    auto bar_kf = [&](int slot) { return bar0 + 8 + 8 * slot; };      // K slot landed
+    auto bar_ke = [&](int slot) { return bar0 + 24 + 8 * slot; };     // K slot read by both S MMAs
+    auto bar_vf = [&](int slot) { return bar0 + 40 + 8 * slot; };     // V slot landed
+    auto bar_ve = [&](int slot) { return bar0 + 56 + 8 * slot; };     // V slot read by both PV MMAs
+    auto bar_s = [&](int w) { return bar0 + 72 + 8 * w; };            // S_w in TMEM
+    auto bar_p = [&](int w) { return bar0 + 88 + 8 * w; };            // P_w in TMEM (128 arrivals)
+    auto bar_o = [&](int w) { return bar0 + 104 + 8 * w; };           // PV_w done
+    const uint32_t tmem_slot = bar0 + 120;
+    volatile int *abort_word = reinterpret_cast<volatile int *>(smem + S::kOffBar + 124);
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) tc::mbar_init(bar_full + 8 * i, 1);
         tc::mbar_init(bar_q, 1);
-        for (int w = 0; w < 2; ++w) {
-            for (int sl = 0; sl < 2; ++sl) tc::mbar_init(bar_sf(w, sl), 1);
-            tc::mbar_init(bar_p(w), kWgThreads);
-            tc::mbar_init(bar_o(w), 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar_kf(i), 1);
+            tc::mbar_init(bar_ke(i), 1);
+            tc::mbar_init(bar_vf(i), 1);
+            tc::mbar_init(bar_ve(i), 1);
+            tc::mbar_init(bar_s(i), 1);
+            tc::mbar_init(bar_p(i), kWgThreads);
+            tc::mbar_init(bar_o(i), 1);
         }
         tc::mbar_fence_init();
         *abort_word = 0;
     }
-    if (warp == kProducerWarp) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(tmem_slot, S::kTmemCols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kOffBar + 136);
-    auto tS = [&](int w, int slot) { return tmem + 256 * w + 64 * slot; };
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kOffBar + 120);
+    auto tS = [&](int w) { return tmem + 256 * w; };
     auto tO = [&](int w) { return tmem + 256 * w + 128; };
-    auto sQ = [&](int w) { return sb + S::kOffQ + w * S::kQBytes; };
-    auto sK = [&](int st) { return sb + S::kOffK + st * 2 * S::kKVBytes; };
-    auto sV = [&](int st) { return sK(st) + S::kKVBytes; };
     auto wait = [&](uint32_t bar, uint32_t phase) {
         return tc::mbar_wait_or_abort(bar, phase, kWaitCycles, abort_word);
     };
 
-    if (warp == kProducerWarp) {
-        // ================= producer + MMA issuer: one thread =================
+    if (warp == kTmaWarp) {
+        // ================= TMA producer: one thread =================
         if (lane == 0) {
             const int pages_in_ctx = (Lk + (1 << a.log2_bs) - 1) >> a.log2_bs;
-            // K and V of keys [kt*kBN, kt*kBN + kBN) into stage kt % kStages, one barrier
-            auto load_kv = [&](int kt) {
-                const int st = kt % kStages;
-                const uint32_t bar = bar_full + 8 * st;
-                const int j0 = kt * kBN;
+            // keys [t*kBN, t*kBN + kBN) of K or V into `dst`, page by page through the block table
+            auto load = [&](const CUtensorMap *map, uint32_t dst, uint32_t bar, int t) {
+                const int j0 = t * kBN;
                 const int x = g * D;
                 if (!paged) {
-                    tc::mbar_arrive_expect_tx(bar, 2 * S::kKVBytes);
-                    for (int hf = 0; hf < S::kHalves; ++hf) {
-                        tc::tma_load_2d(sK(st) + hf * S::kKHalf, &maps.k, x + hf * 64, q_start + j0, bar);
-                        tc::tma_load_2d(sV(st) + hf * S::kKHalf, &maps.v, x + hf * 64, q_start + j0, bar);
-                    }
+                    tc::mbar_arrive_expect_tx(bar, S::kTile);
+                    for (int hf = 0; hf < S::kHalves; ++hf)
+                        tc::tma_load_2d(dst + hf * S::kHalf, map, x + hf * 64, q_start + j0, bar);
                     return;
                 }
                 const int rows = a.box_rows;
@@ -196,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 int n = 0;
                 for (int p = 0; p < npg; ++p)
                     if (((j0 + p * rows) >> a.log2_bs) < pages_in_ctx) ++n;
-                tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * n * rows * 128 * S::kHalves));
+                tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * rows * 128 * S::kHalves));
                 for (int p = 0; p < npg; ++p) {
                     const int jp = j0 + p * rows;
                     const int lp = jp >> a.log2_bs;
@@ -207,94 +204,102 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         page = 0;  // stay inside the pool; the sequence's output is then unspecified
                     }
                     const int y = (page << a.log2_bs) + (jp & ((1 << a.log2_bs) - 1));
-                    for (int hf = 0; hf < S::kHalves; ++hf) {
-                        tc::tma_load_2d(sK(st) + hf * S::kKHalf + p * rows * 128, &maps.k, x + hf * 64, y, bar);
-                        tc::tma_load_2d(sV(st) + hf * S::kKHalf + p * rows * 128, &maps.v, x + hf * 64, y, bar);
-                    }
+                    for (int hf = 0; hf < S::kHalves; ++hf)
+                        tc::tma_load_2d(dst + hf * S::kHalf + p * rows * 128, map, x + hf * 64, y, bar);
                 }
             };
-            constexpr uint32_t kIdS = tc::idesc_f16(kBM, kBN, IsBf16<T>::value, false);
-            constexpr uint32_t kIdO = tc::idesc_f16(kBM, D, IsBf16<T>::value, true);
-            // Descriptors are built once; a k-step or stage moves only the start-address field
-            // (bits 0-13, in 16-byte units), so each MMA issue is a single 64-bit add.
-            const uint64_t dQ0 = tc::smem_desc_sw128(sQ(0), 16, 1024);
-            const uint64_t dK0 = tc::smem_desc_sw128(sK(0), 16, 1024);
-            const uint64_t dV0 = tc::smem_desc_sw128(sV(0), S::kKHalf, 1024);
-            auto issue_s = [&](int w, int kt) {  // S_w[kt & 1] = Q_w K_kt^T
-                const uint64_t dq = dQ0 + static_cast<uint64_t>((w * S::kQBytes) >> 4);
-                const uint64_t dk = dK0 + static_cast<uint64_t>(((kt % kStages) * 2 * S::kKVBytes) >> 4);
-                const uint32_t d = tS(w, kt & 1);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    tc::umma_f16(d, dq + (((ks / 4) * S::kQHalf + (ks % 4) * 32) >> 4),
-                                 dk + (((ks / 4) * S::kKHalf + (ks % 4) * 32) >> 4), kIdS, ks > 0);
-                tc::umma_commit(bar_sf(w, kt & 1));
-            };
-            auto issue_pv = [&](int w, int kt) {  // O_w += P_w V_kt, P_w from its TMEM slot
-                const uint64_t dv = dV0 + static_cast<uint64_t>(((kt % kStages) * 2 * S::kKVBytes) >> 4);
-                const uint32_t a = tS(w, kt & 1), d = tO(w);
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks)
-                    tc::umma_f16_ts(d, a + ks * 8, dv + ((ks * 16 * 128) >> 4), kIdO, (kt > 0 || ks > 0) ? 1u : 0u);
-                tc::umma_commit(bar_o(w));
-            };
-
-            int issued = 0, waited = 0, commits = 0;  // K/V tiles loaded / consumed; MMA commits
-            uint32_t last_bar = 0, last_phase = 0;
-            bool ok = true;
             tc::prefetch_tmap(&maps.q);
             tc::prefetch_tmap(&maps.k);
             tc::prefetch_tmap(&maps.v);
-            tc::mbar_arrive_expect_tx(bar_q, nwg * S::kQBytes);
+            tc::mbar_arrive_expect_tx(bar_q, nwg * S::kTile);
             for (int w = 0; w < nwg; ++w)
                 for (int hf = 0; hf < S::kHalves; ++hf)
-                    tc::tma_load_2d(sQ(w) + hf * S::kQHalf, &maps.q, (h0 + w) * D + hf * 64, q_start + q0, bar_q);
-            for (int t = 0; t < kStages && t < nkt; ++t) {
-                load_kv(t);
-                issued = t + 1;
+                    tc::tma_load_2d(sb + S::kOffQ + w * S::kTile + hf * S::kHalf, &maps.q, (h0 + w) * D + hf * 64,
+                                    q_start + q0, bar_q);
+            int k_issued = 0, v_issued = 0;  // tiles loaded, for the drain on abort
+            bool ok = true;
+            for (int t = 0; t < nkt && ok; ++t) {
+                const int slot = t & 1;
+                if (t >= 2) ok = wait(bar_ke(slot), ((t - 2) >> 1) & 1);
+                if (!ok) break;
+                load(&maps.k, sb + S::kOffK + slot * S::kTile, bar_kf(slot), t);
+                k_issued = t + 1;
+                if (t >= 2) ok = wait(bar_ve(slot), ((t - 2) >> 1) & 1);
+                if (!ok) break;
+                load(&maps.v, sb + S::kOffV + slot * S::kTile, bar_vf(slot), t);
+                v_issued = t + 1;
             }
-            ok = wait(bar_q, 0) && wait(bar_full, 0);
-            waited = 1;
+            if (!ok) {  // let the copies this thread started land (bounded) before the CTA exits
+                raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
+                *abort_word = 1;
+                tc::mbar_wait(bar_q, 0, kWaitCycles);
+                for (int t = max(0, k_issued - 2); t < k_issued; ++t)
+                    tc::mbar_wait(bar_kf(t & 1), (t >> 1) & 1, kWaitCycles);
+                for (int t = max(0, v_issued - 2); t < v_issued; ++t)
+                    tc::mbar_wait(bar_vf(t & 1), (t >> 1) & 1, kWaitCycles);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ================= MMA issuer: one thread =================
+        if (lane == 0) {
+            constexpr uint32_t kIdS = tc::idesc_f16(kBM, kBN, IsBf16<T>::value, false);
+            constexpr uint32_t kIdO = tc::idesc_f16(kBM, D, IsBf16<T>::value, true);
+            // descriptors built once; a k-step or slot moves only the start-address field
+            const uint64_t dQ0 = tc::smem_desc_sw128(sb + S::kOffQ, 16, 1024);
+            const uint64_t dK0 = tc::smem_desc_sw128(sb + S::kOffK, 16, 1024);
+            const uint64_t dV0 = tc::smem_desc_sw128(sb + S::kOffV, S::kHalf, 1024);
+            auto issue_s = [&](int w, int kt) {  // S_w = Q_w K_kt^T
+                const uint64_t dq = dQ0 + static_cast<uint64_t>((w * S::kTile) >> 4);
+                const uint64_t dk = dK0 + static_cast<uint64_t>(((kt & 1) * S::kTile) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = ((ks / 4) * S::kHalf + (ks % 4) * 32) >> 4;
+                    tc::umma_f16(tS(w), dq + off, dk + off, kIdS, ks > 0);
+                }
+                tc::umma_commit(bar_s(w));
+            };
+            auto issue_pv = [&](int w, int kt) {  // O_w += P_w V_kt, P_w from TMEM
+                const uint64_t dv = dV0 + static_cast<uint64_t>(((kt & 1) * S::kTile) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    tc::umma_f16_ts(tO(w), tS(w) + ks * 8, dv + ((ks * 16 * 128) >> 4), kIdO,
+                                    (kt > 0 || ks > 0) ? 1u : 0u);
+                tc::umma_commit(bar_o(w));
+            };
+            int commits = 0;
+            uint32_t last_bar = 0, last_phase = 0;
+            bool ok = wait(bar_q, 0) && wait(bar_kf(0), 0);
             if (ok) {
                 tc::fence_after_sync();
                 for (int w = 0; w < nwg; ++w) issue_s(w, 0);
-                ++commits, last_bar = bar_sf(nwg - 1, 0), last_phase = 0;
+                tc::umma_commit(bar_ke(0));
+                ++commits, last_bar = bar_ke(0), last_phase = 0;
             }
             for (int kt = 0; kt < nkt && ok; ++kt) {
-                // S_{kt+1} for every group into the slot of S/P_{kt-1}: the softmax was done with
-                // that slot before PV_{kt-1} (issued last iteration) and MMAs run in issue order.
-                if (kt + 1 < nkt) {
-                    const int n = kt + 1;
-                    ok = wait(bar_full + 8 * (n % kStages), (n / kStages) & 1);
-                    waited = n + 1;
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    for (int w = 0; w < nwg; ++w) issue_s(w, n);
-                    ++commits, last_bar = bar_sf(nwg - 1, n & 1), last_phase = (n >> 1) & 1;
-                }
-                // refill the stage tile kt-1 used with tile kt+3 once PV_{kt-1} is done everywhere
-                if (kt >= 1 && kt + 3 < nkt) {
-                    for (int w = 0; w < nwg && ok; ++w) ok = wait(bar_o(w), (kt - 1) & 1);
-                    if (!ok) break;
-                    load_kv(kt + 3);
-                    issued = kt + 4;
-                }
-                // O_w += P_w V_kt as each group's P is ready
+                // Per head: O += P V_kt as soon as its softmax is done, then S for the next tile
+                // (it overwrites P, which the PV just issued reads first: MMAs run in issue order).
+                ok = wait(bar_vf(kt & 1), (kt >> 1) & 1);
+                const bool more = kt + 1 < nkt;
+                if (ok && more) ok = wait(bar_kf((kt + 1) & 1), ((kt + 1) >> 1) & 1);
                 for (int w = 0; w < nwg && ok; ++w) {
                     ok = wait(bar_p(w), kt & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
                     issue_pv(w, kt);
-                    ++commits, last_bar = bar_o(w), last_phase = kt & 1;
+                    if (more) issue_s(w, kt + 1);
+                }
+                if (!ok) break;
+                tc::umma_commit(bar_ve(kt & 1));  // V_kt free once both PVs are done
+                ++commits, last_bar = bar_ve(kt & 1), last_phase = (kt >> 1) & 1;
+                if (more) {
+                    tc::umma_commit(bar_ke((kt + 1) & 1));  // K_{kt+1} free once both S are done
+                    last_bar = bar_ke((kt + 1) & 1), last_phase = ((kt + 1) >> 1) & 1;
                 }
             }
             if (!ok) {
-                // drain what this CTA started (bounded, ignoring the abort word), then report
                 raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
                 *abort_word = 1;
-                tc::mbar_wait(bar_q, 0, kWaitCycles);
-                for (int t = waited; t < issued; ++t)
-                    tc::mbar_wait(bar_full + 8 * (t % kStages), (t / kStages) & 1, kWaitCycles);
                 if (commits) tc::mbar_wait(last_bar, last_phase, kWaitCycles);  // covers every earlier MMA
             }
         }
@@ -313,13 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         bool ok = true;
         for (int kt = 0; kt < nkt && ok; ++kt) {
             const int j0 = kt * kBN;
-            ok = __all_sync(0xffffffffu, wait(bar_sf(w, kt & 1), (kt >> 1) & 1));  // warp-uniform
+            // S_w(kt) ready; it was issued after PV_w(kt-1), so O is stable too
+            ok = __all_sync(0xffffffffu, wait(bar_s(w), kt & 1));
             if (!ok) break;
             tc::fence_after_sync();
+            const bool masked = (j0 + kBN - 1 > P + q0) || (j0 + kBN > Lk);  // diagonal or last tile
+            const int lim = min(limit, Lk - 1) - j0;                            // last visible column
+            // the row of S, read from TMEM once, masked in place
             uint32_t sr[kBN];
-            tc::tmem_ld64(tS(w, kt & 1) + lane_base, sr);
-            if ((j0 + kBN - 1 > P + q0) || (j0 + kBN > Lk)) {  // diagonal or last tile: mask
-                const int lim = min(limit, Lk - 1) - j0;          // last visible column of this row
+            tc::tmem_ld128(tS(w) + lane_base, sr);
+            if (masked) {
 #pragma unroll
                 for (int e = 0; e < kBN; ++e)
                     if (e > lim) sr[e] = __float_as_uint(-INFINITY);
@@ -342,49 +350,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 m_used = m_new;
                 rescale = true;
             }
-            // P = 2^(c*s - m), packed to 16 bits
-            const float neg_m = -m_used;
-            uint32_t pw[kBN / 2];
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-            for (int e = 0; e < kBN; e += 2) {
-                const float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[e]), c, neg_m));
-                const float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[e + 1]), c, neg_m));
-                l4[(e >> 1) & 3] += p0 + p1;
-                pw[e >> 1] = Dt<T>::pack(p0, p1);
-            }
-            l_sum = l_sum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-            if (kt > 0) {
-                // PV_{kt-1} must be done before P_kt goes to TMEM: a tcgen05.st into this group's
-                // lanes while its previous PV (A read from TMEM) was still running corrupted the
-                // result on sm_103a.  It also makes O stable for the (rare) rescale.
-                ok = __all_sync(0xffffffffu, wait(bar_o(w), (kt - 1) & 1));
-                if (!ok) break;
-                tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, rescale)) {
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tO(w) + lane_base + 32 * cc, o);
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(tO(w) + lane_base + 32 * cc, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::tmem_st32(tO(w) + lane_base + 32 * cc, o);
-                    }
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc::tmem_st32(tO(w) + lane_base + 32 * cc, o);
                 }
             }
-            tc::tmem_st32(tS(w, kt & 1) + lane_base, pw);  // P_kt over S_kt, read by PV_kt
+            // P = 2^(c*s - m), packed to 16 bits over the first 64 columns of S
+            const float neg_m = -m_used;
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pw[32];
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[64 * half + e]), c, neg_m));
+                    const float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[64 * half + e + 1]), c, neg_m));
+                    l4[(e >> 1) & 3] += p0 + p1;
+                    pw[e >> 1] = Dt<T>::pack(p0, p1);
+                }
+                tc::tmem_st32(tS(w) + lane_base + 32 * half, pw);  // P columns [32*half, 32*half + 32)
+            }
+            l_sum = l_sum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
             const int valid = min(kBN, Lk - j0);
             if (w == 0 && valid < kBN) {
                 // V rows past the context may hold anything (NaN included): zero them so P V stays
-                // finite.  Group 0 does it; the other group's PV is issued after group 0's.
-                const int st = kt % kStages;
-                ok = __all_sync(0xffffffffu, wait(bar_full + 8 * st, (kt / kStages) & 1));
+                // finite.  Head A does it; head B's PV is issued after head A's.
+                ok = __all_sync(0xffffffffu, wait(bar_vf(kt & 1), (kt >> 1) & 1));
                 if (!ok) break;
                 const int per_half = (kBN - valid) * 8;
-                uint4 *vz = reinterpret_cast<uint4 *>(smem + S::kOffK + st * 2 * S::kKVBytes + S::kKVBytes);
+                uint4 *vz = reinterpret_cast<uint4 *>(smem + S::kOffV + (kt & 1) * S::kTile);
                 for (int i = row; i < per_half * S::kHalves; i += kWgThreads) {
                     const int hf = i / per_half, rem = i % per_half;
-                    vz[(hf * S::kKHalf + (valid + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+                    vz[(hf * S::kHalf + (valid + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
                 }
                 tc::fence_async_smem();
             }
@@ -417,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     }
 
-    // teardown: every role is done with TMEM (the producer drained on abort)
+    // teardown: every role is done with TMEM (the MMA issuer drained on abort)
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == kProducerWarp) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, S::kTmemCols);
     }
