@@ -50,6 +50,7 @@ constexpr int kThreads = 2 * kWgThreads + 64;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxRanked = 128;            // (sequence, q tile) items ordered longest first in-kernel
 
 struct PrefillMaps {
     CUtensorMap q;  // [total_q rows, H_q*D cols], 128-row boxes
@@ -70,6 +71,7 @@ struct PrefillArgs {
     int32_t heads_per_cta;  // 2: two query heads of one GQA group share K/V; 1 without GQA
     int32_t total_q;
     int32_t qtiles;
+    int32_t num_seqs;
     float scale_log2;
     void *out;
     int32_t *err_flag;
@@ -105,10 +107,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seq = blockIdx.z;
-    const int h0 = blockIdx.y * a.heads_per_cta;  // first query head of this CTA
     const int nwg = a.heads_per_cta;
-    const int qt = a.qtiles - 1 - static_cast<int>(blockIdx.x);  // later (heavier) tiles start first
+
+    // Work item of this CTA.  CTAs are dispatched in linear block order, so hand
+    // them the (sequence, q tile) items longest first (list scheduling): every CTA
+    // ranks the items by their number of key tiles the same way and takes the item
+    // whose rank is its linear index.  Many items: plain grid order, last q tile first.
+    int seq = blockIdx.z, hp = blockIdx.y, qt = a.qtiles - 1 - static_cast<int>(blockIdx.x);
+    {
+        const int n_items = a.num_seqs * a.qtiles;
+        if (n_items <= kMaxRanked) {
+            __shared__ int s_cost[kMaxRanked];
+            __shared__ int s_inv[kMaxRanked];
+            for (int e = tid; e < n_items; e += kThreads) {
+                const int sq = e / a.qtiles, t = e % a.qtiles;
+                const int lq = a.cu_q[sq + 1] - a.cu_q[sq], lk = a.cu_k[sq + 1] - a.cu_k[sq];
+                const int base = (lk - lq) + t * kBM;  // prefix + first row of the tile
+                s_cost[e] = (t * kBM < lq && lk >= lq) ? (min(lk, base + kBM) + kBN - 1) / kBN : 0;
+            }
+            __syncthreads();
+            for (int e = tid; e < n_items; e += kThreads) {
+                int r = 0;
+                for (int f = 0; f < n_items; ++f)
+                    r += s_cost[f] > s_cost[e] || (s_cost[f] == s_cost[e] && f < e);
+                s_inv[r] = e;
+            }
+            __syncthreads();
+            const int hps = gridDim.y;
+            const int lin = blockIdx.x + gridDim.x * (blockIdx.y + hps * blockIdx.z);
+            const int e = s_inv[lin / hps];
+            seq = e / a.qtiles;
+            qt = e % a.qtiles;
+            hp = lin % hps;
+        }
+    }
+    const int h0 = hp * a.heads_per_cta;  // first query head of this CTA
 
     const int q_start = a.cu_q[seq], q_end = a.cu_q[seq + 1];
     const int Lq = q_end - q_start, Lk = a.cu_k[seq + 1] - a.cu_k[seq];
@@ -526,6 +559,7 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
     a.heads_per_cta = a.group >= 2 ? 2 : 1;
     a.total_q = total_q;
     a.qtiles = (max_seqlen_q + kBM - 1) / kBM;
+    a.num_seqs = num_seqs;
     a.scale_log2 = scale * kLog2e;
     a.out = out;
     a.err_flag = err_flag;
