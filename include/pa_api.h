@@ -23,7 +23,9 @@
  *     A slot is the flattened row index b * block_size + o (section 2.2).
  *   - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
  *   - Supported: head_dim 64 or 128; num_q_heads % num_kv_heads == 0 with a
- *     group size of 1, 2, 4 or 8; block_size a power of two in [8, 1024].
+ *     group size of 1, 2, 4 or 8; block_size a power of two in [8, 1024];
+ *     num_blocks * block_size <= INT32_MAX (pool rows are addressed by TMA
+ *     with 32-bit coordinates).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  Issue pa_store_kv before the attention call of the
  *     same step on the same stream: attention reads the stored rows.
@@ -139,7 +141,8 @@ PA_API size_t pa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int3
  *                 clobbered.  Two calls in flight at once need two workspaces.
  * The work is split over fixed-size context partitions (one CTA per
  * sequence, kv head and partition); a second kernel merges the partitions'
- * softmax partials by log-sum-exp.
+ * softmax partials by log-sum-exp.  Cache pages are fetched by TMA, so
+ * k_cache and v_cache must be 16-byte aligned.
  */
 PA_API int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,

@@ -6,49 +6,56 @@
 // its context, position j read from cache row
 // block_table[j / bs] * bs + j % bs ("nano-vLLM Part 2", section 2.2).
 //
-// Design (GB300): decode is HBM-bound, so everything serves the K/V stream.
+// Design (GB300): decode is HBM-bound, so everything serves the K/V stream,
+// and the instructions spent per cache byte are kept low enough that one SM
+// can pull its share of the HBM bandwidth (and more, when L2 serves pages that
+// several sequences share).
 //   * One CTA per (partition, kv head, sequence).  The G query heads of the
 //     group share every K/V tile, so each cache byte is read once.
-//   * Pages are gathered through the block table into a 3-stage shared-memory
-//     ring with 16-byte cp.async (rows of one kv head are D*2 bytes, strided
-//     by H_kv*D*2 in the pool), XOR-swizzled so the warp-matrix loads below
-//     are bank-conflict free.
-//   * Each warp owns 16 tokens of a 64-token tile.  S^T = K Q^T and
-//     O^T += V^T P^T are m16n8k16 warp MMAs with the G (<= 8) heads in the
-//     N dimension: the contraction is tiny, the point is only to keep the
-//     per-byte instruction count far below the issue budget an HBM-rate
-//     stream leaves (about 90 warp instructions per 512 bytes per SM).
-//   * Softmax is online, in fp32, in the log2 domain; row maxima are reduced
-//     with warp shuffles.  P is rounded to the input dtype for the PV MMA
-//     while the normaliser sums the fp32 values.
+//   * A producer warp (one thread) fetches each 64-token K and V tile with
+//     TMA, one box per page (or per 64 rows of a longer page) and per 128-byte
+//     column slice of the kv head's row, into a 3-stage ring with the 128-byte
+//     swizzle, so the warp-matrix loads below are bank-conflict free.  Full /
+//     empty mbarriers hand stages over; every wait is bounded.
+//   * Each of 4 consumer warps owns 16 tokens of a tile.  It loads its K and
+//     V fragments into registers and releases the stage at once, then
+//     computes S^T = K Q^T and O^T += V^T P^T as m16n8k16 warp MMAs with the
+//     G (<= 8) heads in the N dimension: the contraction is tiny, the tensor
+//     cores only keep the per-byte instruction count low.
+//   * Softmax is online, in fp32, in the log2 domain, with a lazily moved
+//     maximum: the reference maximum changes (and O is rescaled) only when a
+//     score exceeds it by more than 2^8, so most tiles need no warp reduction.
+//     P is rounded to the input dtype for the PV MMA while the normaliser sums
+//     the fp32 values.
 //   * Warps merge through shared memory at the end of the partition; a
 //     sequence with one partition writes its output directly, otherwise the
 //     (max, sum, unnormalised O) partials go to the workspace and a second
-//     kernel merges them by log-sum-exp; it is launched as a programmatic
-//     dependent of the first, so its launch overlaps the partition kernel.
+//     kernel merges them by log-sum-exp; both kernels are launched as
+//     programmatic dependents, so each launch overlaps the kernel before it.
 #include <math.h>
 #include <stdlib.h>
 
-#include "pa_common.cuh"
+#include "tc_common.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps
-constexpr int kWarps = kThreads / 32;
-constexpr int kTile = 64;      // tokens per pipeline stage, 16 per warp
+constexpr int kConsumerWarps = 4;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTile = 64;      // tokens per pipeline stage, 16 per consumer warp
 constexpr int kStages = 3;
 constexpr int kMaxTablePages = 257;  // block-table entries one partition may touch
 constexpr int kMaxPartition = 2048;
 constexpr int kMinPartition = 128;
 constexpr int kTargetCtas = 16 * 152;  // ragged batches: enough waves to absorb the length spread
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 struct DecodeArgs {
     const void *q;
     int64_t q_row_stride;
-    const void *k_cache;
-    const void *v_cache;
     const int32_t *block_tables;
     int32_t max_blocks;
     const int32_t *context_lens;
@@ -60,43 +67,54 @@ struct DecodeArgs {
     float scale_log2;
     void *out;
     float *ws_o;     // [B][H_q][max_parts][D]  unnormalised partial outputs
-    float2 *ws_ml;   // [B][H_q][max_parts]     (running max, running sum), log2 domain
+    float2 *ws_ml;   // [B][H_q][max_parts]     (reference max, sum), log2 domain
     int32_t partition;
     int32_t max_parts;
     int32_t *err_flag;
 };
 
+// Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
+// every slice 1024-byte aligned for the swizzle), then the block-table slice,
+// the mbarriers and the abort word.  After the loop the ring holds the warps'
+// partial outputs for the merge.
 template <int D> struct Shape {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    static constexpr int kTileBytes = kTile * kRowBytes;
+    static constexpr int kSlices = D / 64;
+    static constexpr int kSliceBytes = kTile * 128;
+    static constexpr int kTileBytes = kSlices * kSliceBytes;
     static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
     static constexpr int kKSteps = D / 16;
-    static constexpr int kRowsPerPass = kThreads / kChunks;
-    static constexpr int kPasses = kTile / kRowsPerPass;
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kMergeBytes = kWarps * 8 * (D + 2) * 4;
-    static constexpr int kSmemBytes =
-        (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + kMaxTablePages * 4;
+    static constexpr int kMergeBytes = kConsumerWarps * 8 * (D + 2) * 4;
+    static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+    static constexpr int kTableOff = kBodyBytes;
+    static constexpr int kBarOff = kTableOff + (kMaxTablePages * 4 + 7) / 8 * 8;
+    static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
+    static constexpr int kSmemBytes = kAbortOff + 16 + 1024;  // + slack to align the base to 1024
 };
 
-// Context length of sequence b, or 0 (flagged) when it is out of range.
+// Context length of sequence b, or -1 (to be flagged) when it is out of range.
 __device__ __forceinline__ int context_len(const DecodeArgs &a, int b) {
     const int L = a.context_lens[b];
     const int64_t cap = static_cast<int64_t>(a.max_blocks) << a.log2_bs;
     return (L < 0 || L > cap) ? -1 : L;
 }
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk, int row_bytes) {
-    return row * row_bytes + ((chunk ^ (row & 7)) << 4);
+// Byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r in the swizzled layout.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+    return (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                            const DecodeArgs a) {
     using S = Shape<D>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + (S::kRingBytes > S::kMergeBytes ? S::kRingBytes
-                                                                                         : S::kMergeBytes));
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t bars = smem_u32(smem + S::kBarOff);  // full[s] at 8s, empty[s] at 8(kStages + s)
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
 
     const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -123,18 +141,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     const int end = min(L, start + a.partition);
     const int nparts = (L + a.partition - 1) / a.partition;
     const int ntiles = (end - start + kTile - 1) / kTile;
-    const int bs_mask = (1 << a.log2_bs) - 1;
 
-    // block-table slice of this partition, validated once
+    // block-table slice of this partition, validated once (a bad id is flagged and read as page 0)
     const int first_page = start >> a.log2_bs;
     const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;
     for (int i = tid; i < npages; i += kThreads) {
         int pg = a.block_tables[static_cast<int64_t>(b) * a.max_blocks + first_page + i];
         if (pg < 0 || pg >= a.num_blocks) {
             raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
-            pg = -1;  // read as zeros
+            pg = 0;
         }
         bt_s[i] = pg;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(bars + 8 * s, 1);
+            tc::mbar_init(bars + 8 * (kStages + s), kConsumerWarps);
+        }
+        *abort_s = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
     }
 
     // query fragments (B operand of S^T = K Q^T): head lane/4 of the group
@@ -146,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
                         static_cast<int64_t>(g * a.group + hq) * D;
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) {
-            if (hq < a.group) {
+            if (hq < a.group && warp < kConsumerWarps) {
                 qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + dq);
                 qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + dq);
             } else {
@@ -154,136 +183,159 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
             }
         }
     }
-    __syncthreads();  // bt_s ready
-
-    const T *kc = static_cast<const T *>(a.k_cache);
-    const T *vc = static_cast<const T *>(a.v_cache);
-    const int chunk = tid % S::kChunks;
-    const int row0 = tid / S::kChunks;
-    const int64_t head_off = static_cast<int64_t>(g) * D + chunk * 8;
-    const int64_t row_elems = static_cast<int64_t>(a.num_kv_heads) * D;
-
-    auto load_tile = [&](int t, int stage) {
-        const uint32_t kb = smem_u32(smem + stage * S::kStageBytes);
-        const uint32_t vb = kb + S::kTileBytes;
-        const int tile_start = start + t * kTile;
-#pragma unroll
-        for (int i = 0; i < S::kPasses; ++i) {
-            const int r = row0 + i * S::kRowsPerPass;
-            const int j = tile_start + r;
-            const uint32_t so = swz(r, chunk, S::kRowBytes);
-            const T *ks = kc, *vs = vc;
-            uint32_t nbytes = 0;
-            if (j < end) {
-                const int pg = bt_s[(j >> a.log2_bs) - first_page];
-                if (pg >= 0) {
-                    const int64_t off = ((static_cast<int64_t>(pg) << a.log2_bs) + (j & bs_mask)) * row_elems +
-                                        head_off;
-                    ks = kc + off;
-                    vs = vc + off;
-                    nbytes = 16;
-                }
-            }
-            cp_async_16(kb + so, ks, nbytes);
-            cp_async_16(vb + so, vs, nbytes);
-        }
-    };
-
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < ntiles) load_tile(s, s);
-        cp_async_commit();
-    }
+    __syncthreads();  // table slice, barriers ready
 
     float o[S::kKSteps][4];
 #pragma unroll
     for (int mt = 0; mt < S::kKSteps; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*(lane%4) and +1
-    const int wrow = warp * 16;
+    float mu0 = 0.f, mu1 = 0.f;                                 // exponent references (m, or 0 while m = -inf)
+    int issued = 0;                                             // tiles the producer started
 
-    for (int t = 0; t < ntiles; ++t) {
-        cp_async_wait<kStages - 2>();
-        __syncthreads();  // tile t visible to all; stage of tile t-1 free for reuse
-        {
-            const int nt = t + kStages - 1;
-            if (nt < ntiles) load_tile(nt, nt % kStages);
-            cp_async_commit();
-        }
-        const uint32_t kb = smem_u32(smem + (t % kStages) * S::kStageBytes);
-        const uint32_t vb = kb + S::kTileBytes;
-
-        // S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8)
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            const int r = wrow + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int csel = lane >> 4;
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            const int box_rows = min(1 << a.log2_bs, kTile);
+            const int bs_mask = (1 << a.log2_bs) - 1;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % kStages;
+                if (t >= kStages &&
+                    !tc::mbar_wait_or_abort(bars + 8 * (kStages + s), ((t / kStages) - 1) & 1, kWaitCycles, abort_s)) {
+                    raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
+                    break;
+                }
+                const int tile_start = start + t * kTile;
+                const int nbox = (min(kTile, end - tile_start) + box_rows - 1) / box_rows;
+                const uint32_t full = bars + 8 * s;
+                tc::mbar_arrive_expect_tx(full, nbox * box_rows * D * 2 * 2);
+                const uint32_t kdst = ring + s * S::kStageBytes;
+                const uint32_t vdst = kdst + S::kTileBytes;
+                for (int i = 0; i < nbox; ++i) {
+                    const int j = tile_start + i * box_rows;
+                    const int y = (bt_s[(j >> a.log2_bs) - first_page] << a.log2_bs) + (j & bs_mask);
+                    const uint32_t row_off = i * box_rows * 128;
 #pragma unroll
-            for (int ks = 0; ks < S::kKSteps; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(kb + swz(r, ks * 2 + csel, S::kRowBytes), a0, a1, a2, a3);
-                Mma<T>::run(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    for (int h = 0; h < S::kSlices; ++h) {
+                        tc::tma_load_2d(kdst + h * S::kSliceBytes + row_off, &tm_k, g * D + h * 64, y, full);
+                        tc::tma_load_2d(vdst + h * S::kSliceBytes + row_off, &tm_v, g * D + h * 64, y, full);
+                    }
+                }
+                issued = t + 1;
             }
         }
-        // lane holds tokens j0 (sc[0], sc[1]) and j0 + 8 (sc[2], sc[3]) for heads 2*(lane%4), +1
-        const int j0 = start + t * kTile + wrow + (lane >> 2);
-        const bool v0 = j0 < end, v1 = j0 + 8 < end;
-        const float s0 = v0 ? sc[0] * a.scale_log2 : -INFINITY;
-        const float s1 = v0 ? sc[1] * a.scale_log2 : -INFINITY;
-        const float s2 = v1 ? sc[2] * a.scale_log2 : -INFINITY;
-        const float s3 = v1 ? sc[3] * a.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-        mx0 = warp_max_xor(mx0, 4);
-        mx1 = warp_max_xor(mx1, 4);
-        mx0 = warp_max_xor(mx0, 8);
-        mx1 = warp_max_xor(mx1, 8);
-        mx0 = warp_max_xor(mx0, 16);
-        mx1 = warp_max_xor(mx1, 16);
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;  // all masked so far: keep exp2 finite
-        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float c0 = exp2f(m0 - mu0), c1 = exp2f(m1 - mu1);
-        const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
-        const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
-        l0 = l0 * c0 + (p0 + p2);
-        l1 = l1 * c1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < S::kKSteps; ++mt) {
-            o[mt][0] *= c0;
-            o[mt][1] *= c1;
-            o[mt][2] *= c0;
-            o[mt][3] *= c1;
-        }
-        // P^T as the B operand (16 tokens x 8 heads): transpose the two 8x8 halves
-        const uint32_t pb0 = movmatrix_trans(Dt<T>::pack(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(Dt<T>::pack(p2, p3));
-        // O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 x 8)
-        {
-            const int i = lane >> 3;
-            const int r = wrow + (lane & 7) + (i >> 1) * 8;
-#pragma unroll
-            for (int mt = 0; mt < S::kKSteps; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(vb + swz(r, mt * 2 + (i & 1), S::kRowBytes), a0, a1, a2, a3);
-                Mma<T>::run(o[mt], a0, a1, a2, a3, pb0, pb1);
+    } else {
+        const int wrow = warp * 16;
+        const int rk = wrow + (lane & 7) + ((lane >> 3) & 1) * 8, ck = lane >> 4;
+        const int rv = wrow + (lane & 7) + (lane >> 4) * 8, cv = (lane >> 3) & 1;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % kStages;
+            const bool ok = tc::mbar_wait_or_abort(bars + 8 * s, (t / kStages) & 1, kWaitCycles, abort_s);
+            if (!__all_sync(0xffffffffu, ok)) {  // leave together: the warp-wide instructions below
+                if (lane == 0) raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
+                break;
             }
+            const uint32_t kb = ring + s * S::kStageBytes;
+            const uint32_t vb = kb + S::kTileBytes;
+            uint32_t kf[S::kKSteps][4], vf[S::kKSteps][4];
+#pragma unroll
+            for (int ks = 0; ks < S::kKSteps; ++ks)
+                ldmatrix_x4(kb + tile_off(rk, ks * 2 + ck), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+#pragma unroll
+            for (int mt = 0; mt < S::kKSteps; ++mt)
+                ldmatrix_x4_trans(vb + tile_off(rv, mt * 2 + cv), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bars + 8 * (kStages + s));  // stage free for the next tile
+
+            // S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8), two independent chains
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < S::kKSteps; ks += 2) {
+                Mma<T>::run(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qb[ks][0], qb[ks][1]);
+                Mma<T>::run(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3], qb[ks + 1][0],
+                            qb[ks + 1][1]);
+            }
+            // lane holds tokens lane/4 (s0, s1) and lane/4 + 8 (s2, s3) for heads 2*(lane%4), +1
+            float s0 = (sa[0] + sb[0]) * a.scale_log2, s1 = (sa[1] + sb[1]) * a.scale_log2;
+            float s2 = (sa[2] + sb[2]) * a.scale_log2, s3 = (sa[3] + sb[3]) * a.scale_log2;
+            const int tile_start = start + t * kTile;
+            if (tile_start + kTile > end) {  // last tile, partly past the context
+                const int j0 = tile_start + wrow + (lane >> 2);
+                if (j0 >= end) s0 = s1 = -INFINITY;
+                if (j0 + 8 >= end) s2 = s3 = -INFINITY;
+                // V rows past the end may hold anything (NaN): zero them in the fragments,
+                // whose tokens are 2*(lane%4) + {0, 1} (regs 0, 1) and + 8 (regs 2, 3)
+                const int jt = tile_start + wrow + (lane & 3) * 2;
+                const uint32_t lo = (jt < end ? 0xFFFFu : 0u) | (jt + 1 < end ? 0xFFFF0000u : 0u);
+                const uint32_t hi = (jt + 8 < end ? 0xFFFFu : 0u) | (jt + 9 < end ? 0xFFFF0000u : 0u);
+#pragma unroll
+                for (int mt = 0; mt < S::kKSteps; ++mt) {
+                    vf[mt][0] &= lo;
+                    vf[mt][1] &= lo;
+                    vf[mt][2] &= hi;
+                    vf[mt][3] &= hi;
+                }
+            }
+            // move the reference maximum only when a score exceeds it by more than 2^8
+            const bool grow = fmaxf(s0, s2) > m0 + kRescaleThreshold || fmaxf(s1, s3) > m1 + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, grow)) {
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                mx0 = warp_max_xor(mx0, 4);
+                mx1 = warp_max_xor(mx1, 4);
+                mx0 = warp_max_xor(mx0, 8);
+                mx1 = warp_max_xor(mx1, 8);
+                mx0 = warp_max_xor(mx0, 16);
+                mx1 = warp_max_xor(mx1, 16);
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float nu0 = mn0 == -INFINITY ? 0.f : mn0;  // all masked so far: keep exp2 finite
+                const float nu1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float c0 = tc::ex2_approx(mu0 - nu0), c1 = tc::ex2_approx(mu1 - nu1);
+                l0 *= c0;
+                l1 *= c1;
+#pragma unroll
+                for (int mt = 0; mt < S::kKSteps; ++mt) {
+                    o[mt][0] *= c0;
+                    o[mt][1] *= c1;
+                    o[mt][2] *= c0;
+                    o[mt][3] *= c1;
+                }
+                m0 = mn0;
+                m1 = mn1;
+                mu0 = nu0;
+                mu1 = nu1;
+            }
+            const float p0 = tc::ex2_approx(s0 - mu0), p1 = tc::ex2_approx(s1 - mu1);
+            const float p2 = tc::ex2_approx(s2 - mu0), p3 = tc::ex2_approx(s3 - mu1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            // P^T as the B operand (16 tokens x 8 heads): transpose the two 8x8 halves
+            const uint32_t pb0 = movmatrix_trans(Dt<T>::pack(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(Dt<T>::pack(p2, p3));
+            // O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 x 8)
+#pragma unroll
+            for (int mt = 0; mt < S::kKSteps; ++mt) Mma<T>::run(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();  // ring no longer needed: reuse it to merge the warps
+    __syncthreads();
+    if (*abort_s) {
+        // a wait gave up (flagged above): let every load this CTA started land, then leave
+        if (warp == kProducerWarp && lane == 0)
+            for (int s = 0; s < kStages && s < issued; ++s) {
+                const int t_last = s + kStages * ((issued - 1 - s) / kStages);
+                tc::mbar_wait(bars + 8 * s, (t_last / kStages) & 1, kWaitCycles);
+            }
+        return;
+    }
 
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
-
-    float *mo = reinterpret_cast<float *>(smem);               // [warp][head 8][D]
-    float *mm = mo + kWarps * 8 * D;                           // [warp][head 8]
-    float *ml = mm + kWarps * 8;                               // [warp][head 8]
-    {
+    // merge the consumer warps (the ring is free: every load has landed and been read)
+    float *mo = reinterpret_cast<float *>(smem);    // [warp][head 8][D]
+    float *mm = mo + kConsumerWarps * 8 * D;        // [warp][head 8]  reference max
+    float *ml = mm + kConsumerWarps * 8;            // [warp][head 8]  sum
+    if (warp < kConsumerWarps) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
         const int h0 = (lane & 3) * 2;
         const int dr = lane >> 2;
         float *w = mo + warp * 8 * D;
@@ -294,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
             w[h0 * D + mt * 16 + dr + 8] = o[mt][2];
             w[(h0 + 1) * D + mt * 16 + dr + 8] = o[mt][3];
         }
-        if (lane < 4) {
-            mm[warp * 8 + h0] = m0;
-            mm[warp * 8 + h0 + 1] = m1;
+        if (lane < 4) {  // a warp whose tokens were all masked has m = -inf and sum 0: weight 0 below
+            mm[warp * 8 + h0] = m0 == -INFINITY ? -INFINITY : mu0;
+            mm[warp * 8 + h0 + 1] = m1 == -INFINITY ? -INFINITY : mu1;
             ml[warp * 8 + h0] = l0;
             ml[warp * 8 + h0 + 1] = l1;
         }
@@ -307,10 +359,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         const int h = i / D, d = i % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * 8 + h]);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + h]);
         float acc = 0.f, sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < kConsumerWarps; ++w) {
             const float wt = exp2f(mm[w * 8 + h] - M);  // a warp with no token has max -inf: weight 0
             acc += mo[(w * 8 + h) * D + d] * wt;
             sum += ml[w * 8 + h] * wt;
@@ -414,8 +466,6 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     DecodeArgs a;
     a.q = q;
     a.q_row_stride = q_row_stride;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
     a.block_tables = block_tables;
     a.max_blocks = max_blocks_per_seq;
     a.context_lens = context_lens;
@@ -434,6 +484,16 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.max_parts = plan.max_parts;
     a.err_flag = err_flag;
 
+    // the pool as [num_blocks * block_size rows, H_kv * D columns]; one box = 64 columns of
+    // min(block_size, 64) rows, so a box never crosses a page
+    CUtensorMap tm_k, tm_v;
+    const int64_t rows = static_cast<int64_t>(num_blocks) * block_size;
+    const int64_t cols = static_cast<int64_t>(num_kv_heads) * head_dim;
+    const int box_rows = block_size < kTile ? block_size : kTile;
+    if (!make_tmap_rows(&tm_k, k_cache, dtype, cols, rows, box_rows) ||
+        !make_tmap_rows(&tm_v, v_cache, dtype, cols, rows, box_rows))
+        return cudaErrorInvalidValue;
+
     using S128 = Shape<128>;
     using S64 = Shape<64>;
     cudaError_t e;
@@ -441,19 +501,22 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         // opt in to more than 48 KB of dynamic shared memory (a per-device function attribute)
         cudaError_t err = cudaFuncSetAttribute(kern_part, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
-        kern_part<<<dim3(a.max_parts, a.num_kv_heads, batch), kThreads, smem, stream>>>(a);
-        err = cudaGetLastError();
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.max_parts, a.num_kv_heads, batch);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, kern_part, tm_k, tm_v, a);
         if (err != cudaSuccess) return err;
         if (a.max_parts > 1) {
-            cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(a.num_q_heads, batch);
             cfg.blockDim = dim3(d);
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
+            cfg.dynamicSmemBytes = 0;
             err = cudaLaunchKernelEx(&cfg, kern_comb, a);
         }
         return err;

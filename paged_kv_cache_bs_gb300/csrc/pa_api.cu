@@ -1,6 +1,7 @@
 // C ABI of the paged-KV attention library: argument validation on the host,
 // then a launch on the caller's stream.  No call allocates memory.
 #include <math.h>
+#include <stdint.h>
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -48,6 +49,9 @@ int check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t hea
     if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive (%d)", num_blocks);
     if (!is_pow2(block_size) || block_size < 8 || block_size > 1024)
         return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two in [8, 1024])", block_size);
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "pool of %lld rows (TMA row coordinates are 32-bit)",
+                    (long long)num_blocks * block_size);
     if (!isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
     return PA_OK;
 }

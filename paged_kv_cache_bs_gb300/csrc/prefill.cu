@@ -463,38 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
 // ------------------------------------------------------------------ host side
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-    static EncodeTiled fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    }
-    return fn;
-}
-
-// 2-D map over a row-major [rows, cols] 16-bit matrix with (64 x box_rows) boxes, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows) {
-    EncodeTiled enc = encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = enc(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 int ilog2(int x) {
     int r = 0;
     while ((1 << r) < x) ++r;
@@ -531,16 +499,16 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
     if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return cudaSuccess;
     PrefillMaps maps;
     const int64_t kv_cols = static_cast<int64_t>(num_kv_heads) * head_dim;
-    bool ok = make_map(&maps.q, q, dtype, static_cast<int64_t>(num_q_heads) * head_dim, total_q, kBM);
+    bool ok = make_tmap_rows(&maps.q, q, dtype, static_cast<int64_t>(num_q_heads) * head_dim, total_q, kBM);
     int box_rows = kBN;
     if (block_tables) {
         box_rows = block_size < kBN ? block_size : kBN;
         const int64_t rows = static_cast<int64_t>(num_blocks) * block_size;
-        ok = ok && make_map(&maps.k, k_cache, dtype, kv_cols, rows, box_rows) &&
-             make_map(&maps.v, v_cache, dtype, kv_cols, rows, box_rows);
+        ok = ok && make_tmap_rows(&maps.k, k_cache, dtype, kv_cols, rows, box_rows) &&
+             make_tmap_rows(&maps.v, v_cache, dtype, kv_cols, rows, box_rows);
     } else {
-        ok = ok && make_map(&maps.k, k, dtype, kv_cols, total_q, kBN) &&
-             make_map(&maps.v, v, dtype, kv_cols, total_q, kBN);
+        ok = ok && make_tmap_rows(&maps.k, k, dtype, kv_cols, total_q, kBN) &&
+             make_tmap_rows(&maps.v, v, dtype, kv_cols, total_q, kBN);
     }
     if (!ok) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor too large)";

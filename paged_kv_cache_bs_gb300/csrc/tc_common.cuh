@@ -212,4 +212,10 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 }
 
 }  // namespace tc
+
+// Host: 2-D TMA map over a row-major [rows, cols] 16-bit matrix, boxes of
+// 64 columns (128 bytes) x box_rows rows, 128-byte swizzle.  False when the
+// driver cannot encode it (entry point missing, tensor too large).
+bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows);
+
 }  // namespace pa

@@ -1,0 +1,70 @@
+// Host side of the TMA loads: tensor maps over row-major 16-bit matrices
+// (the paged pool viewed as [num_blocks*block_size rows, H_kv*D columns], or a
+// packed [tokens, heads*D] array), encoded through the driver entry point that
+// the runtime hands out, so the library links against libcudart only.
+#include <string.h>
+
+#include "tc_common.cuh"
+
+namespace pa {
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// The last few maps this thread encoded: a decode step re-encodes the same two
+// pool maps every layer and every step.
+struct MapKey {
+    const void *base;
+    int64_t cols, rows;
+    int box_rows;
+    pa_dtype dt;
+};
+constexpr int kCacheSlots = 8;
+thread_local MapKey t_keys[kCacheSlots];
+thread_local CUtensorMap t_maps[kCacheSlots];
+thread_local int t_next = 0;
+
+}  // namespace
+
+bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows) {
+    for (int i = 0; i < kCacheSlots; ++i) {
+        const MapKey &k = t_keys[i];
+        if (k.base == base && k.cols == cols && k.rows == rows && k.box_rows == box_rows && k.dt == dt) {
+            memcpy(m, &t_maps[i], sizeof(CUtensorMap));
+            return true;
+        }
+    }
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    const int slot = t_next;
+    t_next = (t_next + 1) % kCacheSlots;
+    t_keys[slot] = MapKey{base, cols, rows, box_rows, dt};
+    memcpy(&t_maps[slot], m, sizeof(CUtensorMap));
+    return true;
+}
+
+}  // namespace pa
