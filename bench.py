@@ -51,11 +51,7 @@ DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 # DRAM bytes (read + write) of the dominant kernel per launch, from one ncu
 # capture of the current kernels (profiles/decode_<workload>.md); a workload
 # missing here reports null.
-TRAFFIC_PER_CALL = {
-    "qwen3_0p6b_decode": 573_909_248 + 5_520_128,       # decode_partition_kernel
-    "long_context_decode": 537_001_472 + 3_163_648,     # decode_partition_kernel
-    "qwen3_8b_shared_decode": 859_686_656 + 4_946_688,  # decode_partition_kernel (L2 absorbs shared pages)
-}
+TRAFFIC_PER_CALL = {}
 PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 118_873_856 + 13_274_624}  # prefill_kernel
 
 WORKLOAD_CONFIG = {
@@ -165,7 +161,7 @@ class DecodeWorkload:
         self.batch = st.batch
         row = p.num_kv_heads * p.head_dim * st.q.element_size()
         self.store_bytes = 2 * 2 * int((st.slot_mapping >= 0).sum()) * row   # k and v, read + write
-        self.launches_per_step = 3   # store, decode partitions, log-sum-exp combine
+        self.launches_per_step = 3   # store, decode partitions, log-sum-exp merge
         self.phases = [("store", self.store), ("decode", self.attend)]
         self.prefill_flops = 0
 
@@ -221,7 +217,7 @@ class MixedWorkload(DecodeWorkload):
         self.batch = st.batch + (pf.cu_seqlens_q.numel() - 1)
         row = p.num_kv_heads * p.head_dim * st.q.element_size()
         self.store_bytes = 2 * 2 * int((m.slot_mapping >= 0).sum()) * row
-        self.launches_per_step = 4   # store, prefill, decode partitions, combine
+        self.launches_per_step = 4   # store, prefill, decode partitions, merge
         self.phases = [("store", self.store), ("prefill", self.prefill), ("decode", self.attend)]
         self.prefill_flops = pf.flops()
 
@@ -430,9 +426,13 @@ def run_ours(args, world, rank, local):
                 "peak_source": f"{peak_kind} (bf16_tflops_sustained; timed inside a repeated step)",
                 "traffic": TRAFFIC_PER_CALL.get(args.workload)}
     else:
-        roof = {"bound": "hbm", "kernel": "pa_decode (split-K partitions + combine)", "achieved": decode_gbs,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": decode_gbs / peaks["hbm_gbs"],
-                "peak_source": f"{peak_kind} (hbm_gbs)", "traffic": TRAFFIC_PER_CALL.get(args.workload)}
+        # bytes DRAM must supply: each physical page once (pages shared by several sequences
+        # are counted once; for unshared workloads this equals the logical KV bytes)
+        unique_gbs = w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "pa_decode (split-K partitions + combine)", "achieved": unique_gbs,
+                "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": unique_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",
+                "traffic": TRAFFIC_PER_CALL.get(args.workload)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

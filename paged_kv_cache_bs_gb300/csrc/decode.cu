@@ -14,9 +14,12 @@
 //     group share every K/V tile, so each cache byte is read once.
 //   * A producer warp (one thread) fetches each 64-token K and V tile with
 //     TMA, one box per page (or per 64 rows of a longer page) and per 128-byte
-//     column slice of the kv head's row, into a 3-stage ring with the 128-byte
-//     swizzle, so the warp-matrix loads below are bank-conflict free.  Full /
-//     empty mbarriers hand stages over; every wait is bounded.
+//     column slice of the kv head's row, into a ring with the 128-byte swizzle,
+//     so the warp-matrix loads below are bank-conflict free: 3 stages with two
+//     CTAs per SM, or, when pages are shorter than a tile (several boxes per
+//     tile), 2 stages with three CTAs per SM.  Full / empty mbarriers hand
+//     stages over; every wait is bounded.  The grid is sized from the
+//     occupancy the device reports for the chosen ring.
 //   * Each of 4 consumer warps owns 16 tokens of a tile.  It loads its K and
 //     V fragments into registers and releases the stage at once, then
 //     computes S^T = K Q^T and O^T += V^T P^T as m16n8k16 warp MMAs with the
@@ -30,8 +33,9 @@
 //   * Warps merge through shared memory at the end of the partition; a
 //     sequence with one partition writes its output directly, otherwise the
 //     (max, sum, unnormalised O) partials go to the workspace and a second
-//     kernel merges them by log-sum-exp; both kernels are launched as
-//     programmatic dependents, so each launch overlaps the kernel before it.
+//     kernel merges them by log-sum-exp, eight partitions per memory round
+//     trip; both kernels are launched as programmatic dependents, so each
+//     launch overlaps the kernel before it.
 #include <math.h>
 #include <stdlib.h>
 
@@ -44,11 +48,13 @@ constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTile = 64;      // tokens per pipeline stage, 16 per consumer warp
-constexpr int kStages = 3;
+// Ring depth: 3 stages with 2 CTAs per SM, or 2 stages with 3 CTAs per SM
+// (more producers issuing when pages are short and a tile takes many boxes).
+template <int ST> constexpr int ctas_per_sm() { return ST == 2 ? 3 : 2; }
 constexpr int kMaxTablePages = 257;  // block-table entries one partition may touch
 constexpr int kMaxPartition = 2048;
 constexpr int kMinPartition = 128;
-constexpr int kTargetCtas = 16 * 152;  // ragged batches: enough waves to absorb the length spread
+constexpr int kTargetWaves = 8;  // ragged batches: enough waves to absorb the length spread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
@@ -77,7 +83,8 @@ struct DecodeArgs {
 // every slice 1024-byte aligned for the swizzle), then the block-table slice,
 // the mbarriers and the abort word.  After the loop the ring holds the warps'
 // partial outputs for the merge.
-template <int D> struct Shape {
+template <int D, int ST> struct Shape {
+    static constexpr int kStages = ST;
     static constexpr int kSlices = D / 64;
     static constexpr int kSliceBytes = kTile * 128;
     static constexpr int kTileBytes = kSlices * kSliceBytes;
@@ -104,11 +111,12 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
     return (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 2)
+template <typename T, int D, int ST>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a) {
-    using S = Shape<D>;
+    using S = Shape<D, ST>;
+    constexpr int kStages = ST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
@@ -379,27 +387,46 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // Log-sum-exp merge of the partitions of sequences that have more than one.
+// The partials are loaded eight partitions at a time and folded in with an
+// online maximum: one memory round trip per eight partitions.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
+    constexpr int kBatch = 8;
     const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-    // launched early (programmatic dependent launch): wait until the partition grid has
-    // finished and its partials are visible
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // context_lens is an input of the call: this grid launches only after every partition
+    // CTA has passed its own wait on the previous kernel, so it may be read before the wait
     const int L = max(context_len(a, b), 0);
     const int np = (L + a.partition - 1) / a.partition;
     if (np <= 1) return;
+    // launched early (programmatic dependent launch): wait until the partition grid has
+    // finished and its partials are visible
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int64_t base = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.max_parts;
-    float M = -INFINITY;
-    for (int p = 0; p < np; ++p) M = fmaxf(M, a.ws_ml[base + p].x);
-    float acc = 0.f, sum = 0.f;
-    for (int p = 0; p < np; ++p) {
-        const float2 ml = a.ws_ml[base + p];
-        const float wt = exp2f(ml.x - M);
-        sum += ml.y * wt;
-        acc += a.ws_o[(base + p) * D + d] * wt;
+    float M = -INFINITY, acc = 0.f, sum = 0.f;
+    for (int p0 = 0; p0 < np; p0 += kBatch) {
+        float2 ml[kBatch];
+        float o[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (p0 + j < np) {
+                ml[j] = a.ws_ml[base + p0 + j];
+                o[j] = a.ws_o[(base + p0 + j) * D + d];
+            } else {
+                ml[j] = make_float2(-INFINITY, 0.f);
+                o[j] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const float Mn = fmaxf(M, ml[j].x);
+            if (Mn == -INFINITY) continue;  // padding
+            const float cold = exp2f(M - Mn), cnew = exp2f(ml[j].x - Mn);
+            acc = acc * cold + o[j] * cnew;
+            sum = sum * cold + ml[j].y * cnew;
+            M = Mn;
+        }
     }
-    static_cast<T *>(a.out)[(static_cast<int64_t>(b) * a.num_q_heads + hq) * D + d] =
-        Dt<T>::from_float(acc / sum);
+    static_cast<T *>(a.out)[(static_cast<int64_t>(b) * a.num_q_heads + hq) * D + d] = Dt<T>::from_float(acc / sum);
 }
 
 int ilog2(int x) {
@@ -410,25 +437,61 @@ int ilog2(int x) {
 
 }  // namespace
 
-// Resident decode CTAs the current device holds at once (2 per SM).
-static int resident_ctas() {
-    static int cached[64] = {};
+// Opt the partition kernel in to its shared memory (a per-device function attribute) and ask
+// for the largest shared-memory carveout, so that ctas_per_sm<ST>() CTAs fit on an SM.
+template <typename T, int D, int ST> cudaError_t prepare_partition_kernel() {
+    cudaError_t e = cudaFuncSetAttribute(decode_partition_kernel<T, D, ST>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<D, ST>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(decode_partition_kernel<T, D, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
+template <int D, int ST> int occupancy() {
+    int occ = 0;
+    if (prepare_partition_kernel<__nv_bfloat16, D, ST>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_partition_kernel<__nv_bfloat16, D, ST>, kThreads,
+                                                      Shape<D, ST>::kSmemBytes) != cudaSuccess ||
+        occ < 1)
+        occ = 1;
+    return occ < ctas_per_sm<ST>() ? occ : ctas_per_sm<ST>();
+}
+
+// Resident partition CTAs the current device holds at once for this ring depth and head dim.
+static int resident_ctas(int stages, int head_dim) {
+    static int cached[64][2][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2 * 148;
-    if (!cached[dev]) {
+    const int si = stages == 2 ? 0 : 1, hi = head_dim == 64 ? 0 : 1;
+    if (!cached[dev][si][hi]) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-        cached[dev] = 2 * sms;
+        const int occ = si ? (hi ? occupancy<128, 3>() : occupancy<64, 3>())
+                           : (hi ? occupancy<128, 2>() : occupancy<64, 2>());
+        cached[dev][si][hi] = occ * sms;
     }
-    return cached[dev];
+    return cached[dev][si][hi];
+}
+
+// Ring depth for a block size (PA_DECODE_STAGES = 2 or 3 overrides it for tuning).  Pages
+// shorter than a tile make every tile several TMA boxes; three CTAs per SM (2 stages each)
+// then keep more producers issuing (measured: block size 16, 3-4 % faster without shared
+// pages, 13 % with them), while for longer pages the deeper ring is slightly ahead.
+static int stages_for(int32_t block_size) {
+    if (const char *env = getenv("PA_DECODE_STAGES")) {
+        const int v = atoi(env);
+        if (v == 2 || v == 3) return v;
+    }
+    return block_size < kTile ? 2 : 3;
 }
 
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                        int32_t max_blocks_per_seq, int32_t block_size) {
     DecodePlan pl{};
+    pl.stages = stages_for(block_size);
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int64_t pairs = static_cast<int64_t>(batch) * num_kv_heads;
-    const int64_t slots = resident_ctas();
+    const int64_t slots = resident_ctas(pl.stages, head_dim);
     const int64_t tiles = (cap + kTile - 1) / kTile;
     int64_t part;
     if (pairs >= 2 * slots) {
@@ -441,7 +504,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     } else {
         // ragged batches: enough smaller partitions for the scheduler to even out lengths
         part = kMaxPartition;
-        while (part > kMinPartition && pairs * ((cap + part - 1) / part) < kTargetCtas) part /= 2;
+        while (part > kMinPartition && pairs * ((cap + part - 1) / part) < kTargetWaves * slots) part /= 2;
     }
     if (const char *env = getenv("PA_DECODE_PARTITION")) {  // tuning override
         const int v = atoi(env);
@@ -494,12 +557,8 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         !make_tmap_rows(&tm_v, v_cache, dtype, cols, rows, box_rows))
         return cudaErrorInvalidValue;
 
-    using S128 = Shape<128>;
-    using S64 = Shape<64>;
-    cudaError_t e;
-    auto run = [&](auto kern_part, auto kern_comb, int smem, int d) -> cudaError_t {
-        // opt in to more than 48 KB of dynamic shared memory (a per-device function attribute)
-        cudaError_t err = cudaFuncSetAttribute(kern_part, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto run = [&](auto kern_part, auto kern_comb, auto prepare, int smem, int d) -> cudaError_t {
+        cudaError_t err = prepare();
         if (err != cudaSuccess) return err;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -521,17 +580,18 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         }
         return err;
     };
-    if (dtype == PA_BF16) {
-        e = head_dim == 128 ? run(decode_partition_kernel<__nv_bfloat16, 128>, decode_combine_kernel<__nv_bfloat16, 128>,
-                                  S128::kSmemBytes, 128)
-                            : run(decode_partition_kernel<__nv_bfloat16, 64>, decode_combine_kernel<__nv_bfloat16, 64>,
-                                  S64::kSmemBytes, 64);
-    } else {
-        e = head_dim == 128 ? run(decode_partition_kernel<__half, 128>, decode_combine_kernel<__half, 128>,
-                                  S128::kSmemBytes, 128)
-                            : run(decode_partition_kernel<__half, 64>, decode_combine_kernel<__half, 64>,
-                                  S64::kSmemBytes, 64);
-    }
+#define PA_DECODE_RUN(T, D, ST)                                                                                  \
+    run(decode_partition_kernel<T, D, ST>, decode_combine_kernel<T, D>, prepare_partition_kernel<T, D, ST>,    \
+        Shape<D, ST>::kSmemBytes, D)
+    const bool bf = dtype == PA_BF16, d128 = head_dim == 128, deep = plan.stages == 3;
+    cudaError_t e;
+    if (bf)
+        e = d128 ? (deep ? PA_DECODE_RUN(__nv_bfloat16, 128, 3) : PA_DECODE_RUN(__nv_bfloat16, 128, 2))
+                 : (deep ? PA_DECODE_RUN(__nv_bfloat16, 64, 3) : PA_DECODE_RUN(__nv_bfloat16, 64, 2));
+    else
+        e = d128 ? (deep ? PA_DECODE_RUN(__half, 128, 3) : PA_DECODE_RUN(__half, 128, 2))
+                 : (deep ? PA_DECODE_RUN(__half, 64, 3) : PA_DECODE_RUN(__half, 64, 2));
+#undef PA_DECODE_RUN
     return e;
 }
 

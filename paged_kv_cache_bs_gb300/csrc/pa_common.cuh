@@ -104,6 +104,7 @@ cudaError_t launch_store_kv(const void *k, const void *v, int64_t k_row_stride, 
                             int32_t row_elems, int64_t num_slots, int32_t *err_flag, cudaStream_t stream);
 
 struct DecodePlan {
+    int stages;         // ring depth of the partition kernel (2 or 3)
     int partition;      // tokens per split-K partition (multiple of the tile)
     int max_parts;      // partitions per sequence at the maximum context
     size_t ws_bytes;    // workspace bytes
