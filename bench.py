@@ -51,8 +51,12 @@ DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 # DRAM bytes (read + write) of the dominant kernel per launch, from one ncu
 # capture of the current kernels (profiles/decode_<workload>.md); a workload
 # missing here reports null.
-TRAFFIC_PER_CALL = {}
-PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 118_873_856 + 13_274_624}  # prefill_kernel
+TRAFFIC_PER_CALL = {
+    "qwen3_0p6b_decode": 583_113_472 + 5_264_128,       # decode_partition_kernel
+    "long_context_decode": 536_950_784 + 3_327_232,     # decode_partition_kernel
+    "qwen3_8b_shared_decode": 868_519_936 + 5_361_152,  # decode_partition_kernel (L2 absorbs shared pages)
+}
+PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 117_639_936 + 11_987_968}  # prefill_kernel
 
 WORKLOAD_CONFIG = {
     "tiny_decode": dict(batch=4, context="{1,17,100,255}", H_q=4, H_kv=2, D=64, block_size=16, dtype="fp16"),
@@ -137,6 +141,33 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads
 
+def pack_inputs(host: dict, dev: torch.device):
+    """A step's inputs in one device buffer (each tensor 256-byte aligned), as a
+    caller stages them for a single host-to-device copy.  Returns the device
+    buffer, typed views into it keyed like `host`, and the layout."""
+    layout, off = {}, 0
+    for k, v in host.items():
+        nb = v.numel() * v.element_size()
+        layout[k] = (off, nb)
+        off = (off + nb + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    views = {}
+    for k, v in host.items():
+        o, nb = layout[k]
+        views[k] = buf[o:o + nb].view(v.dtype).view(v.shape)
+        views[k].copy_(v.to(dev))
+    return buf, views, layout
+
+
+def pinned_inputs(host: dict, layout: dict, nbytes: int) -> torch.Tensor:
+    """The same layout in pinned host memory."""
+    buf = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    for k, v in host.items():
+        o, nb = layout[k]
+        buf[o:o + nb].view(v.dtype).view(v.shape).copy_(v)
+    return buf
+
+
 class DecodeWorkload:
     """A decode step (store of one token per sequence + paged decode) with
     all inputs resident on the device."""
@@ -152,7 +183,7 @@ class DecodeWorkload:
         self.kc, self.vc = p.k_cache.to(dev), p.v_cache.to(dev)
         self.host = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "slot_mapping": st.slot_mapping,
                      "block_tables": st.block_tables, "context_lens": st.context_lens}
-        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        self.inputs, self.d, self.layout = pack_inputs(self.host, dev)
         self.out = torch.empty_like(self.d["q"])
         self.ws = pa.alloc_decode_workspace(self.d["q"], self.kc, self.d["block_tables"])
         self.kv_bytes = st.kv_bytes()
@@ -175,14 +206,12 @@ class DecodeWorkload:
                        out=self.out, workspace=self.ws)
 
     def e2e_buffers(self):
-        pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-        return pinned, out_host, h2d, out_host.numel() * out_host.element_size()
+        return pinned, out_host, pinned.numel(), out_host.numel() * out_host.element_size()
 
     def e2e_step(self, pinned, out_host):
-        for k, v in pinned.items():
-            self.d[k].copy_(v, non_blocking=True)
+        self.inputs.copy_(pinned, non_blocking=True)   # the step's inputs, one copy
         for _, fn in self.phases:
             fn()
         out_host.copy_(self.out, non_blocking=True)
@@ -208,7 +237,7 @@ class MixedWorkload(DecodeWorkload):
         self.host = {"q": st.q, "block_tables": st.block_tables, "context_lens": st.context_lens,
                      "k_all": m.k_new, "v_all": m.v_new, "slot_all": m.slot_mapping, "pq": pf.q,
                      "cu_q": pf.cu_seqlens_q, "cu_k": pf.cu_seqlens_k, "pbt": pf.block_tables}
-        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        self.inputs, self.d, self.layout = pack_inputs(self.host, dev)
         self.out = torch.empty_like(self.d["q"])
         self.pout = torch.empty_like(self.d["pq"])
         self.ws = pa.alloc_decode_workspace(self.d["q"], self.kc, self.d["block_tables"])
@@ -231,14 +260,12 @@ class MixedWorkload(DecodeWorkload):
                               pf.max_seqlen_k, d["pbt"], pf.scale, out=self.pout)
 
     def e2e_buffers(self):
-        pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         outs = torch.empty(self.out.numel() + self.pout.numel(), dtype=self.out.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-        return pinned, outs, h2d, outs.numel() * outs.element_size()
+        return pinned, outs, pinned.numel(), outs.numel() * outs.element_size()
 
     def e2e_step(self, pinned, out_host):
-        for k, v in pinned.items():
-            self.d[k].copy_(v, non_blocking=True)
+        self.inputs.copy_(pinned, non_blocking=True)   # the step's inputs, one copy
         for _, fn in self.phases:
             fn()
         n = self.out.numel()
