@@ -81,6 +81,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_CONFIG))
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode workloads: time pa_store_kv + pa_decode as two calls instead of pa_store_decode")
     return ap.parse_args()
 
 
@@ -172,7 +174,7 @@ class DecodeWorkload:
     """A decode step (store of one token per sequence + paged decode) with
     all inputs resident on the device."""
 
-    def __init__(self, name: str, dev: torch.device):
+    def __init__(self, name: str, dev: torch.device, fused: bool = True):
         from tests import inputs
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
@@ -192,9 +194,14 @@ class DecodeWorkload:
         self.batch = st.batch
         row = p.num_kv_heads * p.head_dim * st.q.element_size()
         self.store_bytes = 2 * 2 * int((st.slot_mapping >= 0).sum()) * row   # k and v, read + write
-        self.launches_per_step = 3   # store, decode partitions, log-sum-exp merge
-        self.phases = [("store", self.store), ("decode", self.attend)]
         self.prefill_flops = 0
+        self.fused = fused
+        if fused:   # one call: pa_store_decode (store fused into the partition kernel) + merge kernel
+            self.launches_per_step = 2
+            self.phases = [("store+decode", self.store_and_attend)]
+        else:
+            self.launches_per_step = 3   # store, decode partitions, log-sum-exp merge
+            self.phases = [("store", self.store), ("decode", self.attend)]
 
     def store(self):
         d = self.d
@@ -204,6 +211,11 @@ class DecodeWorkload:
         d = self.d
         self.pa.decode(d["q"], self.kc, self.vc, d["block_tables"], d["context_lens"], self.st.scale,
                        out=self.out, workspace=self.ws)
+
+    def store_and_attend(self):
+        d = self.d
+        self.pa.store_decode(d["k_new"], d["v_new"], d["slot_mapping"], d["q"], self.kc, self.vc, d["block_tables"],
+                             d["context_lens"], self.st.scale, out=self.out, workspace=self.ws)
 
     def e2e_buffers(self):
         pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
@@ -375,7 +387,10 @@ def run_reference(args, world, rank):
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = (MixedWorkload if args.workload == "mixed_chunked_prefill" else DecodeWorkload)(args.workload, dev)
+    if args.workload == "mixed_chunked_prefill":
+        w = MixedWorkload(args.workload, dev)
+    else:
+        w = DecodeWorkload(args.workload, dev, fused=not args.unfused)
     flush_needed = w.kv_unique_bytes < 2 * L2_BYTES
     flush = torch.empty(L2_FLUSH_BYTES // 4 if flush_needed else 1, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -413,7 +428,8 @@ def run_ours(args, world, rank, local):
     phase_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j, (name, _) in enumerate(w.phases)}
     step_ms = sum(phase_ms.values())
     step_ms_max = max_over_ranks(step_ms, world, dev)
-    store_ms, dec_ms_avg = phase_ms["store"], phase_ms["decode"]
+    store_ms = phase_ms.get("store")
+    dec_ms_avg = phase_ms["decode"] if "decode" in phase_ms else phase_ms["store+decode"]
 
     # ---- end to end through the public API, as a caller sees it: host wall
     # clock from the H2D copies of the step's inputs (pinned host memory) to the
@@ -456,7 +472,9 @@ def run_ours(args, world, rank, local):
         # bytes DRAM must supply: each physical page once (pages shared by several sequences
         # are counted once; for unshared workloads this equals the logical KV bytes)
         unique_gbs = w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "pa_decode (split-K partitions + combine)", "achieved": unique_gbs,
+        kern = ("pa_store_decode (store fused into the split-K partition kernel + merge)"
+                if "store+decode" in phase_ms else "pa_decode (split-K partitions + merge)")
+        roof = {"bound": "hbm", "kernel": kern, "achieved": unique_gbs,
                 "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": unique_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",
                 "traffic": TRAFFIC_PER_CALL.get(args.workload)}
@@ -475,7 +493,8 @@ def run_ours(args, world, rank, local):
         "decode_gbs": decode_gbs,
         "decode_unique_gbs": w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9,
         "kv_unique_bytes_per_step": w.kv_unique_bytes,
-        "store_gbs": w.store_bytes / (store_ms / 1e3) / 1e9,
+        "store_gbs": w.store_bytes / (store_ms / 1e3) / 1e9 if store_ms else None,
+        "store_fused_into_decode": "store+decode" in phase_ms,
         "kv_bytes_per_step": w.kv_bytes,
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -151,6 +151,38 @@ PA_API int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, c
               size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag, void *stream);
 
 /*
+ * pa_store_decode -- pa_store_kv of one decode step fused into pa_decode: one
+ * launch stores each sequence's new K/V row and attends over its context.
+ *
+ * The two calls of the attention layer's decode branch in "Inference engine:
+ * inside nano-vLLM" (section "Attention in nano-vLLM": store_kvcache, then
+ * flash_attn_with_kvcache), done by one kernel.  Same result as
+ *   pa_store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache,
+ *               slot_mapping, batch, ...) followed by pa_decode(...),
+ * for decode steps, where the token stored for sequence b is the last
+ * position of its context: slot_mapping[b] must be -1 (nothing stored) or the
+ * slot of position context_lens[b] - 1, i.e.
+ *   block_tables[b][(L-1) / block_size] * block_size + (L-1) % block_size
+ * ("nano-vLLM Part 2", sections 2.2 and 3.1).  Any other slot sets
+ * PA_FLAG_BAD_SLOT and that row is not stored.
+ *   k, v          [batch, num_kv_heads, head_dim]; row b starts at element
+ *                 b * k_row_stride (v_row_stride); strides multiples of 8,
+ *                 pointers 16-byte aligned.
+ *   slot_mapping  int32 [batch].
+ *   other arguments: as pa_decode (k_cache / v_cache are written).
+ * The CTA that holds sequence b's last partition for kv head g writes that
+ * head's slice of the row before it reads the tile containing it; no other
+ * CTA reads that slice.
+ */
+PA_API int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                           const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                           void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, void *out,
+                           void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag,
+                           void *stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate
  * device memory.  The pages describe no such call: it has no counterpart there.
  *

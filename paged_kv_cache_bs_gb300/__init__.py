@@ -10,6 +10,7 @@ The functions mirror the C ABI in ``include/pa_api.h``:
 
 * :func:`store_kv`       -- ``pa_store_kv``
 * :func:`decode`         -- ``pa_decode`` (+ ``pa_decode_workspace_bytes``)
+* :func:`store_decode`   -- ``pa_store_decode`` (the decode step's store fused into decode)
 * :func:`prefill_paged`  -- ``pa_prefill_paged``
 """
 
@@ -38,6 +39,9 @@ _lib.pa_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.pa_decode.restype = ctypes.c_int
 _lib.pa_decode.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
                            ctypes.c_int, _p, _p]
+_lib.pa_store_decode.restype = ctypes.c_int
+_lib.pa_store_decode.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
+                                 _i32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
 _lib.pa_prefill_paged.restype = ctypes.c_int
 _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32,
                                   _i32, _i32, _f32, _p, ctypes.c_int, _p, _p]
@@ -126,12 +130,9 @@ def alloc_decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
 
 
-def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
-           context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
-           workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
-    """Paged decode attention: q [B, H_q, D] -> out [B, H_q, D]."""
+def _decode_checks(q, k_cache, v_cache, block_tables, context_lens):
     n, bs, hkv, d = _cache_shape(k_cache, v_cache)
-    B, hq = q.shape[0], q.shape[1]
+    B = q.shape[0]
     if q.dim() != 3 or q.shape[2] != d:
         raise ValueError("q must be [B, H_q, D]")
     for name, t in (("block_tables", block_tables), ("context_lens", context_lens)):
@@ -139,6 +140,15 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
             raise ValueError(f"{name} must be contiguous int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
         raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
+    return n, bs, hkv, d
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """Paged decode attention: q [B, H_q, D] -> out [B, H_q, D]."""
+    n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    B, hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
     if workspace is None:
@@ -148,6 +158,30 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
                         _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
                         _stream(q))
     _check("pa_decode", rc)
+    return out
+
+
+def store_decode(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                 context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """One decode step in one launch: store k/v ([B, H_kv, D]) at ``slot_mapping`` (the slot of
+    each sequence's last context position, or -1) and attend: q [B, H_q, D] -> out [B, H_q, D]."""
+    n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    B, hq = q.shape[0], q.shape[1]
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous() or slot_mapping.numel() != B:
+        raise ValueError("slot_mapping must be contiguous int32 [B]")
+    if k.shape != (B, hkv, d) or v.shape != (B, hkv, d) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k/v must be [B, H_kv, D] of the cache dtype")
+    if out is None:
+        out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_decode_workspace(q, k_cache, block_tables)
+    rc = _lib.pa_store_decode(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q),
+                              _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                              _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale), _ptr(out), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag), _stream(q))
+    _check("pa_store_decode", rc)
     return out
 
 
@@ -178,6 +212,6 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     return out
 
 
-__all__ = ["store_kv", "decode", "prefill_paged", "decode_workspace_bytes", "alloc_decode_workspace",
+__all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "decode_workspace_bytes", "alloc_decode_workspace",
            "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
            "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL"]

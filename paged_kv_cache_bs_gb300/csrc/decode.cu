@@ -77,6 +77,13 @@ struct DecodeArgs {
     int32_t partition;
     int32_t max_parts;
     int32_t *err_flag;
+    // fused store (null slot_mapping: none): sequence b's new K/V rows go to cache row slot_mapping[b]
+    const int32_t *slot_mapping;
+    const void *k_new;
+    const void *v_new;
+    int64_t k_new_stride, v_new_stride;  // elements between sequences' rows
+    void *k_cache_w;
+    void *v_cache_w;
 };
 
 // Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
@@ -104,6 +111,38 @@ __device__ __forceinline__ int context_len(const DecodeArgs &a, int b) {
     const int L = a.context_lens[b];
     const int64_t cap = static_cast<int64_t>(a.max_blocks) << a.log2_bs;
     return (L < 0 || L > cap) ? -1 : L;
+}
+
+// Fused store, by the producer warp of the CTA that holds the last partition of
+// sequence b for kv head g: this head's slices of the new K and V rows go to
+// cache row slot_mapping[b], which must be the slot of position L-1 (the token
+// stored this step is the last one of the context), else the row is flagged
+// and not written.  No other CTA reads that slice, and the proxy fence makes
+// the plain stores visible to the TMA loads this warp issues next.
+template <typename T, int D>
+__device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g, int L, int lane) {
+    const int slot = a.slot_mapping[b];
+    if (slot == -1) return;
+    const int j = L - 1;
+    const int pg = a.block_tables[static_cast<int64_t>(b) * a.max_blocks + (j >> a.log2_bs)];
+    const int64_t expect =
+        (pg < 0 || pg >= a.num_blocks) ? -2 : (static_cast<int64_t>(pg) << a.log2_bs) + (j & ((1 << a.log2_bs) - 1));
+    if (slot != expect) {
+        if (lane == 0 && g == 0) raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);
+        return;
+    }
+    constexpr int kChunks = D / 8;  // 16-byte chunks of one head's row
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int ci = is_v ? lane - kChunks : lane;
+        const T *src = static_cast<const T *>(is_v ? a.v_new : a.k_new) + b * (is_v ? a.v_new_stride : a.k_new_stride) +
+                       g * D + ci * 8;
+        T *dst = static_cast<T *>(is_v ? a.v_cache_w : a.k_cache_w) +
+                 (static_cast<int64_t>(slot) * a.num_kv_heads + g) * D + ci * 8;
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    }
+    __syncwarp();
 }
 
 // Byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r in the swizzled layout.
@@ -140,10 +179,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
     const int start = p * a.partition;
     T *out = static_cast<T *>(a.out);
     if (start >= L) {
-        if (p == 0)  // empty context (e.g. a padding row): zero output, no page read
+        if (p == 0) {  // empty context (e.g. a padding row): zero output, no page read
             for (int i = tid; i < a.group * D; i += kThreads)
                 out[(static_cast<int64_t>(b) * a.num_q_heads + g * a.group + i / D) * D + i % D] =
                     Dt<T>::from_float(0.f);
+            if (a.slot_mapping && g == 0 && tid == 0 && a.slot_mapping[b] != -1)
+                raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);  // a new token needs a context position
+        }
         return;
     }
     const int end = min(L, start + a.partition);
@@ -201,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
     int issued = 0;                                             // tiles the producer started
 
     if (warp == kProducerWarp) {
+        if (a.slot_mapping && end == L) store_new_row<T, D>(a, b, g, L, lane);
         if (lane == 0) {
             const int box_rows = min(1 << a.log2_bs, kTile);
             const int bs_mask = (1 << a.log2_bs) - 1;
@@ -524,7 +567,8 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                           const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
-                          const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream) {
+                          const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
+                          const FusedStore *fused) {
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
     a.q = q;
@@ -546,6 +590,13 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.partition = plan.partition;
     a.max_parts = plan.max_parts;
     a.err_flag = err_flag;
+    a.slot_mapping = fused ? fused->slot_mapping : nullptr;
+    a.k_new = fused ? fused->k : nullptr;
+    a.v_new = fused ? fused->v : nullptr;
+    a.k_new_stride = fused ? fused->k_row_stride : 0;
+    a.v_new_stride = fused ? fused->v_row_stride : 0;
+    a.k_cache_w = const_cast<void *>(k_cache);
+    a.v_cache_w = const_cast<void *>(v_cache);
 
     // the pool as [num_blocks * block_size rows, H_kv * D columns]; one box = 64 columns of
     // min(block_size, 64) rows, so a box never crosses a page

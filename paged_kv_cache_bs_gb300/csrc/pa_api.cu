@@ -63,6 +63,39 @@ namespace pa {
 int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace pa
 
+namespace {
+
+// Checks of pa_decode's arguments (also those of pa_store_decode); PA_OK or an error code.
+int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                 float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                 pa::DecodePlan *plan) {
+    int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
+    if (rc) return rc;
+    if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch is negative (%d)", batch);
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (1LL << 30))
+        return fail(PA_ERR_INVALID_ARG, "max context of %lld tokens is too large",
+                    (long long)max_blocks_per_seq * block_size);
+    if (batch == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (q_row_stride < static_cast<int64_t>(num_q_heads) * head_dim || q_row_stride % 2)
+        return fail(PA_ERR_INVALID_ARG, "q_row_stride %lld must be even and at least H_q*D",
+                    (long long)q_row_stride);
+    if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 2) ||
+        !aligned(workspace, 256))
+        return fail(PA_ERR_INVALID_ARG, "alignment: q 4 B, caches 16 B, out 2 B, workspace 256 B");
+    *plan = pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+    if (workspace_bytes < plan->ws_bytes)
+        return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
+                    plan->ws_bytes);
+    return PA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char *pa_last_error(void) { return g_err; }
@@ -111,35 +144,49 @@ int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const vo
               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
               float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag,
               void *stream) {
-    int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
+    pa::DecodePlan plan{};
+    const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
+                                workspace, workspace_bytes, dtype, &plan);
     if (rc) return rc;
-    if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch is negative (%d)", batch);
-    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
-    if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (1LL << 30))
-        return fail(PA_ERR_INVALID_ARG, "max context of %lld tokens is too large",
-                    (long long)max_blocks_per_seq * block_size);
     if (batch == 0) {
         g_err[0] = '\0';
         return PA_OK;
     }
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
-        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
-    if (q_row_stride < static_cast<int64_t>(num_q_heads) * head_dim || q_row_stride % 2)
-        return fail(PA_ERR_INVALID_ARG, "q_row_stride %lld must be even and at least H_q*D",
-                    (long long)q_row_stride);
-    if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 2) ||
-        !aligned(workspace, 256))
-        return fail(PA_ERR_INVALID_ARG, "alignment: q 4 B, caches 16 B, out 2 B, workspace 256 B");
-    const pa::DecodePlan plan =
-        pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-    if (workspace_bytes < plan.ws_bytes)
-        return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
-                    plan.ws_bytes);
     return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                          context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
                                          block_size, scale, out, workspace, plan, dtype, err_flag,
                                          static_cast<cudaStream_t>(stream)),
                        "pa_decode launch");
+}
+
+int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                    const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache, void *v_cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                    int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                    int32_t block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+                    pa_dtype dtype, int32_t *err_flag, void *stream) {
+    pa::DecodePlan plan{};
+    const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
+                                workspace, workspace_bytes, dtype, &plan);
+    if (rc) return rc;
+    if (batch == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "k, v and slot_mapping are required");
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (k_row_stride < row || v_row_stride < row || k_row_stride % 8 || v_row_stride % 8)
+        return fail(PA_ERR_INVALID_ARG, "k/v row strides (%lld, %lld) must be multiples of 8 and at least H_kv*D",
+                    (long long)k_row_stride, (long long)v_row_stride);
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    const pa::FusedStore fused{k, v, k_row_stride, v_row_stride, slot_mapping};
+    return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         block_size, scale, out, workspace, plan, dtype, err_flag,
+                                         static_cast<cudaStream_t>(stream), &fused),
+                       "pa_store_decode launch");
 }
 
 int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,

@@ -111,11 +111,20 @@ struct DecodePlan {
 };
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                        int32_t max_blocks_per_seq, int32_t block_size);
+// The store fused into pa_store_decode (the new rows of one decode step).
+struct FusedStore {
+    const void *k;
+    const void *v;
+    int64_t k_row_stride;  // elements between sequences' rows
+    int64_t v_row_stride;
+    const int32_t *slot_mapping;
+};
 cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
-                          const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream);
+                          const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
+                          const FusedStore *fused = nullptr);
 cudaError_t launch_prefill(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
                            int32_t total_q, int32_t max_seqlen_q, const int32_t *block_tables,

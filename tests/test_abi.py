@@ -134,3 +134,20 @@ def test_prefill_validation(lib):
     assert call(q=ctypes.c_void_p((1 << 20) + 8)) == -1   # TMA needs 16-byte alignment
     assert call(scale=0.0) == -1 and call(scale=-0.1) == -1
     assert call(S=0) == 0 and call(tq=0) == 0
+
+
+def test_store_decode_validation(lib):
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, ks=1024, vs=1024, sm=FAKE, q=FAKE, qs=2048, kc=FAKE, vc=FAKE, bt=FAKE, mb=16, cl=FAKE,
+                 B=64, hq=16, hkv=8, d=128, n=700, bs=256, scale=0.088, out=FAKE, ws=FAKE, wsb=1 << 30, dt=1)
+        a.update(kw)
+        return lib.pa_store_decode(a["k"], a["v"], a["ks"], a["vs"], a["sm"], a["q"], a["qs"], a["kc"], a["vc"],
+                                   a["bt"], a["mb"], a["cl"], a["B"], a["hq"], a["hkv"], a["d"], a["n"], a["bs"],
+                                   ctypes.c_float(a["scale"]), a["out"], a["ws"], a["wsb"], a["dt"], None, None)
+    assert call(k=None) == -1
+    assert call(sm=None) == -1
+    assert call(ks=1020) == -1                               # not a multiple of 8
+    assert call(vs=512) == -1                                # shorter than H_kv * D
+    assert call(v=ctypes.c_void_p((1 << 20) + 8)) == -1      # 16-byte alignment
+    assert call(d=96) == -2
+    assert call(B=0, k=None, v=None, sm=None, q=None, out=None, ws=None) == 0

@@ -148,3 +148,51 @@ def test_decode_bad_metadata_is_flagged_not_fatal(pa):
     assert f & pa.FLAG_BAD_BLOCK and f & pa.FLAG_BAD_LENGTH
     # the device is still healthy
     check_decode(pa, inputs.tiny_decode())
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_store_and_decode_replay_from_a_cuda_graph(pa, fused):
+    # A decode step captured once and replayed on new inputs of the same shapes, as an
+    # engine replays its decode graph every step ("nano-vLLM Part 2", section 4.2): padding
+    # rows (context 0, slot -1) included.
+    ctx = [700, 0, 33, 2048, 1, 129, 0, 512]
+    steps = [inputs.make_decode(ctx, num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
+                                dtype=torch.bfloat16, seed=seed) for seed in (71, 72, 73)]
+    for st in steps[1:]:
+        assert st.pool.k_cache.shape == steps[0].pool.k_cache.shape
+        assert st.block_tables.shape == steps[0].block_tables.shape
+    st0 = steps[0]
+    kc, vc = st0.pool.k_cache.cuda(), st0.pool.v_cache.cuda()
+    q, kn, vn = st0.q.cuda(), st0.k_new.cuda(), st0.v_new.cuda()
+    sm, bt, cl = st0.slot_mapping.cuda(), st0.block_tables.cuda(), st0.context_lens.cuda()
+    ws = pa.alloc_decode_workspace(q, kc, bt)
+    out = torch.empty_like(q)
+
+    def step():
+        if fused:
+            pa.store_decode(kn, vn, sm, q, kc, vc, bt, cl, st0.scale, out=out, workspace=ws)
+        else:
+            pa.store_kv(kn, vn, kc, vc, sm)
+            pa.decode(q, kc, vc, bt, cl, st0.scale, out=out, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                                   # first call on the device: set-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for st in steps:
+        for dst, src in ((kc, st.pool.k_cache), (vc, st.pool.v_cache), (q, st.q), (kn, st.k_new), (vn, st.v_new),
+                         (sm, st.slot_mapping), (bt, st.block_tables), (cl, st.context_lens)):
+            dst.copy_(src)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        okc, ovc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+        oracle.store_kv(st.k_new, st.v_new, okc, ovc, st.slot_mapping)
+        assert_bit_equal(kc, okc, "k_cache after a replayed store")
+        ref = oracle.decode(st.q, okc, ovc, st.block_tables, st.context_lens, st.scale)
+        assert max_err(out, ref) <= TOL[torch.bfloat16]

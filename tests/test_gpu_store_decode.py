@@ -1,0 +1,83 @@
+"""GPU parity of pa_store_decode (the decode step's store fused into decode)
+against the oracle, and against pa_store_kv followed by pa_decode."""
+
+import pytest
+import torch
+
+import oracle
+from tests import inputs
+from tests.gpu_cases import TOL, assert_bit_equal, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fused(pa, st, err_flag=None, slots=None):
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    sm = (st.slot_mapping if slots is None else slots).cuda()
+    out = pa.store_decode(st.k_new.cuda(), st.v_new.cuda(), sm, st.q.cuda(), kc, vc, st.block_tables.cuda(),
+                          st.context_lens.cuda(), st.scale, err_flag=err_flag)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def check_fused(pa, st):
+    out, kc, vc = run_fused(pa, st)
+    okc, ovc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+    oracle.store_kv(st.k_new, st.v_new, okc, ovc, st.slot_mapping)
+    assert_bit_equal(kc, okc, "k_cache after the fused store")
+    assert_bit_equal(vc, ovc, "v_cache after the fused store")
+    ref = oracle.decode(st.q, okc, ovc, st.block_tables, st.context_lens, st.scale)
+    err = max_err(out, ref)
+    assert err <= TOL[st.q.dtype], f"max |err| {err}"
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "qwen3_0p6b_decode", "qwen3_8b_shared_decode",
+                                  "long_context_decode"])
+def test_store_decode_workloads_full(pa, name):
+    check_fused(pa, inputs.WORKLOADS[name]())
+
+
+def test_store_decode_equals_separate_calls(pa):
+    st = inputs.qwen3_0p6b_decode()
+    fused = check_fused(pa, st)
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    pa.store_kv(st.k_new.cuda(), st.v_new.cuda(), kc, vc, st.slot_mapping.cuda())
+    sep = pa.decode(st.q.cuda(), kc, vc, st.block_tables.cuda(), st.context_lens.cuda(), st.scale)
+    torch.cuda.synchronize()
+    assert_bit_equal(fused, sep, "fused vs separate store + decode")
+
+
+@pytest.mark.parametrize("bs", [8, 16, 64, 256, 1024])
+@pytest.mark.parametrize("dtype,head_dim", [(torch.bfloat16, 128), (torch.float16, 64)])
+def test_store_decode_block_sizes(pa, bs, dtype, head_dim):
+    # contexts on and off tile, page and partition boundaries, and padding rows
+    ctx = [1, 0, 63, 64, 65, bs, bs + 1, 2049, 0, 5000]
+    st = inputs.make_decode(ctx, num_q_heads=16, num_kv_heads=4, head_dim=head_dim, block_size=bs, dtype=dtype,
+                            seed=100 + bs + head_dim)
+    out = check_fused(pa, st)
+    assert not out[1].any() and not out[8].any()
+
+
+def test_store_decode_flags_a_slot_that_is_not_the_last_position(pa):
+    st = inputs.make_decode([40, 300, 0, 77], num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                            dtype=torch.bfloat16, seed=110)
+    slots = st.slot_mapping.clone()
+    good = int(slots[1])
+    slots[1] = good - 1          # a slot of the same sequence, but not position L-1
+    slots[2] = 5                 # a new row for a sequence with no context
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, kc, vc = run_fused(pa, st, err_flag=flag, slots=slots)
+    assert int(flag.item()) & pa.FLAG_BAD_SLOT
+    # the flagged rows were not written; the others were
+    okc = st.pool.k_cache.clone()
+    ovc = st.pool.v_cache.clone()
+    keep = st.slot_mapping.clone()
+    keep[1] = -1
+    keep[2] = -1
+    oracle.store_kv(st.k_new, st.v_new, okc, ovc, keep)
+    assert_bit_equal(kc, okc, "k_cache with the flagged rows skipped")
+    ref = oracle.decode(st.q[[0, 3]], okc, ovc, st.block_tables[[0, 3]], st.context_lens[[0, 3]], st.scale)
+    assert max_err(out[[0, 3]], ref) <= TOL[torch.bfloat16]
