@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     tc::tmem_st32(tO(w) + lane_base + 32 * cc, o);
                 }
             }
-            // P = 2^(c*s - m), packed to 16 bits over the first 64 columns of S
+            // P = 2^(c*s - m), packed to 16 bits over the first 64 columns of S; the two
+            // halves' stores are issued back to back and waited for once.
             const float neg_m = -m_used;
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -401,13 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 uint32_t pw[32];
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
-                    const float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[64 * half + e]), c, neg_m));
-                    const float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[64 * half + e + 1]), c, neg_m));
+                    const float x0 = fmaf(__uint_as_float(sr[64 * half + e]), c, neg_m);
+                    const float x1 = fmaf(__uint_as_float(sr[64 * half + e + 1]), c, neg_m);
+                    const float p0 = tc::ex2_approx(x0);
+                    const float p1 = tc::ex2_approx(x1);
                     l4[(e >> 1) & 3] += p0 + p1;
                     pw[e >> 1] = Dt<T>::pack(p0, p1);
                 }
-                tc::tmem_st32(tS(w) + lane_base + 32 * half, pw);  // P columns [32*half, 32*half + 32)
+                tc::tmem_st32_nowait(tS(w) + lane_base + 32 * half, pw);  // P columns [32*half, 32*half + 32)
             }
+            tc::tmem_wait_st();
             l_sum = l_sum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
             const int valid = min(kBN, Lk - j0);
             if (w == 0 && valid < kBN) {
