@@ -18,6 +18,23 @@ def oracle_lib():
     return oracle.load()
 
 
+def _build_and_import():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "pa_build", os.path.join(ROOT, "paged_kv_cache_bs_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import paged_kv_cache_bs_gb300
+    return paged_kv_cache_bs_gb300
+
+
+@pytest.fixture(scope="session")
+def pa_host():
+    """The binding for host-only calls (argument checks, the page directory): no GPU needed."""
+    return _build_and_import()
+
+
 @pytest.fixture(scope="session")
 def pa():
     """The CUDA library's binding, built in-tree first.  GPU tests need a GPU:

@@ -1,5 +1,5 @@
 """C-ABI checks that need no GPU: the library loads, exports every function
-``include/pa_api.h`` declares, and rejects invalid arguments on the host
+the headers in ``include/`` declare, and rejects invalid arguments on the host
 before making any CUDA call.  Also checks that the CUDA library and the oracle
 share no symbols."""
 
@@ -11,7 +11,8 @@ import subprocess
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pa_api.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -26,9 +27,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def exported_symbols(path):
@@ -39,7 +42,8 @@ def exported_symbols(path):
 def test_every_declared_function_is_exported(lib):
     import paged_kv_cache_bs_gb300 as pa
     names = declared_functions()
-    assert {"pa_store_kv", "pa_decode", "pa_prefill_paged", "pa_decode_workspace_bytes", "pa_last_error"} <= set(names)
+    assert {"pa_store_kv", "pa_decode", "pa_store_decode", "pa_prefill_paged", "pa_decode_workspace_bytes",
+            "pa_last_error", "pa_bm_create", "pa_bm_prefill_inputs", "pa_bm_decode_inputs"} <= set(names)
     syms = exported_symbols(pa.LIB_PATH)
     for n in names:
         assert n in syms, n
