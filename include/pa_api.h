@@ -60,7 +60,8 @@
 extern "C" {
 #endif
 
-typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+/* PA_F32 is accepted only for the logits of pa_sample. */
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
 
 enum {
     PA_OK = 0,
@@ -75,6 +76,7 @@ enum {
     PA_FLAG_BAD_LENGTH = 4,
     PA_FLAG_TIMEOUT = 8,
     PA_FLAG_INTERNAL = 16,
+    PA_FLAG_BAD_VALUE = 32, /* a value outside its domain (pa_sample: temperature <= 1e-10) */
 };
 
 /* Message describing the calling thread's last failed call ("" if none). */
@@ -249,6 +251,41 @@ PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const v
                      const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_q_heads,
                      int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                      float scale, void *out, pa_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
+ * pa_sample -- one token per row by temperature sampling, written as the
+ * exponential race of "From nano-vLLM to vLLM: Scheduler, Paged KV Cache,
+ * Prefill/Decode, Tensor Parallelism, and Sampling", section 17 (17.1, 17.4,
+ * 17.6).  For row b, in fp32:
+ *   a_i = logits[b, i] / temperatures[b];   p = softmax(a)
+ *   tokens[b] = argmax_i  p_i / max(E_i, 1e-10)   (the first index on ties)
+ * with E_i ~ Exp(1) independent, which selects token i with probability p_i.
+ *
+ *   logits        [batch, vocab], dtype PA_F32, PA_BF16 or PA_F16; row b
+ *                 starts at element b * logits_row_stride (>= vocab).  Rows
+ *                 that start on a 16-byte boundary are read with 16-byte
+ *                 vectors, others element by element.
+ *   temperatures  fp32 [batch], DEVICE; each must exceed 1e-10 (the pages'
+ *                 sampler has no greedy path): a row whose temperature does
+ *                 not gets token -1 and PA_FLAG_BAD_VALUE.
+ *   noise         fp32 [batch, vocab] contiguous, DEVICE: the E_i (drawn by
+ *                 the caller, e.g. torch's exponential_); or NULL: the kernel
+ *                 draws them from Philox4x32-10 (Salmon et al., SC'11) keyed
+ *                 by `seed`, counter (i / 4, b, offset low, offset high),
+ *                 u = ((x >> 8) + 1) * 2^-24 in (0, 1], E = -log(u).  Pass a
+ *                 new offset for every call that needs fresh samples.
+ *   tokens        int32 [batch], DEVICE, written.
+ * The kernel takes the decision in the race's log form, argmax_i
+ * logits[b, i] / T - log(max(E_i, 1e-10)), which section 17.5 of the same
+ * page shows selects the same token (the softmax denominator is common to all
+ * i); only near-ties can resolve differently from the fp32 ratio form.  A row
+ * is split over a cluster of 8 CTAs that compare their winners through
+ * distributed shared memory; batch <= 65535.  A row with no finite logit
+ * gets -1.
+ */
+PA_API int pa_sample(const void *logits, int64_t logits_row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
+                     const float *temperatures, const float *noise, uint64_t seed, uint64_t offset,
+                     int32_t *tokens, int32_t *err_flag, void *stream);
 
 #ifdef __cplusplus
 }

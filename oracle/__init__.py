@@ -47,6 +47,8 @@ def _declare(lib):
     lib.oracle_decode.restype = ci
     lib.oracle_prefill_paged.argtypes = [p, p, p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, f32, ci, p]
     lib.oracle_prefill_paged.restype = ci
+    lib.oracle_sample.argtypes = [p, i64, i32, i32, i32, p, p, p]
+    lib.oracle_sample.restype = ci
     lib.oracle_half_to_float.argtypes = [ctypes.c_uint16, ci]
     lib.oracle_half_to_float.restype = f32
     return lib
@@ -130,3 +132,19 @@ def prefill_paged(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_t
 def half_to_float(bits: int, dtype: torch.dtype, lib=None) -> float:
     lib = lib or load()
     return lib.oracle_half_to_float(bits, _DT[dtype])
+
+
+def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor, lib=None) -> torch.Tensor:
+    """Exponential-race sampling of one token per row: logits [B, V] (fp32, bf16
+    or fp16), temperatures [B] fp32, noise [B, V] fp32 (the Exp(1) draws)."""
+    lib = lib or load()
+    logits = logits.contiguous()
+    B, V = logits.shape
+    dt = {torch.float32: 2, torch.bfloat16: BF16, torch.float16: F16}[logits.dtype]
+    temps = temperatures.to(torch.float32).contiguous()
+    noise = noise.to(torch.float32).contiguous()
+    out = torch.empty(B, dtype=torch.int32)
+    rc = lib.oracle_sample(logits.data_ptr(), V, B, V, dt, temps.data_ptr(), noise.data_ptr(), out.data_ptr())
+    if rc:
+        raise OracleError(f"oracle_sample returned {rc}")
+    return out

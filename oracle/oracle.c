@@ -262,3 +262,60 @@ int oracle_prefill_paged(const uint16_t *q, const uint16_t *k, const uint16_t *v
     free(kc); free(vc); free(s); free(qh); free(res);
     return rc;
 }
+
+/* ---------------------------------------------------------------- sample */
+
+/* Temperature sampling as the exponential race of "From nano-vLLM to vLLM:
+ * Scheduler, Paged KV Cache, Prefill/Decode, Tensor Parallelism, and
+ * Sampling", section 17 (17.1, 17.4, 17.6), in fp32 and in the pages' order:
+ * a_i = x_i / T; p = softmax(a) with the row maximum subtracted and the
+ * denominator summed in index order; score_i = p_i / max(E_i, 1e-10); the
+ * first index of the largest score.  -inf and NaN logits never win (a row
+ * with no finite logit gives -1); T <= 1e-10 gives -1 (the pages' sampler
+ * has no greedy path).  dtype 2 = fp32 logits, else 16-bit as to_float. */
+int oracle_sample(const void *logits, int64_t row_stride, int32_t batch, int32_t vocab, int32_t dtype,
+                  const float *temps, const float *noise, int32_t *tokens)
+{
+    if (batch < 0 || vocab <= 0 || row_stride < vocab)
+        return -1;
+    for (int32_t b = 0; b < batch; ++b) {
+        const float t = temps[b];
+        tokens[b] = -1;
+        if (!(t > 1e-10f) || isinf(t))
+            continue;
+        float m = -INFINITY;
+        for (int32_t i = 0; i < vocab; ++i) {
+            const int64_t at = (int64_t)b * row_stride + i;
+            const float x = dtype == 2 ? ((const float *)logits)[at] : to_float(((const uint16_t *)logits)[at], dtype);
+            const float a = x / t;
+            if (a > m)
+                m = a;
+        }
+        if (!(m > -INFINITY))
+            continue;
+        float sum = 0.0f;
+        for (int32_t i = 0; i < vocab; ++i) {
+            const int64_t at = (int64_t)b * row_stride + i;
+            const float x = dtype == 2 ? ((const float *)logits)[at] : to_float(((const uint16_t *)logits)[at], dtype);
+            const float a = x / t;
+            if (a > -INFINITY)
+                sum += expf(a - m);
+        }
+        float best = -1.0f;
+        for (int32_t i = 0; i < vocab; ++i) {
+            const int64_t at = (int64_t)b * row_stride + i;
+            const float x = dtype == 2 ? ((const float *)logits)[at] : to_float(((const uint16_t *)logits)[at], dtype);
+            const float a = x / t;
+            if (!(a > -INFINITY))
+                continue;
+            const float p = expf(a - m) / sum;
+            const float e = noise[(int64_t)b * vocab + i];
+            const float score = p / (e > 1e-10f ? e : 1e-10f);
+            if (score > best) {
+                best = score;
+                tokens[b] = i;
+            }
+        }
+    }
+    return 0;
+}

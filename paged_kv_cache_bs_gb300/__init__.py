@@ -12,6 +12,7 @@ The functions mirror the C ABI in ``include/pa_api.h``:
 * :func:`decode`         -- ``pa_decode`` (+ ``pa_decode_workspace_bytes``)
 * :func:`store_decode`   -- ``pa_store_decode`` (the decode step's store fused into decode)
 * :func:`prefill_paged`  -- ``pa_prefill_paged``
+* :func:`sample`         -- ``pa_sample`` (temperature sampling, exponential race)
 """
 
 from __future__ import annotations
@@ -42,13 +43,15 @@ _lib.pa_decode.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i3
 _lib.pa_store_decode.restype = ctypes.c_int
 _lib.pa_store_decode.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                  _i32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
+_lib.pa_sample.restype = ctypes.c_int
+_lib.pa_sample.argtypes = [_p, _i64, _i32, _i32, ctypes.c_int, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
 _lib.pa_prefill_paged.restype = ctypes.c_int
 _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32,
                                   _i32, _i32, _f32, _p, ctypes.c_int, _p, _p]
 
-PA_F16, PA_BF16 = 0, 1
+PA_F16, PA_BF16, PA_F32 = 0, 1, 2
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
-FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_INTERNAL = 1, 2, 4, 8, 16
+FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_INTERNAL, FLAG_BAD_VALUE = 1, 2, 4, 8, 16, 32
 
 
 class PagedAttentionError(RuntimeError):
@@ -212,6 +215,28 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     return out
 
 
-__all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "decode_workspace_bytes", "alloc_decode_workspace",
-           "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
-           "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL"]
+def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor | None = None, seed: int = 0,
+           offset: int = 0, out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """One token per row of logits [B, V] (fp32/bf16/fp16): argmax of softmax(logits / T) / max(E, 1e-10),
+    E ~ Exp(1) from ``noise`` [B, V] fp32 or, if None, drawn in-kernel from Philox4x32-10 at (seed, offset)."""
+    if logits.dim() != 2 or logits.stride(1) != 1 or not logits.is_cuda:
+        raise ValueError("logits must be a CUDA [B, V] tensor with contiguous rows")
+    dt = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}.get(logits.dtype)
+    if dt is None:
+        raise TypeError("logits must be fp32, bf16 or fp16")
+    B, V = logits.shape
+    if temperatures.dtype != torch.float32 or temperatures.numel() != B or not temperatures.is_contiguous():
+        raise ValueError("temperatures must be contiguous fp32 [B]")
+    if noise is not None and (noise.dtype != torch.float32 or tuple(noise.shape) != (B, V) or not noise.is_contiguous()):
+        raise ValueError("noise must be contiguous fp32 [B, V]")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    rc = _lib.pa_sample(_ptr(logits), logits.stride(0), B, V, dt, _ptr(temperatures), _ptr(noise), seed, offset,
+                        _ptr(out), _ptr(err_flag), _stream(logits))
+    _check("pa_sample", rc)
+    return out
+
+
+__all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "sample", "decode_workspace_bytes", "alloc_decode_workspace",
+           "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
+           "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL", "FLAG_BAD_VALUE"]

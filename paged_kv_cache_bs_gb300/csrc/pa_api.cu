@@ -225,4 +225,25 @@ int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_
     return cuda_status(e, "pa_prefill_paged launch");
 }
 
+int pa_sample(const void *logits, int64_t logits_row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
+              const float *temperatures, const float *noise, uint64_t seed, uint64_t offset, int32_t *tokens,
+              int32_t *err_flag, void *stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_F16)
+        return fail(PA_ERR_UNSUPPORTED, "logits dtype %d is not PA_F32, PA_BF16 or PA_F16", (int)dtype);
+    if (batch < 0 || batch > 65535 || vocab <= 0)
+        return fail(PA_ERR_INVALID_ARG, "batch %d (at most 65535), vocab %d", batch, vocab);
+    if (batch == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    if (!logits || !temperatures || !tokens) return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (logits_row_stride < vocab)
+        return fail(PA_ERR_INVALID_ARG, "logits_row_stride %lld is shorter than vocab", (long long)logits_row_stride);
+    if (!aligned(logits, dtype == PA_F32 ? 4 : 2) || (noise && !aligned(noise, 4)))
+        return fail(PA_ERR_INVALID_ARG, "logits and noise must be aligned to their element size");
+    return cuda_status(pa::launch_sample(logits, logits_row_stride, batch, vocab, dtype, temperatures, noise, seed,
+                                         offset, tokens, err_flag, static_cast<cudaStream_t>(stream)),
+                       "pa_sample launch");
+}
+
 }  // extern "C"

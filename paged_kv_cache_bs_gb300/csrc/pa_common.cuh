@@ -125,6 +125,9 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
                           const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
                           const FusedStore *fused = nullptr);
+cudaError_t launch_sample(const void *logits, int64_t row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
+                          const float *temperatures, const float *noise, uint64_t seed, uint64_t offset,
+                          int32_t *tokens, int32_t *err_flag, cudaStream_t stream);
 cudaError_t launch_prefill(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
                            int32_t total_q, int32_t max_seqlen_q, const int32_t *block_tables,

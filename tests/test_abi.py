@@ -155,3 +155,18 @@ def test_store_decode_validation(lib):
     assert call(v=ctypes.c_void_p((1 << 20) + 8)) == -1      # 16-byte alignment
     assert call(d=96) == -2
     assert call(B=0, k=None, v=None, sm=None, q=None, out=None, ws=None) == 0
+
+
+def test_sample_validation(lib):
+    def call(**kw):
+        a = dict(lg=FAKE, rs=152000, B=4, V=151936, dt=1, t=FAKE, n=None, out=FAKE)
+        a.update(kw)
+        return lib.pa_sample(a["lg"], a["rs"], a["B"], a["V"], a["dt"], a["t"], a["n"], ctypes.c_uint64(0),
+                             ctypes.c_uint64(0), a["out"], None, None)
+    assert call(dt=7) == -2
+    assert call(V=0) == -1
+    assert call(rs=1000) == -1                                # shorter than vocab
+    assert call(lg=ctypes.c_void_p((1 << 20) + 1)) == -1      # element alignment
+    assert call(dt=2, lg=ctypes.c_void_p((1 << 20) + 2)) == -1
+    assert call(t=None) == -1
+    assert call(B=0, lg=None, t=None, out=None) == 0

@@ -27,6 +27,11 @@ MUTANTS = {
     "bf16_shift_wrong": ("(uint32_t)h << 16;", "(uint32_t)h << 15;"),
     "f16_bias_wrong": ("e - 25);", "e - 24);"),
     "f16_subnormal_wrong": ("ldexpf((float)m, -24);", "ldexpf((float)m, -25);"),
+    "sample_noise_multiplies": ("const float score = p / (e > 1e-10f ? e : 1e-10f);",
+                                "const float score = p * (e > 1e-10f ? e : 1e-10f);"),
+    "sample_temperature_ignored": ("const float a = x / t;\n            if (!(a > -INFINITY))\n                continue;",
+                                   "const float a = x;\n            if (!(a > -INFINITY))\n                continue;"),
+    "sample_last_index_on_ties": ("if (score > best) {", "if (score >= best) {"),
     "minus_one_block_read_as_block_0": ("if (page < 0 || page >= num_blocks)\n            return -2;",
                                         "if (page >= num_blocks)\n            return -2;\n        if (page < 0) page = 0;"),
 }

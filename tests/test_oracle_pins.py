@@ -19,6 +19,12 @@ What pins what:
                 Lq rows of library causal attention over the whole contiguous
                 sequence (bottom-right alignment); Lq = 1 equals decode.
 * dtype      -- fp16/bf16 decoding matches numpy/torch on all 65536 words.
+* sample     -- unit noise gives the first argmax of the logits (closed form);
+                scores match a float64 evaluation of the pages' formula except
+                at near-ties; scaling logits and temperature by a power of two
+                changes nothing; -inf logits never win, T <= 1e-10 gives -1;
+                with Exp(1) noise the frequencies follow softmax(z / T)
+                (chi-square, the exponential-race theorem of the pages).
 """
 
 import math
@@ -293,11 +299,72 @@ def pin_half_decoding(lib):
         assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
 
 
+def _sample_rows(seed, B, V, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    logits = (3 * torch.randn(B, V, generator=g)).to(dtype)
+    temps = 0.3 + 1.5 * torch.rand(B, generator=g)
+    noise = torch.empty(B, V).exponential_(1, generator=g)
+    return logits, temps, noise
+
+
+def pin_sample_unit_noise_is_first_argmax(lib):
+    logits, temps, _ = _sample_rows(1, 40, 97)
+    logits[3, [5, 60]] = 50.0                     # a tie: the first index wins
+    for dt in (torch.float32, torch.bfloat16, torch.float16):
+        lg = logits.to(dt)
+        got = oracle.sample(lg, temps, torch.ones(40, 97), lib=lib)
+        ref = torch.tensor([int(np.argmax(row.float().numpy())) for row in lg], dtype=torch.int32)
+        assert torch.equal(got, ref), dt
+    assert int(oracle.sample(logits, temps, torch.ones(40, 97), lib=lib)[3]) == 5
+
+
+def pin_sample_matches_float64_formula(lib):
+    logits, temps, noise = _sample_rows(2, 300, 50)
+    got = oracle.sample(logits, temps, noise, lib=lib)
+    a = logits.double() / temps.double()[:, None]
+    p = torch.softmax(a, dim=-1)
+    score = p / noise.double().clamp_min(1e-10)
+    ref = score.argmax(dim=-1)
+    for b in torch.nonzero(got != ref.to(torch.int32)).flatten().tolist():
+        s1, s2 = float(score[b, got[b]]), float(score[b, ref[b]])
+        assert abs(s1 - s2) <= 1e-5 * s2, (b, s1, s2)  # only a near-tie may differ
+
+
+def pin_sample_power_of_two_scaling(lib):
+    logits, temps, noise = _sample_rows(3, 200, 64)
+    a = oracle.sample(logits, temps, noise, lib=lib)
+    b = oracle.sample(logits * 8, temps * 8, noise, lib=lib)
+    assert torch.equal(a, b)
+
+
+def pin_sample_masked_and_invalid(lib):
+    logits, temps, noise = _sample_rows(4, 30, 40)
+    logits[:, ::2] = float("-inf")
+    temps[7] = 0.0
+    got = oracle.sample(logits, temps, noise, lib=lib)
+    assert int(got[7]) == -1
+    ok = torch.arange(30) != 7
+    assert bool((got[ok] % 2 == 1).all())
+
+
+def pin_sample_frequencies_follow_softmax(lib):
+    V, N, T = 6, 120000, 0.8
+    z = torch.tensor([0.0, 1.0, 2.0, 4.0, -1.0, 3.0])
+    g = torch.Generator().manual_seed(5)
+    noise = torch.empty(N, V).exponential_(1, generator=g)
+    got = oracle.sample(z.repeat(N, 1), torch.full((N,), T), noise, lib=lib)
+    counts = torch.bincount(got.long(), minlength=V).double()
+    expect = torch.softmax(z.double() / T, dim=0) * N
+    chi2 = float(((counts - expect) ** 2 / expect).sum())
+    assert chi2 < 33.4, chi2  # 5 degrees of freedom: p < 1e-5 beyond this
+
+
 PINS = [pin_store_matches_index_put, pin_store_rejects_bad_slot, pin_decode_vs_library,
         pin_decode_permutation_invariance, pin_decode_sharing, pin_identical_keys_give_mean_of_v,
         pin_one_key_gives_v0, pin_two_three_keys_brute_force, pin_empty_context_gives_zeros,
         pin_bad_block_rejected, pin_prefill_vs_library, pin_prefill_single_query_equals_decode,
-        pin_half_decoding]
+        pin_half_decoding, pin_sample_unit_noise_is_first_argmax, pin_sample_matches_float64_formula,
+        pin_sample_power_of_two_scaling, pin_sample_masked_and_invalid, pin_sample_frequencies_follow_softmax]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
