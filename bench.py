@@ -69,7 +69,15 @@ WORKLOAD_CONFIG = {
     "mixed_chunked_prefill": dict(batch=128, prefill="8 x 512-token chunks over prefixes U[0,3584]",
                                   decode="120 sequences, context U[256,4096]", H_q=32, H_kv=8, D=128,
                                   block_size=256, dtype="bf16"),
+    "sampler_qwen3_vocab": dict(batch=64, vocab=151936, dtype="bf16", logits="3 * N(0,1)",
+                                temperature="U[0.5, 1.5]", noise="in-kernel Philox4x32-10, new offset per step"),
 }
+SAMPLER_METRIC = "temperature-sampling logits GB/s and rows/s on 1 GPU"
+# Warp instructions one pa_sample launch executes on the sampler workload (ncu
+# smsp__inst_executed.sum of sample_kernel, profiles/sample_sampler_qwen3_vocab.md): the
+# kernel is issue-bound (Philox4x32-10 and two accurate logarithms per vocabulary entry).
+SAMPLER_INSTRUCTIONS_PER_CALL = 11_920_704
+ISSUE_PER_SM_PER_CLK = 4  # warp instructions: four schedulers per SM
 
 
 def parse_args():
@@ -352,6 +360,30 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
+    if args.workload == "sampler_qwen3_vocab":
+        logits, temps = _sampler_inputs()
+        g = torch.Generator().manual_seed(13)
+        noise = torch.empty(1, logits.shape[1]).exponential_(1, generator=g)
+        step_bytes = logits.shape[1] * logits.element_size()
+        for i in range(args.warmup):
+            oracle.sample(logits[i % 64:i % 64 + 1], temps[i % 64:i % 64 + 1], noise)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            b = (args.warmup + i) % logits.shape[0]
+            oracle.sample(logits[b:b + 1], temps[b:b + 1], noise)
+        dt = time.perf_counter() - t0
+        value = args.steps * step_bytes / dt / 1e9
+        print(json.dumps({"metric": SAMPLER_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                          "data": "synthetic", "impl": "reference",
+                          "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+                                     "sample": "one row per step"},
+                          "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                           "sample": "one row of the workload per step"},
+                          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
     st = _decode_part(args.workload)
     p = st.pool
     kc, vc = p.k_cache.clone(), p.v_cache.clone()
@@ -384,7 +416,117 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def _sampler_inputs():
+    cfg = WORKLOAD_CONFIG["sampler_qwen3_vocab"]
+    g = torch.Generator().manual_seed(9)
+    logits = (3 * torch.randn(cfg["batch"], cfg["vocab"], generator=g)).to(torch.bfloat16)
+    temps = 0.5 + torch.rand(cfg["batch"], generator=g)
+    return logits, temps
+
+
+def sampler_cpu_baseline(seconds: float):
+    """The oracle sampler single-threaded on this host, row by row, with Exp(1) noise drawn by torch."""
+    import oracle
+    logits, temps = _sampler_inputs()
+    g = torch.Generator().manual_seed(11)
+    n, t_total = 0, 0.0
+    while t_total < seconds:
+        b = n % logits.shape[0]
+        noise = torch.empty(1, logits.shape[1]).exponential_(1, generator=g)
+        t0 = time.perf_counter()
+        oracle.sample(logits[b:b + 1], temps[b:b + 1], noise)
+        t_total += time.perf_counter() - t0
+        n += 1
+    nbytes = n * logits.shape[1] * logits.element_size()
+    return {"value": nbytes / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} rows of the workload sampled one at a time (noise drawn outside the timing), "
+                      f"single-threaded C oracle, {os.cpu_count()} host cores present"}
+
+
+def run_sampler(args, world, rank, local):
+    """pa_sample on 64 rows of a 151936-token vocabulary, in-kernel noise, a new offset every step."""
+    import paged_kv_cache_bs_gb300 as pa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    logits_h, temps_h = _sampler_inputs()
+    B, V = logits_h.shape
+    logits, temps = logits_h.to(dev), temps_h.to(dev)
+    tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = B * V * logits.element_size()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)  # the logits fit in L2
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        pa.sample(logits, temps, seed=1, offset=i, out=tokens)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world, local)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()                                      # L2 flushed between steps, outside the events
+        torch.cuda._sleep(PRE_STEP_SPIN_CYCLES)
+        ev[i][0].record(stream)
+        pa.sample(logits, temps, seed=1, offset=args.warmup + i, out=tokens)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, local)
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    ms_max = max_over_ranks(ms, world, dev)
+    # end to end: the logits from pinned host memory (one copy), the call, the tokens back
+    pin_l, pin_t, out_h = logits_h.pin_memory(), temps_h.pin_memory(), torch.empty(B, dtype=torch.int32).pin_memory()
+    Ke = min(K, 300)
+    e2e_s = 0.0
+    for i in range(Ke):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        logits.copy_(pin_l, non_blocking=True)
+        temps.copy_(pin_t, non_blocking=True)
+        pa.sample(logits, temps, seed=2, offset=i, out=tokens)
+        out_h.copy_(tokens, non_blocking=True)
+        stream.synchronize()
+        e2e_s += time.perf_counter() - t0
+    e2e_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    issue_peak = ISSUE_PER_SM_PER_CLK * sms * sm_mhz * 1e6
+    if SAMPLER_INSTRUCTIONS_PER_CALL:
+        achieved = SAMPLER_INSTRUCTIONS_PER_CALL / (ms / 1e3)
+        roof = {"bound": "alu", "kernel": "sample_kernel (Philox4x32-10 + two logf per entry, issue-bound)",
+                "achieved": achieved, "peak": issue_peak, "unit": "warp-instr/s", "frac": achieved / issue_peak,
+                "peak_source": f"derived: {ISSUE_PER_SM_PER_CLK} warp instructions/clock/SM x {sms} SMs x "
+                               f"{sm_mhz:.0f} MHz sampled", "traffic": nbytes,
+                "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    else:
+        roof = {"bound": "alu", "kernel": "sample_kernel", "achieved": None, "peak": issue_peak,
+                "unit": "warp-instr/s", "frac": None, "traffic": None,
+                "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    line = {
+        "metric": SAMPLER_METRIC, "value": world * nbytes / (ms_max / 1e3) / 1e9, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+                   "l2": "flushed (256 MB write) between steps, outside the timed events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "rows_per_s": world * B / (ms_max / 1e3),
+        "roofline": roof,
+        "cpu_baseline": sampler_cpu_baseline(args.cpu_seconds) if world == 1 and not args.no_cpu_baseline else None,
+        "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": nbytes + B * 4, "d2h_bytes_per_step": B * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, world, rank, local):
+    if args.workload == "sampler_qwen3_vocab":
+        return run_sampler(args, world, rank, local)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.workload == "mixed_chunked_prefill":
