@@ -47,6 +47,14 @@ def _declare(lib):
     lib.oracle_decode.restype = ci
     lib.oracle_prefill_paged.argtypes = [p, p, p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, f32, ci, p]
     lib.oracle_prefill_paged.restype = ci
+    lib.oracle_store_kv_fp8.argtypes = [p, p, i64, i64, p, p, p, i32, i32, i32, i32, i32, ci, f32, f32]
+    lib.oracle_store_kv_fp8.restype = ci
+    lib.oracle_decode_fp8.argtypes = [p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, f32, f32, f32, ci, p]
+    lib.oracle_decode_fp8.restype = ci
+    lib.oracle_e4m3_to_float.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_float.restype = f32
+    lib.oracle_float_to_e4m3.argtypes = [f32]
+    lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
     lib.oracle_sample.argtypes = [p, i64, i32, i32, i32, p, p, p]
     lib.oracle_sample.restype = ci
     lib.oracle_half_to_float.argtypes = [ctypes.c_uint16, ci]
@@ -147,4 +155,33 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
     rc = lib.oracle_sample(logits.data_ptr(), V, B, V, dt, temps.data_ptr(), noise.data_ptr(), out.data_ptr())
     if rc:
         raise OracleError(f"oracle_sample returned {rc}")
+    return out
+
+
+def store_kv_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale, lib=None) -> None:
+    """Quantizing store into uint8 E4M3 caches [N, bs, H_kv, D] (in place): e4m3(x / scale)."""
+    lib = lib or load()
+    T = slot_mapping.numel()
+    n, bs, hkv, d = k_cache.shape
+    assert k_cache.dtype == torch.uint8 and v_cache.dtype == torch.uint8
+    rc = lib.oracle_store_kv_fp8(k.data_ptr(), v.data_ptr(), k.stride(0), v.stride(0), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), slot_mapping.contiguous().data_ptr(), T, hkv, d, n, bs,
+                                 _DT[k.dtype], float(k_scale), float(v_scale))
+    if rc:
+        raise OracleError(f"oracle_store_kv_fp8 returned {rc}")
+
+
+def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale, lib=None) -> torch.Tensor:
+    """Decode over uint8 E4M3 caches, fp32 result [B, H_q, D]."""
+    lib = lib or load()
+    q = q.contiguous()
+    B, hq, d = q.shape
+    n, bs, hkv, _ = k_cache.shape
+    out = torch.empty(B, hq, d, dtype=torch.float32)
+    bt = block_tables.contiguous()
+    rc = lib.oracle_decode_fp8(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), bt.data_ptr(), bt.shape[1],
+                               context_lens.contiguous().data_ptr(), B, hq, hkv, d, n, bs, float(scale), float(k_scale),
+                               float(v_scale), _DT[q.dtype], out.data_ptr())
+    if rc:
+        raise OracleError(f"oracle_decode_fp8 returned {rc}")
     return out

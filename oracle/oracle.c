@@ -319,3 +319,124 @@ int oracle_sample(const void *logits, int64_t row_stride, int32_t batch, int32_t
     }
     return 0;
 }
+
+/* ------------------------------------------------------------ fp8 cache */
+
+/* OCP 8-bit floating point E4M3 ("fn": no infinities): sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals
+ * m/8 * 2^-6; S.1111.111 is NaN; the largest finite value is 448. */
+static float e4m3_to_float(uint8_t b)
+{
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    float v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexpf((float)m, -9);
+    else
+        v = ldexpf((float)(m + 8), e - 10);
+    return sign ? -v : v;
+}
+
+float oracle_e4m3_to_float(uint8_t b) { return e4m3_to_float(b); }
+
+/* Nearest E4M3 code to x, ties to the even code, saturating at +-448 (the
+ * fp8 KV cache's reading); NaN gives 0x7F.  Plain search over the 127
+ * non-negative finite codes. */
+static uint8_t float_to_e4m3(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const float a = fabsf(x);
+    int best = 0;
+    float best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const float d = fabsf(e4m3_to_float((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+uint8_t oracle_float_to_e4m3(float x) { return float_to_e4m3(x); }
+
+/* The store into an E4M3 pool with per-tensor scales: cache = e4m3(x / scale)
+ * (fp32 division, then the nearest code as above). */
+int oracle_store_kv_fp8(const uint16_t *k, const uint16_t *v, int64_t k_row_stride, int64_t v_row_stride,
+                        uint8_t *k_cache, uint8_t *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                        int dtype, float k_scale, float v_scale)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    const int64_t rows = (int64_t)num_blocks * block_size;
+    for (int32_t t = 0; t < num_tokens; ++t)
+        if (slot_mapping[t] < -1 || slot_mapping[t] >= rows)
+            return -1;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s == -1)
+            continue;
+        for (int64_t e = 0; e < row; ++e) {
+            k_cache[s * row + e] = float_to_e4m3(to_float(k[t * k_row_stride + e], dtype) / k_scale);
+            v_cache[s * row + e] = float_to_e4m3(to_float(v[t * v_row_stride + e], dtype) / v_scale);
+        }
+    }
+    return 0;
+}
+
+/* Decode over an E4M3 pool: gather the context dequantized (code value *
+ * scale, fp32), then the same attention as oracle_decode. */
+int oracle_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                      int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t num_blocks, int32_t block_size, float scale, float k_scale, float v_scale, int dtype,
+                      float *out)
+{
+    if (check_heads(num_q_heads, num_kv_heads, head_dim))
+        return -3;
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    int32_t max_len = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (context_lens[b] < 0)
+            return -4;
+        if (context_lens[b] > max_len)
+            max_len = context_lens[b];
+    }
+    float *kc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
+    float *vc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
+    float *s = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1));
+    float *qh = malloc(sizeof(float) * (size_t)head_dim);
+    float *res = malloc(sizeof(float) * (size_t)batch * num_q_heads * head_dim + 1);
+    int rc = (kc && vc && s && qh && res) ? 0 : -5;
+    for (int32_t b = 0; b < batch && !rc; ++b) {
+        const int32_t n = context_lens[b];
+        const int32_t *table = block_tables + (int64_t)b * max_blocks_per_seq;
+        for (int32_t j = 0; j < n && !rc; ++j) {
+            const int32_t logical = j / block_size;
+            if (logical >= max_blocks_per_seq || table[logical] < 0 || table[logical] >= num_blocks) {
+                rc = -2;
+                break;
+            }
+            const int64_t r = (int64_t)table[logical] * block_size + j % block_size;
+            for (int64_t e = 0; e < row; ++e) {
+                kc[j * row + e] = e4m3_to_float(k_cache[r * row + e]) * k_scale;
+                vc[j * row + e] = e4m3_to_float(v_cache[r * row + e]) * v_scale;
+            }
+        }
+        for (int32_t h = 0; h < num_q_heads && !rc; ++h) {
+            const uint16_t *qb = q + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                qh[d] = to_float(qb[d], dtype);
+            attend(qh, kc, vc, n, h / group, num_kv_heads, head_dim, scale, s,
+                   res + ((int64_t)b * num_q_heads + h) * head_dim);
+        }
+    }
+    if (!rc)
+        memcpy(out, res, sizeof(float) * (size_t)batch * num_q_heads * head_dim);
+    free(kc); free(vc); free(s); free(qh); free(res);
+    return rc;
+}

@@ -32,6 +32,13 @@ MUTANTS = {
     "sample_temperature_ignored": ("const float a = x / t;\n            if (!(a > -INFINITY))\n                continue;",
                                    "const float a = x;\n            if (!(a > -INFINITY))\n                continue;"),
     "sample_last_index_on_ties": ("if (score > best) {", "if (score >= best) {"),
+    "e4m3_bias_wrong": ("v = ldexpf((float)(m + 8), e - 10);", "v = ldexpf((float)(m + 8), e - 9);"),
+    "e4m3_subnormal_wrong": ("v = ldexpf((float)m, -9);", "v = ldexpf((float)m, -10);"),
+    "e4m3_ties_to_odd": ("(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)"),
+    "fp8_store_multiplies_scale": ("float_to_e4m3(to_float(k[t * k_row_stride + e], dtype) / k_scale)",
+                                   "float_to_e4m3(to_float(k[t * k_row_stride + e], dtype) * k_scale)"),
+    "fp8_decode_drops_v_scale": ("vc[j * row + e] = e4m3_to_float(v_cache[r * row + e]) * v_scale;",
+                                 "vc[j * row + e] = e4m3_to_float(v_cache[r * row + e]);"),
     "minus_one_block_read_as_block_0": ("if (page < 0 || page >= num_blocks)\n            return -2;",
                                         "if (page >= num_blocks)\n            return -2;\n        if (page < 0) page = 0;"),
 }

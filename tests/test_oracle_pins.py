@@ -19,6 +19,13 @@ What pins what:
                 Lq rows of library causal attention over the whole contiguous
                 sequence (bottom-right alignment); Lq = 1 equals decode.
 * dtype      -- fp16/bf16 decoding matches numpy/torch on all 65536 words.
+* fp8 cache  -- E4M3 decoding equals torch's float8_e4m3fn on all 256 codes;
+                encoding equals torch's rounding (nearest, ties to even) on
+                random values and on every midpoint, and saturates at +-448;
+                the quantizing store equals torch's conversion of x / scale;
+                fp8 decode with power-of-two scales is bit-identical to the
+                16-bit decode on the dequantized cache, and matches library
+                attention on the dequantized values for any scales.
 * sample     -- unit noise gives the first argmax of the logits (closed form);
                 scores match a float64 evaluation of the pages' formula except
                 at near-ties; scaling logits and temperature by a power of two
@@ -359,12 +366,90 @@ def pin_sample_frequencies_follow_softmax(lib):
     assert chi2 < 33.4, chi2  # 5 degrees of freedom: p < 1e-5 beyond this
 
 
+def pin_e4m3_decoding(lib):
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float()
+    got = torch.tensor([lib.oracle_e4m3_to_float(int(c)) for c in codes])
+    nan = torch.isnan(ref)
+    assert torch.equal(torch.isnan(got), nan) and torch.equal(got[~nan], ref[~nan])
+
+
+def pin_e4m3_encoding(lib):
+    vals = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    mids = (vals[:-1] + vals[1:]) / 2                    # exact ties: nearest-even decides
+    g = torch.Generator().manual_seed(6)
+    rnd = (torch.randn(4000, generator=g) * 60).clamp(-448, 448)
+    for x in (mids, -mids, rnd, torch.tensor([0.0, -0.0, 1e-9, -1e-9])):
+        ref = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        got = torch.tensor([lib.oracle_float_to_e4m3(float(v)) for v in x], dtype=torch.uint8)
+        assert torch.equal(got, ref)
+    assert lib.oracle_float_to_e4m3(1000.0) == 0x7E and lib.oracle_float_to_e4m3(-5e5) == 0xFE  # +-448
+    assert lib.oracle_float_to_e4m3(float("nan")) == 0x7F
+
+
+def _fp8_step(seed, bs=16, hkv=2, hq=8, d=64, ctx=(40, 1, 130), dtype=torch.bfloat16):
+    st = inputs.make_decode(list(ctx), num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs, dtype=dtype,
+                            seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    kc = torch.randint(0, 255, st.pool.k_cache.shape, generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 255, st.pool.v_cache.shape, generator=g, dtype=torch.uint8)
+    kc[kc == 0x7F] = 0
+    vc[vc == 0x7F] = 0
+    kc[kc == 0xFF] = 0
+    vc[vc == 0xFF] = 0
+    return st, kc, vc
+
+
+def pin_store_fp8_matches_torch(lib):
+    st, kc, vc = _fp8_step(61)
+    ks, vs = 0.37, 1.9
+    k0, v0 = kc.clone(), vc.clone()
+    oracle.store_kv_fp8(st.k_new, st.v_new, kc, vc, st.slot_mapping, ks, vs, lib=lib)
+    rk, rv = k0.view(-1, k0.shape[2], k0.shape[3]), v0.view(-1, v0.shape[2], v0.shape[3])
+    rows = st.slot_mapping.long()
+    keep = rows >= 0
+    rk[rows[keep]] = (st.k_new.float()[keep] / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+    rv[rows[keep]] = (st.v_new.float()[keep] / vs).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(kc, k0) and torch.equal(vc, v0)
+
+
+def pin_decode_fp8_power_of_two_scales_equals_16bit_decode(lib):
+    st, kc, vc = _fp8_step(62)
+    ks, vs = 0.25, 4.0
+    deq_k = (kc.view(torch.float8_e4m3fn).float() * ks).to(torch.bfloat16)
+    deq_v = (vc.view(torch.float8_e4m3fn).float() * vs).to(torch.bfloat16)
+    a = oracle.decode_fp8(st.q, kc, vc, st.block_tables, st.context_lens, st.scale, ks, vs, lib=lib)
+    b = oracle.decode(st.q, deq_k, deq_v, st.block_tables, st.context_lens, st.scale, lib=lib)
+    assert torch.equal(a, b)
+
+
+def pin_decode_fp8_vs_library(lib):
+    st, kc, vc = _fp8_step(63, ctx=(77, 300, 5))
+    ks, vs = 0.0731, 2.33
+    got = oracle.decode_fp8(st.q, kc, vc, st.block_tables, st.context_lens, st.scale, ks, vs, lib=lib)
+    deq_k = kc.view(torch.float8_e4m3fn).double() * ks
+    deq_v = vc.view(torch.float8_e4m3fn).double() * vs
+    p = st.pool
+    for b in range(st.batch):
+        n = int(st.context_lens[b])
+        rows = [inputs.slot_of(p.tables[b], p.block_size, j) for j in range(n)]
+        K = deq_k.view(-1, p.num_kv_heads, p.head_dim)[rows]
+        V = deq_v.view(-1, p.num_kv_heads, p.head_dim)[rows]
+        group = st.q.shape[1] // p.num_kv_heads
+        for h in range(st.q.shape[1]):
+            s = (st.q[b, h].double() @ K[:, h // group].T) * st.scale
+            ref = torch.softmax(s, dim=0) @ V[:, h // group]
+            assert float((got[b, h].double() - ref).abs().max()) < 1e-4 * max(1.0, float(ref.abs().max()))
+
+
 PINS = [pin_store_matches_index_put, pin_store_rejects_bad_slot, pin_decode_vs_library,
         pin_decode_permutation_invariance, pin_decode_sharing, pin_identical_keys_give_mean_of_v,
         pin_one_key_gives_v0, pin_two_three_keys_brute_force, pin_empty_context_gives_zeros,
         pin_bad_block_rejected, pin_prefill_vs_library, pin_prefill_single_query_equals_decode,
         pin_half_decoding, pin_sample_unit_noise_is_first_argmax, pin_sample_matches_float64_formula,
-        pin_sample_power_of_two_scaling, pin_sample_masked_and_invalid, pin_sample_frequencies_follow_softmax]
+        pin_sample_power_of_two_scaling, pin_sample_masked_and_invalid, pin_sample_frequencies_follow_softmax,
+        pin_e4m3_decoding, pin_e4m3_encoding, pin_store_fp8_matches_torch,
+        pin_decode_fp8_power_of_two_scales_equals_16bit_decode, pin_decode_fp8_vs_library]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
