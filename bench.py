@@ -69,6 +69,8 @@ WORKLOAD_CONFIG = {
     "mixed_chunked_prefill": dict(batch=128, prefill="8 x 512-token chunks over prefixes U[0,3584]",
                                   decode="120 sequences, context U[256,4096]", H_q=32, H_kv=8, D=128,
                                   block_size=256, dtype="bf16"),
+    "qwen3_0p6b_decode_fp8": dict(batch=64, context="U[128,4096]", H_q=16, H_kv=8, D=128, block_size=256,
+                                  dtype="e4m3 KV (per-tensor scales), bf16 q/out", pool="1.25x need, shuffled"),
     "sampler_qwen3_vocab": dict(batch=64, vocab=151936, dtype="bf16", logits="3 * N(0,1)",
                                 temperature="U[0.5, 1.5]", noise="in-kernel Philox4x32-10, new offset per step"),
 }
@@ -237,6 +239,49 @@ class DecodeWorkload:
         out_host.copy_(self.out, non_blocking=True)
 
 
+class Fp8DecodeWorkload(DecodeWorkload):
+    """A decode step over an E4M3 pool: pa_store_kv_fp8 of one token per sequence,
+    then pa_decode_fp8 (split-K partitions + merge)."""
+
+    def __init__(self, name: str, dev: torch.device):
+        from tests import inputs
+        import paged_kv_cache_bs_gb300 as pa
+        self.pa = pa
+        self.name = name
+        fs = inputs.WORKLOADS[name]()
+        self.fs, self.st = fs, fs.step
+        st = fs.step
+        p = st.pool
+        self.dev = dev
+        self.kc, self.vc = fs.k_cache.to(dev), fs.v_cache.to(dev)
+        self.host = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "slot_mapping": st.slot_mapping,
+                     "block_tables": st.block_tables, "context_lens": st.context_lens}
+        self.inputs, self.d, self.layout = pack_inputs(self.host, dev)
+        self.out = torch.empty_like(self.d["q"])
+        nbytes = pa.decode_fp8_workspace_bytes(st.batch, st.num_q_heads, p.num_kv_heads, p.head_dim,
+                                               st.block_tables.shape[1], p.block_size)
+        self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.kv_bytes = fs.kv_bytes()
+        self.kv_unique_bytes = self.kv_bytes
+        self.batch = st.batch
+        row = p.num_kv_heads * p.head_dim
+        # k and v: 16-bit rows read, one-byte codes written
+        self.store_bytes = 2 * int((st.slot_mapping >= 0).sum()) * row * (st.q.element_size() + 1)
+        self.prefill_flops = 0
+        self.fused = False
+        self.launches_per_step = 3   # quantising store, decode partitions, log-sum-exp merge
+        self.phases = [("store", self.store), ("decode", self.attend)]
+
+    def store(self):
+        d, fs = self.d, self.fs
+        self.pa.store_kv_fp8(d["k_new"], d["v_new"], self.kc, self.vc, d["slot_mapping"], fs.k_scale, fs.v_scale)
+
+    def attend(self):
+        d, fs = self.d, self.fs
+        self.pa.decode_fp8(d["q"], self.kc, self.vc, d["block_tables"], d["context_lens"], self.st.scale,
+                           fs.k_scale, fs.v_scale, out=self.out, workspace=self.ws)
+
+
 class MixedWorkload(DecodeWorkload):
     """A mixed chunked-prefill step over one pool: store of every new token
     (prefill chunks and decode tokens), causal prefill of the chunks over
@@ -330,21 +375,40 @@ def _decode_part(name: str):
     return st.decode if hasattr(st, "decode") else st
 
 
+def _oracle_step(name: str):
+    """(decode step, fn(b), K + V bytes of one context token): the oracle's store + decode
+    of sequence b of the workload."""
+    import oracle
+    st = _decode_part(name)
+    if hasattr(st, "step"):  # E4M3 pool
+        fs, st = st, st.step
+        kc, vc = fs.k_cache.clone(), fs.v_cache.clone()
+
+        def step(b):
+            sl = slice(b, b + 1)
+            oracle.store_kv_fp8(st.k_new[sl], st.v_new[sl], kc, vc, st.slot_mapping[sl], fs.k_scale, fs.v_scale)
+            oracle.decode_fp8(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale, fs.k_scale,
+                              fs.v_scale)
+        return st, step, 2 * st.pool.num_kv_heads * st.pool.head_dim  # one byte per element
+    p = st.pool
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+
+    def step(b):
+        sl = slice(b, b + 1)
+        oracle.store_kv(st.k_new[sl], st.v_new[sl], kc, vc, st.slot_mapping[sl])
+        oracle.decode(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale)
+    return st, step, 2 * p.num_kv_heads * p.head_dim * st.q.element_size()
+
+
 def cpu_baseline(name: str, seconds: float):
     """The oracle as it stands, single-threaded on this host: store + decode of
     the workload's sequences one at a time until the time budget is spent."""
-    import oracle
-    st = _decode_part(name)
-    p = st.pool
-    kc, vc = p.k_cache.clone(), p.v_cache.clone()
-    row = 2 * p.num_kv_heads * p.head_dim * st.q.element_size()
+    st, step, row = _oracle_step(name)
     done_bytes, n, t_total = 0, 0, 0.0
     while t_total < seconds:          # whole passes over the batch until the budget is spent
         b = n % st.batch
-        sl = slice(b, b + 1)
         t0 = time.perf_counter()
-        oracle.store_kv(st.k_new[sl], st.v_new[sl], kc, vc, st.slot_mapping[sl])
-        oracle.decode(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale)
+        step(b)
         t_total += time.perf_counter() - t0
         done_bytes += int(st.context_lens[b]) * row
         n += 1
@@ -384,17 +448,11 @@ def run_reference(args, world, rank):
                           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}), flush=True)
         return
-    st = _decode_part(args.workload)
-    p = st.pool
-    kc, vc = p.k_cache.clone(), p.v_cache.clone()
-    oracle.store_kv(st.k_new, st.v_new, kc, vc, st.slot_mapping)
-    row = 2 * p.num_kv_heads * p.head_dim * st.q.element_size()
+    st, one, row = _oracle_step(args.workload)
 
     def step(i):
         b = i % st.batch
-        sl = slice(b, b + 1)
-        oracle.store_kv(st.k_new[sl], st.v_new[sl], kc, vc, st.slot_mapping[sl])
-        oracle.decode(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale)
+        one(b)
         return int(st.context_lens[b]) * row
 
     for i in range(args.warmup):
@@ -531,6 +589,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     if args.workload == "mixed_chunked_prefill":
         w = MixedWorkload(args.workload, dev)
+    elif args.workload.endswith("_fp8"):
+        w = Fp8DecodeWorkload(args.workload, dev)
     else:
         w = DecodeWorkload(args.workload, dev, fused=not args.unfused)
     flush_needed = w.kv_unique_bytes < 2 * L2_BYTES
@@ -615,7 +675,9 @@ def run_ours(args, world, rank, local):
         # are counted once; for unshared workloads this equals the logical KV bytes)
         unique_gbs = w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9
         kern = ("pa_store_decode (store fused into the split-K partition kernel + merge)"
-                if "store+decode" in phase_ms else "pa_decode (split-K partitions + merge)")
+                if "store+decode" in phase_ms else
+                "pa_decode_fp8 (E4M3 split-K partitions + merge)" if isinstance(w, Fp8DecodeWorkload) else
+                "pa_decode (split-K partitions + merge)")
         roof = {"bound": "hbm", "kernel": kern, "achieved": unique_gbs,
                 "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": unique_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",

@@ -8,13 +8,17 @@
  *                     context (split-K over context partitions)
  *   pa_prefill_paged  chunked prefill: new query tokens attending causally over
  *                     a cached paged prefix plus themselves
+ * plus the decode step's store fused into decode (pa_store_decode), the same
+ * store and decode over an FP8 pool (pa_store_kv_fp8, pa_decode_fp8) and the
+ * sampler that turns the step's logits into tokens (pa_sample).
  *
  * Conventions shared by every call
  *   - All tensor arguments are DEVICE pointers to caller-owned memory; the
  *     library allocates nothing and keeps no state besides cached device
  *     properties.  Integer size arguments are host values.
  *   - Element type: PA_F16 or PA_BF16 (IEEE binary16 / bfloat16) for every
- *     q/k/v/cache/out buffer of a call.  Arithmetic is fp32.
+ *     q/k/v/cache/out buffer of a call (the pool of the *_fp8 calls is E4M3).
+ *     Arithmetic is fp32.
  *   - The pool of one layer is two buffers k_cache and v_cache, each
  *     [num_blocks, block_size, num_kv_heads, head_dim] contiguous: physical
  *     block b, token offset o, kv head g, dim d is element
@@ -60,8 +64,11 @@
 extern "C" {
 #endif
 
-/* PA_F32 is accepted only for the logits of pa_sample. */
-typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+/* PA_F32 is accepted only for the logits of pa_sample; PA_E4M3 (one byte,
+ * OCP FP8 E4M3: bias 7, no infinities, 0x7F / 0xFF NaN, largest finite 448)
+ * only as the element type of an fp8 pool, which the *_fp8 calls take
+ * implicitly. */
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_E4M3 = 3 } pa_dtype;
 
 enum {
     PA_OK = 0,
@@ -212,6 +219,56 @@ PA_API int pa_decode_static_workspace(const void *q, int64_t q_row_stride, const
                                       int32_t head_dim, int32_t num_blocks, int32_t block_size,
                                       float scale, void *out, pa_dtype dtype, int32_t *err_flag,
                                       void *stream);
+
+/*
+ * FP8 pools.  "Inference engine: inside nano-vLLM" (Appendix B, the KV cache
+ * sizing) lists fp8 (1 byte) beside fp16 (2 bytes) as the cache's element
+ * type, which halves a pool's bytes and with them what decode streams.  The
+ * pages fix no format; this library's reading: the pool holds E4M3 codes
+ * (PA_E4M3 above) in the same [num_blocks, block_size, num_kv_heads,
+ * head_dim] layout, one byte per element, with one fp32 scale per tensor for K
+ * and one for V: element x is stored as the E4M3 code nearest to x / scale
+ * (ties to the even code, saturating at +-448) and read back as
+ * code_value * scale.  The scales are the caller's (e.g. calibrated amax / 448).
+ */
+
+/*
+ * pa_store_kv_fp8 -- pa_store_kv into an E4M3 pool: the same slot mapping,
+ * padding (-1) and error rules, each element quantised as above (fp32
+ * division by the scale, round to nearest even, saturating; NaN stays NaN).
+ *   k, v          16-bit rows of dtype (PA_F16 / PA_BF16) as pa_store_kv.
+ *   k_cache/v_cache  E4M3 pool, one byte per element, written in place.
+ *   k_scale, v_scale  finite and > 0.
+ *   num_kv_heads*head_dim and the row strides multiples of 8; k and v
+ *   16-byte aligned, the caches 8-byte aligned (16-byte and 8-byte vectors).
+ * The result equals the element-wise rule exactly (bit-exact codes).
+ */
+PA_API int pa_store_kv_fp8(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                    void *k_cache, void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                    pa_dtype dtype, float k_scale, float v_scale, int32_t *err_flag, void *stream);
+
+/* pa_decode_fp8_workspace_bytes -- as pa_decode_workspace_bytes, for pa_decode_fp8. */
+PA_API size_t pa_decode_fp8_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_blocks_per_seq, int32_t block_size);
+
+/*
+ * pa_decode_fp8 -- pa_decode over an E4M3 pool: the same attention with
+ * K_j = k_code * k_scale and V_j = v_code * v_scale.
+ *   q, out        dtype (PA_F16 / PA_BF16), as pa_decode.
+ *   k_cache/v_cache  E4M3 pool, 16-byte aligned.
+ *   workspace     at least pa_decode_fp8_workspace_bytes(...) bytes.
+ *   other arguments: as pa_decode.
+ * head_dim must be 128 (PA_ERR_UNSUPPORTED otherwise).  The codes are
+ * widened to fp16 (exactly) for the tensor-core products, q is converted to
+ * fp16 (exact for bf16 values of magnitude in [2^-14, 65504]), P is rounded
+ * to fp16 and the scales are applied to the fp32 scores and outputs.
+ */
+PA_API int pa_decode_fp8(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                  int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t num_blocks, int32_t block_size, float scale, float k_scale, float v_scale, void *out,
+                  void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag, void *stream);
 
 /*
  * pa_prefill_paged -- causal varlen prefill over a paged prefix.

@@ -11,6 +11,8 @@ The functions mirror the C ABI in ``include/pa_api.h``:
 * :func:`store_kv`       -- ``pa_store_kv``
 * :func:`decode`         -- ``pa_decode`` (+ ``pa_decode_workspace_bytes``)
 * :func:`store_decode`   -- ``pa_store_decode`` (the decode step's store fused into decode)
+* :func:`store_kv_fp8`   -- ``pa_store_kv_fp8`` (quantising store into an E4M3 pool)
+* :func:`decode_fp8`     -- ``pa_decode_fp8`` (+ ``pa_decode_fp8_workspace_bytes``)
 * :func:`prefill_paged`  -- ``pa_prefill_paged``
 * :func:`sample`         -- ``pa_sample`` (temperature sampling, exponential race)
 """
@@ -43,13 +45,22 @@ _lib.pa_decode.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i3
 _lib.pa_store_decode.restype = ctypes.c_int
 _lib.pa_store_decode.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                  _i32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
+_lib.pa_store_kv_fp8.restype = ctypes.c_int
+_lib.pa_store_kv_fp8.argtypes = [_p, _p, _i64, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _f32,
+                                 _p, _p]
+_lib.pa_decode_fp8_workspace_bytes.restype = _sz
+_lib.pa_decode_fp8_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+_lib.pa_decode_fp8.restype = ctypes.c_int
+_lib.pa_decode_fp8.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _p,
+                               _p, _sz, ctypes.c_int, _p, _p]
 _lib.pa_sample.restype = ctypes.c_int
 _lib.pa_sample.argtypes = [_p, _i64, _i32, _i32, ctypes.c_int, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
 _lib.pa_prefill_paged.restype = ctypes.c_int
 _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32,
                                   _i32, _i32, _f32, _p, ctypes.c_int, _p, _p]
 
-PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+PA_F16, PA_BF16, PA_F32, PA_E4M3 = 0, 1, 2, 3
+_FP8_POOL = (torch.uint8, torch.float8_e4m3fn)  # E4M3 codes, one byte per element
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_INTERNAL, FLAG_BAD_VALUE = 1, 2, 4, 8, 16, 32
 
@@ -215,6 +226,59 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     return out
 
 
+def _fp8_pool(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    if k_cache.dtype not in _FP8_POOL or v_cache.dtype not in _FP8_POOL:
+        raise TypeError("an fp8 pool holds E4M3 codes: torch.uint8 or torch.float8_e4m3fn")
+    return _cache_shape(k_cache, v_cache)
+
+
+def store_kv_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+                 err_flag: torch.Tensor | None = None) -> None:
+    """Quantise rows of k/v ([T, H_kv, D], fp16/bf16) to E4M3 codes (x / scale, nearest even,
+    saturating) into the fp8 pool at ``slot_mapping`` (int32; -1 skips)."""
+    n, bs, hkv, d = _fp8_pool(k_cache, v_cache)
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int32")
+    if k.shape[0] != slot_mapping.numel() or v.shape[0] != slot_mapping.numel():
+        raise ValueError("k/v rows must match slot_mapping")
+    if k.shape[1:] != (hkv, d) or v.shape[1:] != (hkv, d):
+        raise ValueError("k/v must be [T, H_kv, D] matching the cache")
+    if k.dtype != v.dtype:
+        raise TypeError("k and v must have one dtype")
+    rc = _lib.pa_store_kv_fp8(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(slot_mapping), slot_mapping.numel(), hkv, d, n, bs, _dtype(k), float(k_scale),
+                              float(v_scale), _ptr(err_flag), _stream(k_cache))
+    _check("pa_store_kv_fp8", rc)
+
+
+def decode_fp8_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               max_blocks_per_seq: int, block_size: int) -> int:
+    return int(_lib.pa_decode_fp8_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                  block_size))
+
+
+def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+               out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """Paged decode over an fp8 pool (K = code * k_scale, V = code * v_scale): q [B, H_q, D] -> out."""
+    _fp8_pool(k_cache, v_cache)
+    n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    B, hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        nbytes = decode_fp8_workspace_bytes(B, hq, hkv, d, block_tables.shape[1], bs)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    rc = _lib.pa_decode_fp8(_ptr(q), _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale),
+                            float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag), _stream(q))
+    _check("pa_decode_fp8", rc)
+    return out
+
+
 def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor | None = None, seed: int = 0,
            offset: int = 0, out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
     """One token per row of logits [B, V] (fp32/bf16/fp16): argmax of softmax(logits / T) / max(E, 1e-10),
@@ -237,6 +301,7 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
     return out
 
 
-__all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "sample", "decode_workspace_bytes", "alloc_decode_workspace",
-           "library", "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
+__all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
+           "decode_workspace_bytes", "decode_fp8_workspace_bytes", "alloc_decode_workspace", "library",
+           "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "PA_E4M3", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
            "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL", "FLAG_BAD_VALUE"]

@@ -39,6 +39,10 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <type_traits>
+
+#include <cuda_fp8.h>
+
 #include "tc_common.cuh"
 
 namespace pa {
@@ -50,7 +54,9 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTile = 64;      // tokens per pipeline stage, 16 per consumer warp
 // Ring depth: 3 stages with 2 CTAs per SM, or 2 stages with 3 CTAs per SM
 // (more producers issuing when pages are short and a tile takes many boxes).
-template <int ST> constexpr int ctas_per_sm() { return ST == 2 ? 3 : 2; }
+// An E4M3 pool halves the tile, so its kernel keeps 3 stages with 3 CTAs per SM.
+template <int ST, bool F8 = false> constexpr int ctas_per_sm() { return (ST == 2 || F8) ? 3 : 2; }
+constexpr int kF8Stages = 3;
 constexpr int kMaxTablePages = 257;  // block-table entries one partition may touch
 constexpr int kMaxPartition = 2048;
 constexpr int kMinPartition = 128;
@@ -84,15 +90,17 @@ struct DecodeArgs {
     int64_t k_new_stride, v_new_stride;  // elements between sequences' rows
     void *k_cache_w;
     void *v_cache_w;
+    float v_scale;  // E4M3 pool: V = code * v_scale (1 for 16-bit pools)
 };
 
 // Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
 // every slice 1024-byte aligned for the swizzle), then the block-table slice,
 // the mbarriers and the abort word.  After the loop the ring holds the warps'
 // partial outputs for the merge.
-template <int D, int ST> struct Shape {
+template <int D, int ST, bool F8 = false> struct Shape {
     static constexpr int kStages = ST;
-    static constexpr int kSlices = D / 64;
+    static constexpr int kRowBytes = F8 ? D : 2 * D;  // one kv head's row
+    static constexpr int kSlices = kRowBytes / 128;
     static constexpr int kSliceBytes = kTile * 128;
     static constexpr int kTileBytes = kSlices * kSliceBytes;
     static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
@@ -150,11 +158,29 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
     return (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <typename T, int D, int ST>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
+// Two E4M3 codes (low byte first) as an fp16 pair (low half first): exact,
+// every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// F8: the pool holds E4M3 codes (one byte per element, D = 128).  K and V are
+// converted to fp16 in registers and the warp MMAs run in fp16 (q converted
+// once).  ldmatrix moves 16-bit units, i.e. pairs of codes, so the fragments
+// use the contraction index in a fixed permutation, applied alike to both
+// operands: for S^T = K Q^T, k-step ks and lane quad j = lane % 4 hold
+// d = 16 ks + 4j + {0, 1} (fragment k = 2j, 2j+1) and 16 ks + 4j + {2, 3}
+// (k = 2j + 8, 2j + 9); for O^T = V^T P^T, row m = lane / 4 of block mt is
+// d = 16 mt + 2m and row m + 8 is d = 16 mt + 2m + 1 (the transposed load
+// gives each lane two tokens of two neighbouring d; one byte permutation
+// splits them by d).
+template <typename T, int D, int ST, bool F8>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a) {
-    using S = Shape<D, ST>;
+    using S = Shape<D, ST, F8>;
+    using MT = typename std::conditional<F8, __half, T>::type;  // MMA operand type
     constexpr int kStages = ST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,8 +252,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) {
             if (hq < a.group && warp < kConsumerWarps) {
-                qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + dq);
-                qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + dq);
+                if constexpr (F8) {  // d = 16 ks + 4j + {0..3}, as fp16
+                    const T *qd = qrow + ks * 16 + 2 * dq;
+                    qb[ks][0] = Dt<__half>::pack(static_cast<float>(qd[0]), static_cast<float>(qd[1]));
+                    qb[ks][1] = Dt<__half>::pack(static_cast<float>(qd[2]), static_cast<float>(qd[3]));
+                } else {
+                    qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + dq);
+                    qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + dq);
+                }
             } else {
                 qb[ks][0] = qb[ks][1] = 0u;
             }
@@ -243,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
     int issued = 0;                                             // tiles the producer started
 
     if (warp == kProducerWarp) {
-        if (a.slot_mapping && end == L) store_new_row<T, D>(a, b, g, L, lane);
+        if constexpr (!F8)
+            if (a.slot_mapping && end == L) store_new_row<T, D>(a, b, g, L, lane);
         if (lane == 0) {
             const int box_rows = min(1 << a.log2_bs, kTile);
             const int bs_mask = (1 << a.log2_bs) - 1;
@@ -257,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
                 const int tile_start = start + t * kTile;
                 const int nbox = (min(kTile, end - tile_start) + box_rows - 1) / box_rows;
                 const uint32_t full = bars + 8 * s;
-                tc::mbar_arrive_expect_tx(full, nbox * box_rows * D * 2 * 2);
+                tc::mbar_arrive_expect_tx(full, nbox * box_rows * S::kRowBytes * 2);
                 const uint32_t kdst = ring + s * S::kStageBytes;
                 const uint32_t vdst = kdst + S::kTileBytes;
                 for (int i = 0; i < nbox; ++i) {
@@ -266,8 +299,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
                     const uint32_t row_off = i * box_rows * 128;
 #pragma unroll
                     for (int h = 0; h < S::kSlices; ++h) {
-                        tc::tma_load_2d(kdst + h * S::kSliceBytes + row_off, &tm_k, g * D + h * 64, y, full);
-                        tc::tma_load_2d(vdst + h * S::kSliceBytes + row_off, &tm_v, g * D + h * 64, y, full);
+                        const int x = g * D + h * (F8 ? 128 : 64);  // elements: 128 bytes per slice
+                        tc::tma_load_2d(kdst + h * S::kSliceBytes + row_off, &tm_k, x, y, full);
+                        tc::tma_load_2d(vdst + h * S::kSliceBytes + row_off, &tm_v, x, y, full);
                     }
                 }
                 issued = t + 1;
@@ -287,12 +321,41 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
             const uint32_t kb = ring + s * S::kStageBytes;
             const uint32_t vb = kb + S::kTileBytes;
             uint32_t kf[S::kKSteps][4], vf[S::kKSteps][4];
+            if constexpr (F8) {
+                // one x4 load covers two 16-byte d chunks of the warp's 16 tokens
 #pragma unroll
-            for (int ks = 0; ks < S::kKSteps; ++ks)
-                ldmatrix_x4(kb + tile_off(rk, ks * 2 + ck), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+                for (int kp = 0; kp < S::kKSteps / 2; ++kp) {
+                    uint32_t r0, r1, r2, r3;
+                    ldmatrix_x4(kb + tile_off(rk, kp * 2 + ck), r0, r1, r2, r3);
+                    kf[2 * kp][0] = e4m3x2_to_f16x2(r0);
+                    kf[2 * kp][1] = e4m3x2_to_f16x2(r1);
+                    kf[2 * kp][2] = e4m3x2_to_f16x2(r0 >> 16);
+                    kf[2 * kp][3] = e4m3x2_to_f16x2(r1 >> 16);
+                    kf[2 * kp + 1][0] = e4m3x2_to_f16x2(r2);
+                    kf[2 * kp + 1][1] = e4m3x2_to_f16x2(r3);
+                    kf[2 * kp + 1][2] = e4m3x2_to_f16x2(r2 >> 16);
+                    kf[2 * kp + 1][3] = e4m3x2_to_f16x2(r3 >> 16);
+                    ldmatrix_x4_trans(vb + tile_off(rk, kp * 2 + ck), r0, r1, r2, r3);
+                    // bytes (token 2j, d 2m), (2j, 2m+1), (2j+1, 2m), (2j+1, 2m+1) -> split by d
+                    const uint32_t p0 = __byte_perm(r0, 0, 0x3120), p1 = __byte_perm(r1, 0, 0x3120);
+                    const uint32_t p2 = __byte_perm(r2, 0, 0x3120), p3 = __byte_perm(r3, 0, 0x3120);
+                    vf[2 * kp][0] = e4m3x2_to_f16x2(p0);
+                    vf[2 * kp][1] = e4m3x2_to_f16x2(p0 >> 16);
+                    vf[2 * kp][2] = e4m3x2_to_f16x2(p1);
+                    vf[2 * kp][3] = e4m3x2_to_f16x2(p1 >> 16);
+                    vf[2 * kp + 1][0] = e4m3x2_to_f16x2(p2);
+                    vf[2 * kp + 1][1] = e4m3x2_to_f16x2(p2 >> 16);
+                    vf[2 * kp + 1][2] = e4m3x2_to_f16x2(p3);
+                    vf[2 * kp + 1][3] = e4m3x2_to_f16x2(p3 >> 16);
+                }
+            } else {
 #pragma unroll
-            for (int mt = 0; mt < S::kKSteps; ++mt)
-                ldmatrix_x4_trans(vb + tile_off(rv, mt * 2 + cv), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+                for (int ks = 0; ks < S::kKSteps; ++ks)
+                    ldmatrix_x4(kb + tile_off(rk, ks * 2 + ck), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+#pragma unroll
+                for (int mt = 0; mt < S::kKSteps; ++mt)
+                    ldmatrix_x4_trans(vb + tile_off(rv, mt * 2 + cv), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+            }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bars + 8 * (kStages + s));  // stage free for the next tile
 
@@ -300,9 +363,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < S::kKSteps; ks += 2) {
-                Mma<T>::run(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qb[ks][0], qb[ks][1]);
-                Mma<T>::run(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3], qb[ks + 1][0],
-                            qb[ks + 1][1]);
+                Mma<MT>::run(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qb[ks][0], qb[ks][1]);
+                Mma<MT>::run(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3], qb[ks + 1][0],
+                             qb[ks + 1][1]);
             }
             // lane holds tokens lane/4 (s0, s1) and lane/4 + 8 (s2, s3) for heads 2*(lane%4), +1
             float s0 = (sa[0] + sb[0]) * a.scale_log2, s1 = (sa[1] + sb[1]) * a.scale_log2;
@@ -358,11 +421,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
             l0 += p0 + p2;
             l1 += p1 + p3;
             // P^T as the B operand (16 tokens x 8 heads): transpose the two 8x8 halves
-            const uint32_t pb0 = movmatrix_trans(Dt<T>::pack(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(Dt<T>::pack(p2, p3));
+            const uint32_t pb0 = movmatrix_trans(Dt<MT>::pack(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(Dt<MT>::pack(p2, p3));
             // O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 x 8)
 #pragma unroll
-            for (int mt = 0; mt < S::kKSteps; ++mt) Mma<T>::run(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
+            for (int mt = 0; mt < S::kKSteps; ++mt)
+                Mma<MT>::run(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
         }
     }
     __syncthreads();
@@ -389,13 +453,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
         l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
         const int h0 = (lane & 3) * 2;
         const int dr = lane >> 2;
+        // the two d of this lane's O^T fragment rows (see the F8 permutation above)
+        const int d_lo = F8 ? 2 * dr : dr, d_hi = F8 ? 2 * dr + 1 : dr + 8;
         float *w = mo + warp * 8 * D;
 #pragma unroll
         for (int mt = 0; mt < S::kKSteps; ++mt) {
-            w[h0 * D + mt * 16 + dr] = o[mt][0];
-            w[(h0 + 1) * D + mt * 16 + dr] = o[mt][1];
-            w[h0 * D + mt * 16 + dr + 8] = o[mt][2];
-            w[(h0 + 1) * D + mt * 16 + dr + 8] = o[mt][3];
+            w[h0 * D + mt * 16 + d_lo] = o[mt][0];
+            w[(h0 + 1) * D + mt * 16 + d_lo] = o[mt][1];
+            w[h0 * D + mt * 16 + d_hi] = o[mt][2];
+            w[(h0 + 1) * D + mt * 16 + d_hi] = o[mt][3];
         }
         if (lane < 4) {  // a warp whose tokens were all masked has m = -inf and sum 0: weight 0 below
             mm[warp * 8 + h0] = m0 == -INFINITY ? -INFINITY : mu0;
@@ -418,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST>())
             acc += mo[(w * 8 + h) * D + d] * wt;
             sum += ml[w * 8 + h] * wt;
         }
+        if constexpr (F8) acc *= a.v_scale;
         const int hq = g * a.group + h;
         if (nparts == 1) {
             out[(static_cast<int64_t>(b) * a.num_q_heads + hq) * D + d] = Dt<T>::from_float(acc / sum);
@@ -482,38 +549,41 @@ int ilog2(int x) {
 
 // Opt the partition kernel in to its shared memory (a per-device function attribute) and ask
 // for the largest shared-memory carveout, so that ctas_per_sm<ST>() CTAs fit on an SM.
-template <typename T, int D, int ST> cudaError_t prepare_partition_kernel() {
-    cudaError_t e = cudaFuncSetAttribute(decode_partition_kernel<T, D, ST>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<D, ST>::kSmemBytes);
+template <typename T, int D, int ST, bool F8 = false> cudaError_t prepare_partition_kernel() {
+    cudaError_t e = cudaFuncSetAttribute(decode_partition_kernel<T, D, ST, F8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Shape<D, ST, F8>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(decode_partition_kernel<T, D, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(decode_partition_kernel<T, D, ST, F8>,
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
 }
 
-template <int D, int ST> int occupancy() {
+template <int D, int ST, bool F8 = false> int occupancy() {
     int occ = 0;
-    if (prepare_partition_kernel<__nv_bfloat16, D, ST>() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_partition_kernel<__nv_bfloat16, D, ST>, kThreads,
-                                                      Shape<D, ST>::kSmemBytes) != cudaSuccess ||
+    if (prepare_partition_kernel<__nv_bfloat16, D, ST, F8>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_partition_kernel<__nv_bfloat16, D, ST, F8>,
+                                                      kThreads, Shape<D, ST, F8>::kSmemBytes) != cudaSuccess ||
         occ < 1)
         occ = 1;
-    return occ < ctas_per_sm<ST>() ? occ : ctas_per_sm<ST>();
+    return occ < ctas_per_sm<ST, F8>() ? occ : ctas_per_sm<ST, F8>();
 }
 
-// Resident partition CTAs the current device holds at once for this ring depth and head dim.
-static int resident_ctas(int stages, int head_dim) {
-    static int cached[64][2][2] = {};
+// Resident partition CTAs the current device holds at once for this kernel variant:
+// 16-bit pool with 2 or 3 stages and head dim 64 or 128, or the E4M3 pool (head dim 128).
+static int resident_ctas(int stages, int head_dim, bool fp8) {
+    static int cached[64][3][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2 * 148;
-    const int si = stages == 2 ? 0 : 1, hi = head_dim == 64 ? 0 : 1;
-    if (!cached[dev][si][hi]) {
+    const int vi = fp8 ? 2 : stages == 2 ? 0 : 1, hi = head_dim == 64 ? 0 : 1;
+    if (!cached[dev][vi][hi]) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-        const int occ = si ? (hi ? occupancy<128, 3>() : occupancy<64, 3>())
-                           : (hi ? occupancy<128, 2>() : occupancy<64, 2>());
-        cached[dev][si][hi] = occ * sms;
+        const int occ = vi == 2 ? occupancy<128, kF8Stages, true>()
+                        : vi == 1 ? (hi ? occupancy<128, 3>() : occupancy<64, 3>())
+                                  : (hi ? occupancy<128, 2>() : occupancy<64, 2>());
+        cached[dev][vi][hi] = occ * sms;
     }
-    return cached[dev][si][hi];
+    return cached[dev][vi][hi];
 }
 
 // Ring depth for a block size (PA_DECODE_STAGES = 2 or 3 overrides it for tuning).  Pages
@@ -529,12 +599,12 @@ static int stages_for(int32_t block_size) {
 }
 
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t max_blocks_per_seq, int32_t block_size) {
+                       int32_t max_blocks_per_seq, int32_t block_size, bool fp8) {
     DecodePlan pl{};
-    pl.stages = stages_for(block_size);
+    pl.stages = fp8 ? kF8Stages : stages_for(block_size);
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int64_t pairs = static_cast<int64_t>(batch) * num_kv_heads;
-    const int64_t slots = resident_ctas(pl.stages, head_dim);
+    const int64_t slots = resident_ctas(pl.stages, head_dim, fp8);
     const int64_t tiles = (cap + kTile - 1) / kTile;
     int64_t part;
     if (pairs >= 2 * slots) {
@@ -568,7 +638,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
                           const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
-                          const FusedStore *fused) {
+                          const FusedStore *fused, const Fp8Scales *fp8) {
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
     a.q = q;
@@ -581,7 +651,8 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.group = num_q_heads / num_kv_heads;
     a.num_blocks = num_blocks;
     a.log2_bs = ilog2(block_size);
-    a.scale_log2 = scale * kLog2e;
+    a.scale_log2 = scale * kLog2e * (fp8 ? fp8->k_scale : 1.f);
+    a.v_scale = fp8 ? fp8->v_scale : 1.f;
     a.out = out;
     const size_t n = static_cast<size_t>(batch) * num_q_heads * plan.max_parts;
     const size_t ml_bytes = (n * sizeof(float2) + 255) / 256 * 256;
@@ -604,8 +675,9 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     const int64_t rows = static_cast<int64_t>(num_blocks) * block_size;
     const int64_t cols = static_cast<int64_t>(num_kv_heads) * head_dim;
     const int box_rows = block_size < kTile ? block_size : kTile;
-    if (!make_tmap_rows(&tm_k, k_cache, dtype, cols, rows, box_rows) ||
-        !make_tmap_rows(&tm_v, v_cache, dtype, cols, rows, box_rows))
+    const pa_dtype pool = fp8 ? PA_E4M3 : dtype;
+    if (!make_tmap_rows(&tm_k, k_cache, pool, cols, rows, box_rows) ||
+        !make_tmap_rows(&tm_v, v_cache, pool, cols, rows, box_rows))
         return cudaErrorInvalidValue;
 
     auto run = [&](auto kern_part, auto kern_comb, auto prepare, int smem, int d) -> cudaError_t {
@@ -632,17 +704,23 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         return err;
     };
 #define PA_DECODE_RUN(T, D, ST)                                                                                  \
-    run(decode_partition_kernel<T, D, ST>, decode_combine_kernel<T, D>, prepare_partition_kernel<T, D, ST>,    \
-        Shape<D, ST>::kSmemBytes, D)
+    run(decode_partition_kernel<T, D, ST, false>, decode_combine_kernel<T, D>,                                 \
+        prepare_partition_kernel<T, D, ST, false>, Shape<D, ST>::kSmemBytes, D)
+#define PA_DECODE_RUN_F8(T)                                                                                      \
+    run(decode_partition_kernel<T, 128, kF8Stages, true>, decode_combine_kernel<T, 128>,                       \
+        prepare_partition_kernel<T, 128, kF8Stages, true>, Shape<128, kF8Stages, true>::kSmemBytes, 128)
     const bool bf = dtype == PA_BF16, d128 = head_dim == 128, deep = plan.stages == 3;
     cudaError_t e;
-    if (bf)
+    if (fp8)  // head_dim 128, checked by the caller
+        e = bf ? PA_DECODE_RUN_F8(__nv_bfloat16) : PA_DECODE_RUN_F8(__half);
+    else if (bf)
         e = d128 ? (deep ? PA_DECODE_RUN(__nv_bfloat16, 128, 3) : PA_DECODE_RUN(__nv_bfloat16, 128, 2))
                  : (deep ? PA_DECODE_RUN(__nv_bfloat16, 64, 3) : PA_DECODE_RUN(__nv_bfloat16, 64, 2));
     else
         e = d128 ? (deep ? PA_DECODE_RUN(__half, 128, 3) : PA_DECODE_RUN(__half, 128, 2))
                  : (deep ? PA_DECODE_RUN(__half, 64, 3) : PA_DECODE_RUN(__half, 64, 2));
 #undef PA_DECODE_RUN
+#undef PA_DECODE_RUN_F8
     return e;
 }
 

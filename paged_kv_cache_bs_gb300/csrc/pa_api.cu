@@ -31,6 +31,10 @@ bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 bool aligned(const void *p, int bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
 bool valid_dtype(int d) { return d == PA_F16 || d == PA_BF16; }
 
+bool valid_scales(const pa::Fp8Scales &sc) {
+    return isfinite(sc.k_scale) && sc.k_scale > 0.f && isfinite(sc.v_scale) && sc.v_scale > 0.f;
+}
+
 // Checks shared by the attention calls.  Returns PA_OK or an error code.
 int check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                           int32_t block_size, float scale, pa_dtype dtype) {
@@ -70,9 +74,15 @@ int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const
                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                  float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype,
-                 pa::DecodePlan *plan) {
+                 pa::DecodePlan *plan, const pa::Fp8Scales *fp8 = nullptr) {
     int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
     if (rc) return rc;
+    if (fp8) {
+        if (head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: head_dim %d (supported: 128)", head_dim);
+        if (!valid_scales(*fp8))
+            return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive (%g, %g)",
+                        fp8->k_scale, fp8->v_scale);
+    }
     if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch is negative (%d)", batch);
     if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (1LL << 30))
@@ -87,26 +97,24 @@ int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const
     if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 2) ||
         !aligned(workspace, 256))
         return fail(PA_ERR_INVALID_ARG, "alignment: q 4 B, caches 16 B, out 2 B, workspace 256 B");
-    *plan = pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+    *plan = pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                            fp8 != nullptr);
     if (workspace_bytes < plan->ws_bytes)
         return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
                     plan->ws_bytes);
     return PA_OK;
 }
 
-}  // namespace
 
-extern "C" {
-
-const char *pa_last_error(void) { return g_err; }
-
-int pa_version(void) { return 100; }
-
-int pa_store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache,
-                void *v_cache, const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
-                int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype, int32_t *err_flag,
-                void *stream) {
+// pa_store_kv, or pa_store_kv_fp8 when fp8 is given (an E4M3 pool).
+int store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache, void *v_cache,
+             const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+             int32_t num_blocks, int32_t block_size, pa_dtype dtype, int32_t *err_flag, void *stream,
+             const pa::Fp8Scales *fp8) {
     if (!valid_dtype(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not PA_F16 or PA_BF16", (int)dtype);
+    if (fp8 && !valid_scales(*fp8))
+        return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive (%g, %g)", fp8->k_scale,
+                    fp8->v_scale);
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens is negative (%d)", num_tokens);
     if (num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
         return fail(PA_ERR_INVALID_ARG, "sizes must be positive (H_kv=%d, D=%d, N=%d, bs=%d)", num_kv_heads,
@@ -124,19 +132,67 @@ int pa_store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_ro
                     (long long)k_row_stride, (long long)v_row_stride, (long long)row);
     if (!aligned(k, 2) || !aligned(v, 2) || !aligned(k_cache, 2) || !aligned(v_cache, 2))
         return fail(PA_ERR_INVALID_ARG, "buffers must be 2-byte aligned");
+    if (fp8 && (row % 8 || k_row_stride % 8 || v_row_stride % 8 || !aligned(k, 16) || !aligned(v, 16) ||
+                !aligned(k_cache, 8) || !aligned(v_cache, 8)))
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_store_kv_fp8: rows and strides must be multiples of 8 elements, k/v 16-byte and the "
+                    "caches 8-byte aligned");
     const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
+    if (fp8)
+        return cuda_status(pa::launch_store_kv_fp8(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping,
+                                                   num_tokens, static_cast<int32_t>(row), slots, dtype,
+                                                   fp8->k_scale, fp8->v_scale, err_flag,
+                                                   static_cast<cudaStream_t>(stream)),
+                           "pa_store_kv_fp8 launch");
     return cuda_status(pa::launch_store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping,
                                            num_tokens, static_cast<int32_t>(row), slots, err_flag,
                                            static_cast<cudaStream_t>(stream)),
                        "pa_store_kv launch");
 }
 
-size_t pa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                 int32_t max_blocks_per_seq, int32_t block_size) {
+
+size_t decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t max_blocks_per_seq, int32_t block_size, bool fp8) {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
         !is_pow2(block_size))
         return 0;
-    return pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size).ws_bytes;
+    return pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, fp8)
+        .ws_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_last_error(void) { return g_err; }
+
+int pa_version(void) { return 100; }
+
+int pa_store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache,
+                void *v_cache, const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype, int32_t *err_flag,
+                void *stream) {
+    return store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                    head_dim, num_blocks, block_size, dtype, err_flag, stream, nullptr);
+}
+
+int pa_store_kv_fp8(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache,
+                    void *v_cache, const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype, float k_scale,
+                    float v_scale, int32_t *err_flag, void *stream) {
+    const pa::Fp8Scales sc{k_scale, v_scale};
+    return store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                    head_dim, num_blocks, block_size, dtype, err_flag, stream, &sc);
+}
+
+size_t pa_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_blocks_per_seq, int32_t block_size) {
+    return decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, false);
+}
+
+size_t pa_decode_fp8_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t max_blocks_per_seq, int32_t block_size) {
+    return decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, true);
 }
 
 int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
@@ -187,6 +243,28 @@ int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t 
                                          block_size, scale, out, workspace, plan, dtype, err_flag,
                                          static_cast<cudaStream_t>(stream), &fused),
                        "pa_store_decode launch");
+}
+
+int pa_decode_fp8(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                  int32_t block_size, float scale, float k_scale, float v_scale, void *out, void *workspace,
+                  size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag, void *stream) {
+    pa::DecodePlan plan{};
+    const pa::Fp8Scales sc{k_scale, v_scale};
+    const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
+                                workspace, workspace_bytes, dtype, &plan, &sc);
+    if (rc) return rc;
+    if (batch == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         block_size, scale, out, workspace, plan, dtype, err_flag,
+                                         static_cast<cudaStream_t>(stream), nullptr, &sc),
+                       "pa_decode_fp8 launch");
 }
 
 int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,

@@ -103,14 +103,24 @@ cudaError_t launch_store_kv(const void *k, const void *v, int64_t k_row_stride, 
                             void *k_cache, void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
                             int32_t row_elems, int64_t num_slots, int32_t *err_flag, cudaStream_t stream);
 
+cudaError_t launch_store_kv_fp8(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                                void *k_cache, void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                                int32_t row_elems, int64_t num_slots, pa_dtype dtype, float k_scale, float v_scale,
+                                int32_t *err_flag, cudaStream_t stream);
+
 struct DecodePlan {
     int stages;         // ring depth of the partition kernel (2 or 3)
     int partition;      // tokens per split-K partition (multiple of the tile)
     int max_parts;      // partitions per sequence at the maximum context
     size_t ws_bytes;    // workspace bytes
 };
+// The E4M3 pool of the fp8 calls: K = code * k_scale, V = code * v_scale.
+struct Fp8Scales {
+    float k_scale, v_scale;
+};
+// fp8: the plan of the E4M3 partition kernel (its own ring and occupancy).
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t max_blocks_per_seq, int32_t block_size);
+                       int32_t max_blocks_per_seq, int32_t block_size, bool fp8 = false);
 // The store fused into pa_store_decode (the new rows of one decode step).
 struct FusedStore {
     const void *k;
@@ -124,7 +134,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
                           const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
-                          const FusedStore *fused = nullptr);
+                          const FusedStore *fused = nullptr, const Fp8Scales *fp8 = nullptr);
 cudaError_t launch_sample(const void *logits, int64_t row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
                           const float *temperatures, const float *noise, uint64_t seed, uint64_t offset,
                           int32_t *tokens, int32_t *err_flag, cudaStream_t stream);

@@ -7,6 +7,8 @@
 // moves one token's K and V rows with 16-byte vector accesses (when the
 // pointers and strides allow), every lane holding all its loads in flight
 // before it stores, so each SM keeps tens of KB of reads outstanding.
+#include <cuda_fp8.h>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -71,7 +73,70 @@ cudaError_t launch_vec(const void *k, const void *v, int64_t k_row_stride, int64
 
 bool aligned(const void *p, int64_t bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
 
+// The same store into an E4M3 pool with per-tensor scales: each element
+// becomes the nearest E4M3 value of x / scale (fp32 division; ties to even;
+// saturating at +-448).  A lane converts 8 elements: one 16-byte load, one
+// 8-byte store.
+template <typename T>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+store_kv_fp8_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t k_stride, int64_t v_stride,
+                    uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+                    const int32_t *__restrict__ slot_mapping, int32_t num_tokens, int32_t row, int64_t num_slots,
+                    float k_scale, float v_scale, int32_t *err_flag) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int32_t t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) return;
+    if (slot < -1 || slot >= num_slots) {
+        if (lane == 0) raise_flag(err_flag, PA_FLAG_BAD_SLOT);
+        return;
+    }
+    auto convert = [](const T *src, uint8_t *dst, float scale) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+        const T *x = reinterpret_cast<const T *>(&raw);
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const float2 f = make_float2(static_cast<float>(x[4 * h + e]) / scale,
+                                             static_cast<float>(x[4 * h + e + 1]) / scale);
+                const __nv_fp8x2_storage_t pair = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+                bytes |= static_cast<uint32_t>(pair) << (8 * e);
+            }
+            w[h] = bytes;
+        }
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    };
+    for (int i = 8 * lane; i < row; i += 32 * 8) {
+        convert(k + t * k_stride + i, k_cache + slot * row + i, k_scale);
+        convert(v + t * v_stride + i, v_cache + slot * row + i, v_scale);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_store_kv_fp8(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                                void *k_cache, void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                                int32_t row_elems, int64_t num_slots, pa_dtype dtype, float k_scale, float v_scale,
+                                int32_t *err_flag, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const dim3 grid((num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if (dtype == PA_BF16)
+        store_kv_fp8_kernel<__nv_bfloat16><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v), k_row_stride, v_row_stride,
+            static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, num_tokens, row_elems,
+            num_slots, k_scale, v_scale, err_flag);
+    else
+        store_kv_fp8_kernel<__half><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+            static_cast<const __half *>(k), static_cast<const __half *>(v), k_row_stride, v_row_stride,
+            static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, num_tokens, row_elems,
+            num_slots, k_scale, v_scale, err_flag);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
                             void *k_cache, void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,

@@ -1,4 +1,4 @@
-// Host side of the TMA loads: tensor maps over row-major 16-bit matrices
+// Host side of the TMA loads: tensor maps over row-major 16-bit (or E4M3) matrices
 // (the paged pool viewed as [num_blocks*block_size rows, H_kv*D columns], or a
 // packed [tokens, heads*D] array), encoded through the driver entry point that
 // the runtime hands out, so the library links against libcudart only.
@@ -52,11 +52,15 @@ bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols,
     EncodeTiled enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    // one box row is 128 bytes (the swizzle span): 64 16-bit elements or 128 E4M3 codes
+    const bool f8 = dt == PA_E4M3;
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * (f8 ? 1 : 2))};
+    const cuuint32_t box[2] = {f8 ? 128u : 64u, static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = enc(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType type = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = enc(m, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;

@@ -22,7 +22,9 @@ Workload recipe (all values drawn from one ``torch.Generator`` seeded with the
 workload's index): q, new k/v and every cached token are N(0, 1) cast to the
 workload dtype; unused pool rows hold the NaN sentinel 0x7FC1 so that a stray
 read poisons the result; physical block ids are ``randperm(pool)[:need]``
-assigned in logical order.
+assigned in logical order.  An fp8 pool (``make_decode_fp8``) holds the E4M3
+codes of N(0, 1) values over per-tensor scales 4/448 (K) and 3/448 (V), made
+by torch's float8_e4m3fn cast, and the NaN code 0x7F in unused rows.
 """
 
 from __future__ import annotations
@@ -411,10 +413,78 @@ def store_stress(seed: int = 6, tokens: int = 16384, num_kv_heads: int = 8, head
     return k, v, kc, vc, slots
 
 
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) pools
+# ---------------------------------------------------------------------------
+
+FP8_SENTINEL = 0x7F  # an E4M3 NaN code: unused fp8 pool rows
+FP8_K_SCALE = 4.0 / 448.0  # per-tensor scales: N(0, 1) values up to 4 (K) and 3 (V) sigma use
+FP8_V_SCALE = 3.0 / 448.0  # the whole code range
+
+
+def random_e4m3_codes(n_rows: int, row: int, scale: float, gen: torch.Generator) -> torch.Tensor:
+    """uint8 E4M3 codes of N(0, 1) values divided by ``scale`` (torch's float8_e4m3fn
+    cast after clamping to +-448): synthetic contents of an fp8 pool."""
+    x = (torch.randn(n_rows, row, generator=gen) / scale).clamp(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+@dataclass
+class Fp8DecodeStep:
+    """A decode step over an E4M3 pool: ``step`` gives q, the new 16-bit k/v rows
+    (quantised by the store), slot mapping, tables and lengths; the pools hold codes,
+    K = code * k_scale and V = code * v_scale."""
+
+    step: DecodeStep
+    k_cache: torch.Tensor  # uint8 [N, bs, H_kv, D], pre-store contents
+    v_cache: torch.Tensor
+    k_scale: float
+    v_scale: float
+
+    def kv_bytes(self) -> int:
+        return self.step.kv_bytes() // self.step.q.element_size()
+
+    def unique_kv_bytes(self) -> int:
+        return self.step.unique_kv_bytes() // self.step.q.element_size()
+
+
+def make_decode_fp8(ctx: list[int], *, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                    dtype: torch.dtype, seed: int, num_blocks: int | None = None, share_groups: int = 0,
+                    share_tokens: int = 0, k_scale: float = FP8_K_SCALE, v_scale: float = FP8_V_SCALE
+                    ) -> Fp8DecodeStep:
+    """``make_decode``'s step with the pool's cached rows as random E4M3 codes and the
+    unused rows as the NaN code."""
+    st = make_decode(ctx, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                     block_size=block_size, dtype=dtype, seed=seed, num_blocks=num_blocks,
+                     share_groups=share_groups, share_tokens=share_tokens)
+    p = st.pool
+    row = num_kv_heads * head_dim
+    filled = (p.k_cache.view(torch.int16).view(-1, row) != SENTINEL_BITS).any(dim=1).nonzero().flatten()
+    gen = torch.Generator().manual_seed(seed + 7919)
+    kc = torch.full((p.num_blocks * block_size, row), FP8_SENTINEL, dtype=torch.uint8)
+    vc = torch.full((p.num_blocks * block_size, row), FP8_SENTINEL, dtype=torch.uint8)
+    kc[filled] = random_e4m3_codes(filled.numel(), row, k_scale, gen)
+    vc[filled] = random_e4m3_codes(filled.numel(), row, v_scale, gen)
+    # the 16-bit pool is no longer needed: keep only its geometry and tables
+    st.pool = Pool(p.dtype, p.num_blocks, p.block_size, p.num_kv_heads, p.head_dim, torch.empty(0, dtype=dtype),
+                   torch.empty(0, dtype=dtype), p.tables, p.specs)
+    shape = (p.num_blocks, block_size, num_kv_heads, head_dim)
+    return Fp8DecodeStep(st, kc.view(shape), vc.view(shape), k_scale, v_scale)
+
+
+def qwen3_0p6b_decode_fp8(seed: int = 2, batch: int = 64) -> Fp8DecodeStep:
+    """``qwen3_0p6b_decode``'s shapes and lengths over an E4M3 pool."""
+    gen = torch.Generator().manual_seed(seed)
+    ctx = torch.randint(128, 4097, (batch,), generator=gen).tolist()
+    return make_decode_fp8(ctx, num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=256,
+                           dtype=torch.bfloat16, seed=seed + 1000)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "qwen3_0p6b_decode": qwen3_0p6b_decode,
     "qwen3_8b_shared_decode": qwen3_8b_shared_decode,
     "long_context_decode": long_context_decode,
     "mixed_chunked_prefill": mixed_chunked_prefill,
+    "qwen3_0p6b_decode_fp8": qwen3_0p6b_decode_fp8,
 }

@@ -170,3 +170,41 @@ def test_sample_validation(lib):
     assert call(dt=2, lg=ctypes.c_void_p((1 << 20) + 2)) == -1
     assert call(t=None) == -1
     assert call(B=0, lg=None, t=None, out=None) == 0
+
+
+def test_fp8_store_validation(lib):
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, ks=1024, vs=1024, kc=FAKE, vc=FAKE, sm=FAKE, T=4, hkv=8, d=128, n=10, bs=16, dt=1,
+                 ksc=0.01, vsc=0.01)
+        a.update(kw)
+        return lib.pa_store_kv_fp8(a["k"], a["v"], a["ks"], a["vs"], a["kc"], a["vc"], a["sm"], a["T"], a["hkv"],
+                                   a["d"], a["n"], a["bs"], a["dt"], ctypes.c_float(a["ksc"]),
+                                   ctypes.c_float(a["vsc"]), None, None)
+    assert call(dt=3) == -2                                   # the 16-bit input rows are fp16 / bf16
+    assert call(ksc=0.0) == -1 and call(vsc=-1.0) == -1
+    assert call(ksc=float("inf")) == -1 and call(vsc=float("nan")) == -1
+    assert call(ks=1028) == -1                                # not a multiple of 8
+    assert call(d=60, hkv=1, ks=64, vs=64) == -1              # row of 60 elements
+    assert call(k=ctypes.c_void_p((1 << 20) + 8)) == -1       # k needs 16-byte alignment
+    assert call(kc=ctypes.c_void_p((1 << 20) + 4)) == -1      # caches need 8-byte alignment
+    assert call(T=0, k=None, v=None, sm=None) == 0
+
+
+def test_fp8_decode_validation(lib):
+    def call(**kw):
+        a = dict(q=FAKE, qs=2048, kc=FAKE, vc=FAKE, bt=FAKE, mb=16, cl=FAKE, B=64, hq=16, hkv=8, d=128, n=700,
+                 bs=256, scale=0.088, ksc=0.01, vsc=0.01, out=FAKE, ws=FAKE, wsb=1 << 30, dt=1)
+        a.update(kw)
+        return lib.pa_decode_fp8(a["q"], a["qs"], a["kc"], a["vc"], a["bt"], a["mb"], a["cl"], a["B"], a["hq"],
+                                 a["hkv"], a["d"], a["n"], a["bs"], ctypes.c_float(a["scale"]),
+                                 ctypes.c_float(a["ksc"]), ctypes.c_float(a["vsc"]), a["out"], a["ws"], a["wsb"],
+                                 a["dt"], None, None)
+    assert call(d=64, qs=1024) == -2                          # head_dim 128 only
+    assert call(ksc=0.0) == -1 and call(vsc=float("inf")) == -1
+    assert call(dt=3) == -2                                   # q / out are fp16 / bf16
+    assert call(wsb=16) == -1
+    assert call(kc=ctypes.c_void_p((1 << 20) + 8)) == -1      # TMA: 16-byte aligned pool
+    assert call(B=0, q=None, out=None, ws=None) == 0
+    lib.pa_decode_fp8_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.pa_decode_fp8_workspace_bytes(64, 16, 8, 128, 16, 256) > 0
+    assert lib.pa_decode_fp8_workspace_bytes(64, 16, 8, 128, 16, 12) == 0
