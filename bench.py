@@ -240,10 +240,11 @@ class DecodeWorkload:
 
 
 class Fp8DecodeWorkload(DecodeWorkload):
-    """A decode step over an E4M3 pool: pa_store_kv_fp8 of one token per sequence,
-    then pa_decode_fp8 (split-K partitions + merge)."""
+    """A decode step over an E4M3 pool: pa_store_decode_fp8 (the quantising store of one
+    token per sequence fused into the split-K partition kernel, + merge), or with
+    fused=False pa_store_kv_fp8 then pa_decode_fp8."""
 
-    def __init__(self, name: str, dev: torch.device):
+    def __init__(self, name: str, dev: torch.device, fused: bool = True):
         from tests import inputs
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
@@ -268,9 +269,13 @@ class Fp8DecodeWorkload(DecodeWorkload):
         # k and v: 16-bit rows read, one-byte codes written
         self.store_bytes = 2 * int((st.slot_mapping >= 0).sum()) * row * (st.q.element_size() + 1)
         self.prefill_flops = 0
-        self.fused = False
-        self.launches_per_step = 3   # quantising store, decode partitions, log-sum-exp merge
-        self.phases = [("store", self.store), ("decode", self.attend)]
+        self.fused = fused
+        if fused:
+            self.launches_per_step = 2   # partitions (with the store) + log-sum-exp merge
+            self.phases = [("store+decode", self.store_and_attend)]
+        else:
+            self.launches_per_step = 3   # quantising store, decode partitions, log-sum-exp merge
+            self.phases = [("store", self.store), ("decode", self.attend)]
 
     def store(self):
         d, fs = self.d, self.fs
@@ -280,6 +285,12 @@ class Fp8DecodeWorkload(DecodeWorkload):
         d, fs = self.d, self.fs
         self.pa.decode_fp8(d["q"], self.kc, self.vc, d["block_tables"], d["context_lens"], self.st.scale,
                            fs.k_scale, fs.v_scale, out=self.out, workspace=self.ws)
+
+    def store_and_attend(self):
+        d, fs = self.d, self.fs
+        self.pa.store_decode_fp8(d["k_new"], d["v_new"], d["slot_mapping"], d["q"], self.kc, self.vc,
+                                 d["block_tables"], d["context_lens"], self.st.scale, fs.k_scale, fs.v_scale,
+                                 out=self.out, workspace=self.ws)
 
 
 class MixedWorkload(DecodeWorkload):
@@ -590,7 +601,7 @@ def run_ours(args, world, rank, local):
     if args.workload == "mixed_chunked_prefill":
         w = MixedWorkload(args.workload, dev)
     elif args.workload.endswith("_fp8"):
-        w = Fp8DecodeWorkload(args.workload, dev)
+        w = Fp8DecodeWorkload(args.workload, dev, fused=not args.unfused)
     else:
         w = DecodeWorkload(args.workload, dev, fused=not args.unfused)
     flush_needed = w.kv_unique_bytes < 2 * L2_BYTES
@@ -674,10 +685,12 @@ def run_ours(args, world, rank, local):
         # bytes DRAM must supply: each physical page once (pages shared by several sequences
         # are counted once; for unshared workloads this equals the logical KV bytes)
         unique_gbs = w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9
-        kern = ("pa_store_decode (store fused into the split-K partition kernel + merge)"
-                if "store+decode" in phase_ms else
-                "pa_decode_fp8 (E4M3 split-K partitions + merge)" if isinstance(w, Fp8DecodeWorkload) else
-                "pa_decode (split-K partitions + merge)")
+        f8 = isinstance(w, Fp8DecodeWorkload)
+        kern = ("pa_store_decode_fp8 (E4M3 store fused into the split-K partition kernel + merge)"
+                if f8 and "store+decode" in phase_ms else
+                "pa_decode_fp8 (E4M3 split-K partitions + merge)" if f8 else
+                "pa_store_decode (store fused into the split-K partition kernel + merge)"
+                if "store+decode" in phase_ms else "pa_decode (split-K partitions + merge)")
         roof = {"bound": "hbm", "kernel": kern, "achieved": unique_gbs,
                 "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": unique_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",

@@ -9,7 +9,8 @@
  *   pa_prefill_paged  chunked prefill: new query tokens attending causally over
  *                     a cached paged prefix plus themselves
  * plus the decode step's store fused into decode (pa_store_decode), the same
- * store and decode over an FP8 pool (pa_store_kv_fp8, pa_decode_fp8) and the
+ * store and decode over an FP8 pool (pa_store_kv_fp8, pa_decode_fp8,
+ * pa_store_decode_fp8) and the
  * sampler that turns the step's logits into tokens (pa_sample).
  *
  * Conventions shared by every call
@@ -269,6 +270,23 @@ PA_API int pa_decode_fp8(const void *q, int64_t q_row_stride, const void *k_cach
                   int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                   int32_t num_blocks, int32_t block_size, float scale, float k_scale, float v_scale, void *out,
                   void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
+ * pa_store_decode_fp8 -- pa_store_decode over an E4M3 pool: each sequence's
+ * new K/V row is quantised as pa_store_kv_fp8 does (same codes) into slot
+ * slot_mapping[b], which must be -1 or the slot of position
+ * context_lens[b] - 1 (else PA_FLAG_BAD_SLOT and the row is not stored), and
+ * the same launch attends as pa_decode_fp8.  Argument rules: those of
+ * pa_store_decode for k, v, their strides and slot_mapping, those of
+ * pa_decode_fp8 for the rest (workspace: pa_decode_fp8_workspace_bytes).
+ */
+PA_API int pa_store_decode_fp8(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                        const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                        void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                        const int32_t *context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, float k_scale,
+                        float v_scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                        int32_t *err_flag, void *stream);
 
 /*
  * pa_prefill_paged -- causal varlen prefill over a paged prefix.

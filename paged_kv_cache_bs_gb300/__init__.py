@@ -13,6 +13,7 @@ The functions mirror the C ABI in ``include/pa_api.h``:
 * :func:`store_decode`   -- ``pa_store_decode`` (the decode step's store fused into decode)
 * :func:`store_kv_fp8`   -- ``pa_store_kv_fp8`` (quantising store into an E4M3 pool)
 * :func:`decode_fp8`     -- ``pa_decode_fp8`` (+ ``pa_decode_fp8_workspace_bytes``)
+* :func:`store_decode_fp8` -- ``pa_store_decode_fp8`` (the fp8 store fused into fp8 decode)
 * :func:`prefill_paged`  -- ``pa_prefill_paged``
 * :func:`sample`         -- ``pa_sample`` (temperature sampling, exponential race)
 """
@@ -53,6 +54,9 @@ _lib.pa_decode_fp8_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i3
 _lib.pa_decode_fp8.restype = ctypes.c_int
 _lib.pa_decode_fp8.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _p,
                                _p, _sz, ctypes.c_int, _p, _p]
+_lib.pa_store_decode_fp8.restype = ctypes.c_int
+_lib.pa_store_decode_fp8.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
+                                     _i32, _i32, _f32, _f32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
 _lib.pa_sample.restype = ctypes.c_int
 _lib.pa_sample.argtypes = [_p, _i64, _i32, _i32, ctypes.c_int, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
 _lib.pa_prefill_paged.restype = ctypes.c_int
@@ -268,14 +272,46 @@ def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     B, hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
-    if workspace is None:
-        nbytes = decode_fp8_workspace_bytes(B, hq, hkv, d, block_tables.shape[1], bs)
-        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    workspace = _fp8_workspace(q, hkv, d, block_tables, bs, workspace)
     rc = _lib.pa_decode_fp8(_ptr(q), _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale),
                             float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag), _stream(q))
     _check("pa_decode_fp8", rc)
+    return out
+
+
+def _fp8_workspace(q, hkv, d, block_tables, bs, workspace):
+    if workspace is None:
+        nbytes = decode_fp8_workspace_bytes(q.shape[0], q.shape[1], hkv, d, block_tables.shape[1], bs)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    return workspace
+
+
+def store_decode_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q: torch.Tensor,
+                     k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """One decode step over an fp8 pool in one launch: quantise k/v ([B, H_kv, D]) into slot
+    ``slot_mapping`` (each sequence's last context position, or -1) and attend."""
+    _fp8_pool(k_cache, v_cache)
+    n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    B, hq = q.shape[0], q.shape[1]
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous() or slot_mapping.numel() != B:
+        raise ValueError("slot_mapping must be contiguous int32 [B]")
+    if k.shape != (B, hkv, d) or v.shape != (B, hkv, d) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k/v must be [B, H_kv, D] of the query dtype")
+    if out is None:
+        out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
+    workspace = _fp8_workspace(q, hkv, d, block_tables, bs, workspace)
+    rc = _lib.pa_store_decode_fp8(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q),
+                                  _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale),
+                                  float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
+                                  _stream(q))
+    _check("pa_store_decode_fp8", rc)
     return out
 
 
@@ -302,6 +338,7 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
 
 
 __all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
+           "store_decode_fp8",
            "decode_workspace_bytes", "decode_fp8_workspace_bytes", "alloc_decode_workspace", "library",
            "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "PA_E4M3", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
            "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL", "FLAG_BAD_VALUE"]

@@ -41,8 +41,6 @@
 
 #include <type_traits>
 
-#include <cuda_fp8.h>
-
 #include "tc_common.cuh"
 
 namespace pa {
@@ -90,7 +88,7 @@ struct DecodeArgs {
     int64_t k_new_stride, v_new_stride;  // elements between sequences' rows
     void *k_cache_w;
     void *v_cache_w;
-    float v_scale;  // E4M3 pool: V = code * v_scale (1 for 16-bit pools)
+    float k_scale, v_scale;  // E4M3 pool: K = code * k_scale, V = code * v_scale (1 for 16-bit pools)
 };
 
 // Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
@@ -123,11 +121,12 @@ __device__ __forceinline__ int context_len(const DecodeArgs &a, int b) {
 
 // Fused store, by the producer warp of the CTA that holds the last partition of
 // sequence b for kv head g: this head's slices of the new K and V rows go to
-// cache row slot_mapping[b], which must be the slot of position L-1 (the token
-// stored this step is the last one of the context), else the row is flagged
-// and not written.  No other CTA reads that slice, and the proxy fence makes
-// the plain stores visible to the TMA loads this warp issues next.
-template <typename T, int D>
+// cache row slot_mapping[b] (quantised to E4M3 codes for an F8 pool), which
+// must be the slot of position L-1 (the token stored this step is the last one
+// of the context), else the row is flagged and not written.  No other CTA
+// reads that slice, and the proxy fence makes the plain stores visible to the
+// TMA loads this warp issues next.
+template <typename T, int D, bool F8>
 __device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g, int L, int lane) {
     const int slot = a.slot_mapping[b];
     if (slot == -1) return;
@@ -139,15 +138,19 @@ __device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g,
         if (lane == 0 && g == 0) raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);
         return;
     }
-    constexpr int kChunks = D / 8;  // 16-byte chunks of one head's row
+    constexpr int kChunks = D / 8;  // 8-element (16-byte) chunks of one head's new row
     if (lane < 2 * kChunks) {
         const bool is_v = lane >= kChunks;
         const int ci = is_v ? lane - kChunks : lane;
         const T *src = static_cast<const T *>(is_v ? a.v_new : a.k_new) + b * (is_v ? a.v_new_stride : a.k_new_stride) +
                        g * D + ci * 8;
-        T *dst = static_cast<T *>(is_v ? a.v_cache_w : a.k_cache_w) +
-                 (static_cast<int64_t>(slot) * a.num_kv_heads + g) * D + ci * 8;
-        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+        const int64_t e = (static_cast<int64_t>(slot) * a.num_kv_heads + g) * D + ci * 8;  // pool element
+        if constexpr (F8)
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(is_v ? a.v_cache_w : a.k_cache_w) + e) =
+                quantize8_e4m3<T>(raw, is_v ? a.v_scale : a.k_scale);
+        else
+            *reinterpret_cast<uint4 *>(static_cast<T *>(is_v ? a.v_cache_w : a.k_cache_w) + e) = raw;
         asm volatile("fence.proxy.async.global;\n" ::: "memory");
     }
     __syncwarp();
@@ -159,22 +162,30 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 }
 
 // Two E4M3 codes (low byte first) as an fp16 pair (low half first): exact,
-// every E4M3 value is an fp16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// every E4M3 value is an fp16 value.  e4m3x2_lo converts bytes 0-1 of the
+// word, e4m3x2_hi bytes 2-3 (the half is picked by the register move, no shift).
+__device__ __forceinline__ uint32_t e4m3x2_lo(uint32_t codes) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(out) : "r"(codes));
+    return out;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t codes) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(out) : "r"(codes));
+    return out;
 }
 
 // F8: the pool holds E4M3 codes (one byte per element, D = 128).  K and V are
-// converted to fp16 in registers and the warp MMAs run in fp16 (q converted
-// once).  ldmatrix moves 16-bit units, i.e. pairs of codes, so the fragments
-// use the contraction index in a fixed permutation, applied alike to both
-// operands: for S^T = K Q^T, k-step ks and lane quad j = lane % 4 hold
-// d = 16 ks + 4j + {0, 1} (fragment k = 2j, 2j+1) and 16 ks + 4j + {2, 3}
-// (k = 2j + 8, 2j + 9); for O^T = V^T P^T, row m = lane / 4 of block mt is
-// d = 16 mt + 2m and row m + 8 is d = 16 mt + 2m + 1 (the transposed load
-// gives each lane two tokens of two neighbouring d; one byte permutation
-// splits them by d).
+// widened to fp16 in registers (exactly: every E4M3 value is an fp16 value)
+// and the warp MMAs run in fp16, q converted once.  ldmatrix moves 16-bit
+// units, i.e. pairs of codes, so the fragments use the contraction index in a
+// fixed permutation, applied alike to both operands: for S^T = K Q^T, k-step
+// ks and lane quad j = lane % 4 hold d = 16 ks + 4j + {0, 1} (fragment k = 2j,
+// 2j+1) and 16 ks + 4j + {2, 3} (k = 2j + 8, 2j + 9); for O^T = V^T P^T, the
+// transposed load gives each lane two tokens of two neighbouring d, one byte
+// permutation splits them by d, and row m = lane / 4 of block mt holds
+// d = 16 mt + 2m, row m + 8 holds d = 16 mt + 2m + 1.  V stays in codes until
+// its MMA (fewer live registers).
 template <typename T, int D, int ST, bool F8>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -244,7 +255,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
 
     // query fragments (B operand of S^T = K Q^T): head lane/4 of the group
     uint32_t qb[S::kKSteps][2];
-    {
+    if constexpr (F8) {  // fp16, contraction index d = 16 ks + 4j + {0..3} (see the F8 note above)
+        const int hq = lane >> 2, j = lane & 3;
+        const T *qrow = static_cast<const T *>(a.q) + static_cast<int64_t>(b) * a.q_row_stride +
+                        static_cast<int64_t>(g * a.group + hq) * D;
+#pragma unroll
+        for (int ks = 0; ks < S::kKSteps; ++ks) {
+            if (hq < a.group && warp < kConsumerWarps) {
+                const T *qd = qrow + ks * 16 + 4 * j;
+                qb[ks][0] = Dt<__half>::pack(static_cast<float>(qd[0]), static_cast<float>(qd[1]));
+                qb[ks][1] = Dt<__half>::pack(static_cast<float>(qd[2]), static_cast<float>(qd[3]));
+            } else {
+                qb[ks][0] = qb[ks][1] = 0u;
+            }
+        }
+    } else {
         const int hq = lane >> 2;
         const int dq = (lane & 3) * 2;
         const T *qrow = static_cast<const T *>(a.q) + static_cast<int64_t>(b) * a.q_row_stride +
@@ -252,14 +277,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) {
             if (hq < a.group && warp < kConsumerWarps) {
-                if constexpr (F8) {  // d = 16 ks + 4j + {0..3}, as fp16
-                    const T *qd = qrow + ks * 16 + 2 * dq;
-                    qb[ks][0] = Dt<__half>::pack(static_cast<float>(qd[0]), static_cast<float>(qd[1]));
-                    qb[ks][1] = Dt<__half>::pack(static_cast<float>(qd[2]), static_cast<float>(qd[3]));
-                } else {
-                    qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + dq);
-                    qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + dq);
-                }
+                qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + dq);
+                qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + dq);
             } else {
                 qb[ks][0] = qb[ks][1] = 0u;
             }
@@ -275,8 +294,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     int issued = 0;                                             // tiles the producer started
 
     if (warp == kProducerWarp) {
-        if constexpr (!F8)
-            if (a.slot_mapping && end == L) store_new_row<T, D>(a, b, g, L, lane);
+        if (a.slot_mapping && end == L) store_new_row<T, D, F8>(a, b, g, L, lane);
         if (lane == 0) {
             const int box_rows = min(1 << a.log2_bs, kTile);
             const int bs_mask = (1 << a.log2_bs) - 1;
@@ -320,33 +338,29 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
             }
             const uint32_t kb = ring + s * S::kStageBytes;
             const uint32_t vb = kb + S::kTileBytes;
-            uint32_t kf[S::kKSteps][4], vf[S::kKSteps][4];
+            uint32_t kf[S::kKSteps][4];
+            uint32_t vf[F8 ? S::kKSteps / 2 : S::kKSteps][4];  // F8: byte-permuted codes, widened at the MMA
             if constexpr (F8) {
                 // one x4 load covers two 16-byte d chunks of the warp's 16 tokens
 #pragma unroll
                 for (int kp = 0; kp < S::kKSteps / 2; ++kp) {
                     uint32_t r0, r1, r2, r3;
                     ldmatrix_x4(kb + tile_off(rk, kp * 2 + ck), r0, r1, r2, r3);
-                    kf[2 * kp][0] = e4m3x2_to_f16x2(r0);
-                    kf[2 * kp][1] = e4m3x2_to_f16x2(r1);
-                    kf[2 * kp][2] = e4m3x2_to_f16x2(r0 >> 16);
-                    kf[2 * kp][3] = e4m3x2_to_f16x2(r1 >> 16);
-                    kf[2 * kp + 1][0] = e4m3x2_to_f16x2(r2);
-                    kf[2 * kp + 1][1] = e4m3x2_to_f16x2(r3);
-                    kf[2 * kp + 1][2] = e4m3x2_to_f16x2(r2 >> 16);
-                    kf[2 * kp + 1][3] = e4m3x2_to_f16x2(r3 >> 16);
+                    kf[2 * kp][0] = e4m3x2_lo(r0);
+                    kf[2 * kp][1] = e4m3x2_lo(r1);
+                    kf[2 * kp][2] = e4m3x2_hi(r0);
+                    kf[2 * kp][3] = e4m3x2_hi(r1);
+                    kf[2 * kp + 1][0] = e4m3x2_lo(r2);
+                    kf[2 * kp + 1][1] = e4m3x2_lo(r3);
+                    kf[2 * kp + 1][2] = e4m3x2_hi(r2);
+                    kf[2 * kp + 1][3] = e4m3x2_hi(r3);
                     ldmatrix_x4_trans(vb + tile_off(rk, kp * 2 + ck), r0, r1, r2, r3);
-                    // bytes (token 2j, d 2m), (2j, 2m+1), (2j+1, 2m), (2j+1, 2m+1) -> split by d
-                    const uint32_t p0 = __byte_perm(r0, 0, 0x3120), p1 = __byte_perm(r1, 0, 0x3120);
-                    const uint32_t p2 = __byte_perm(r2, 0, 0x3120), p3 = __byte_perm(r3, 0, 0x3120);
-                    vf[2 * kp][0] = e4m3x2_to_f16x2(p0);
-                    vf[2 * kp][1] = e4m3x2_to_f16x2(p0 >> 16);
-                    vf[2 * kp][2] = e4m3x2_to_f16x2(p1);
-                    vf[2 * kp][3] = e4m3x2_to_f16x2(p1 >> 16);
-                    vf[2 * kp + 1][0] = e4m3x2_to_f16x2(p2);
-                    vf[2 * kp + 1][1] = e4m3x2_to_f16x2(p2 >> 16);
-                    vf[2 * kp + 1][2] = e4m3x2_to_f16x2(p3);
-                    vf[2 * kp + 1][3] = e4m3x2_to_f16x2(p3 >> 16);
+                    // bytes (token 2j, d 2m), (2j, 2m+1), (2j+1, 2m), (2j+1, 2m+1) -> split by d:
+                    // bytes 0-1 are tokens 2j, 2j+1 of d 2m, bytes 2-3 those of d 2m+1
+                    vf[kp][0] = __byte_perm(r0, 0, 0x3120);
+                    vf[kp][1] = __byte_perm(r1, 0, 0x3120);
+                    vf[kp][2] = __byte_perm(r2, 0, 0x3120);
+                    vf[kp][3] = __byte_perm(r3, 0, 0x3120);
                 }
             } else {
 #pragma unroll
@@ -359,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bars + 8 * (kStages + s));  // stage free for the next tile
 
-            // S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8), two independent chains
+            // S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8), independent chains
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < S::kKSteps; ks += 2) {
@@ -378,14 +392,26 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
                 // V rows past the end may hold anything (NaN): zero them in the fragments,
                 // whose tokens are 2*(lane%4) + {0, 1} (regs 0, 1) and + 8 (regs 2, 3)
                 const int jt = tile_start + wrow + (lane & 3) * 2;
-                const uint32_t lo = (jt < end ? 0xFFFFu : 0u) | (jt + 1 < end ? 0xFFFF0000u : 0u);
-                const uint32_t hi = (jt + 8 < end ? 0xFFFFu : 0u) | (jt + 9 < end ? 0xFFFF0000u : 0u);
+                if constexpr (F8) {  // codes: bytes 0, 2 are token 2j (+8 in regs 1, 3), bytes 1, 3 token 2j+1
+                    const uint32_t lo = (jt < end ? 0x00FF00FFu : 0u) | (jt + 1 < end ? 0xFF00FF00u : 0u);
+                    const uint32_t hi = (jt + 8 < end ? 0x00FF00FFu : 0u) | (jt + 9 < end ? 0xFF00FF00u : 0u);
 #pragma unroll
-                for (int mt = 0; mt < S::kKSteps; ++mt) {
-                    vf[mt][0] &= lo;
-                    vf[mt][1] &= lo;
-                    vf[mt][2] &= hi;
-                    vf[mt][3] &= hi;
+                    for (int kp = 0; kp < S::kKSteps / 2; ++kp) {
+                        vf[kp][0] &= lo;
+                        vf[kp][1] &= hi;
+                        vf[kp][2] &= lo;
+                        vf[kp][3] &= hi;
+                    }
+                } else {
+                    const uint32_t lo = (jt < end ? 0xFFFFu : 0u) | (jt + 1 < end ? 0xFFFF0000u : 0u);
+                    const uint32_t hi = (jt + 8 < end ? 0xFFFFu : 0u) | (jt + 9 < end ? 0xFFFF0000u : 0u);
+#pragma unroll
+                    for (int mt = 0; mt < S::kKSteps; ++mt) {
+                        vf[mt][0] &= lo;
+                        vf[mt][1] &= lo;
+                        vf[mt][2] &= hi;
+                        vf[mt][3] &= hi;
+                    }
                 }
             }
             // move the reference maximum only when a score exceeds it by more than 2^8
@@ -424,9 +450,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
             const uint32_t pb0 = movmatrix_trans(Dt<MT>::pack(p0, p1));
             const uint32_t pb1 = movmatrix_trans(Dt<MT>::pack(p2, p3));
             // O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 x 8)
+            if constexpr (F8) {
 #pragma unroll
-            for (int mt = 0; mt < S::kKSteps; ++mt)
-                Mma<MT>::run(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
+                for (int mt = 0; mt < S::kKSteps; ++mt) {
+                    const uint32_t pa = vf[mt >> 1][(mt & 1) * 2], pc = vf[mt >> 1][(mt & 1) * 2 + 1];
+                    Mma<MT>::run(o[mt], e4m3x2_lo(pa), e4m3x2_hi(pa), e4m3x2_lo(pc), e4m3x2_hi(pc), pb0, pb1);
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < S::kKSteps; ++mt)
+                    Mma<MT>::run(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
+            }
         }
     }
     __syncthreads();
@@ -652,6 +686,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.num_blocks = num_blocks;
     a.log2_bs = ilog2(block_size);
     a.scale_log2 = scale * kLog2e * (fp8 ? fp8->k_scale : 1.f);
+    a.k_scale = fp8 ? fp8->k_scale : 1.f;
     a.v_scale = fp8 ? fp8->v_scale : 1.f;
     a.out = out;
     const size_t n = static_cast<size_t>(batch) * num_q_heads * plan.max_parts;

@@ -160,6 +160,36 @@ size_t decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads
         .ws_bytes;
 }
 
+// pa_store_decode, or with scales pa_store_decode_fp8 (E4M3 pool).
+int store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                 const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache, void *v_cache,
+                 const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                 float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag,
+                 void *stream, const pa::Fp8Scales *fp8) {
+    pa::DecodePlan plan{};
+    const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
+                                workspace, workspace_bytes, dtype, &plan, fp8);
+    if (rc) return rc;
+    if (batch == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "k, v and slot_mapping are required");
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (k_row_stride < row || v_row_stride < row || k_row_stride % 8 || v_row_stride % 8)
+        return fail(PA_ERR_INVALID_ARG, "k/v row strides (%lld, %lld) must be multiples of 8 and at least H_kv*D",
+                    (long long)k_row_stride, (long long)v_row_stride);
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    const pa::FusedStore fused{k, v, k_row_stride, v_row_stride, slot_mapping};
+    return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         block_size, scale, out, workspace, plan, dtype, err_flag,
+                                         static_cast<cudaStream_t>(stream), &fused, fp8),
+                       fp8 ? "pa_store_decode_fp8 launch" : "pa_store_decode launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -222,27 +252,23 @@ int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t 
                     int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                     int32_t block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
                     pa_dtype dtype, int32_t *err_flag, void *stream) {
-    pa::DecodePlan plan{};
-    const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                                batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
-                                workspace, workspace_bytes, dtype, &plan);
-    if (rc) return rc;
-    if (batch == 0) {
-        g_err[0] = '\0';
-        return PA_OK;
-    }
-    if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "k, v and slot_mapping are required");
-    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
-    if (k_row_stride < row || v_row_stride < row || k_row_stride % 8 || v_row_stride % 8)
-        return fail(PA_ERR_INVALID_ARG, "k/v row strides (%lld, %lld) must be multiples of 8 and at least H_kv*D",
-                    (long long)k_row_stride, (long long)v_row_stride);
-    if (!aligned(k, 16) || !aligned(v, 16)) return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
-    const pa::FusedStore fused{k, v, k_row_stride, v_row_stride, slot_mapping};
-    return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                         context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
-                                         block_size, scale, out, workspace, plan, dtype, err_flag,
-                                         static_cast<cudaStream_t>(stream), &fused),
-                       "pa_store_decode launch");
+    return store_decode(k, v, k_row_stride, v_row_stride, slot_mapping, q, q_row_stride, k_cache, v_cache,
+                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                        num_blocks, block_size, scale, out, workspace, workspace_bytes, dtype, err_flag, stream,
+                        nullptr);
+}
+
+int pa_store_decode_fp8(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                        const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                        void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                        const int32_t *context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, float k_scale,
+                        float v_scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                        int32_t *err_flag, void *stream) {
+    const pa::Fp8Scales sc{k_scale, v_scale};
+    return store_decode(k, v, k_row_stride, v_row_stride, slot_mapping, q, q_row_stride, k_cache, v_cache,
+                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                        num_blocks, block_size, scale, out, workspace, workspace_bytes, dtype, err_flag, stream, &sc);
 }
 
 int pa_decode_fp8(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,

@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,6 +28,27 @@ template <> struct Dt<__nv_bfloat16> {
     }
     static __device__ __forceinline__ __nv_bfloat16 from_float(float a) { return __float2bfloat16_rn(a); }
 };
+
+// Eight 16-bit elements (one 16-byte vector) as eight E4M3 codes, element i in
+// byte i: the nearest E4M3 value of x / scale (IEEE fp32 division, ties to
+// even, saturating at +-448, NaN stays NaN).
+template <typename T> __device__ __forceinline__ uint2 quantize8_e4m3(const uint4 raw, float scale) {
+    const T *x = reinterpret_cast<const T *>(&raw);
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            const float2 f = make_float2(static_cast<float>(x[4 * h + e]) / scale,
+                                         static_cast<float>(x[4 * h + e + 1]) / scale);
+            const __nv_fp8x2_storage_t pair = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+            bytes |= static_cast<uint32_t>(pair) << (8 * e);
+        }
+        w[h] = bytes;
+    }
+    return make_uint2(w[0], w[1]);
+}
 
 // ------------------------------------------------------------ error flag
 

@@ -7,7 +7,6 @@
 // moves one token's K and V rows with 16-byte vector accesses (when the
 // pointers and strides allow), every lane holding all its loads in flight
 // before it stores, so each SM keeps tens of KB of reads outstanding.
-#include <cuda_fp8.h>
 
 #include "pa_common.cuh"
 
@@ -93,27 +92,11 @@ store_kv_fp8_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t k_
         if (lane == 0) raise_flag(err_flag, PA_FLAG_BAD_SLOT);
         return;
     }
-    auto convert = [](const T *src, uint8_t *dst, float scale) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(src);
-        const T *x = reinterpret_cast<const T *>(&raw);
-        uint32_t w[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                const float2 f = make_float2(static_cast<float>(x[4 * h + e]) / scale,
-                                             static_cast<float>(x[4 * h + e + 1]) / scale);
-                const __nv_fp8x2_storage_t pair = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
-                bytes |= static_cast<uint32_t>(pair) << (8 * e);
-            }
-            w[h] = bytes;
-        }
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
-    };
     for (int i = 8 * lane; i < row; i += 32 * 8) {
-        convert(k + t * k_stride + i, k_cache + slot * row + i, k_scale);
-        convert(v + t * v_stride + i, v_cache + slot * row + i, v_scale);
+        *reinterpret_cast<uint2 *>(k_cache + slot * row + i) =
+            quantize8_e4m3<T>(*reinterpret_cast<const uint4 *>(k + t * k_stride + i), k_scale);
+        *reinterpret_cast<uint2 *>(v_cache + slot * row + i) =
+            quantize8_e4m3<T>(*reinterpret_cast<const uint4 *>(v + t * v_stride + i), v_scale);
     }
 }
 

@@ -208,3 +208,21 @@ def test_fp8_decode_validation(lib):
     lib.pa_decode_fp8_workspace_bytes.restype = ctypes.c_size_t
     assert lib.pa_decode_fp8_workspace_bytes(64, 16, 8, 128, 16, 256) > 0
     assert lib.pa_decode_fp8_workspace_bytes(64, 16, 8, 128, 16, 12) == 0
+
+
+def test_fp8_store_decode_validation(lib):
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, ks=1024, vs=1024, sm=FAKE, q=FAKE, qs=2048, kc=FAKE, vc=FAKE, bt=FAKE, mb=16, cl=FAKE,
+                 B=64, hq=16, hkv=8, d=128, n=700, bs=256, scale=0.088, ksc=0.01, vsc=0.01, out=FAKE, ws=FAKE,
+                 wsb=1 << 30, dt=1)
+        a.update(kw)
+        return lib.pa_store_decode_fp8(a["k"], a["v"], a["ks"], a["vs"], a["sm"], a["q"], a["qs"], a["kc"], a["vc"],
+                                       a["bt"], a["mb"], a["cl"], a["B"], a["hq"], a["hkv"], a["d"], a["n"], a["bs"],
+                                       ctypes.c_float(a["scale"]), ctypes.c_float(a["ksc"]), ctypes.c_float(a["vsc"]),
+                                       a["out"], a["ws"], a["wsb"], a["dt"], None, None)
+    assert call(k=None) == -1 and call(sm=None) == -1
+    assert call(ks=1020) == -1                                # not a multiple of 8
+    assert call(v=ctypes.c_void_p((1 << 20) + 8)) == -1      # 16-byte alignment
+    assert call(d=64, qs=1024, ks=512, vs=512) == -2          # head_dim 128 only
+    assert call(vsc=0.0) == -1
+    assert call(B=0, k=None, v=None, sm=None, q=None, out=None, ws=None) == 0

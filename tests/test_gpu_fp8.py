@@ -212,3 +212,87 @@ def test_decode_fp8_accepts_float8_tensors(pa):
                            s.block_tables.cuda(), s.context_lens.cuda(), s.scale, fs.k_scale, fs.v_scale)
     torch.cuda.synchronize()
     assert torch.equal(out_u8, out_f8)
+
+
+# ---- the fused step (pa_store_decode_fp8)
+
+
+def _fused_fp8(pa, fs, err_flag=None):
+    s = fs.step
+    kc, vc = fs.k_cache.cuda(), fs.v_cache.cuda()
+    out = pa.store_decode_fp8(s.k_new.cuda(), s.v_new.cuda(), s.slot_mapping.cuda(), s.q.cuda(), kc, vc,
+                              s.block_tables.cuda(), s.context_lens.cuda(), s.scale, fs.k_scale, fs.v_scale,
+                              err_flag=err_flag)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+@pytest.mark.parametrize("name", ["qwen3_0p6b", "shapes_bs16", "bs8_long"])
+def test_store_decode_fp8_equals_store_then_decode(pa, name):
+    if name == "qwen3_0p6b":
+        fs = inputs.qwen3_0p6b_decode_fp8()
+    elif name == "shapes_bs16":
+        fs = inputs.make_decode_fp8([0, 1, 2, 15, 16, 17, 63, 64, 65, 500, 1025, 3000], num_q_heads=32,
+                                    num_kv_heads=8, head_dim=128, block_size=16, dtype=torch.float16, seed=160)
+    else:
+        fs = inputs.make_decode_fp8([8, 9, 4000, 777], num_q_heads=8, num_kv_heads=1, head_dim=128, block_size=8,
+                                    dtype=torch.bfloat16, seed=161)
+    s = fs.step
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fused, kc, vc = _fused_fp8(pa, fs, err_flag=flag)
+    assert int(flag.item()) == 0
+    two, kc2, vc2 = _run_fp8_step(pa, fs)
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2), "pools differ between fused and two-call steps"
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16)), "outputs differ"
+    okc, ovc = fs.k_cache.clone(), fs.v_cache.clone()
+    oracle.store_kv_fp8(s.k_new, s.v_new, okc, ovc, s.slot_mapping, fs.k_scale, fs.v_scale)
+    assert torch.equal(kc.cpu(), okc)
+    ref = oracle.decode_fp8(s.q, okc, ovc, s.block_tables, s.context_lens, s.scale, fs.k_scale, fs.v_scale)
+    assert max_err(fused, ref) <= TOL[s.q.dtype]
+
+
+def test_store_decode_fp8_wrong_slot_is_flagged_and_not_stored(pa):
+    fs = inputs.make_decode_fp8([40, 100, 7], num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                                dtype=torch.bfloat16, seed=162)
+    s = fs.step
+    bad = s.slot_mapping.clone()
+    bad[1] = bad[1] - 1  # the slot of position L-2: not this step's token
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kc, vc = fs.k_cache.cuda(), fs.v_cache.cuda()
+    pa.store_decode_fp8(s.k_new.cuda(), s.v_new.cuda(), bad.cuda(), s.q.cuda(), kc, vc, s.block_tables.cuda(),
+                        s.context_lens.cuda(), s.scale, fs.k_scale, fs.v_scale, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) & pa.FLAG_BAD_SLOT
+    row = lambda c, slot: c.view(-1, c.shape[2] * c.shape[3])[slot]  # noqa: E731
+    assert torch.equal(row(kc.cpu(), int(bad[1])), row(fs.k_cache, int(bad[1]))), "the wrong slot was written"
+
+
+def test_store_decode_fp8_graph_replay(pa):
+    """The fused fp8 step captured in a CUDA graph and replayed gives the eager result."""
+    fs = inputs.make_decode_fp8([300, 1000, 77, 4096], num_q_heads=16, num_kv_heads=8, head_dim=128,
+                                block_size=256, dtype=torch.bfloat16, seed=163)
+    s = fs.step
+    d = {k: t.cuda() for k, t in dict(k=s.k_new, v=s.v_new, sm=s.slot_mapping, q=s.q, bt=s.block_tables,
+                                      cl=s.context_lens).items()}
+    kc, vc = fs.k_cache.cuda(), fs.v_cache.cuda()
+    out = torch.empty_like(d["q"])
+    nbytes = pa.decode_fp8_workspace_bytes(4, 16, 8, 128, s.block_tables.shape[1], 256)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+
+    def step():
+        pa.store_decode_fp8(d["k"], d["v"], d["sm"], d["q"], kc, vc, d["bt"], d["cl"], s.scale, fs.k_scale,
+                            fs.v_scale, out=out, workspace=ws)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        step()
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
