@@ -58,7 +58,10 @@ constexpr int kF8Stages = 3;
 constexpr int kMaxTablePages = 257;  // block-table entries one partition may touch
 constexpr int kMaxPartition = 2048;
 constexpr int kMinPartition = 128;
-constexpr int kTargetWaves = 8;  // ragged batches: enough waves to absorb the length spread
+// Ragged batches: enough waves to absorb the length spread.  Measured on the Qwen3-0.6B-like
+// workload (64 sequences, context U[128, 4096]): 4 waves (1024-token partitions) beat 8 (512)
+// by 1.4 % on the bf16 pool and by 9 % on the E4M3 pool, whose CTAs stream half the bytes.
+constexpr int kTargetWaves = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
