@@ -52,7 +52,8 @@ DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 # capture of the current kernels (profiles/decode_<workload>.md); a workload
 # missing here reports null.
 TRAFFIC_PER_CALL = {
-    "qwen3_0p6b_decode": 583_113_472 + 5_264_128,       # decode_partition_kernel
+    "qwen3_0p6b_decode": 583_123_968 + 4_384_000,       # decode_partition_kernel (store fused)
+    "qwen3_0p6b_decode_fp8": 291_855_872 + 3_784_448,   # decode_partition_kernel, E4M3 pool (store fused)
     "long_context_decode": 536_950_784 + 3_327_232,     # decode_partition_kernel
     "qwen3_8b_shared_decode": 868_519_936 + 5_361_152,  # decode_partition_kernel (L2 absorbs shared pages)
 }
