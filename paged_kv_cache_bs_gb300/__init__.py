@@ -16,6 +16,10 @@ The functions mirror the C ABI in ``include/pa_api.h``:
 * :func:`store_decode_fp8` -- ``pa_store_decode_fp8`` (the fp8 store fused into fp8 decode)
 * :func:`prefill_paged`  -- ``pa_prefill_paged``
 * :func:`sample`         -- ``pa_sample`` (temperature sampling, exponential race)
+
+``paged_kv_cache_bs_gb300.graphs.DecodeGraphRunner`` replays the decode step of a layer
+from CUDA graphs captured per padded batch size; ``paged_kv_cache_bs_gb300.block_manager``
+binds the native page directory.
 """
 
 from __future__ import annotations

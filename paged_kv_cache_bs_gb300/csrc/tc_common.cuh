@@ -173,6 +173,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 2^x on the FMA pipe, for the share of a softmax's exponentials that the MUFU
+// pipe would otherwise queue: x = n + r with n = round(x) (adding 1.5 * 2^23
+// leaves round(x) in the low mantissa bits) and |r| <= 1/2, 2^r = e^(r ln 2)
+// by its Taylor series to degree 4 (relative error below 7e-5, far under the
+// 16-bit rounding of P), and n added to the exponent field.  x is clamped at
+// -126 (a result far below any 16-bit P), so -inf gives 2^-126, not 0.
+__device__ __forceinline__ float exp2_fma(float x) {
+    const float xc = fmaxf(x, -126.f);
+    const float t = xc + 12582912.f;
+    const int n = __float_as_int(t) - 0x4B400000;
+    const float r = xc - (t - 12582912.f);
+    float p = fmaf(r, 0.009618129107628477f, 0.05550410866482158f);  // ln2^4 / 4!, ln2^3 / 3!
+    p = fmaf(p, r, 0.2402265069591007f);                               // ln2^2 / 2!
+    p = fmaf(p, r, 0.6931471805599453f);                               // ln2
+    p = fmaf(p, r, 1.0f);
+    return __int_as_float(__float_as_int(p) + (n << 23));
+}
+
 // ---------------------------------------------------------------------- UMMA
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled tile whose 8-row

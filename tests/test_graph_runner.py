@@ -1,0 +1,76 @@
+"""The bucketed CUDA-graph decode runner ("nano-vLLM Part 2", section 4.2): bucket sizes on
+the CPU; on the GPU, a replayed step equals the eager fused call on the same inputs (output
+and pool bit-identical), for batch sizes that fill a bucket and ones that need padding rows,
+over 16-bit and E4M3 pools."""
+
+import pytest
+import torch
+
+import oracle
+from tests import inputs
+from tests.gpu_cases import TOL, max_err
+
+
+def test_graph_batch_sizes():
+    from paged_kv_cache_bs_gb300.graphs import graph_batch_sizes
+    assert graph_batch_sizes(1) == [1]
+    assert graph_batch_sizes(8) == [1, 2, 4, 8]
+    assert graph_batch_sizes(64) == [1, 2, 4, 8, 16, 32, 48, 64]
+    assert graph_batch_sizes(100) == [1, 2, 4, 8, 16, 32, 48, 64, 80, 96, 100]
+    assert graph_batch_sizes(512)[-1] == 512 and len(graph_batch_sizes(512)) == 4 + 32
+    with pytest.raises(ValueError):
+        graph_batch_sizes(0)
+
+
+def _eager(pa, st, kc, vc, fs=None):
+    d = {k: t.cuda() for k, t in dict(k=st.k_new, v=st.v_new, sm=st.slot_mapping, q=st.q, bt=st.block_tables,
+                                      cl=st.context_lens).items()}
+    if fs is None:
+        out = pa.store_decode(d["k"], d["v"], d["sm"], d["q"], kc, vc, d["bt"], d["cl"], st.scale)
+    else:
+        out = pa.store_decode_fp8(d["k"], d["v"], d["sm"], d["q"], kc, vc, d["bt"], d["cl"], st.scale, fs.k_scale,
+                                  fs.v_scale)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fp8", [False, True])
+def test_runner_equals_eager_step(pa, fp8):
+    from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
+    ctx_all = torch.randint(1, 3000, (40,), generator=torch.Generator().manual_seed(170)).tolist()
+    kw = dict(num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=16, dtype=torch.bfloat16, seed=171)
+    fs = inputs.make_decode_fp8(ctx_all, **kw) if fp8 else None
+    st = fs.step if fp8 else inputs.make_decode(ctx_all, **kw)
+    pool_k, pool_v = (fs.k_cache, fs.v_cache) if fp8 else (st.pool.k_cache, st.pool.v_cache)
+    width = st.block_tables.shape[1]
+    kc, vc = pool_k.cuda(), pool_v.cuda()
+    runner = DecodeGraphRunner(kc, vc, 16, 40, width, st.scale, torch.bfloat16,
+                               k_scale=fs.k_scale if fp8 else None, v_scale=fs.v_scale if fp8 else None)
+    for batch in (1, 3, 16, 17, 40):  # exact buckets and padded ones
+        b = runner.bucket(batch)
+        # the eager call on the bucket's padded inputs (slot -1, context 0 past `batch`): the split-K
+        # plan depends on the batch size, so the graph of bucket b matches the eager call of size b
+        pad = lambda t, v: torch.cat([t[:batch], torch.full((b - batch,) + tuple(t.shape[1:]), v, dtype=t.dtype)])  # noqa: E731
+        sub = type(st)(st.pool, st.num_q_heads, pad(st.q, 0), pad(st.k_new, 0), pad(st.v_new, 0),
+                       pad(st.slot_mapping, -1), pad(st.block_tables, -1), pad(st.context_lens, 0), st.scale)
+        kc2, vc2 = pool_k.cuda(), pool_v.cuda()
+        ref = _eager(pa, sub, kc2, vc2, fs)[:batch]
+        kc.copy_(pool_k.cuda())
+        vc.copy_(pool_v.cuda())
+        sl = slice(0, batch)
+        got = runner.step(st.q[sl], st.k_new[sl], st.v_new[sl], st.slot_mapping[sl], st.context_lens[sl],
+                          st.block_tables[sl])
+        assert got.shape == ref.shape
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"batch {batch}: output differs"
+        bits = (lambda t: t.cpu().view(torch.uint8))  # noqa: E731  (NaN sentinels compare by bits)
+        assert torch.equal(bits(kc), bits(kc2)) and torch.equal(bits(vc), bits(vc2)), f"batch {batch}: pool differs"
+    # and the replayed step against the oracle on the real rows
+    okc, ovc = pool_k.clone(), pool_v.clone()
+    if fp8:
+        oracle.store_kv_fp8(st.k_new, st.v_new, okc, ovc, st.slot_mapping, fs.k_scale, fs.v_scale)
+        ref = oracle.decode_fp8(st.q, okc, ovc, st.block_tables, st.context_lens, st.scale, fs.k_scale, fs.v_scale)
+    else:
+        oracle.store_kv(st.k_new, st.v_new, okc, ovc, st.slot_mapping)
+        ref = oracle.decode(st.q, okc, ovc, st.block_tables, st.context_lens, st.scale)
+    assert max_err(got, ref) <= TOL[st.q.dtype]
