@@ -365,13 +365,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int e = 0; e < kBN; ++e)
                     if (e > lim) sr[e] = __float_as_uint(-INFINITY);
             }
+            // row maximum: three-input maxima, eight independent chains
             float m8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(sr[e]);
 #pragma unroll
-            for (int e = 8; e < kBN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * c;
+            for (int e = 8; e < kBN; e += 16)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    m8[j] = tc::max3(m8[j], __uint_as_float(sr[e + j]), __uint_as_float(sr[e + 8 + j]));
+            const float mx = tc::max3(tc::max3(m8[0], m8[1], m8[2]), tc::max3(m8[3], m8[4], m8[5]),
+                                      fmaxf(m8[6], m8[7])) * c;
             // running maximum, moved only when this tile exceeds it by more than 2^8
             const float m_new = fmaxf(m_used, mx);
             float alpha = 1.f;
@@ -395,24 +399,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             // P = 2^(c*s - m), packed to 16 bits over the first 64 columns of S; the two
             // halves' stores are issued back to back and waited for once.
-            const float neg_m = -m_used;
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            // scale and shift two scores per instruction (packed fp32 pairs), sum P in pairs too
+            const unsigned long long cc2 = tc::f32x2(c, c), nm2 = tc::f32x2(-m_used, -m_used);
+            unsigned long long l2[2] = {0ull, 0ull};
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pw[32];
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
-                    const float x0 = fmaf(__uint_as_float(sr[64 * half + e]), c, neg_m);
-                    const float x1 = fmaf(__uint_as_float(sr[64 * half + e + 1]), c, neg_m);
-                    const float p0 = tc::ex2_approx(x0);
-                    const float p1 = tc::ex2_approx(x1);
-                    l4[(e >> 1) & 3] += p0 + p1;
+                    const unsigned long long x = tc::fma_f32x2(
+                        tc::f32x2(__uint_as_float(sr[64 * half + e]), __uint_as_float(sr[64 * half + e + 1])), cc2,
+                        nm2);
+                    const float p0 = tc::ex2_approx(tc::f32x2_lo(x));
+                    const float p1 = tc::ex2_approx(tc::f32x2_hi(x));
+                    l2[(e >> 1) & 1] = tc::add_f32x2(l2[(e >> 1) & 1], tc::f32x2(p0, p1));
                     pw[e >> 1] = Dt<T>::pack(p0, p1);
                 }
                 tc::tmem_st32_nowait(tS(w) + lane_base + 32 * half, pw);  // P columns [32*half, 32*half + 32)
             }
             tc::tmem_wait_st();
-            l_sum = l_sum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+            const unsigned long long ls = tc::add_f32x2(l2[0], l2[1]);
+            l_sum = l_sum * alpha + (tc::f32x2_lo(ls) + tc::f32x2_hi(ls));
             const int valid = min(kBN, Lk - j0);
             if (w == 0 && valid < kBN) {
                 // V rows past the context may hold anything (NaN included): zero them so P V stays

@@ -173,22 +173,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// 2^x on the FMA pipe, for the share of a softmax's exponentials that the MUFU
-// pipe would otherwise queue: x = n + r with n = round(x) (adding 1.5 * 2^23
-// leaves round(x) in the low mantissa bits) and |r| <= 1/2, 2^r = e^(r ln 2)
-// by its Taylor series to degree 4 (relative error below 7e-5, far under the
-// 16-bit rounding of P), and n added to the exponent field.  x is clamped at
-// -126 (a result far below any 16-bit P), so -inf gives 2^-126, not 0.
-__device__ __forceinline__ float exp2_fma(float x) {
-    const float xc = fmaxf(x, -126.f);
-    const float t = xc + 12582912.f;
-    const int n = __float_as_int(t) - 0x4B400000;
-    const float r = xc - (t - 12582912.f);
-    float p = fmaf(r, 0.009618129107628477f, 0.05550410866482158f);  // ln2^4 / 4!, ln2^3 / 3!
-    p = fmaf(p, r, 0.2402265069591007f);                               // ln2^2 / 2!
-    p = fmaf(p, r, 0.6931471805599453f);                               // ln2
-    p = fmaf(p, r, 1.0f);
-    return __int_as_float(__float_as_int(p) + (n << 23));
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction does two fp32 operations)
+// and the three-input maximum.
+__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
+    return static_cast<unsigned long long>(__float_as_uint(lo)) |
+           (static_cast<unsigned long long>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float f32x2_lo(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f32x2_hi(unsigned long long v) {
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // ---------------------------------------------------------------------- UMMA
