@@ -211,12 +211,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
+    // The block-table entries this partition can touch are loaded together with the context
+    // length (one memory round trip before the first TMA instead of two); entries past the
+    // context are loaded (they lie inside the table's row) but never used.
+    const int start = p * a.partition;
+    const int first_page = start >> a.log2_bs;
+    const int span = min(a.max_blocks, ((start + a.partition - 1) >> a.log2_bs) + 1) - first_page;
+    constexpr int kPerThread = (kMaxTablePages + kThreads - 1) / kThreads;
+    int pg_pre[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int i = tid + k * kThreads;
+        pg_pre[k] = i < span ? a.block_tables[static_cast<int64_t>(b) * a.max_blocks + first_page + i] : 0;
+    }
     int L = context_len(a, b);
     if (L < 0) {
         if (p == 0 && tid == 0) raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
         L = 0;
     }
-    const int start = p * a.partition;
     T *out = static_cast<T *>(a.out);
     if (start >= L) {
         if (p == 0) {  // empty context (e.g. a padding row): zero output, no page read
@@ -233,15 +245,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     const int ntiles = (end - start + kTile - 1) / kTile;
 
     // block-table slice of this partition, validated once (a bad id is flagged and read as page 0)
-    const int first_page = start >> a.log2_bs;
-    const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;
-    for (int i = tid; i < npages; i += kThreads) {
-        int pg = a.block_tables[static_cast<int64_t>(b) * a.max_blocks + first_page + i];
-        if (pg < 0 || pg >= a.num_blocks) {
-            raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
-            pg = 0;
+    const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;  // <= span
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int i = tid + k * kThreads;
+        if (i < npages) {
+            int pg = pg_pre[k];
+            if (pg < 0 || pg >= a.num_blocks) {
+                raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
+                pg = 0;
+            }
+            bt_s[i] = pg;
         }
-        bt_s[i] = pg;
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
