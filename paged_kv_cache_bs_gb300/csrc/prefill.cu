@@ -168,11 +168,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     // mbarriers (8 bytes each) after the tiles
     const uint32_t bar0 = sb + S::kOffBar;
+    // Stage t = {V_t, K_(t+1)} lands on one barrier, and the MMA issuer frees both with one
+    // commit after PV(t) and S(t+1): per key tile, one wait and one commit for the tiles.
     const uint32_t bar_q = bar0;                                      // Q tiles landed
-    auto bar_kf = [&](int slot) { return bar0 + 8 + 8 * slot; };      // K slot landed
-    auto bar_ke = [&](int slot) { return bar0 + 24 + 8 * slot; };     // K slot read by both S MMAs
-    auto bar_vf = [&](int slot) { return bar0 + 40 + 8 * slot; };     // V slot landed
-    auto bar_ve = [&](int slot) { return bar0 + 56 + 8 * slot; };     // V slot read by both PV MMAs
+    const uint32_t bar_k0 = bar0 + 8;                                 // K_0 landed
+    auto bar_st = [&](int t) { return bar0 + 16 + 8 * (t & 1); };     // stage t landed (2 arrivals)
+    auto bar_done = [&](int i) { return bar0 + 32 + 8 * (i & 1); };   // MMAs of step i-1 done (see below)
     auto bar_s = [&](int w) { return bar0 + 72 + 8 * w; };            // S_w in TMEM
     auto bar_p = [&](int w) { return bar0 + 88 + 8 * w; };            // P_w in TMEM (128 arrivals)
     auto bar_o = [&](int w) { return bar0 + 104 + 8 * w; };           // PV_w done
@@ -181,11 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     if (tid == 0) {
         tc::mbar_init(bar_q, 1);
+        tc::mbar_init(bar_k0, 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar_kf(i), 1);
-            tc::mbar_init(bar_ke(i), 1);
-            tc::mbar_init(bar_vf(i), 1);
-            tc::mbar_init(bar_ve(i), 1);
+            tc::mbar_init(bar_st(i), 2);  // the V part and the K part (or a plain arrival)
+            tc::mbar_init(bar_done(i), 1);
             tc::mbar_init(bar_s(i), 1);
             tc::mbar_init(bar_p(i), kWgThreads);
             tc::mbar_init(bar_o(i), 1);
@@ -249,27 +249,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int hf = 0; hf < S::kHalves; ++hf)
                     tc::tma_load_2d(sb + S::kOffQ + w * S::kTile + hf * S::kHalf, &maps.q, (h0 + w) * D + hf * 64,
                                     q_start + q0, bar_q);
-            int k_issued = 0, v_issued = 0;  // tiles loaded, for the drain on abort
+            load(&maps.k, sb + S::kOffK, bar_k0, 0);
+            int issued = 0;  // stages loaded, for the drain on abort
             bool ok = true;
             for (int t = 0; t < nkt && ok; ++t) {
-                const int slot = t & 1;
-                if (t >= 2) ok = wait(bar_ke(slot), ((t - 2) >> 1) & 1);
+                // V_t goes to V slot t&1 (last read by PV(t-2)), K_(t+1) to K slot (t+1)&1 (last read
+                // by S(t-1)): both are free once step t-2's MMAs are done (for t = 1: S(0))
+                if (t >= 1) ok = wait(bar_done(t - 1), ((t - 1) >> 1) & 1);
                 if (!ok) break;
-                load(&maps.k, sb + S::kOffK + slot * S::kTile, bar_kf(slot), t);
-                k_issued = t + 1;
-                if (t >= 2) ok = wait(bar_ve(slot), ((t - 2) >> 1) & 1);
-                if (!ok) break;
-                load(&maps.v, sb + S::kOffV + slot * S::kTile, bar_vf(slot), t);
-                v_issued = t + 1;
+                load(&maps.v, sb + S::kOffV + (t & 1) * S::kTile, bar_st(t), t);
+                if (t + 1 < nkt)
+                    load(&maps.k, sb + S::kOffK + ((t + 1) & 1) * S::kTile, bar_st(t), t + 1);
+                else
+                    tc::mbar_arrive(bar_st(t));
+                issued = t + 1;
             }
             if (!ok) {  // let the copies this thread started land (bounded) before the CTA exits
                 raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
                 *abort_word = 1;
                 tc::mbar_wait(bar_q, 0, kWaitCycles);
-                for (int t = max(0, k_issued - 2); t < k_issued; ++t)
-                    tc::mbar_wait(bar_kf(t & 1), (t >> 1) & 1, kWaitCycles);
-                for (int t = max(0, v_issued - 2); t < v_issued; ++t)
-                    tc::mbar_wait(bar_vf(t & 1), (t >> 1) & 1, kWaitCycles);
+                tc::mbar_wait(bar_k0, 0, kWaitCycles);
+                for (int t = max(0, issued - 2); t < issued; ++t) tc::mbar_wait(bar_st(t), (t >> 1) & 1, kWaitCycles);
             }
         }
         __syncwarp();
@@ -290,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     const uint32_t off = ((ks / 4) * S::kHalf + (ks % 4) * 32) >> 4;
                     tc::umma_f16(tS(w), dq + off, dk + off, kIdS, ks > 0);
                 }
-                tc::umma_commit(bar_s(w));
             };
             auto issue_pv = [&](int w, int kt) {  // O_w += P_w V_kt, P_w from TMEM
                 const uint64_t dv = dV0 + static_cast<uint64_t>(((kt & 1) * S::kTile) >> 4);
@@ -298,42 +297,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int ks = 0; ks < kBN / 16; ++ks)
                     tc::umma_f16_ts(tO(w), tS(w) + ks * 8, dv + ((ks * 16 * 128) >> 4), kIdO,
                                     (kt > 0 || ks > 0) ? 1u : 0u);
-                tc::umma_commit(bar_o(w));
             };
+            // bar_done(i) completes when the MMAs issued before its i-th commit are done: i = 0
+            // after S(0) of both heads, i = t + 1 after PV(t) and S(t+1) of both heads
             int commits = 0;
-            uint32_t last_bar = 0, last_phase = 0;
-            bool ok = wait(bar_q, 0) && wait(bar_kf(0), 0);
+            bool ok = wait(bar_q, 0) && wait(bar_k0, 0);
             if (ok) {
                 tc::fence_after_sync();
-                for (int w = 0; w < nwg; ++w) issue_s(w, 0);
-                tc::umma_commit(bar_ke(0));
-                ++commits, last_bar = bar_ke(0), last_phase = 0;
+                for (int w = 0; w < nwg; ++w) {
+                    issue_s(w, 0);
+                    tc::umma_commit(bar_s(w));
+                }
+                tc::umma_commit(bar_done(0));
+                ++commits;
             }
             for (int kt = 0; kt < nkt && ok; ++kt) {
                 // Per head: O += P V_kt as soon as its softmax is done, then S for the next tile
                 // (it overwrites P, which the PV just issued reads first: MMAs run in issue order).
-                ok = wait(bar_vf(kt & 1), (kt >> 1) & 1);
+                ok = wait(bar_st(kt), (kt >> 1) & 1);
                 const bool more = kt + 1 < nkt;
-                if (ok && more) ok = wait(bar_kf((kt + 1) & 1), ((kt + 1) >> 1) & 1);
                 for (int w = 0; w < nwg && ok; ++w) {
                     ok = wait(bar_p(w), kt & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
                     issue_pv(w, kt);
-                    if (more) issue_s(w, kt + 1);
+                    if (more) {
+                        issue_s(w, kt + 1);
+                        tc::umma_commit(bar_s(w));
+                    } else {
+                        tc::umma_commit(bar_o(w));
+                    }
                 }
                 if (!ok) break;
-                tc::umma_commit(bar_ve(kt & 1));  // V_kt free once both PVs are done
-                ++commits, last_bar = bar_ve(kt & 1), last_phase = (kt >> 1) & 1;
-                if (more) {
-                    tc::umma_commit(bar_ke((kt + 1) & 1));  // K_{kt+1} free once both S are done
-                    last_bar = bar_ke((kt + 1) & 1), last_phase = ((kt + 1) >> 1) & 1;
-                }
+                tc::umma_commit(bar_done(kt + 1));
+                ++commits;
             }
             if (!ok) {
                 raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
                 *abort_word = 1;
-                if (commits) tc::mbar_wait(last_bar, last_phase, kWaitCycles);  // covers every earlier MMA
+                // the last commit covers every earlier MMA of this thread
+                if (commits) tc::mbar_wait(bar_done(commits - 1), ((commits - 1) >> 1) & 1, kWaitCycles);
             }
         }
         __syncwarp();
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (w == 0 && valid < kBN) {
                 // V rows past the context may hold anything (NaN included): zero them so P V stays
                 // finite.  Head A does it; head B's PV is issued after head A's.
-                ok = __all_sync(0xffffffffu, wait(bar_vf(kt & 1), (kt >> 1) & 1));
+                ok = __all_sync(0xffffffffu, wait(bar_st(kt), (kt >> 1) & 1));
                 if (!ok) break;
                 const int per_half = (kBN - valid) * 8;
                 uint4 *vz = reinterpret_cast<uint4 *>(smem + S::kOffV + (kt & 1) * S::kTile);
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc::fence_before_sync();
             tc::mbar_arrive(bar_p(w));
         }
-        if (ok) ok = wait(bar_o(w), (nkt - 1) & 1);
+        if (ok) ok = wait(bar_o(w), 0);  // committed once, after the last PV
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc::fence_after_sync();
