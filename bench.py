@@ -57,7 +57,7 @@ TRAFFIC_PER_CALL = {
     "long_context_decode": 536_950_784 + 3_327_232,     # decode_partition_kernel
     "qwen3_8b_shared_decode": 868_519_936 + 5_361_152,  # decode_partition_kernel (L2 absorbs shared pages)
 }
-PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 118_655_488 + 12_742_400}  # prefill_kernel
+PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 117_771_520 + 12_707_584}  # prefill_kernel
 
 WORKLOAD_CONFIG = {
     "tiny_decode": dict(batch=4, context="{1,17,100,255}", H_q=4, H_kv=2, D=64, block_size=16, dtype="fp16"),

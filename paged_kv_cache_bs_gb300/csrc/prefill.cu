@@ -14,15 +14,19 @@
 // (one head without GQA), so every 128-key K/V tile serves two Q tiles.
 // Warp-specialised: warp 9 issues every TMA load, warp 8 every tcgen05.mma
 // (one thread each); warpgroups 0 and 1 run the softmax of heads A and B
-// (TMEM lane r = query row r); all hand-offs are mbarriers.  A single
-// tcgen05.mma issue takes ~100 cycles on this part, so S MMAs use N = 128
-// keys.  The heads ping-pong: while head A's softmax runs, the tensor core
-// does head B's PV and next S, and vice versa.  Each head's S tile is
-// overwritten in TMEM by its P, which the PV MMA reads from TMEM.
+// (TMEM lane r = query row r); all hand-offs are mbarriers.  Back-to-back
+// tcgen05.mma instructions issue at about their execution time (the tensor
+// core queues one or two), so the issuing thread is the critical path: S
+// MMAs use N = 128 keys, and per key tile the issuer does one wait and one
+// commit for the K/V tiles (V_t and K_(t+1) share a stage barrier).  The heads
+// ping-pong: while head A's softmax runs, the tensor core does head B's PV and
+// next S, and vice versa.  Each head's S tile is overwritten in TMEM by its P,
+// which the PV MMA reads from TMEM.
 //   * Q (once) and each 128-key K/V tile arrive by TMA with the 128-byte
 //     swizzle the MMA descriptors expect; K/V tiles are double-buffered and
 //     fetched page by page through the block table (one box per page when a
-//     page is shorter than the tile).
+//     page is shorter than the tile); stage t = {V_t, K_(t+1)} is refilled
+//     once the MMAs of step t-2 are done.
 //   * S = Q K^T: 128x128x16 tcgen05.mma steps, fp32 accumulator in TMEM.
 //   * Softmax: each thread owns one row; it loads its S row from TMEM, masks
 //     (causal, bottom-right aligned, and past the context), and exponentiates
