@@ -42,6 +42,7 @@ METRIC = "paged decode KV GB/s (% of GB300 HBM peak) and decode tokens/s on 1 GP
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the roofline's denominator)
 # GPU-side delay queued before each timed step (outside its events) so that the
 # host has enqueued the whole step before the GPU reaches it: the events then
 # time the kernels, not the host's launch latency.
@@ -72,10 +73,13 @@ WORKLOAD_CONFIG = {
                                   block_size=256, dtype="bf16"),
     "qwen3_0p6b_decode_fp8": dict(batch=64, context="U[128,4096]", H_q=16, H_kv=8, D=128, block_size=256,
                                   dtype="e4m3 KV (per-tensor scales), bf16 q/out", pool="1.25x need, shuffled"),
+    "store_stress": dict(tokens=16384, H_kv=8, D=128, block_size=256, dtype="bf16",
+                         slots="distinct random slots of a 1.25x pool"),
     "sampler_qwen3_vocab": dict(batch=64, vocab=151936, dtype="bf16", logits="3 * N(0,1)",
                                 temperature="U[0.5, 1.5]", noise="in-kernel Philox4x32-10, new offset per step"),
 }
 SAMPLER_METRIC = "temperature-sampling logits GB/s and rows/s on 1 GPU"
+STORE_METRIC = "slot-mapped KV store GB/s (read + write) on 1 GPU"
 # Warp instructions one pa_sample launch executes on the sampler workload (ncu
 # smsp__inst_executed.sum of sample_kernel, profiles/sample_sampler_qwen3_vocab.md): the
 # kernel is issue-bound (Philox4x32-10 and two accurate logarithms per vocabulary entry).
@@ -153,6 +157,22 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- workloads
+
+class L2Flush:
+    """Evicts the L2 between timed steps by READING a 256 MB buffer (a sum into one float):
+    a write flush would leave ~129 MB of dirty lines whose write-back lands in the next
+    timed step; read lines are clean, and the previous step's dirty lines are written back
+    during the flush, outside the events."""
+
+    def __init__(self, dev: torch.device, enabled: bool = True):
+        self.buf = torch.ones(L2_FLUSH_BYTES // 4 if enabled else 1, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+        self.enabled = enabled
+
+    def __call__(self):
+        if self.enabled:
+            torch.sum(self.buf, dim=0, out=self.out)
+
 
 def pack_inputs(host: dict, dev: torch.device):
     """A step's inputs in one device buffer (each tensor 256-byte aligned), as a
@@ -456,6 +476,29 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
+    if args.workload == "store_stress":
+        k, v, kc, vc, slots = _store_inputs()
+        row = k.shape[1] * k.shape[2] * k.element_size()
+        T = k.shape[0]
+        for i in range(args.warmup):
+            oracle.store_kv(k[i % T:i % T + 1], v[i % T:i % T + 1], kc, vc, slots[i % T:i % T + 1])
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            j = (args.warmup + i) % T
+            oracle.store_kv(k[j:j + 1], v[j:j + 1], kc, vc, slots[j:j + 1])
+        dt = time.perf_counter() - t0
+        value = 4 * row * args.steps / dt / 1e9
+        print(json.dumps({"metric": STORE_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                          "data": "synthetic", "impl": "reference",
+                          "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+                                     "sample": "one token per step"},
+                          "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                           "sample": "one token of the workload stored per step"},
+                          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
     if args.workload == "sampler_qwen3_vocab":
         logits, temps = _sampler_inputs()
         g = torch.Generator().manual_seed(13)
@@ -543,7 +586,7 @@ def run_sampler(args, world, rank, local):
     logits, temps = logits_h.to(dev), temps_h.to(dev)
     tokens = torch.empty(B, dtype=torch.int32, device=dev)
     nbytes = B * V * logits.element_size()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)  # the logits fit in L2
+    flush = L2Flush(dev)  # the logits fit in L2
     stream = torch.cuda.current_stream(dev)
     for i in range(args.warmup):
         pa.sample(logits, temps, seed=1, offset=i, out=tokens)
@@ -555,7 +598,7 @@ def run_sampler(args, world, rank, local):
     barrier(world, local)
     torch.cuda.synchronize(dev)
     for i in range(K):
-        flush.zero_()                                      # L2 flushed between steps, outside the events
+        flush()                                            # L2 flushed between steps, outside the events
         torch.cuda._sleep(PRE_STEP_SPIN_CYCLES)
         ev[i][0].record(stream)
         pa.sample(logits, temps, seed=1, offset=args.warmup + i, out=tokens)
@@ -601,7 +644,7 @@ def run_sampler(args, world, rank, local):
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
-                   "l2": "flushed (256 MB write) between steps, outside the timed events",
+                   "l2": "flushed (256 MB read) between steps, outside the timed events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "rows_per_s": world * B / (ms_max / 1e3),
         "roofline": roof,
@@ -614,9 +657,106 @@ def run_sampler(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def _store_inputs():
+    from tests import inputs
+    return inputs.store_stress()
+
+
+def store_cpu_baseline(seconds: float):
+    """The oracle's store single-threaded on this host, token by token (the whole 16384 once it fits)."""
+    import oracle
+    k, v, kc, vc, slots = _store_inputs()
+    row = k.shape[1] * k.shape[2] * k.element_size()
+    n, t_total = 0, 0.0
+    while t_total < seconds:
+        i = n % k.shape[0]
+        t0 = time.perf_counter()
+        oracle.store_kv(k[i:i + 1], v[i:i + 1], kc, vc, slots[i:i + 1])
+        t_total += time.perf_counter() - t0
+        n += 1
+    return {"value": 4 * row * n / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} tokens of the workload stored one at a time, single-threaded C oracle, "
+                      f"{os.cpu_count()} host cores present"}
+
+
+def run_store(args, world, rank, local):
+    """pa_store_kv of 16384 tokens (the engine's max batched tokens) into distinct random slots."""
+    import paged_kv_cache_bs_gb300 as pa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    k_h, v_h, kc_h, vc_h, slots_h = _store_inputs()
+    k, v, kc, vc, slots = k_h.to(dev), v_h.to(dev), kc_h.to(dev), vc_h.to(dev), slots_h.to(dev)
+    T, row = k.shape[0], k.shape[1] * k.shape[2] * k.element_size()
+    nbytes = 2 * 2 * T * row  # K and V rows, read + written
+    flush = L2Flush(dev)  # 134 MB of rows: about the L2
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        pa.store_kv(k, v, kc, vc, slots)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world, local)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush()
+        torch.cuda._sleep(PRE_STEP_SPIN_CYCLES)
+        ev[i][0].record(stream)
+        pa.store_kv(k, v, kc, vc, slots)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, local)
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(times) / K
+    ms_max = max_over_ranks(ms, world, dev)
+    # end to end: the new rows and slots from pinned host memory, the store, a sync
+    pin_k, pin_v, pin_s = k_h.pin_memory(), v_h.pin_memory(), slots_h.pin_memory()
+    Ke = min(K, 300)
+    e2e_s = 0.0
+    for _ in range(Ke):
+        flush()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        k.copy_(pin_k, non_blocking=True)
+        v.copy_(pin_v, non_blocking=True)
+        slots.copy_(pin_s, non_blocking=True)
+        pa.store_kv(k, v, kc, vc, slots)
+        stream.synchronize()
+        e2e_s += time.perf_counter() - t0
+    e2e_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": STORE_METRIC, "value": world * nbytes / (ms_max / 1e3) / 1e9, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "ms_per_step_median": statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+                   "l2": "flushed (256 MB read) between steps, outside the timed events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": world * T / (ms_max / 1e3),
+        "roofline": {"bound": "hbm", "kernel": "store_kv_kernel (one warp per token, 16-byte vectors)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_kind} (hbm_gbs)", "traffic": None},
+        "cpu_baseline": store_cpu_baseline(args.cpu_seconds) if world == 1 and not args.no_cpu_baseline else None,
+        "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": 2 * T * row + 4 * T, "d2h_bytes_per_step": 0, "ms_per_step": e2e_ms,
+                "path": "H2D copies of the new K/V rows and slots from pinned memory, pa_store_kv, stream sync; "
+                        "host wall clock (a store returns nothing to read back)"},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, world, rank, local):
     if args.workload == "sampler_qwen3_vocab":
         return run_sampler(args, world, rank, local)
+    if args.workload == "store_stress":
+        return run_store(args, world, rank, local)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.workload == "mixed_chunked_prefill":
@@ -626,12 +766,12 @@ def run_ours(args, world, rank, local):
     else:
         w = DecodeWorkload(args.workload, dev, fused=not args.unfused)
     flush_needed = w.kv_unique_bytes < 2 * L2_BYTES
-    flush = torch.empty(L2_FLUSH_BYTES // 4 if flush_needed else 1, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, flush_needed)
     stream = torch.cuda.current_stream(dev)
 
     def between_steps():
         if flush_needed:
-            flush.zero_()
+            flush()
 
     for _ in range(args.warmup):
         between_steps()
@@ -661,6 +801,7 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     phase_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j, (name, _) in enumerate(w.phases)}
     step_ms = sum(phase_ms.values())
+    step_ms_median = statistics.median(e[0].elapsed_time(e[nph]) for e in ev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
     store_ms = phase_ms.get("store")
     dec_ms_avg = phase_ms["decode"] if "decode" in phase_ms else phase_ms["store+decode"]
@@ -715,13 +856,14 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "hbm", "kernel": kern, "achieved": unique_gbs,
                 "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": unique_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",
+                "frac_of_nominal": unique_gbs / NOMINAL_HBM_GBS,
                 "traffic": TRAFFIC_PER_CALL.get(args.workload)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": WORKLOAD_CONFIG[args.workload]["dtype"], "data": "synthetic",
+        "ms_per_step": step_ms_max, "ms_per_step_median": step_ms_median, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": WORKLOAD_CONFIG[args.workload]["dtype"], "data": "synthetic",
         "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
-                   "l2": ("flushed (256 MB write) between steps, outside the timed events" if flush_needed else
+                   "l2": ("flushed (256 MB read) between steps, outside the timed events" if flush_needed else
                           f"not flushed: inputs larger than L2 ({w.kv_unique_bytes / 2**20:.0f} MiB of KV per step "
                           f"vs 129 MB L2, read in the same order every step)"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},

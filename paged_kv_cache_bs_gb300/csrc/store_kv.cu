@@ -26,17 +26,11 @@ store_kv_kernel(const V *__restrict__ k, const V *__restrict__ v, int64_t k_stri
     const int lane = threadIdx.x & 31;
     const int32_t t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= num_tokens) return;
-    const int64_t slot = slot_mapping[t];
-    if (slot == -1) return;
-    if (slot < -1 || slot >= num_slots) {
-        if (lane == 0) raise_flag(err_flag, PA_FLAG_BAD_SLOT);
-        return;
-    }
     const V *ks = k + t * k_stride_v;
     const V *vs = v + t * v_stride_v;
-    V *kd = k_cache + slot * row_v;
-    V *vd = v_cache + slot * row_v;
     for (int base = 0; base < row_v; base += 32 * kUnroll) {
+        // the row loads do not depend on the slot: issue them with the slot load, so a warp
+        // waits for one memory round trip before its stores instead of two
         V kr[kUnroll], vr[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -46,6 +40,14 @@ store_kv_kernel(const V *__restrict__ k, const V *__restrict__ v, int64_t k_stri
                 vr[u] = __ldg(vs + i);
             }
         }
+        const int64_t slot = slot_mapping[t];
+        if (slot == -1) return;
+        if (slot < -1 || slot >= num_slots) {
+            if (lane == 0 && base == 0) raise_flag(err_flag, PA_FLAG_BAD_SLOT);
+            return;
+        }
+        V *kd = k_cache + slot * row_v;
+        V *vd = v_cache + slot * row_v;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int i = base + u * 32 + lane;
@@ -86,17 +88,18 @@ store_kv_fp8_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t k_
     const int lane = threadIdx.x & 31;
     const int32_t t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= num_tokens) return;
-    const int64_t slot = slot_mapping[t];
-    if (slot == -1) return;
-    if (slot < -1 || slot >= num_slots) {
-        if (lane == 0) raise_flag(err_flag, PA_FLAG_BAD_SLOT);
-        return;
-    }
     for (int i = 8 * lane; i < row; i += 32 * 8) {
-        *reinterpret_cast<uint2 *>(k_cache + slot * row + i) =
-            quantize8_e4m3<T>(*reinterpret_cast<const uint4 *>(k + t * k_stride + i), k_scale);
-        *reinterpret_cast<uint2 *>(v_cache + slot * row + i) =
-            quantize8_e4m3<T>(*reinterpret_cast<const uint4 *>(v + t * v_stride + i), v_scale);
+        // the row loads are issued with the slot load (they do not depend on it)
+        const uint4 kr = *reinterpret_cast<const uint4 *>(k + t * k_stride + i);
+        const uint4 vr = *reinterpret_cast<const uint4 *>(v + t * v_stride + i);
+        const int64_t slot = slot_mapping[t];
+        if (slot == -1) return;
+        if (slot < -1 || slot >= num_slots) {
+            if (lane == 0 && i == 0) raise_flag(err_flag, PA_FLAG_BAD_SLOT);
+            return;
+        }
+        *reinterpret_cast<uint2 *>(k_cache + slot * row + i) = quantize8_e4m3<T>(kr, k_scale);
+        *reinterpret_cast<uint2 *>(v_cache + slot * row + i) = quantize8_e4m3<T>(vr, v_scale);
     }
 }
 
