@@ -59,6 +59,9 @@ TRAFFIC_PER_CALL = {
     "qwen3_8b_shared_decode": 868_519_936 + 5_361_152,  # decode_partition_kernel (L2 absorbs shared pages)
 }
 PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 117_771_520 + 12_707_584}  # prefill_kernel
+# store_kv_kernel on store_stress: DRAM read + write inside the launch (the L2 holds most written
+# rows as dirty lines until after the launch, so this is below the algorithmic 134,217,728 B)
+STORE_TRAFFIC_PER_CALL = 67_182_848 + 15_672_576
 
 WORKLOAD_CONFIG = {
     "tiny_decode": dict(batch=4, context="{1,17,100,255}", H_q=4, H_kv=2, D=64, block_size=16, dtype="fp16"),
@@ -740,7 +743,7 @@ def run_store(args, world, rank, local):
         "tokens_per_s": world * T / (ms_max / 1e3),
         "roofline": {"bound": "hbm", "kernel": "store_kv_kernel (one warp per token, 16-byte vectors)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "peak_source": f"{peak_kind} (hbm_gbs)", "traffic": None},
+                     "peak_source": f"{peak_kind} (hbm_gbs)", "traffic": STORE_TRAFFIC_PER_CALL},
         "cpu_baseline": store_cpu_baseline(args.cpu_seconds) if world == 1 and not args.no_cpu_baseline else None,
         "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": 2 * T * row + 4 * T, "d2h_bytes_per_step": 0, "ms_per_step": e2e_ms,
