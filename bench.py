@@ -254,19 +254,25 @@ class DecodeWorkload:
     e2e_path = ("one packed H2D copy of the step's inputs from pinned memory, the step's calls, "
                 "D2H of the output, stream sync; host wall clock")
 
+    def make_runner(self, zero_copy: bool):
+        from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
+        st, fs = self.st, getattr(self, "fs", None)
+        runner = DecodeGraphRunner(self.kc, self.vc, st.num_q_heads, st.batch, st.block_tables.shape[1],
+                                   st.scale, st.q.dtype, k_scale=fs.k_scale if fs else None,
+                                   v_scale=fs.v_scale if fs else None, zero_copy=zero_copy)
+        runner.set_inputs(st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables)
+        return runner
+
     def e2e_buffers(self):
         if self.fused:
-            # the engine's decode path: one CUDA graph per padded batch size holding the packed H2D
-            # copy, the fused store + decode and the D2H copy of the output (captured here, untimed)
-            from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
-            st, fs = self.st, getattr(self, "fs", None)
-            self.runner = DecodeGraphRunner(self.kc, self.vc, st.num_q_heads, st.batch, st.block_tables.shape[1],
-                                            st.scale, st.q.dtype, k_scale=fs.k_scale if fs else None,
-                                            v_scale=fs.v_scale if fs else None)
-            self.runner.set_inputs(st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables)
-            self.e2e_path = ("DecodeGraphRunner: CUDA-graph replay of the packed H2D copy of the step's inputs "
-                             "from pinned memory, the fused store + decode and the D2H copy of the output, then "
-                             "a stream sync; host wall clock")
+            # the engine's decode path: one CUDA graph per padded batch size holding the fused store +
+            # decode, whose kernels read the step's packed inputs from pinned host memory and write the
+            # output into pinned host memory (captured here, untimed)
+            st = self.st
+            self.runner = self.make_runner(zero_copy=True)
+            self.e2e_path = ("DecodeGraphRunner (zero copy): CUDA-graph replay of the fused store + decode, its "
+                             "kernels reading the step's packed inputs from pinned host memory and writing the "
+                             "output into pinned host memory over NVLink-C2C, then a stream sync; host wall clock")
             return None, None, self.runner.h2d_bytes(st.batch), self.runner.d2h_bytes(st.batch)
         pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
@@ -828,6 +834,23 @@ def run_ours(args, world, rank, local):
         e2e_s += time.perf_counter() - t0
     barrier(world, local)
     e2e_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
+    # the same step with the graph's copy-engine transfers instead of zero-copy operands (context)
+    e2e_copy_ms = None
+    if getattr(w, "runner", None) is not None:
+        rc = w.make_runner(zero_copy=False)
+        for _ in range(args.warmup):
+            rc.replay(w.st.batch)
+        torch.cuda.synchronize(dev)
+        e2e_s = 0.0
+        for i in range(Ke):
+            between_steps()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            rc.replay(w.st.batch)
+            stream.synchronize()
+            e2e_s += time.perf_counter() - t0
+        e2e_copy_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
+        del rc
 
     peaks, peak_kind = measured_peaks()
     value = world * w.kv_bytes / (step_ms_max / 1e3) / 1e9
@@ -882,7 +905,8 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": world * w.kv_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "path": w.e2e_path},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "path": w.e2e_path,
+                **({"ms_per_step_with_copy_engine": e2e_copy_ms} if e2e_copy_ms is not None else {})},
         "gpu_launches": K * w.launches_per_step,
         "clocks": clk,
         "wall_s_timed_region": t_wall,

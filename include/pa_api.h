@@ -16,7 +16,16 @@
  * Conventions shared by every call
  *   - All tensor arguments are DEVICE pointers to caller-owned memory; the
  *     library allocates nothing and keeps no state besides cached device
- *     properties.  Integer size arguments are host values.
+ *     properties.  Integer size arguments are host values.  Exception: the
+ *     per-step operands of pa_store_decode and pa_store_decode_fp8 (k, v,
+ *     slot_mapping, q, block_tables, context_lens and out) may instead be
+ *     page-locked host memory from cudaHostAlloc / cudaMallocHost, which under
+ *     unified addressing is device-accessible through its host pointer: the
+ *     kernels then read and write it directly over the CPU-GPU link (zero
+ *     copy; NVLink-C2C on a Grace-based GB300), so a step needs no separate
+ *     copy.  The pool, the workspace and err_flag stay device memory, and the
+ *     caller keeps the host buffers unchanged until the call has completed on
+ *     the stream.
  *   - Element type: PA_F16 or PA_BF16 (IEEE binary16 / bfloat16) for every
  *     q/k/v/cache/out buffer of a call (the pool of the *_fp8 calls is E4M3).
  *     Arithmetic is fp32.

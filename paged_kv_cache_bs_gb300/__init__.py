@@ -149,7 +149,22 @@ def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head
 def alloc_decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor) -> torch.Tensor:
     n, bs, hkv, d = k_cache.shape
     nbytes = decode_workspace_bytes(q.shape[0], q.shape[1], hkv, d, block_tables.shape[1], bs)
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=k_cache.device)
+
+
+def _step_operands(k_cache: torch.Tensor, **tensors) -> None:
+    """The small per-step operands of the decode calls (q, the new k/v rows, slot mapping,
+    block tables, context lengths, out) may live on the pool's device or in page-locked host
+    memory, which the kernels then read and write directly over the CPU-GPU link (with unified
+    addressing a pinned host pointer is also a device pointer).  Pageable host memory is refused."""
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if t.device == k_cache.device:
+            continue
+        if t.device.type == "cpu" and t.is_pinned():
+            continue
+        raise ValueError(f"{name} must be on {k_cache.device} or in pinned host memory")
 
 
 def _decode_checks(q, k_cache, v_cache, block_tables, context_lens):
@@ -195,14 +210,17 @@ def store_decode(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q
         raise ValueError("slot_mapping must be contiguous int32 [B]")
     if k.shape != (B, hkv, d) or v.shape != (B, hkv, d) or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k/v must be [B, H_kv, D] of the cache dtype")
+    _step_operands(k_cache, q=q, k=k, v=v, slot_mapping=slot_mapping, block_tables=block_tables,
+                   context_lens=context_lens, out=out)
     if out is None:
-        out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
+        out = torch.empty(B, hq, d, dtype=q.dtype, device=k_cache.device)
     if workspace is None:
         workspace = alloc_decode_workspace(q, k_cache, block_tables)
     rc = _lib.pa_store_decode(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q),
                               _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
                               _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale), _ptr(out), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag), _stream(q))
+                              workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
+                              _stream(k_cache))
     _check("pa_store_decode", rc)
     return out
 
@@ -285,10 +303,10 @@ def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     return out
 
 
-def _fp8_workspace(q, hkv, d, block_tables, bs, workspace):
+def _fp8_workspace(q, hkv, d, block_tables, bs, workspace, device=None):
     if workspace is None:
         nbytes = decode_fp8_workspace_bytes(q.shape[0], q.shape[1], hkv, d, block_tables.shape[1], bs)
-        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or q.device)
     return workspace
 
 
@@ -306,15 +324,17 @@ def store_decode_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tenso
         raise ValueError("slot_mapping must be contiguous int32 [B]")
     if k.shape != (B, hkv, d) or v.shape != (B, hkv, d) or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k/v must be [B, H_kv, D] of the query dtype")
+    _step_operands(k_cache, q=q, k=k, v=v, slot_mapping=slot_mapping, block_tables=block_tables,
+                   context_lens=context_lens, out=out)
     if out is None:
-        out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
-    workspace = _fp8_workspace(q, hkv, d, block_tables, bs, workspace)
+        out = torch.empty(B, hq, d, dtype=q.dtype, device=k_cache.device)
+    workspace = _fp8_workspace(q, hkv, d, block_tables, bs, workspace, k_cache.device)
     rc = _lib.pa_store_decode_fp8(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q),
                                   _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                   block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale),
                                   float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
-                                  _stream(q))
+                                  _stream(k_cache))
     _check("pa_store_decode_fp8", rc)
     return out
 

@@ -131,23 +131,27 @@ __device__ __forceinline__ int context_len(const DecodeArgs &a, int b) {
 // TMA loads this warp issues next.
 template <typename T, int D, bool F8>
 __device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g, int L, int lane) {
-    const int slot = a.slot_mapping[b];
-    if (slot == -1) return;
+    constexpr int kChunks = D / 8;  // 8-element (16-byte) chunks of one head's new row
+    const bool is_v = lane >= kChunks;
+    const int ci = is_v ? lane - kChunks : lane;
+    // The slot, the page of position L-1 and this lane's chunk of the new row do not depend on
+    // one another: they are loaded together, one memory round trip before the checks (the row
+    // of a padding sequence, slot -1, is read and dropped).
     const int j = L - 1;
+    const int slot = a.slot_mapping[b];
     const int pg = a.block_tables[static_cast<int64_t>(b) * a.max_blocks + (j >> a.log2_bs)];
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 2 * kChunks)
+        raw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(is_v ? a.v_new : a.k_new) +
+                                               b * (is_v ? a.v_new_stride : a.k_new_stride) + g * D + ci * 8);
+    if (slot == -1) return;
     const int64_t expect =
         (pg < 0 || pg >= a.num_blocks) ? -2 : (static_cast<int64_t>(pg) << a.log2_bs) + (j & ((1 << a.log2_bs) - 1));
     if (slot != expect) {
         if (lane == 0 && g == 0) raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);
         return;
     }
-    constexpr int kChunks = D / 8;  // 8-element (16-byte) chunks of one head's new row
     if (lane < 2 * kChunks) {
-        const bool is_v = lane >= kChunks;
-        const int ci = is_v ? lane - kChunks : lane;
-        const T *src = static_cast<const T *>(is_v ? a.v_new : a.k_new) + b * (is_v ? a.v_new_stride : a.k_new_stride) +
-                       g * D + ci * 8;
-        const uint4 raw = *reinterpret_cast<const uint4 *>(src);
         const int64_t e = (static_cast<int64_t>(slot) * a.num_kv_heads + g) * D + ci * 8;  // pool element
         if constexpr (F8)
             *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(is_v ? a.v_cache_w : a.k_cache_w) + e) =

@@ -8,10 +8,16 @@ tables into the graph's fixed buffers, pads the unused rows (slot -1, context
 length 0), replays the smallest graph that fits and keeps the first rows of
 the output.
 
-Here one graph holds the whole step of one attention layer: the host-to-device
-copy of the packed step inputs from pinned memory, the fused store + decode
-(``pa_store_decode``, or ``pa_store_decode_fp8`` over an E4M3 pool) and the
-device-to-host copy of the output into pinned memory.  Argument marshalling
+Here one graph holds the whole step of one attention layer.  By default
+(``zero_copy=True``) it is the fused store + decode (``pa_store_decode``, or
+``pa_store_decode_fp8`` over an E4M3 pool) with its small per-step operands in
+pinned host memory: the kernels read q, the new K/V rows, the slot mapping,
+context lengths and block tables from the pinned staging and write the output
+into pinned memory directly over the CPU-GPU link (NVLink-C2C on a Grace-based
+GB300), so the step has no copy-engine transfer, whose start-up latency is
+longer than the transfer of these few hundred KB.  With ``zero_copy=False``
+the graph holds a host-to-device copy of the packed inputs, the fused call on
+device buffers and a device-to-host copy of the output.  Argument marshalling
 only: every step of the path runs in the library's kernels.
 """
 
@@ -43,13 +49,15 @@ class DecodeGraphRunner:
 
     ``k_cache`` / ``v_cache``: the layer's pool (16-bit, or E4M3 codes as ``torch.uint8`` /
     ``torch.float8_e4m3fn`` with ``k_scale`` and ``v_scale`` given).  ``dtype``: the type of q,
-    the new K/V rows and the output.  Steps are issued on the current stream of the pool's
-    device; one runner serves one step at a time.
+    the new K/V rows and the output.  ``zero_copy``: the kernels read the step's inputs from, and
+    write its output to, the pinned staging (default), or the graph copies them to and from
+    device buffers.  Steps are issued on the current stream of the pool's device; one runner
+    serves one step at a time.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_q_heads: int, max_batch: int,
                  max_blocks_per_seq: int, scale: float, dtype: torch.dtype = torch.bfloat16,
-                 k_scale: float | None = None, v_scale: float | None = None):
+                 k_scale: float | None = None, v_scale: float | None = None, zero_copy: bool = True):
         self.fp8 = k_cache.dtype in _FP8_POOL
         if self.fp8:
             if k_scale is None or v_scale is None:
@@ -61,6 +69,7 @@ class DecodeGraphRunner:
         self.max_blocks = max_blocks_per_seq
         self.scale, self.k_scale, self.v_scale = float(scale), k_scale, v_scale
         self.dtype = dtype
+        self.zero_copy = zero_copy
         self.sizes = graph_batch_sizes(max_batch)
         dev = k_cache.device
         esz = torch.empty(0, dtype=dtype).element_size()
@@ -69,9 +78,12 @@ class DecodeGraphRunner:
         in_bytes = max(lay["_bytes"] for lay in self._layout.values())
         out_bytes = max(self.sizes) * num_q_heads * d * esz
         self.host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
-        self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
         self.host_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
-        self.dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
+        if zero_copy:
+            self.dev_in = self.dev_out = None
+        else:
+            self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
+            self.dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
         ws_fn = decode_fp8_workspace_bytes if self.fp8 else decode_workspace_bytes
         ws = max(ws_fn(b, num_q_heads, hkv, d, max_blocks_per_seq, bs) for b in self.sizes)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
@@ -110,9 +122,13 @@ class DecodeGraphRunner:
     # ----------------------------------------------------------------- capture
     def _launch(self, b: int) -> None:
         lay = self._layout[b]
-        self.dev_in[:lay["_bytes"]].copy_(self.host_in[:lay["_bytes"]], non_blocking=True)
-        v = self._views(self.dev_in, b)
-        out = self._out_view(self.dev_out, b)
+        if self.zero_copy:
+            v = self._views(self.host_in, b)
+            out = self._out_view(self.host_out, b)
+        else:
+            self.dev_in[:lay["_bytes"]].copy_(self.host_in[:lay["_bytes"]], non_blocking=True)
+            v = self._views(self.dev_in, b)
+            out = self._out_view(self.dev_out, b)
         if self.fp8:
             store_decode_fp8(v["k_new"], v["v_new"], v["slot_mapping"], v["q"], self.k_cache, self.v_cache,
                              v["block_tables"], v["context_lens"], self.scale, self.k_scale, self.v_scale,
@@ -120,7 +136,8 @@ class DecodeGraphRunner:
         else:
             store_decode(v["k_new"], v["v_new"], v["slot_mapping"], v["q"], self.k_cache, self.v_cache,
                          v["block_tables"], v["context_lens"], self.scale, out=out, workspace=self.workspace)
-        self._out_view(self.host_out, b).copy_(out, non_blocking=True)
+        if not self.zero_copy:
+            self._out_view(self.host_out, b).copy_(out, non_blocking=True)
 
     def _capture(self) -> None:
         # capture with every row padded (slot -1, context 0): no page is read, nothing is stored

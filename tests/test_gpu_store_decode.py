@@ -81,3 +81,34 @@ def test_store_decode_flags_a_slot_that_is_not_the_last_position(pa):
     assert_bit_equal(kc, okc, "k_cache with the flagged rows skipped")
     ref = oracle.decode(st.q[[0, 3]], okc, ovc, st.block_tables[[0, 3]], st.context_lens[[0, 3]], st.scale)
     assert max_err(out[[0, 3]], ref) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_store_decode_with_pinned_host_operands(pa, fp8):
+    """The per-step operands (q, the new rows, slot mapping, tables, lengths, out) in pinned host
+    memory, read and written by the kernels directly: output and pool bit-identical to the call
+    on device copies of the same operands.  Pageable host memory is refused."""
+    ctx = torch.randint(1, 5000, (37,), generator=torch.Generator().manual_seed(181)).tolist()
+    kw = dict(num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=256, dtype=torch.bfloat16, seed=182)
+    fs = inputs.make_decode_fp8(ctx, **kw) if fp8 else None
+    st = fs.step if fp8 else inputs.make_decode(ctx, **kw)
+    pool_k, pool_v = (fs.k_cache, fs.v_cache) if fp8 else (st.pool.k_cache, st.pool.v_cache)
+    ops = dict(k=st.k_new, v=st.v_new, sm=st.slot_mapping, q=st.q, bt=st.block_tables, cl=st.context_lens)
+
+    def call(d, kc, vc, out):
+        if fp8:
+            return pa.store_decode_fp8(d["k"], d["v"], d["sm"], d["q"], kc, vc, d["bt"], d["cl"], st.scale,
+                                       fs.k_scale, fs.v_scale, out=out)
+        return pa.store_decode(d["k"], d["v"], d["sm"], d["q"], kc, vc, d["bt"], d["cl"], st.scale, out=out)
+
+    kc_d, vc_d = pool_k.cuda(), pool_v.cuda()
+    ref = call({n: t.cuda() for n, t in ops.items()}, kc_d, vc_d, None)
+    kc_h, vc_h = pool_k.cuda(), pool_v.cuda()
+    out_h = torch.full(tuple(st.q.shape), float("nan"), dtype=st.q.dtype).pin_memory()
+    call({n: t.pin_memory() for n, t in ops.items()}, kc_h, vc_h, out_h)
+    torch.cuda.synchronize()
+    assert_bit_equal(out_h, ref.cpu(), "output written to pinned host memory")
+    bits = (lambda t: t.cpu().view(torch.uint8))  # noqa: E731
+    assert torch.equal(bits(kc_h), bits(kc_d)) and torch.equal(bits(vc_h), bits(vc_d)), "pool differs"
+    with pytest.raises(ValueError):
+        call(dict(ops), kc_h, vc_h, None)  # pageable host tensors

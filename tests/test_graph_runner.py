@@ -1,7 +1,8 @@
 """The bucketed CUDA-graph decode runner ("nano-vLLM Part 2", section 4.2): bucket sizes on
 the CPU; on the GPU, a replayed step equals the eager fused call on the same inputs (output
 and pool bit-identical), for batch sizes that fill a bucket and ones that need padding rows,
-over 16-bit and E4M3 pools."""
+over 16-bit and E4M3 pools, with the kernels reading the step's operands from pinned host
+memory (zero copy) and with copies to and from device buffers."""
 
 import pytest
 import torch
@@ -35,8 +36,9 @@ def _eager(pa, st, kc, vc, fs=None):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("zero_copy", [True, False])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_runner_equals_eager_step(pa, fp8):
+def test_runner_equals_eager_step(pa, fp8, zero_copy):
     from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
     ctx_all = torch.randint(1, 3000, (40,), generator=torch.Generator().manual_seed(170)).tolist()
     kw = dict(num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=16, dtype=torch.bfloat16, seed=171)
@@ -46,7 +48,8 @@ def test_runner_equals_eager_step(pa, fp8):
     width = st.block_tables.shape[1]
     kc, vc = pool_k.cuda(), pool_v.cuda()
     runner = DecodeGraphRunner(kc, vc, 16, 40, width, st.scale, torch.bfloat16,
-                               k_scale=fs.k_scale if fp8 else None, v_scale=fs.v_scale if fp8 else None)
+                               k_scale=fs.k_scale if fp8 else None, v_scale=fs.v_scale if fp8 else None,
+                               zero_copy=zero_copy)
     for batch in (1, 3, 16, 17, 40):  # exact buckets and padded ones
         b = runner.bucket(batch)
         # the eager call on the bucket's padded inputs (slot -1, context 0 past `batch`): the split-K
