@@ -99,6 +99,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_CONFIG))
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--split-sms", type=int, default=96,
+                    help="mixed chunked-prefill step: SMs of the prefill's partition (0: no SM split)")
     ap.add_argument("--unfused", action="store_true",
                     help="decode workloads: time pa_store_kv + pa_decode as two calls instead of pa_store_decode")
     return ap.parse_args()
@@ -347,11 +349,13 @@ class MixedWorkload(DecodeWorkload):
     (prefill chunks and decode tokens), causal prefill of the chunks over
     their cached prefixes, decode of the other sequences."""
 
-    def __init__(self, name: str, dev: torch.device):
+    def __init__(self, name: str, dev: torch.device, split_sms: int = 0):
         from tests import inputs
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
         self.name = name
+        # the whole step in one call, the prefill and the decode side by side on disjoint SM sets
+        self.split = pa.SmSplit(split_sms) if split_sms else None
         m = inputs.WORKLOADS[name]()
         self.st = st = m.decode
         pf = m.prefill
@@ -371,7 +375,9 @@ class MixedWorkload(DecodeWorkload):
         self.batch = st.batch + (pf.cu_seqlens_q.numel() - 1)
         row = p.num_kv_heads * p.head_dim * st.q.element_size()
         self.store_bytes = 2 * 2 * int((m.slot_mapping >= 0).sum()) * row
-        self.launches_per_step = 4   # store, prefill, decode partitions, merge
+        # store, prefill, decode partitions (960 (sequence, kv head) pairs fill two waves: no split-K,
+        # so no merge launch)
+        self.launches_per_step = 3
         self.phases = [("store", self.store), ("prefill", self.prefill), ("decode", self.attend)]
         self.prefill_flops = pf.flops()
         self.fused = False
@@ -385,15 +391,28 @@ class MixedWorkload(DecodeWorkload):
         self.pa.prefill_paged(d["pq"], None, None, self.kc, self.vc, d["cu_q"], d["cu_k"], pf.max_seqlen_q,
                               pf.max_seqlen_k, d["pbt"], pf.scale, out=self.pout)
 
+    def split_step(self):
+        d, pf = self.d, self.pf
+        self.pa.mixed_step(d["k_all"], d["v_all"], d["slot_all"], d["pq"], d["cu_q"], d["cu_k"], pf.max_seqlen_q,
+                           pf.max_seqlen_k, d["pbt"], d["q"], d["block_tables"], d["context_lens"], self.kc, self.vc,
+                           pf.scale, prefill_out=self.pout, decode_out=self.out, workspace=self.ws, split=self.split)
+
     def e2e_buffers(self):
         pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         outs = torch.empty(self.out.numel() + self.pout.numel(), dtype=self.out.dtype).pin_memory()
+        if self.split is not None:
+            self.e2e_path = ("one packed H2D copy of the step's inputs from pinned memory, pa_mixed_step (store, then "
+                             f"prefill on {self.split.sms[0]} SMs beside decode on {self.split.sms[1]}), D2H of the "
+                             "outputs, stream sync; host wall clock")
         return pinned, outs, pinned.numel(), outs.numel() * outs.element_size()
 
     def e2e_step(self, pinned, out_host):
         self.inputs.copy_(pinned, non_blocking=True)   # the step's inputs, one copy
-        for _, fn in self.phases:
-            fn()
+        if self.split is not None:
+            self.split_step()
+        else:
+            for _, fn in self.phases:
+                fn()
         n = self.out.numel()
         out_host[:n].copy_(self.out.view(-1), non_blocking=True)
         out_host[n:].copy_(self.pout.view(-1), non_blocking=True)
@@ -769,7 +788,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.workload == "mixed_chunked_prefill":
-        w = MixedWorkload(args.workload, dev)
+        w = MixedWorkload(args.workload, dev, split_sms=args.split_sms)
     elif args.workload.endswith("_fp8"):
         w = Fp8DecodeWorkload(args.workload, dev, fused=not args.unfused)
     else:
@@ -814,6 +833,32 @@ def run_ours(args, world, rank, local):
     step_ms_max = max_over_ranks(step_ms, world, dev)
     store_ms = phase_ms.get("store")
     dec_ms_avg = phase_ms["decode"] if "decode" in phase_ms else phase_ms["store+decode"]
+
+    # ---- the mixed step as one pa_mixed_step call with its prefill and decode side by side on
+    # disjoint SM partitions: this is the step's time; the phases above (one after the other)
+    # give each kernel's own rate for its roofline
+    split_ms = None
+    if getattr(w, "split", None) is not None:
+        for _ in range(args.warmup):
+            between_steps()
+            w.split_step()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        barrier(world, local)
+        torch.cuda.synchronize(dev)
+        for i in range(K):
+            between_steps()
+            torch.cuda._sleep(PRE_STEP_SPIN_CYCLES)
+            evs[i][0].record(stream)
+            w.split_step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, local)
+        split_times = [a.elapsed_time(b) for a, b in evs]
+        split_ms = sum(split_times) / K
+        step_ms_sequential = step_ms
+        step_ms_max = max_over_ranks(split_ms, world, dev)
+        step_ms_median = statistics.median(split_times)
 
     # ---- end to end through the public API, as a caller sees it: host wall
     # clock from the H2D copies of the step's inputs (pinned host memory) to the
@@ -896,6 +941,11 @@ def run_ours(args, world, rank, local):
         "tokens_per_s": world * w.batch / (step_ms_max / 1e3),
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "phase_ms": phase_ms,
+        **({"step_ms_phases_in_sequence": step_ms_sequential,
+            "sm_split": {"prefill_sms": w.split.sms[0], "decode_sms": w.split.sms[1],
+                         "note": "ms_per_step is pa_mixed_step with the prefill and the decode on disjoint SM "
+                                 "partitions at once; phase_ms times the three calls one after the other"}}
+           if split_ms is not None else {}),
         "decode_gbs": decode_gbs,
         "decode_unique_gbs": w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9,
         "kv_unique_bytes_per_step": w.kv_unique_bytes,

@@ -337,6 +337,72 @@ PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const v
                      float scale, void *out, pa_dtype dtype, int32_t *err_flag, void *stream);
 
 /*
+ * pa_sm_split -- the GPU's SMs as two disjoint partitions, each with its own
+ * stream (CUDA green contexts), for pa_mixed_step.  The pages run a mixed
+ * step's chunked prefill and decode as one batch ("nano-vLLM Part 2", section
+ * 4; "From nano-vLLM to vLLM", chunked prefill); here the prefill, bound by
+ * the tensor cores, runs on the first partition while the decode, bound by
+ * HBM bandwidth (which it reaches with well under half of the SMs), runs on
+ * the second.  This split is this library's choice; the pages describe none.
+ *
+ * pa_sm_split_create(first_sms, &split) partitions the current device:
+ * first_sms SMs for the first partition, the rest for the second.  first_sms
+ * must be a multiple of the device's co-scheduling granularity (8 on GB300),
+ * at least its minimum partition (8), and leave at least that many SMs;
+ * otherwise PA_ERR_INVALID_ARG.  PA_ERR_UNSUPPORTED when the driver lacks
+ * green contexts.  It creates driver objects (two green contexts, two
+ * streams, three events) and no device buffer: make one per device at
+ * start-up and reuse it.  pa_sm_split_info returns the two SM counts and the
+ * two streams (cudaStream_t; the split owns them: do not destroy them).
+ * pa_sm_split_destroy waits for the split's streams and releases everything.
+ * A split serves one step at a time: steps issued concurrently from several
+ * threads on one split race on its events.
+ */
+typedef struct pa_sm_split pa_sm_split;
+PA_API int pa_sm_split_create(int32_t first_sms, pa_sm_split **split);
+PA_API int pa_sm_split_info(const pa_sm_split *split, int32_t *first_sms, int32_t *second_sms, void **first_stream,
+                            void **second_stream);
+PA_API void pa_sm_split_destroy(pa_sm_split *split);
+
+/*
+ * pa_mixed_step -- one mixed chunked-prefill step of an attention layer: the
+ * store of every new token of the step (the prefill chunks' and the decode
+ * sequences'), then the chunked prefill of the prefill sequences over their
+ * cached prefixes and the decode of the others ("Inference engine: inside
+ * nano-vLLM", section "Attention in nano-vLLM": store_kvcache, then
+ * flash_attn_varlen_func or flash_attn_with_kvcache).  Same results, bit for
+ * bit, as
+ *   pa_store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache,
+ *               slot_mapping, num_tokens, ...);
+ *   pa_prefill_paged(prefill_q, NULL, NULL, k_cache, v_cache, cu_seqlens_q,
+ *                    cu_seqlens_k, num_prefill_seqs, total_prefill_q,
+ *                    max_seqlen_q, max_seqlen_k, prefill_block_tables,
+ *                    prefill_max_blocks, ..., prefill_out, ...);
+ *   pa_decode(decode_q, decode_q_row_stride, k_cache, v_cache,
+ *             decode_block_tables, decode_max_blocks, context_lens,
+ *             decode_batch, ..., decode_out, workspace, workspace_bytes, ...);
+ * on `stream` (the prefill reads its chunk's keys from the pool, so the store
+ * comes first), the argument rules being those of the three calls; a prefill
+ * with num_prefill_seqs == 0 or a decode with decode_batch == 0 is skipped.
+ * With `split` (nullable) the store runs on `stream`, then the prefill on the
+ * split's first partition and the decode on its second, at the same time,
+ * and `stream` waits for both before anything issued on it later; the split
+ * must belong to the current device.  Every argument is checked before
+ * anything is launched.
+ */
+PA_API int pa_mixed_step(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                         const int32_t *slot_mapping, int32_t num_tokens, const void *prefill_q,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_prefill_seqs,
+                         int32_t total_prefill_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                         const int32_t *prefill_block_tables, int32_t prefill_max_blocks, void *prefill_out,
+                         const void *decode_q, int64_t decode_q_row_stride, const int32_t *decode_block_tables,
+                         int32_t decode_max_blocks, const int32_t *context_lens, int32_t decode_batch,
+                         void *decode_out, void *workspace, size_t workspace_bytes, void *k_cache, void *v_cache,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                         int32_t block_size, float scale, pa_dtype dtype, int32_t *err_flag,
+                         const pa_sm_split *split, void *stream);
+
+/*
  * pa_sample -- one token per row by temperature sampling, written as the
  * exponential race of "From nano-vLLM to vLLM: Scheduler, Paged KV Cache,
  * Prefill/Decode, Tensor Parallelism, and Sampling", section 17 (17.1, 17.4,

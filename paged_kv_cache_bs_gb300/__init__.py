@@ -15,6 +15,8 @@ The functions mirror the C ABI in ``include/pa_api.h``:
 * :func:`decode_fp8`     -- ``pa_decode_fp8`` (+ ``pa_decode_fp8_workspace_bytes``)
 * :func:`store_decode_fp8` -- ``pa_store_decode_fp8`` (the fp8 store fused into fp8 decode)
 * :func:`prefill_paged`  -- ``pa_prefill_paged``
+* :func:`mixed_step`     -- ``pa_mixed_step`` (store, chunked prefill and decode of one step;
+  with an :class:`SmSplit` (``pa_sm_split_*``) the prefill and the decode run side by side)
 * :func:`sample`         -- ``pa_sample`` (temperature sampling, exponential race)
 
 ``paged_kv_cache_bs_gb300.graphs.DecodeGraphRunner`` replays the decode step of a layer
@@ -63,6 +65,16 @@ _lib.pa_store_decode_fp8.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _
                                      _i32, _i32, _f32, _f32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
 _lib.pa_sample.restype = ctypes.c_int
 _lib.pa_sample.argtypes = [_p, _i64, _i32, _i32, ctypes.c_int, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
+_lib.pa_sm_split_create.restype = ctypes.c_int
+_lib.pa_sm_split_create.argtypes = [_i32, ctypes.POINTER(ctypes.c_void_p)]
+_lib.pa_sm_split_info.restype = ctypes.c_int
+_lib.pa_sm_split_info.argtypes = [_p, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _p, _p]
+_lib.pa_sm_split_destroy.restype = None
+_lib.pa_sm_split_destroy.argtypes = [_p]
+_lib.pa_mixed_step.restype = ctypes.c_int
+_lib.pa_mixed_step.argtypes = [_p, _p, _i64, _i64, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _p, _p, _i64,
+                               _p, _i32, _p, _i32, _p, _p, _sz, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32,
+                               ctypes.c_int, _p, _p, _p]
 _lib.pa_prefill_paged.restype = ctypes.c_int
 _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32,
                                   _i32, _i32, _f32, _p, ctypes.c_int, _p, _p]
@@ -252,6 +264,77 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     return out
 
 
+class SmSplit:
+    """``pa_sm_split``: the current device's SMs as two disjoint partitions with their own streams
+    (``first_sms`` SMs, a multiple of 8, and the rest), for :func:`mixed_step`.  Create one at
+    start-up and reuse it; :meth:`close` (or garbage collection) releases it."""
+
+    def __init__(self, first_sms: int):
+        self._h = None
+        h = ctypes.c_void_p()
+        _check("pa_sm_split_create", _lib.pa_sm_split_create(int(first_sms), ctypes.byref(h)))
+        self._h = h
+        a, b = ctypes.c_int32(), ctypes.c_int32()
+        _check("pa_sm_split_info", _lib.pa_sm_split_info(h, ctypes.byref(a), ctypes.byref(b), None, None))
+        self.sms = (a.value, b.value)
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise ValueError("the SM split is closed")
+        return self._h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None:
+            _lib.pa_sm_split_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+
+def mixed_step(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, prefill_q: torch.Tensor,
+               cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+               prefill_block_tables: torch.Tensor, decode_q: torch.Tensor, decode_block_tables: torch.Tensor,
+               context_lens: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float,
+               prefill_out: torch.Tensor | None = None, decode_out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, split: SmSplit | None = None,
+               err_flag: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """``pa_mixed_step``: store every new token (k/v [T, H_kv, D] at ``slot_mapping``), then the
+    chunked prefill of ``prefill_q`` [Tq, H_q, D] over the pool and the decode of ``decode_q``
+    [B, H_q, D]; with ``split`` the prefill and the decode run at once on its two SM partitions.
+    Returns (prefill_out, decode_out)."""
+    n, bs, hkv, d = _decode_checks(decode_q, k_cache, v_cache, decode_block_tables, context_lens)
+    B, hq = decode_q.shape[0], decode_q.shape[1]
+    tq = prefill_q.shape[0]
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int32")
+    if k.shape != (slot_mapping.numel(), hkv, d) or v.shape != k.shape or k.dtype != k_cache.dtype or v.dtype != k.dtype:
+        raise ValueError("k/v must be [T, H_kv, D] of the cache dtype, one row per slot")
+    if not prefill_q.is_contiguous() or prefill_q.dim() != 3 or prefill_q.shape[1:] != (hq, d):
+        raise ValueError("prefill_q must be contiguous [Tq, H_q, D]")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k),
+                    ("prefill_block_tables", prefill_block_tables)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if prefill_out is None:
+        prefill_out = torch.empty(tq, hq, d, dtype=prefill_q.dtype, device=k_cache.device)
+    if decode_out is None:
+        decode_out = torch.empty(B, hq, d, dtype=decode_q.dtype, device=k_cache.device)
+    if workspace is None:
+        workspace = alloc_decode_workspace(decode_q, k_cache, decode_block_tables)
+    rc = _lib.pa_mixed_step(
+        _ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), slot_mapping.numel(),
+        _ptr(prefill_q), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq, int(max_seqlen_q),
+        int(max_seqlen_k), _ptr(prefill_block_tables), prefill_block_tables.shape[1], _ptr(prefill_out),
+        _ptr(decode_q), _rows(decode_q, "decode_q"), _ptr(decode_block_tables), decode_block_tables.shape[1],
+        _ptr(context_lens), B, _ptr(decode_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(k_cache), _ptr(v_cache), hq, hkv, d, n, bs, float(scale), _dtype(decode_q), _ptr(err_flag),
+        split.handle if split is not None else None, _stream(k_cache))
+    _check("pa_mixed_step", rc)
+    return prefill_out, decode_out
+
+
 def _fp8_pool(k_cache: torch.Tensor, v_cache: torch.Tensor):
     if k_cache.dtype not in _FP8_POOL or v_cache.dtype not in _FP8_POOL:
         raise TypeError("an fp8 pool holds E4M3 codes: torch.uint8 or torch.float8_e4m3fn")
@@ -362,7 +445,7 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
 
 
 __all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
-           "store_decode_fp8",
+           "store_decode_fp8", "mixed_step", "SmSplit",
            "decode_workspace_bytes", "decode_fp8_workspace_bytes", "alloc_decode_workspace", "library",
            "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "PA_E4M3", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",
            "FLAG_BAD_LENGTH", "FLAG_TIMEOUT", "FLAG_INTERNAL", "FLAG_BAD_VALUE"]

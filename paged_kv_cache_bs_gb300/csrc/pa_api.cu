@@ -106,11 +106,10 @@ int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const
 }
 
 
-// pa_store_kv, or pa_store_kv_fp8 when fp8 is given (an E4M3 pool).
-int store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache, void *v_cache,
-             const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
-             int32_t num_blocks, int32_t block_size, pa_dtype dtype, int32_t *err_flag, void *stream,
-             const pa::Fp8Scales *fp8) {
+// Checks of pa_store_kv's (or with scales pa_store_kv_fp8's) arguments; PA_OK or an error code.
+int check_store(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, const void *k_cache,
+                const void *v_cache, const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype, const pa::Fp8Scales *fp8) {
     if (!valid_dtype(dtype)) return fail(PA_ERR_UNSUPPORTED, "dtype %d is not PA_F16 or PA_BF16", (int)dtype);
     if (fp8 && !valid_scales(*fp8))
         return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive (%g, %g)", fp8->k_scale,
@@ -120,10 +119,7 @@ int store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_s
         return fail(PA_ERR_INVALID_ARG, "sizes must be positive (H_kv=%d, D=%d, N=%d, bs=%d)", num_kv_heads,
                     head_dim, num_blocks, block_size);
     if (!k_cache || !v_cache) return fail(PA_ERR_INVALID_ARG, "k_cache/v_cache is NULL");
-    if (num_tokens == 0) {
-        g_err[0] = '\0';
-        return PA_OK;
-    }
+    if (num_tokens == 0) return PA_OK;
     if (!k || !v || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "k, v or slot_mapping is NULL");
     const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
     if (row > (1 << 30)) return fail(PA_ERR_INVALID_ARG, "row of %lld elements is too large", (long long)row);
@@ -137,6 +133,22 @@ int store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_s
         return fail(PA_ERR_INVALID_ARG,
                     "pa_store_kv_fp8: rows and strides must be multiples of 8 elements, k/v 16-byte and the "
                     "caches 8-byte aligned");
+    return PA_OK;
+}
+
+// pa_store_kv, or pa_store_kv_fp8 when fp8 is given (an E4M3 pool).
+int store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride, void *k_cache, void *v_cache,
+             const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+             int32_t num_blocks, int32_t block_size, pa_dtype dtype, int32_t *err_flag, void *stream,
+             const pa::Fp8Scales *fp8) {
+    const int rc = check_store(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping, num_tokens,
+                               num_kv_heads, head_dim, num_blocks, block_size, dtype, fp8);
+    if (rc) return rc;
+    if (num_tokens == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
     const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
     if (fp8)
         return cuda_status(pa::launch_store_kv_fp8(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping,
@@ -293,22 +305,24 @@ int pa_decode_fp8(const void *q, int64_t q_row_stride, const void *k_cache, cons
                        "pa_decode_fp8 launch");
 }
 
-int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
-                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
-                     int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
-                     int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                     int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
-                     int32_t *err_flag, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks of pa_prefill_paged's arguments; PA_OK or an error code (*work: something to compute).
+int check_prefill(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
+                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                  int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                  float scale, const void *out, pa_dtype dtype, bool *work) {
+    *work = false;
     int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
     if (rc) return rc;
     if (!(scale > 0.f)) return fail(PA_ERR_INVALID_ARG, "pa_prefill_paged needs scale > 0 (got %g)", scale);
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < max_seqlen_q)
         return fail(PA_ERR_INVALID_ARG, "sizes: num_seqs %d, total_q %d, max_seqlen_q %d, max_seqlen_k %d", num_seqs,
                     total_q, max_seqlen_q, max_seqlen_k);
-    if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) {
-        g_err[0] = '\0';
-        return PA_OK;
-    }
+    if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PA_OK;
     if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !out)
         return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
     if (!block_tables && (!k || !v)) return fail(PA_ERR_INVALID_ARG, "k and v are required without block_tables");
@@ -320,6 +334,29 @@ int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         (!block_tables && (!aligned(k, 16) || !aligned(v, 16))))
         return fail(PA_ERR_INVALID_ARG, "q, k, v, caches and out must be 16-byte aligned");
+    *work = true;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                     int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
+                     int32_t *err_flag, void *stream) {
+    bool work = false;
+    const int rc = check_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
+                                 max_seqlen_q, max_seqlen_k, block_tables, max_blocks_per_seq, num_q_heads,
+                                 num_kv_heads, head_dim, num_blocks, block_size, scale, out, dtype, &work);
+    if (rc) return rc;
+    if (!work) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
     const char *why = nullptr;
     const cudaError_t e = pa::launch_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs,
                                              total_q, max_seqlen_q, block_tables, max_blocks_per_seq, num_q_heads,
@@ -348,6 +385,70 @@ int pa_sample(const void *logits, int64_t logits_row_stride, int32_t batch, int3
     return cuda_status(pa::launch_sample(logits, logits_row_stride, batch, vocab, dtype, temperatures, noise, seed,
                                          offset, tokens, err_flag, static_cast<cudaStream_t>(stream)),
                        "pa_sample launch");
+}
+
+int pa_mixed_step(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                  const int32_t *slot_mapping, int32_t num_tokens, const void *prefill_q, const int32_t *cu_seqlens_q,
+                  const int32_t *cu_seqlens_k, int32_t num_prefill_seqs, int32_t total_prefill_q,
+                  int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *prefill_block_tables,
+                  int32_t prefill_max_blocks, void *prefill_out, const void *decode_q, int64_t decode_q_row_stride,
+                  const int32_t *decode_block_tables, int32_t decode_max_blocks, const int32_t *context_lens,
+                  int32_t decode_batch, void *decode_out, void *workspace, size_t workspace_bytes, void *k_cache,
+                  void *v_cache, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                  int32_t block_size, float scale, pa_dtype dtype, int32_t *err_flag, const pa_sm_split *split,
+                  void *stream) {
+    // every check first: nothing is launched unless all three parts are valid
+    int rc = check_store(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                         head_dim, num_blocks, block_size, dtype, nullptr);
+    if (rc) return rc;
+    bool prefill = false;
+    if (num_prefill_seqs != 0) {
+        if (!prefill_block_tables)
+            return fail(PA_ERR_INVALID_ARG, "pa_mixed_step: the prefill reads its keys through prefill_block_tables");
+        rc = check_prefill(prefill_q, nullptr, nullptr, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                           num_prefill_seqs, total_prefill_q, max_seqlen_q, max_seqlen_k, prefill_block_tables,
+                           prefill_max_blocks, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                           prefill_out, dtype, &prefill);
+        if (rc) return rc;
+    }
+    pa::DecodePlan plan{};
+    if (decode_batch != 0) {
+        rc = check_decode(decode_q, decode_q_row_stride, k_cache, v_cache, decode_block_tables, decode_max_blocks,
+                          context_lens, decode_batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                          scale, decode_out, workspace, workspace_bytes, dtype, &plan);
+        if (rc) return rc;
+    }
+    const bool decode = decode_batch > 0;
+    if (split) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev != pa::split_device(split))
+            return fail(PA_ERR_INVALID_ARG, "pa_mixed_step: the split belongs to device %d, not the current one",
+                        pa::split_device(split));
+    }
+    const cudaStream_t main = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (num_tokens > 0)
+        e = pa::launch_store_kv(k, v, k_row_stride, v_row_stride, k_cache, v_cache, slot_mapping, num_tokens,
+                                num_kv_heads * head_dim, static_cast<int64_t>(num_blocks) * block_size, err_flag,
+                                main);
+    const bool both = split && prefill && decode;
+    if (e == cudaSuccess && both) e = pa::split_fork(split, main);
+    const cudaStream_t s_prefill = both ? pa::split_stream(split, 0) : main;
+    const cudaStream_t s_decode = both ? pa::split_stream(split, 1) : main;
+    if (e == cudaSuccess && prefill) {
+        const char *why = nullptr;
+        e = pa::launch_prefill(prefill_q, nullptr, nullptr, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                               num_prefill_seqs, total_prefill_q, max_seqlen_q, prefill_block_tables,
+                               prefill_max_blocks, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                               prefill_out, dtype, err_flag, s_prefill, &why);
+        if (why) return fail(PA_ERR_CUDA, "pa_mixed_step: %s", why);
+    }
+    if (e == cudaSuccess && decode)
+        e = pa::launch_decode(decode_q, decode_q_row_stride, k_cache, v_cache, decode_block_tables, decode_max_blocks,
+                              context_lens, decode_batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                              block_size, scale, decode_out, workspace, plan, dtype, err_flag, s_decode);
+    if (e == cudaSuccess && both) e = pa::split_join(split, main);
+    return cuda_status(e, "pa_mixed_step launch");
 }
 
 }  // extern "C"

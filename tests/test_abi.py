@@ -226,3 +226,34 @@ def test_fp8_store_decode_validation(lib):
     assert call(d=64, qs=1024, ks=512, vs=512) == -2          # head_dim 128 only
     assert call(vsc=0.0) == -1
     assert call(B=0, k=None, v=None, sm=None, q=None, out=None, ws=None) == 0
+
+
+def test_mixed_step_validation(lib):
+    """pa_mixed_step checks all three parts before launching anything."""
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, ks=1024, vs=1024, sm=FAKE, T=4216, pq=FAKE, cuq=FAKE, cuk=FAKE, ns=8, tq=4096,
+                 mq=512, mk=4096, pbt=FAKE, pmb=16, pout=FAKE, dq=FAKE, dqs=4096, dbt=FAKE, dmb=16, cl=FAKE, B=120,
+                 dout=FAKE, ws=FAKE, wsb=1 << 30, kc=FAKE, vc=FAKE, hq=32, hkv=8, d=128, n=2000, bs=256, scale=0.088,
+                 dt=1)
+        a.update(kw)
+        return lib.pa_mixed_step(a["k"], a["v"], a["ks"], a["vs"], a["sm"], a["T"], a["pq"], a["cuq"], a["cuk"],
+                                 a["ns"], a["tq"], a["mq"], a["mk"], a["pbt"], a["pmb"], a["pout"], a["dq"], a["dqs"],
+                                 a["dbt"], a["dmb"], a["cl"], a["B"], a["dout"], a["ws"], a["wsb"], a["kc"], a["vc"],
+                                 a["hq"], a["hkv"], a["d"], a["n"], a["bs"], ctypes.c_float(a["scale"]), a["dt"], None,
+                                 None, None)
+    assert call(dt=5) == -2
+    assert call(T=-1) == -1
+    assert call(sm=None) == -1                                 # the store's slots
+    assert call(pbt=None) == -1                                # the prefill reads the pool through its tables
+    assert call(mk=100) == -1                                  # max_seqlen_k < max_seqlen_q
+    assert call(pout=ctypes.c_void_p((1 << 20) + 8)) == -1    # prefill out 16-byte aligned
+    assert call(dqs=100) == -1                                 # decode q rows shorter than H_q * D
+    assert call(wsb=16) == -1                                  # decode workspace too small
+    assert call(hq=20) == -1                                   # H_q not a multiple of H_kv
+    assert call(hq=24) == -2                                   # GQA group of 3
+
+
+def test_sm_split_validation(lib):
+    assert lib.pa_sm_split_create(96, None) == -1
+    assert lib.pa_sm_split_info(None, None, None, None, None) == -1
+    lib.pa_sm_split_destroy(None)
