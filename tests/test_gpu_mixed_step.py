@@ -78,3 +78,30 @@ def test_sm_split_sizes(pa, split):
     for bad in (0, 12, 4, split.sms[0] + split.sms[1]):
         with pytest.raises(pa.PagedAttentionError):
             pa.SmSplit(bad)
+
+
+def test_mixed_step_with_one_side_empty(pa, split):
+    """A step with no decode sequences (store + prefill) or no prefill sequences (store + decode):
+    the split is not used and the results equal the separate calls."""
+    m = inputs.mixed_chunked_prefill(seed=43, n_prefill=2, chunk=64, n_decode=5, max_prefix=400)
+    pf, st = m.prefill, m.decode
+    n_pf = int(pf.cu_seqlens_q[-1])  # the prefill tokens come first in the step's store
+    pout, dout, kc, vc = _separate(pa, m)
+    d = _device(m)
+    # no decode sequences: store only the prefill tokens, then the prefill
+    kc1, vc1 = pf.pool.k_cache.cuda(), pf.pool.v_cache.cuda()
+    empty_q = d["dq"][:0]
+    p1, d1 = pa.mixed_step(d["k"][:n_pf], d["v"][:n_pf], d["sm"][:n_pf].contiguous(), d["pq"], d["cuq"], d["cuk"],
+                           pf.max_seqlen_q, pf.max_seqlen_k, d["pbt"], empty_q, d["dbt"][:0], d["cl"][:0], kc1, vc1,
+                           pf.scale, split=split)
+    torch.cuda.synchronize()
+    assert d1.shape[0] == 0
+    assert_bit_equal(p1, pout, "prefill out without decode sequences")
+    # no prefill sequences: store only the decode tokens, then the decode
+    kc2, vc2 = pf.pool.k_cache.cuda(), pf.pool.v_cache.cuda()
+    cu0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p2, d2 = pa.mixed_step(d["k"][n_pf:], d["v"][n_pf:], d["sm"][n_pf:].contiguous(), d["pq"][:0], cu0, cu0, 0, 0,
+                           d["pbt"][:0], d["dq"], d["dbt"], d["cl"], kc2, vc2, st.scale, split=split)
+    torch.cuda.synchronize()
+    assert p2.shape[0] == 0
+    assert_bit_equal(d2, dout, "decode out without prefill sequences")
