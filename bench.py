@@ -85,8 +85,9 @@ SAMPLER_METRIC = "temperature-sampling logits GB/s and rows/s on 1 GPU"
 STORE_METRIC = "slot-mapped KV store GB/s (read + write) on 1 GPU"
 # Warp instructions one pa_sample launch executes on the sampler workload (ncu
 # smsp__inst_executed.sum of sample_kernel, profiles/sample_sampler_qwen3_vocab.md): the
-# kernel is issue-bound (Philox4x32-10 and two accurate logarithms per vocabulary entry).
-SAMPLER_INSTRUCTIONS_PER_CALL = 11_920_704
+# kernel is issue-bound (Philox4x32-10 and two accurate logarithms per vocabulary entry;
+# 36 warp instructions per entry).
+SAMPLER_INSTRUCTIONS_PER_CALL = 10_966_336
 ISSUE_PER_SM_PER_CLK = 4  # warp instructions: four schedulers per SM
 
 

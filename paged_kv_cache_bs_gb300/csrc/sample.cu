@@ -44,52 +44,71 @@ struct SampleArgs {
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
 // as 1, 2, 3", SC'11): ten rounds, each two 32x32 -> 64-bit products of
 // counter words with the round multipliers, the high halves xored with the
-// other counter words and the key; the key is advanced by the Weyl
-// increments between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// other counter words and the round key.  The round keys (the key advanced by
+// the Weyl increments between rounds) depend only on the seed, so a thread
+// derives them once.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+    __device__ __forceinline__ PhiloxKeys(uint32_t s0, uint32_t s1) {
+#pragma unroll
+        for (int r = 0; r < 10; ++r) {
+            k0[r] = s0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+            k1[r] = s1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+        }
+    }
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &k) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
         const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+        c = make_uint4(hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0);
     }
     return c;
 }
 
-// Natural logarithm from the hardware base-2 logarithm (MUFU): absolute error
-// about 1e-7, far below what moves a decision between two different scores.
-__device__ __forceinline__ float log_hw(float x) {
+// Hardware base-2 logarithm (MUFU): absolute error about 2^-22.
+__device__ __forceinline__ float lg2_hw(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-    return y * 0.6931471805599453f;
+    return y;
 }
 
-// Exp(1) sample from 24 random bits: u = ((x >> 8) + 1) 2^-24 in (0, 1],
-// E = -log(u).  Near u = 1, where E is small and decides the race's
-// winners, -log(1 - v) = v + v^2/2 + v^3/3 + v^4/4 + v^5/5 + ... with
-// v = 1 - u exact (relative error below 3e-7 for v < 1/16, rounding included);
-// elsewhere E >= 0.0645 and the hardware logarithm is within 2e-6.
-__device__ __forceinline__ float exp1(uint32_t x) {
+// An Exp(1) sample from 24 random bits, in units of 1/ln 2 (E' = E / ln 2, E = -ln u):
+// u = ((x >> 8) + 1) 2^-24 in (0, 1], E' = -log2(u).  Near u = 1, where E is small
+// and decides the race's winners, -ln(1 - v) = v + v^2/2 + v^3/3 + v^4/4 + v^5/5 +
+// ... with v = 1 - u exact (relative error below 3e-7 for v < 1/16, rounding
+// included); elsewhere E >= 0.0645 and the hardware logarithm is within 2e-6.  Both
+// forms are computed and one is selected (no divergent branch).  The race only
+// compares log E_i + const, so the common factor 1/ln 2 does not change the winner.
+__device__ __forceinline__ float exp1_scaled(uint32_t x) {
     const float u = static_cast<float>((x >> 8) + 1u) * 0x1p-24f;
     const float v = 1.f - u;
-    if (v < 0.0625f) return v * fmaf(v, fmaf(v, fmaf(v, fmaf(v, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f);
-    return -log_hw(u);
+    const float series = v * fmaf(v, fmaf(v, fmaf(v, fmaf(v, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.f) *
+                         1.4426950408889634f;
+    const float hw = -lg2_hw(u);
+    return v < 0.0625f ? series : hw;
 }
 
-// Eight consecutive logits as floats (from a 16-byte aligned address).
+// Eight consecutive logits (from a 16-byte aligned address): loaded raw, widened to floats.
 template <typename T> struct Vec8;
 template <> struct Vec8<float> {
-    static __device__ __forceinline__ void load(const float *p, float (&v)[8]) {
-        const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
-        v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    struct Raw {
+        float4 a, b;
+    };
+    static __device__ __forceinline__ Raw load(const float *p) {
+        return Raw{*reinterpret_cast<const float4 *>(p), *reinterpret_cast<const float4 *>(p + 4)};
+    }
+    static __device__ __forceinline__ void unpack(const Raw &r, float (&v)[8]) {
+        v[0] = r.a.x, v[1] = r.a.y, v[2] = r.a.z, v[3] = r.a.w, v[4] = r.b.x, v[5] = r.b.y, v[6] = r.b.z, v[7] = r.b.w;
     }
     static __device__ __forceinline__ float one(const float *p) { return *p; }
 };
 template <> struct Vec8<__nv_bfloat16> {
-    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8]) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(p);
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint4 *>(p); }
+    static __device__ __forceinline__ void unpack(const Raw &a, float (&v)[8]) {
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -100,8 +119,9 @@ template <> struct Vec8<__nv_bfloat16> {
     static __device__ __forceinline__ float one(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 };
 template <> struct Vec8<__half> {
-    static __device__ __forceinline__ void load(const __half *p, float (&v)[8]) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(p);
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const __half *p) { return *reinterpret_cast<const uint4 *>(p); }
+    static __device__ __forceinline__ void unpack(const Raw &a, float (&v)[8]) {
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -140,47 +160,52 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     const int tail0 = 8 * ngroups, tail_per = (V - tail0 + kCluster - 1) / kCluster;
     const int t0 = min(V, tail0 + part * tail_per), t1 = min(V, t0 + tail_per);
 
-    float best = 0.f;
+    // Scores in base 2: a_i log2(e) - log2(max(E_i, 1e-10)), the race's ln form times log2(e) > 0
+    // (same winner).  The in-kernel draws are E_i / ln 2, clamped at 1e-10 / ln 2: a common shift.
+    float best = -INFINITY;  // -inf never wins: a row with no finite score keeps index -1
     int best_i = -1;
-    const float inv_t = 1.f / temp;
-    auto visit = [&](int i, float x, float e) {
-        const float sc = x * inv_t - log_hw(fmaxf(e, kMinNoise));
-        if (sc > -INFINITY && (best_i < 0 || sc > best)) {  // a thread visits its indices in increasing order
+    const float inv_t2 = 1.4426950408889634f / temp;
+    auto visit = [&](int i, float x, float e, float min_noise) {
+        const float sc = x * inv_t2 - lg2_hw(fmaxf(e, min_noise));
+        if (sc > best) {  // a thread visits its indices in increasing order: ties keep the first
             best = sc;
             best_i = i;
         }
     };
+    constexpr float kMinScaledNoise = kMinNoise * 1.4426950408889634f;
     const float *noise = a.noise ? a.noise + static_cast<int64_t>(b) * V : nullptr;
     if (valid_t) {
+        const PhiloxKeys keys(a.seed_lo, a.seed_hi);
+        const float min_noise = noise ? kMinNoise : kMinScaledNoise;
         for (int g = g0 + tid; g < g1; g += kThreads) {
             float v[8], e[8];
-            Vec8<T>::load(row + 8 * g, v);
+            Vec8<T>::unpack(Vec8<T>::load(row + 8 * g), v);
             if (noise) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) e[j] = noise[8 * g + j];
             } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint4 r = philox4x32_10(make_uint4(2 * g + h, b, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
-                    e[4 * h] = exp1(r.x);
-                    e[4 * h + 1] = exp1(r.y);
-                    e[4 * h + 2] = exp1(r.z);
-                    e[4 * h + 3] = exp1(r.w);
+                    const uint4 r = philox4x32_10(make_uint4(2 * g + h, b, a.off_lo, a.off_hi), keys);
+                    e[4 * h] = exp1_scaled(r.x);
+                    e[4 * h + 1] = exp1_scaled(r.y);
+                    e[4 * h + 2] = exp1_scaled(r.z);
+                    e[4 * h + 3] = exp1_scaled(r.w);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) visit(8 * g + j, v[j], e[j]);
+            for (int j = 0; j < 8; ++j) visit(8 * g + j, v[j], e[j], min_noise);
         }
         for (int i = t0 + tid; i < t1; i += kThreads) {
             float e;
             if (noise) {
                 e = noise[i];
             } else {
-                const uint4 r = philox4x32_10(make_uint4(i >> 2, b, a.off_lo, a.off_hi), a.seed_lo, a.seed_hi);
+                const uint4 r = philox4x32_10(make_uint4(i >> 2, b, a.off_lo, a.off_hi), keys);
                 const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-                e = exp1(w[i & 3]);
+                e = exp1_scaled(w[i & 3]);
             }
-            visit(i, Vec8<T>::one(row + i), e);
+            visit(i, Vec8<T>::one(row + i), e, min_noise);
         }
     }
     // CTA winner
