@@ -53,10 +53,10 @@ DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 # capture of the current kernels (profiles/decode_<workload>.md); a workload
 # missing here reports null.
 TRAFFIC_PER_CALL = {
-    "qwen3_0p6b_decode": 583_123_968 + 4_384_000,       # decode_partition_kernel (store fused)
-    "qwen3_0p6b_decode_fp8": 291_855_872 + 3_784_448,   # decode_partition_kernel, E4M3 pool (store fused)
-    "long_context_decode": 536_950_784 + 3_327_232,     # decode_partition_kernel
-    "qwen3_8b_shared_decode": 868_519_936 + 5_361_152,  # decode_partition_kernel (L2 absorbs shared pages)
+    "qwen3_0p6b_decode": 583_162_368 + 3_883_264,       # decode_partition_kernel (store fused)
+    "qwen3_0p6b_decode_fp8": 291_831_808 + 4_151_040,   # decode_partition_kernel, E4M3 pool (store fused)
+    "long_context_decode": 536_967_936 + 3_231_744,     # decode_partition_kernel (store fused)
+    "qwen3_8b_shared_decode": 869_958_912 + 5_998_592,  # decode_partition_kernel (store fused; L2 absorbs shared pages)
 }
 PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 117_771_520 + 12_707_584}  # prefill_kernel
 # store_kv_kernel on store_stress: DRAM read + write inside the launch (the L2 holds most written
@@ -88,6 +88,7 @@ STORE_METRIC = "slot-mapped KV store GB/s (read + write) on 1 GPU"
 # kernel is issue-bound (Philox4x32-10 and two accurate logarithms per vocabulary entry;
 # 36 warp instructions per entry).
 SAMPLER_INSTRUCTIONS_PER_CALL = 10_966_336
+SAMPLER_TRAFFIC_PER_CALL = 19_469_824  # sample_kernel DRAM read + write (ncu, one launch)
 ISSUE_PER_SM_PER_CLK = 4  # warp instructions: four schedulers per SM
 
 
@@ -662,7 +663,7 @@ def run_sampler(args, world, rank, local):
         roof = {"bound": "alu", "kernel": "sample_kernel (Philox4x32-10 + two logf per entry, issue-bound)",
                 "achieved": achieved, "peak": issue_peak, "unit": "warp-instr/s", "frac": achieved / issue_peak,
                 "peak_source": f"derived: {ISSUE_PER_SM_PER_CLK} warp instructions/clock/SM x {sms} SMs x "
-                               f"{sm_mhz:.0f} MHz sampled", "traffic": nbytes,
+                               f"{sm_mhz:.0f} MHz sampled", "traffic": SAMPLER_TRAFFIC_PER_CALL,
                 "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
     else:
         roof = {"bound": "alu", "kernel": "sample_kernel", "achieved": None, "peak": issue_peak,
