@@ -290,7 +290,10 @@ class SmSplit:
             self._h = None
 
     def __del__(self):
-        self.close()
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may already be unloaded
+            pass
 
 
 def mixed_step(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, prefill_q: torch.Tensor,
