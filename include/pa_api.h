@@ -17,8 +17,10 @@
  *   - All tensor arguments are DEVICE pointers to caller-owned memory; the
  *     library allocates nothing and keeps no state besides cached device
  *     properties.  Integer size arguments are host values.  Exception: the
- *     per-step operands of pa_store_decode and pa_store_decode_fp8 (k, v,
- *     slot_mapping, q, block_tables, context_lens and out) may instead be
+ *     per-step operands of pa_store_kv (k, v, slot_mapping), of
+ *     pa_store_decode and pa_store_decode_fp8 (k, v, slot_mapping, q,
+ *     block_tables, context_lens and out) and of pa_sample (logits,
+ *     temperatures, noise, tokens) may instead be
  *     page-locked host memory from cudaHostAlloc / cudaMallocHost, which under
  *     unified addressing is device-accessible through its host pointer: the
  *     kernels then read and write it directly over the CPU-GPU link (zero

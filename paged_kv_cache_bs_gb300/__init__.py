@@ -146,6 +146,7 @@ def store_kv(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: t
         raise ValueError("k/v must be [T, H_kv, D] matching the cache")
     if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype:
         raise TypeError("k/v dtype must match the cache")
+    _step_operands(k_cache, k=k, v=v, slot_mapping=slot_mapping)
     rc = _lib.pa_store_kv(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(k_cache), _ptr(v_cache),
                           _ptr(slot_mapping), slot_mapping.numel(), hkv, d, n, bs, _dtype(k_cache), _ptr(err_flag),
                           _stream(k_cache))
@@ -165,10 +166,11 @@ def alloc_decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables:
 
 
 def _step_operands(k_cache: torch.Tensor, **tensors) -> None:
-    """The small per-step operands of the decode calls (q, the new k/v rows, slot mapping,
-    block tables, context lengths, out) may live on the pool's device or in page-locked host
-    memory, which the kernels then read and write directly over the CPU-GPU link (with unified
-    addressing a pinned host pointer is also a device pointer).  Pageable host memory is refused."""
+    """The per-step operands of the store, the fused decode calls and the sampler (q, the new k/v
+    rows, slot mapping, block tables, context lengths, logits, temperatures, out) may live on the
+    device or in page-locked host memory, which the kernels then read and write directly over the
+    CPU-GPU link (with unified addressing a pinned host pointer is also a device pointer).
+    Pageable host memory is refused.  ``k_cache``: any tensor on the device the call runs on."""
     for name, t in tensors.items():
         if t is None:
             continue
@@ -426,11 +428,18 @@ def store_decode_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tenso
 
 
 def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor | None = None, seed: int = 0,
-           offset: int = 0, out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+           offset: int = 0, out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+           device: torch.device | None = None) -> torch.Tensor:
     """One token per row of logits [B, V] (fp32/bf16/fp16): argmax of softmax(logits / T) / max(E, 1e-10),
-    E ~ Exp(1) from ``noise`` [B, V] fp32 or, if None, drawn in-kernel from Philox4x32-10 at (seed, offset)."""
-    if logits.dim() != 2 or logits.stride(1) != 1 or not logits.is_cuda:
-        raise ValueError("logits must be a CUDA [B, V] tensor with contiguous rows")
+    E ~ Exp(1) from ``noise`` [B, V] fp32 or, if None, drawn in-kernel from Philox4x32-10 at (seed, offset).
+    The operands may be on the GPU or in pinned host memory (read and written by the kernel directly);
+    ``device`` (default: that of ``logits`` if on the GPU, else the current device) runs the kernel."""
+    if device is None:
+        device = logits.device if logits.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    anchor = torch.empty(0, device=device)
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a [B, V] tensor with contiguous rows")
+    _step_operands(anchor, logits=logits, temperatures=temperatures, noise=noise, out=out)
     dt = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}.get(logits.dtype)
     if dt is None:
         raise TypeError("logits must be fp32, bf16 or fp16")
@@ -440,9 +449,9 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
     if noise is not None and (noise.dtype != torch.float32 or tuple(noise.shape) != (B, V) or not noise.is_contiguous()):
         raise ValueError("noise must be contiguous fp32 [B, V]")
     if out is None:
-        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+        out = torch.empty(B, dtype=torch.int32, device=device)
     rc = _lib.pa_sample(_ptr(logits), logits.stride(0), B, V, dt, _ptr(temperatures), _ptr(noise), seed, offset,
-                        _ptr(out), _ptr(err_flag), _stream(logits))
+                        _ptr(out), _ptr(err_flag), _stream(anchor))
     _check("pa_sample", rc)
     return out
 

@@ -78,3 +78,19 @@ def test_in_kernel_noise_frequencies_follow_softmax(pa, T):
     expect = torch.softmax(z.double() / T, dim=0) * N
     chi2 = float(((counts - expect) ** 2 / expect).sum())
     assert chi2 < 33.4, (chi2, counts.tolist(), expect.tolist())
+
+
+def test_sample_from_pinned_host_operands(pa):
+    """Logits, temperatures and noise in pinned host memory and the tokens written there by the
+    kernel directly: the same tokens as with device operands (given noise and in-kernel noise)."""
+    logits, temps, noise = rows(77, 16, 151936, torch.bfloat16)
+    dev = torch.device("cuda", 0)
+    pl, pt, pn = logits.pin_memory(), temps.pin_memory(), noise.pin_memory()
+    for use_noise in (True, False):
+        ref = pa.sample(logits.cuda(), temps.cuda(), noise.cuda() if use_noise else None, seed=5, offset=3).cpu()
+        out = torch.full((16,), -7, dtype=torch.int32).pin_memory()
+        pa.sample(pl, pt, pn if use_noise else None, seed=5, offset=3, out=out, device=dev)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    with pytest.raises(ValueError):
+        pa.sample(logits, temps, device=dev)

@@ -100,3 +100,18 @@ def test_store_out_of_range_slot_is_flagged_and_skipped(pa):
     assert int(flag.item()) & pa.FLAG_BAD_SLOT
     assert_bit_equal(dkc, okc, "k_cache (valid rows written, bad ones skipped)")
     assert_bit_equal(dvc, ovc, "v_cache")
+
+
+def test_store_from_pinned_host_rows(pa):
+    """The new rows and slots in pinned host memory, read by the kernel directly: the pool equals the
+    oracle's bit for bit; pageable host memory is refused."""
+    k, v, kc, vc, slots = inputs.store_stress(tokens=2048)
+    dkc, dvc = kc.cuda(), vc.cuda()
+    pa.store_kv(k.pin_memory(), v.pin_memory(), dkc, dvc, slots.pin_memory())
+    torch.cuda.synchronize()
+    okc, ovc = kc.clone(), vc.clone()
+    oracle.store_kv(k, v, okc, ovc, slots)
+    assert_bit_equal(dkc, okc, "k_cache after a store from pinned host rows")
+    assert_bit_equal(dvc, ovc, "v_cache after a store from pinned host rows")
+    with pytest.raises(ValueError):
+        pa.store_kv(k, v, dkc, dvc, slots)
