@@ -339,6 +339,18 @@ PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const v
                      float scale, void *out, pa_dtype dtype, int32_t *err_flag, void *stream);
 
 /*
+ * pa_selftest_wait_timeout -- a diagnostic with no counterpart on the pages:
+ * shows on a live GPU that the library's bounded waits end with a status
+ * instead of a hang.  Launches one thread on `stream` that waits on an
+ * mbarrier nothing ever arrives on, with the bounded wait the store, decode
+ * and prefill kernels use on their own asynchronous copies and tensor-core
+ * work; after `max_cycles` SM clock cycles (in (0, 4e9]) it gives up, ORs
+ * PA_FLAG_TIMEOUT into the DEVICE int32 *err_flag (required) and returns,
+ * and the context stays usable.
+ */
+PA_API int pa_selftest_wait_timeout(int64_t max_cycles, int32_t *err_flag, void *stream);
+
+/*
  * pa_sm_split -- the GPU's SMs as two disjoint partitions, each with its own
  * stream (CUDA green contexts), for pa_mixed_step.  The pages run a mixed
  * step's chunked prefill and decode as one batch ("nano-vLLM Part 2", section

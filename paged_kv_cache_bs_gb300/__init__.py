@@ -65,6 +65,8 @@ _lib.pa_store_decode_fp8.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _
                                      _i32, _i32, _f32, _f32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
 _lib.pa_sample.restype = ctypes.c_int
 _lib.pa_sample.argtypes = [_p, _i64, _i32, _i32, ctypes.c_int, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
+_lib.pa_selftest_wait_timeout.restype = ctypes.c_int
+_lib.pa_selftest_wait_timeout.argtypes = [_i64, _p, _p]
 _lib.pa_sm_split_create.restype = ctypes.c_int
 _lib.pa_sm_split_create.argtypes = [_i32, ctypes.POINTER(ctypes.c_void_p)]
 _lib.pa_sm_split_info.restype = ctypes.c_int
@@ -264,6 +266,15 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
                                hq, hkv, d, n, bs, float(scale), _ptr(out), _dtype(q), _ptr(err_flag), _stream(q))
     _check("pa_prefill_paged", rc)
     return out
+
+
+def selftest_wait_timeout(err_flag: torch.Tensor, max_cycles: int = 2_000_000) -> None:
+    """``pa_selftest_wait_timeout``: a bounded wait that nothing satisfies gives up after
+    ``max_cycles`` and ORs FLAG_TIMEOUT into ``err_flag`` (a CUDA int32 tensor)."""
+    if err_flag.dtype != torch.int32 or not err_flag.is_cuda:
+        raise ValueError("err_flag must be a CUDA int32 tensor")
+    _check("pa_selftest_wait_timeout", _lib.pa_selftest_wait_timeout(int(max_cycles), _ptr(err_flag),
+                                                                      _stream(err_flag)))
 
 
 class SmSplit:

@@ -257,3 +257,9 @@ def test_sm_split_validation(lib):
     assert lib.pa_sm_split_create(96, None) == -1
     assert lib.pa_sm_split_info(None, None, None, None, None) == -1
     lib.pa_sm_split_destroy(None)
+
+
+def test_selftest_wait_timeout_validation(lib):
+    assert lib.pa_selftest_wait_timeout(0, FAKE, None) == -1
+    assert lib.pa_selftest_wait_timeout(5_000_000_000, FAKE, None) == -1
+    assert lib.pa_selftest_wait_timeout(1000, None, None) == -1
