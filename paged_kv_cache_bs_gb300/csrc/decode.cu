@@ -163,9 +163,15 @@ __device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g,
     __syncwarp();
 }
 
-// Byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r in the swizzled layout.
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {
-    return (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+// Byte offset of 16-byte chunk c (0 .. D/8-1) of tile row r in the swizzled layout.  A tile is
+// kept as groups of 2^lbr rows (one TMA box: a page, or 64 rows of a longer page); inside a group
+// the row's 128-byte slices follow one another, each 2^lbr rows of 128 bytes (with one slice per
+// row this is plain row order).
+template <int kSlices>
+__device__ __forceinline__ uint32_t tile_off(int r, int c, int lbr) {
+    const int rows = 1 << lbr;
+    return (r >> lbr) * (rows * 128 * kSlices) + (c >> 3) * (rows * 128) + (r & (rows - 1)) * 128 +
+           (((c & 7) ^ (r & 7)) << 4);
 }
 
 // Two E4M3 codes (low byte first) as an fp16 pair (low half first): exact,
@@ -336,12 +342,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
                 for (int i = 0; i < nbox; ++i) {
                     const int j = tile_start + i * box_rows;
                     const int y = (bt_s[(j >> a.log2_bs) - first_page] << a.log2_bs) + (j & bs_mask);
-                    const uint32_t row_off = i * box_rows * 128;
-#pragma unroll
-                    for (int h = 0; h < S::kSlices; ++h) {
-                        const int x = g * D + h * (F8 ? 128 : 64);  // elements: 128 bytes per slice
-                        tc::tma_load_2d(kdst + h * S::kSliceBytes + row_off, &tm_k, x, y, full);
-                        tc::tma_load_2d(vdst + h * S::kSliceBytes + row_off, &tm_v, x, y, full);
+                    const uint32_t box_off = i * box_rows * 128 * S::kSlices;
+                    if constexpr (S::kSlices == 1) {
+                        const int x = g * D;  // elements: one 128-byte slice holds the kv head's row
+                        tc::tma_load_2d(kdst + box_off, &tm_k, x, y, full);
+                        tc::tma_load_2d(vdst + box_off, &tm_v, x, y, full);
+                    } else {
+                        // both 128-byte slices of the kv head's rows in one 3-D box, slice by slice
+                        tc::tma_load_3d(kdst + box_off, &tm_k, 0, y, g * S::kSlices, full);
+                        tc::tma_load_3d(vdst + box_off, &tm_v, 0, y, g * S::kSlices, full);
                     }
                 }
                 issued = t + 1;
@@ -349,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
         }
     } else {
         const int wrow = warp * 16;
+        const int lbr = min(a.log2_bs, 6);  // log2 of the rows of one TMA box (at most the 64-row tile)
         const int rk = wrow + (lane & 7) + ((lane >> 3) & 1) * 8, ck = lane >> 4;
         const int rv = wrow + (lane & 7) + (lane >> 4) * 8, cv = (lane >> 3) & 1;
         for (int t = 0; t < ntiles; ++t) {
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
 #pragma unroll
                 for (int kp = 0; kp < S::kKSteps / 2; ++kp) {
                     uint32_t r0, r1, r2, r3;
-                    ldmatrix_x4(kb + tile_off(rk, kp * 2 + ck), r0, r1, r2, r3);
+                    ldmatrix_x4(kb + tile_off<S::kSlices>(rk, kp * 2 + ck, lbr), r0, r1, r2, r3);
                     kf[2 * kp][0] = e4m3x2_lo(r0);
                     kf[2 * kp][1] = e4m3x2_lo(r1);
                     kf[2 * kp][2] = e4m3x2_hi(r0);
@@ -376,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
                     kf[2 * kp + 1][1] = e4m3x2_lo(r3);
                     kf[2 * kp + 1][2] = e4m3x2_hi(r2);
                     kf[2 * kp + 1][3] = e4m3x2_hi(r3);
-                    ldmatrix_x4_trans(vb + tile_off(rk, kp * 2 + ck), r0, r1, r2, r3);
+                    ldmatrix_x4_trans(vb + tile_off<S::kSlices>(rk, kp * 2 + ck, lbr), r0, r1, r2, r3);
                     // bytes (token 2j, d 2m), (2j, 2m+1), (2j+1, 2m), (2j+1, 2m+1) -> split by d:
                     // bytes 0-1 are tokens 2j, 2j+1 of d 2m, bytes 2-3 those of d 2m+1
                     vf[kp][0] = __byte_perm(r0, 0, 0x3120);
@@ -387,10 +397,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
             } else {
 #pragma unroll
                 for (int ks = 0; ks < S::kKSteps; ++ks)
-                    ldmatrix_x4(kb + tile_off(rk, ks * 2 + ck), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+                    ldmatrix_x4(kb + tile_off<S::kSlices>(rk, ks * 2 + ck, lbr), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
 #pragma unroll
                 for (int mt = 0; mt < S::kKSteps; ++mt)
-                    ldmatrix_x4_trans(vb + tile_off(rv, mt * 2 + cv), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+                    ldmatrix_x4_trans(vb + tile_off<S::kSlices>(rv, mt * 2 + cv, lbr), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bars + 8 * (kStages + s));  // stage free for the next tile
@@ -726,16 +736,21 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.k_cache_w = const_cast<void *>(k_cache);
     a.v_cache_w = const_cast<void *>(v_cache);
 
-    // the pool as [num_blocks * block_size rows, H_kv * D columns]; one box = 64 columns of
-    // min(block_size, 64) rows, so a box never crosses a page
+    // the pool as [num_blocks * block_size rows, H_kv * D columns]; one box = min(block_size, 64)
+    // rows (a box never crosses a page) of one kv head's row: 128 bytes (E4M3 codes, or 16-bit at
+    // D = 64) by a 2-D map, or both 128-byte halves of a 16-bit D = 128 row by a 3-D map
     CUtensorMap tm_k, tm_v;
     const int64_t rows = static_cast<int64_t>(num_blocks) * block_size;
     const int64_t cols = static_cast<int64_t>(num_kv_heads) * head_dim;
     const int box_rows = block_size < kTile ? block_size : kTile;
     const pa_dtype pool = fp8 ? PA_E4M3 : dtype;
-    if (!make_tmap_rows(&tm_k, k_cache, pool, cols, rows, box_rows) ||
-        !make_tmap_rows(&tm_v, v_cache, pool, cols, rows, box_rows))
-        return cudaErrorInvalidValue;
+    const bool two_slices = !fp8 && head_dim == 128;
+    const bool maps_ok =
+        two_slices ? make_tmap_row_slices(&tm_k, k_cache, pool, cols, rows, box_rows, 2) &&
+                         make_tmap_row_slices(&tm_v, v_cache, pool, cols, rows, box_rows, 2)
+                   : make_tmap_rows(&tm_k, k_cache, pool, cols, rows, box_rows) &&
+                         make_tmap_rows(&tm_v, v_cache, pool, cols, rows, box_rows);
+    if (!maps_ok) return cudaErrorInvalidValue;
 
     auto run = [&](auto kern_part, auto kern_comb, auto prepare, int smem, int d) -> cudaError_t {
         cudaError_t err = prepare();

@@ -71,6 +71,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+// 3-D tiled bulk tensor load: x innermost (elements), then y, then z.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -258,5 +266,10 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 // 64 columns (128 bytes) x box_rows rows, 128-byte swizzle.  False when the
 // driver cannot encode it (entry point missing, tensor too large).
 bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows);
+// Host: 3-D TMA map over the same 16-bit [rows, cols] matrix seen as (64 elements of a 128-byte slice,
+// rows, slices of a row), so one box takes box_rows rows of box_slices adjacent slices (a kv head's
+// whole row) and lands in shared memory slice by slice; 128-byte swizzle.
+bool make_tmap_row_slices(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows,
+                          int box_slices);
 
 }  // namespace pa

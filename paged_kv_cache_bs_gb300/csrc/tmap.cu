@@ -32,6 +32,7 @@ struct MapKey {
     const void *base;
     int64_t cols, rows;
     int box_rows;
+    int box_slices;  // 0: the 2-D map
     pa_dtype dt;
 };
 constexpr int kCacheSlots = 8;
@@ -41,14 +42,37 @@ thread_local int t_next = 0;
 
 }  // namespace
 
-bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows) {
+namespace {
+
+bool cached(CUtensorMap *m, const MapKey &key) {
     for (int i = 0; i < kCacheSlots; ++i) {
         const MapKey &k = t_keys[i];
-        if (k.base == base && k.cols == cols && k.rows == rows && k.box_rows == box_rows && k.dt == dt) {
+        if (k.base == key.base && k.cols == key.cols && k.rows == key.rows && k.box_rows == key.box_rows &&
+            k.box_slices == key.box_slices && k.dt == key.dt) {
             memcpy(m, &t_maps[i], sizeof(CUtensorMap));
             return true;
         }
     }
+    return false;
+}
+
+void remember(const CUtensorMap *m, const MapKey &key) {
+    const int slot = t_next;
+    t_next = (t_next + 1) % kCacheSlots;
+    t_keys[slot] = key;
+    memcpy(&t_maps[slot], m, sizeof(CUtensorMap));
+}
+
+CUtensorMapDataType tma_type(pa_dtype dt) {
+    return dt == PA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                         : dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+}  // namespace
+
+bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows) {
+    const MapKey key{base, cols, rows, box_rows, 0, dt};
+    if (cached(m, key)) return true;
     EncodeTiled enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -57,17 +81,30 @@ bool make_tmap_rows(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols,
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * (f8 ? 1 : 2))};
     const cuuint32_t box[2] = {f8 ? 128u : 64u, static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1u, 1u};
-    const CUtensorMapDataType type = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                     : dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const CUresult r = enc(m, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUresult r = enc(m, tma_type(dt), 2, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
-    const int slot = t_next;
-    t_next = (t_next + 1) % kCacheSlots;
-    t_keys[slot] = MapKey{base, cols, rows, box_rows, dt};
-    memcpy(&t_maps[slot], m, sizeof(CUtensorMap));
+    remember(m, key);
+    return true;
+}
+
+bool make_tmap_row_slices(CUtensorMap *m, const void *base, pa_dtype dt, int64_t cols, int64_t rows, int box_rows,
+                          int box_slices) {
+    const MapKey key{base, cols, rows, box_rows, box_slices, dt};
+    if (cached(m, key)) return true;
+    EncodeTiled enc = encoder();
+    if (!enc || dt == PA_E4M3 || cols % 64) return false;
+    // dims: 64 elements of a 128-byte slice, the rows, the slices of a row
+    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2), 128u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_slices)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(m, tma_type(dt), 3, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    remember(m, key);
     return true;
 }
 
