@@ -53,10 +53,10 @@ DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 # capture of the current kernels (profiles/decode_<workload>.md); a workload
 # missing here reports null.
 TRAFFIC_PER_CALL = {
-    "qwen3_0p6b_decode": 583_162_368 + 3_883_264,       # decode_partition_kernel (store fused)
+    "qwen3_0p6b_decode": 583_122_944 + 4_789_248,       # decode_partition_kernel (store fused)
     "qwen3_0p6b_decode_fp8": 291_831_808 + 4_151_040,   # decode_partition_kernel, E4M3 pool (store fused)
-    "long_context_decode": 536_967_936 + 3_231_744,     # decode_partition_kernel (store fused)
-    "qwen3_8b_shared_decode": 869_958_912 + 5_998_592,  # decode_partition_kernel (store fused; L2 absorbs shared pages)
+    "long_context_decode": 536_962_560 + 3_218_944,     # decode_partition_kernel (store fused)
+    "qwen3_8b_shared_decode": 869_801_728 + 5_674_752,  # decode_partition_kernel (store fused; L2 absorbs shared pages)
 }
 PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 117_771_520 + 12_707_584}  # prefill_kernel
 # store_kv_kernel on store_stress: DRAM read + write inside the launch (the L2 holds most written
