@@ -58,7 +58,7 @@ TRAFFIC_PER_CALL = {
     "long_context_decode": 536_962_560 + 3_218_944,     # decode_partition_kernel (store fused)
     "qwen3_8b_shared_decode": 869_801_728 + 5_674_752,  # decode_partition_kernel (store fused; L2 absorbs shared pages)
 }
-PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 117_771_520 + 12_707_584}  # prefill_kernel
+PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 119_218_432 + 13_745_408}  # prefill_kernel (ncu, current code)
 # store_kv_kernel on store_stress: DRAM read + write inside the launch (the L2 holds most written
 # rows as dirty lines until after the launch, so this is below the algorithmic 134,217,728 B)
 STORE_TRAFFIC_PER_CALL = 67_182_848 + 15_672_576
