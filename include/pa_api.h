@@ -354,7 +354,7 @@ PA_API int pa_selftest_wait_timeout(int64_t max_cycles, int32_t *err_flag, void 
  * pa_sm_split -- the GPU's SMs as two disjoint partitions, each with its own
  * stream (CUDA green contexts), for pa_mixed_step.  The pages run a mixed
  * step's chunked prefill and decode as one batch ("nano-vLLM Part 2", section
- * 4; "From nano-vLLM to vLLM", chunked prefill); here the prefill, bound by
+ * 4; "From nano-vLLM to vLLM", section 6.3); here the prefill, bound by
  * the tensor cores, runs on the first partition while the decode, bound by
  * HBM bandwidth (which it reaches with well under half of the SMs), runs on
  * the second.  This split is this library's choice; the pages describe none.
@@ -402,7 +402,8 @@ PA_API void pa_sm_split_destroy(pa_sm_split *split);
  * split's first partition and the decode on its second, at the same time,
  * and `stream` waits for both before anything issued on it later; the split
  * must belong to the current device.  Every argument is checked before
- * anything is launched.
+ * anything is launched.  16-bit pools only (dtype PA_F16 or PA_BF16; the
+ * E4M3 pool has no prefill and so no mixed step).
  */
 PA_API int pa_mixed_step(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
                          const int32_t *slot_mapping, int32_t num_tokens, const void *prefill_q,
