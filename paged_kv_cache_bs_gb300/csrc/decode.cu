@@ -202,7 +202,8 @@ __device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t codes) {
 template <typename T, int D, int ST, bool F8>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                            const DecodeArgs a) {
+                            const __grid_constant__ CUtensorMap tm_k_tail,
+                            const __grid_constant__ CUtensorMap tm_v_tail, const DecodeArgs a) {
     using S = Shape<D, ST, F8>;
     using MT = typename std::conditional<F8, __half, T>::type;  // MMA operand type
     constexpr int kStages = ST;
@@ -334,11 +335,31 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
                     break;
                 }
                 const int tile_start = start + t * kTile;
-                const int nbox = (min(kTile, end - tile_start) + box_rows - 1) / box_rows;
+                const int valid = min(kTile, end - tile_start);
                 const uint32_t full = bars + 8 * s;
-                tc::mbar_arrive_expect_tx(full, nbox * box_rows * S::kRowBytes * 2);
                 const uint32_t kdst = ring + s * S::kStageBytes;
                 const uint32_t vdst = kdst + S::kTileBytes;
+                if (valid < kTile && box_rows == kTile) {
+                    // the context ends inside this tile of one page: fetch it in 16-row boxes up to the
+                    // end instead of a whole 64-row box (rows past the end are masked either way)
+                    constexpr int kTailRows = 16;
+                    const int nsub = (valid + kTailRows - 1) / kTailRows;
+                    tc::mbar_arrive_expect_tx(full, nsub * kTailRows * S::kRowBytes * 2);
+                    const int y0 = (bt_s[(tile_start >> a.log2_bs) - first_page] << a.log2_bs) + (tile_start & bs_mask);
+                    for (int i = 0; i < nsub; ++i) {
+#pragma unroll
+                        for (int h = 0; h < S::kSlices; ++h) {
+                            const int x = g * D + h * (F8 ? 128 : 64);  // elements: 128 bytes per slice
+                            const uint32_t off = h * (kTile * 128) + i * kTailRows * 128;
+                            tc::tma_load_2d(kdst + off, &tm_k_tail, x, y0 + i * kTailRows, full);
+                            tc::tma_load_2d(vdst + off, &tm_v_tail, x, y0 + i * kTailRows, full);
+                        }
+                    }
+                    issued = t + 1;
+                    continue;
+                }
+                const int nbox = (valid + box_rows - 1) / box_rows;
+                tc::mbar_arrive_expect_tx(full, nbox * box_rows * S::kRowBytes * 2);
                 for (int i = 0; i < nbox; ++i) {
                     const int j = tile_start + i * box_rows;
                     const int y = (bt_s[(j >> a.log2_bs) - first_page] << a.log2_bs) + (j & bs_mask);
@@ -750,7 +771,12 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                          make_tmap_row_slices(&tm_v, v_cache, pool, cols, rows, box_rows, 2)
                    : make_tmap_rows(&tm_k, k_cache, pool, cols, rows, box_rows) &&
                          make_tmap_rows(&tm_v, v_cache, pool, cols, rows, box_rows);
-    if (!maps_ok) return cudaErrorInvalidValue;
+    // the tail of a context inside a 64-row tile of a long page is fetched in 16-row boxes (2-D maps,
+    // one 128-byte slice each); with pages shorter than a tile the boxes are already a page long
+    CUtensorMap tm_k_tail = tm_k, tm_v_tail = tm_v;
+    const bool tails_ok = box_rows != kTile || (make_tmap_rows(&tm_k_tail, k_cache, pool, cols, rows, 16) &&
+                                                make_tmap_rows(&tm_v_tail, v_cache, pool, cols, rows, 16));
+    if (!maps_ok || !tails_ok) return cudaErrorInvalidValue;
 
     auto run = [&](auto kern_part, auto kern_comb, auto prepare, int smem, int d) -> cudaError_t {
         cudaError_t err = prepare();
@@ -765,7 +791,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, kern_part, tm_k, tm_v, a);
+        err = cudaLaunchKernelEx(&cfg, kern_part, tm_k, tm_v, tm_k_tail, tm_v_tail, a);
         if (err != cudaSuccess) return err;
         if (a.max_parts > 1) {
             cfg.gridDim = dim3(a.num_q_heads, batch);

@@ -35,7 +35,7 @@ struct MapKey {
     int box_slices;  // 0: the 2-D map
     pa_dtype dt;
 };
-constexpr int kCacheSlots = 8;
+constexpr int kCacheSlots = 16;
 thread_local MapKey t_keys[kCacheSlots];
 thread_local CUtensorMap t_maps[kCacheSlots];
 thread_local int t_next = 0;
