@@ -53,8 +53,8 @@ DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 # capture of the current kernels (profiles/decode_<workload>.md); a workload
 # missing here reports null.
 TRAFFIC_PER_CALL = {
-    "qwen3_0p6b_decode": 583_122_944 + 4_789_248,       # decode_partition_kernel (store fused)
-    "qwen3_0p6b_decode_fp8": 291_831_808 + 4_151_040,   # decode_partition_kernel, E4M3 pool (store fused)
+    "qwen3_0p6b_decode": 575_843_072 + 4_158_720,       # decode_partition_kernel (store fused)
+    "qwen3_0p6b_decode_fp8": 288_197_120 + 4_085_248,   # decode_partition_kernel, E4M3 pool (store fused)
     "long_context_decode": 536_962_560 + 3_218_944,     # decode_partition_kernel (store fused)
     "qwen3_8b_shared_decode": 869_801_728 + 5_674_752,  # decode_partition_kernel (store fused; L2 absorbs shared pages)
 }
