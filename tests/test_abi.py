@@ -263,3 +263,13 @@ def test_selftest_wait_timeout_validation(lib):
     assert lib.pa_selftest_wait_timeout(0, FAKE, None) == -1
     assert lib.pa_selftest_wait_timeout(5_000_000_000, FAKE, None) == -1
     assert lib.pa_selftest_wait_timeout(1000, None, None) == -1
+
+
+def test_headers_compile_as_plain_c(tmp_path):
+    """The C ABI headers are plain C99: a C translation unit includes them without warnings."""
+    src = tmp_path / "abi.c"
+    src.write_text("".join(f'#include "{os.path.basename(h)}"\n' for h in HEADERS) +
+                   "int main(void) { return pa_version() > 0 ? 0 : 1; }\n")
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-c", str(src), "-o", str(tmp_path / "abi.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
