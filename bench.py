@@ -49,8 +49,8 @@ PRE_STEP_SPIN_CYCLES = 400_000
 DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
 
 # DRAM bytes (read + write) of the dominant kernel per launch, from one ncu
-# capture of the current kernels (profiles/decode_<workload>.md); a workload
-# missing here reports null.
+# capture of the current kernels on that workload; a workload missing here
+# reports null.
 TRAFFIC_PER_CALL = {
     "qwen3_0p6b_decode": 575_843_072 + 4_158_720,       # decode_partition_kernel (store fused)
     "qwen3_0p6b_decode_fp8": 288_197_120 + 4_085_248,   # decode_partition_kernel, E4M3 pool (store fused)
@@ -83,7 +83,7 @@ WORKLOAD_CONFIG = {
 SAMPLER_METRIC = "temperature-sampling logits GB/s and rows/s on 1 GPU"
 STORE_METRIC = "slot-mapped KV store GB/s (read + write) on 1 GPU"
 # Warp instructions one pa_sample launch executes on the sampler workload (ncu
-# smsp__inst_executed.sum of sample_kernel, profiles/sample_sampler_qwen3_vocab.md): the
+# smsp__inst_executed.sum of sample_kernel on this workload): the
 # kernel is issue-bound (Philox4x32-10 and two accurate logarithms per vocabulary entry;
 # 36 warp instructions per entry).
 SAMPLER_INSTRUCTIONS_PER_CALL = 10_966_336

@@ -204,6 +204,51 @@ PA_API int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, i
                            void *stream);
 
 /*
+ * pa_decode_options -- optional settings of pa_decode_ex / pa_store_decode_ex.
+ * Zero-initialise it and set only what you need; a NULL pointer or an
+ * all-zero struct gives exactly pa_decode / pa_store_decode.  Host memory,
+ * read during the call only.
+ *   partition     tokens per split-K context partition, overriding the
+ *                 library's plan (0: the plan).  A multiple of 64 in
+ *                 [64, 2^20]; it is lowered to a multiple of 64 that keeps a
+ *                 partition within 256 pages of the block table.  The result
+ *                 is the same attention up to the fp32 rounding of the
+ *                 log-sum-exp merge.
+ *   stages        TMA ring depth of the partition kernel over a 16-bit pool,
+ *                 2 or 3 (0: the plan); ignored over an E4M3 pool.
+ * Use: tuning and tests; the plan needs no help for ordinary shapes.
+ */
+typedef struct pa_decode_options {
+    int32_t partition;
+    int32_t stages;
+} pa_decode_options;
+
+/* Workspace bytes of pa_decode_ex / pa_store_decode_ex with these options
+ * (NULL: as pa_decode_workspace_bytes).  0 on invalid arguments. */
+PA_API size_t pa_decode_ex_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t max_blocks_per_seq, int32_t block_size,
+                                           const pa_decode_options *options);
+
+/* pa_decode with options (see pa_decode_options); the workspace must hold
+ * pa_decode_ex_workspace_bytes(..., options) bytes.  Errors as pa_decode, and
+ * INVALID_ARG for an option outside its range. */
+PA_API int pa_decode_ex(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
+                        size_t workspace_bytes, const pa_decode_options *options, pa_dtype dtype,
+                        int32_t *err_flag, void *stream);
+
+/* pa_store_decode with options; as pa_decode_ex for the workspace and errors. */
+PA_API int pa_store_decode_ex(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                              const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                              void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                              float scale, void *out, void *workspace, size_t workspace_bytes,
+                              const pa_decode_options *options, pa_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate
  * device memory.  The pages describe no such call: it has no counterpart there.
  *

@@ -52,6 +52,22 @@ _lib.pa_decode.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i3
 _lib.pa_store_decode.restype = ctypes.c_int
 _lib.pa_store_decode.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                  _i32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
+
+
+class _Options(ctypes.Structure):
+    """Mirror of pa_decode_options."""
+    _fields_ = [("partition", _i32), ("stages", _i32)]
+
+
+_opt_p = ctypes.POINTER(_Options)
+_lib.pa_decode_ex_workspace_bytes.restype = _sz
+_lib.pa_decode_ex_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _opt_p]
+_lib.pa_decode_ex.restype = ctypes.c_int
+_lib.pa_decode_ex.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
+                              _opt_p, ctypes.c_int, _p, _p]
+_lib.pa_store_decode_ex.restype = ctypes.c_int
+_lib.pa_store_decode_ex.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
+                                    _i32, _i32, _f32, _p, _p, _sz, _opt_p, ctypes.c_int, _p, _p]
 _lib.pa_store_kv_fp8.restype = ctypes.c_int
 _lib.pa_store_kv_fp8.argtypes = [_p, _p, _i64, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _f32,
                                  _p, _p]
@@ -155,15 +171,36 @@ def store_kv(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     _check("pa_store_kv", rc)
 
 
+class DecodeOptions:
+    """Optional settings of :func:`decode` / :func:`store_decode` (``pa_decode_options``).
+
+    ``partition``: tokens per split-K partition (a multiple of 64; 0 = the library's plan).
+    ``stages``: TMA ring depth of the partition kernel, 2 or 3 (0 = the plan)."""
+
+    def __init__(self, partition: int = 0, stages: int = 0):
+        self.partition, self.stages = int(partition), int(stages)
+
+    def _c(self) -> _Options:
+        return _Options(self.partition, self.stages)
+
+
+def _opts(options: DecodeOptions | None):
+    return None if options is None else ctypes.byref(options._c())
+
+
 def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                           max_blocks_per_seq: int, block_size: int) -> int:
-    return int(_lib.pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                                              block_size))
+                           max_blocks_per_seq: int, block_size: int, options: DecodeOptions | None = None) -> int:
+    if options is None:
+        return int(_lib.pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                  block_size))
+    return int(_lib.pa_decode_ex_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                 block_size, _opts(options)))
 
 
-def alloc_decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor) -> torch.Tensor:
+def alloc_decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                           options: DecodeOptions | None = None) -> torch.Tensor:
     n, bs, hkv, d = k_cache.shape
-    nbytes = decode_workspace_bytes(q.shape[0], q.shape[1], hkv, d, block_tables.shape[1], bs)
+    nbytes = decode_workspace_bytes(q.shape[0], q.shape[1], hkv, d, block_tables.shape[1], bs, options)
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=k_cache.device)
 
 
@@ -198,28 +235,35 @@ def _decode_checks(q, k_cache, v_cache, block_tables, context_lens):
 
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
-           workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
-    """Paged decode attention: q [B, H_q, D] -> out [B, H_q, D]."""
+           workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+           options: DecodeOptions | None = None) -> torch.Tensor:
+    """Paged decode attention: q [B, H_q, D] -> out [B, H_q, D] (``pa_decode``, or
+    ``pa_decode_ex`` with ``options``)."""
     n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
     B, hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
     if workspace is None:
-        workspace = alloc_decode_workspace(q, k_cache, block_tables)
-    rc = _lib.pa_decode(_ptr(q), _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                        block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale), _ptr(out),
-                        _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
-                        _stream(q))
-    _check("pa_decode", rc)
+        workspace = alloc_decode_workspace(q, k_cache, block_tables, options)
+    args = (_ptr(q), _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+            _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size())
+    tail = (_dtype(q), _ptr(err_flag), _stream(q))
+    if options is None:
+        _check("pa_decode", _lib.pa_decode(*args, *tail))
+    else:
+        _check("pa_decode_ex", _lib.pa_decode_ex(*args, _opts(options), *tail))
     return out
 
 
 def store_decode(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q: torch.Tensor,
                  k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                  context_lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+                 workspace: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+                 options: DecodeOptions | None = None) -> torch.Tensor:
     """One decode step in one launch: store k/v ([B, H_kv, D]) at ``slot_mapping`` (the slot of
-    each sequence's last context position, or -1) and attend: q [B, H_q, D] -> out [B, H_q, D]."""
+    each sequence's last context position, or -1) and attend: q [B, H_q, D] -> out [B, H_q, D]
+    (``pa_store_decode``, or ``pa_store_decode_ex`` with ``options``)."""
     n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
     B, hq = q.shape[0], q.shape[1]
     if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous() or slot_mapping.numel() != B:
@@ -231,13 +275,15 @@ def store_decode(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=k_cache.device)
     if workspace is None:
-        workspace = alloc_decode_workspace(q, k_cache, block_tables)
-    rc = _lib.pa_store_decode(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q),
-                              _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
-                              _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale), _ptr(out), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
-                              _stream(k_cache))
-    _check("pa_store_decode", rc)
+        workspace = alloc_decode_workspace(q, k_cache, block_tables, options)
+    args = (_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q), _rows(q, "q"),
+            _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, hq, hkv,
+            d, n, bs, float(scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size())
+    tail = (_dtype(q), _ptr(err_flag), _stream(k_cache))
+    if options is None:
+        _check("pa_store_decode", _lib.pa_store_decode(*args, *tail))
+    else:
+        _check("pa_store_decode_ex", _lib.pa_store_decode_ex(*args, _opts(options), *tail))
     return out
 
 

@@ -37,7 +37,6 @@
 //     trip; both kernels are launched as programmatic dependents, so each
 //     launch overlaps the kernel before it.
 #include <math.h>
-#include <stdlib.h>
 
 #include <type_traits>
 
@@ -673,22 +672,16 @@ static int resident_ctas(int stages, int head_dim, bool fp8) {
     return cached[dev][vi][hi];
 }
 
-// Ring depth for a block size (PA_DECODE_STAGES = 2 or 3 overrides it for tuning).  Pages
-// shorter than a tile make every tile several TMA boxes; three CTAs per SM (2 stages each)
-// then keep more producers issuing (measured: block size 16, 3-4 % faster without shared
-// pages, 13 % with them), while for longer pages the deeper ring is slightly ahead.
-static int stages_for(int32_t block_size) {
-    if (const char *env = getenv("PA_DECODE_STAGES")) {
-        const int v = atoi(env);
-        if (v == 2 || v == 3) return v;
-    }
-    return block_size < kTile ? 2 : 3;
-}
+// Ring depth for a block size.  Pages shorter than a tile make every tile several TMA boxes;
+// three CTAs per SM (2 stages each) then keep more producers issuing (measured: block size 16,
+// 3-4 % faster without shared pages, 13 % with them), while for longer pages the deeper ring
+// is slightly ahead.
+static int stages_for(int32_t block_size) { return block_size < kTile ? 2 : 3; }
 
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t max_blocks_per_seq, int32_t block_size, bool fp8) {
+                       int32_t max_blocks_per_seq, int32_t block_size, bool fp8, const pa_decode_options *opt) {
     DecodePlan pl{};
-    pl.stages = fp8 ? kF8Stages : stages_for(block_size);
+    pl.stages = fp8 ? kF8Stages : (opt && opt->stages) ? opt->stages : stages_for(block_size);
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * block_size;
     const int64_t pairs = static_cast<int64_t>(batch) * num_kv_heads;
     const int64_t slots = resident_ctas(pl.stages, head_dim, fp8);
@@ -706,10 +699,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
         part = kMaxPartition;
         while (part > kMinPartition && pairs * ((cap + part - 1) / part) < kTargetWaves * slots) part /= 2;
     }
-    if (const char *env = getenv("PA_DECODE_PARTITION")) {  // tuning override
-        const int v = atoi(env);
-        if (v >= kTile && v % kTile == 0 && v <= (1 << 20)) part = v;
-    }
+    if (opt && opt->partition) part = opt->partition;  // caller's override (validated by the C ABI)
     while (part / block_size > kMaxTablePages - 1) part = (part / 2 + kTile - 1) / kTile * kTile;  // table slice fits
     if (part < kTile) part = kTile;
     pl.partition = static_cast<int>(part);

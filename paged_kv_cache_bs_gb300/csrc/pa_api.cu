@@ -69,12 +69,24 @@ int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
 namespace {
 
+// Checks of the optional settings of pa_decode_ex / pa_store_decode_ex (NULL: none).
+int check_options(const pa_decode_options *opt) {
+    if (!opt) return PA_OK;
+    if (opt->partition && (opt->partition < 64 || opt->partition % 64 || opt->partition > (1 << 20)))
+        return fail(PA_ERR_INVALID_ARG, "options.partition %d must be 0 or a multiple of 64 in [64, 2^20]",
+                    opt->partition);
+    if (opt->stages && opt->stages != 2 && opt->stages != 3)
+        return fail(PA_ERR_INVALID_ARG, "options.stages %d must be 0, 2 or 3", opt->stages);
+    return PA_OK;
+}
+
 // Checks of pa_decode's arguments (also those of pa_store_decode); PA_OK or an error code.
 int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                  float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype,
-                 pa::DecodePlan *plan, const pa::Fp8Scales *fp8 = nullptr) {
+                 pa::DecodePlan *plan, const pa::Fp8Scales *fp8 = nullptr,
+                 const pa_decode_options *opt = nullptr) {
     int rc = check_attention_shape(num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, dtype);
     if (rc) return rc;
     if (fp8) {
@@ -84,6 +96,8 @@ int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const
                         fp8->k_scale, fp8->v_scale);
     }
     if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch is negative (%d)", batch);
+    rc = check_options(opt);
+    if (rc) return rc;
     if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (1LL << 30))
         return fail(PA_ERR_INVALID_ARG, "max context of %lld tokens is too large",
@@ -98,7 +112,7 @@ int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const
         !aligned(workspace, 256))
         return fail(PA_ERR_INVALID_ARG, "alignment: q 4 B, caches 16 B, out 2 B, workspace 256 B");
     *plan = pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
-                            fp8 != nullptr);
+                            fp8 != nullptr, opt);
     if (workspace_bytes < plan->ws_bytes)
         return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
                     plan->ws_bytes);
@@ -164,11 +178,13 @@ int store_kv(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_s
 
 
 size_t decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                        int32_t max_blocks_per_seq, int32_t block_size, bool fp8) {
+                        int32_t max_blocks_per_seq, int32_t block_size, bool fp8,
+                        const pa_decode_options *opt = nullptr) {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
         !is_pow2(block_size))
         return 0;
-    return pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, fp8)
+    if (check_options(opt)) return 0;
+    return pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, fp8, opt)
         .ws_bytes;
 }
 
@@ -178,11 +194,11 @@ int store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t v_r
                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                  float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag,
-                 void *stream, const pa::Fp8Scales *fp8) {
+                 void *stream, const pa::Fp8Scales *fp8, const pa_decode_options *opt = nullptr) {
     pa::DecodePlan plan{};
     const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                 batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
-                                workspace, workspace_bytes, dtype, &plan, fp8);
+                                workspace, workspace_bytes, dtype, &plan, fp8, opt);
     if (rc) return rc;
     if (batch == 0) {
         g_err[0] = '\0';
@@ -242,10 +258,27 @@ int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const vo
               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
               float scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *err_flag,
               void *stream) {
+    return pa_decode_ex(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                        num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out, workspace,
+                        workspace_bytes, nullptr, dtype, err_flag, stream);
+}
+
+size_t pa_decode_ex_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t max_blocks_per_seq, int32_t block_size,
+                                    const pa_decode_options *options) {
+    return decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, false,
+                            options);
+}
+
+int pa_decode_ex(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                 int32_t block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+                 const pa_decode_options *options, pa_dtype dtype, int32_t *err_flag, void *stream) {
     pa::DecodePlan plan{};
     const int rc = check_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                 batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out,
-                                workspace, workspace_bytes, dtype, &plan);
+                                workspace, workspace_bytes, dtype, &plan, nullptr, options);
     if (rc) return rc;
     if (batch == 0) {
         g_err[0] = '\0';
@@ -256,6 +289,19 @@ int pa_decode(const void *q, int64_t q_row_stride, const void *k_cache, const vo
                                          block_size, scale, out, workspace, plan, dtype, err_flag,
                                          static_cast<cudaStream_t>(stream)),
                        "pa_decode launch");
+}
+
+int pa_store_decode_ex(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                       const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                       void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                       const int32_t *context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, void *out,
+                       void *workspace, size_t workspace_bytes, const pa_decode_options *options, pa_dtype dtype,
+                       int32_t *err_flag, void *stream) {
+    return store_decode(k, v, k_row_stride, v_row_stride, slot_mapping, q, q_row_stride, k_cache, v_cache,
+                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                        num_blocks, block_size, scale, out, workspace, workspace_bytes, dtype, err_flag, stream,
+                        nullptr, options);
 }
 
 int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,

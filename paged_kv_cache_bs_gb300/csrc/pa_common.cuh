@@ -141,8 +141,10 @@ struct Fp8Scales {
     float k_scale, v_scale;
 };
 // fp8: the plan of the E4M3 partition kernel (its own ring and occupancy).
+// opt (nullable): the caller's overrides of the partition size and the ring depth.
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t max_blocks_per_seq, int32_t block_size, bool fp8 = false);
+                       int32_t max_blocks_per_seq, int32_t block_size, bool fp8 = false,
+                       const pa_decode_options *opt = nullptr);
 // The store fused into pa_store_decode (the new rows of one decode step).
 struct FusedStore {
     const void *k;

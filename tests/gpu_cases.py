@@ -30,14 +30,14 @@ def max_err(gpu_out: torch.Tensor, ref: torch.Tensor) -> float:
     return float((g - ref).abs().max()) if g.numel() else 0.0
 
 
-def run_decode_gpu(pa, st, dev="cuda", err_flag=None):
-    """Store the step's new tokens and run decode on the GPU.  Returns
-    (out, k_cache, v_cache) on the device."""
+def run_decode_gpu(pa, st, dev="cuda", err_flag=None, options=None):
+    """Store the step's new tokens and run decode on the GPU (with ``options``: through
+    pa_decode_ex).  Returns (out, k_cache, v_cache) on the device."""
     p = st.pool
     kc, vc = p.k_cache.to(dev), p.v_cache.to(dev)
     pa.store_kv(st.k_new.to(dev), st.v_new.to(dev), kc, vc, st.slot_mapping.to(dev), err_flag=err_flag)
     out = pa.decode(st.q.to(dev), kc, vc, st.block_tables.to(dev), st.context_lens.to(dev), st.scale,
-                    err_flag=err_flag)
+                    err_flag=err_flag, options=options)
     torch.cuda.synchronize()
     return out, kc, vc
 
@@ -48,10 +48,10 @@ def oracle_store(st_pool_k, st_pool_v, k_new, v_new, slots):
     return kc, vc
 
 
-def check_decode(pa, st, rows=None):
+def check_decode(pa, st, rows=None, options=None):
     """Full parity of one decode step: caches bit-exact after the store,
     attention within tolerance on all (or the sampled) sequences."""
-    out, kc, vc = run_decode_gpu(pa, st)
+    out, kc, vc = run_decode_gpu(pa, st, options=options)
     okc, ovc = oracle_store(st.pool.k_cache, st.pool.v_cache, st.k_new, st.v_new, st.slot_mapping)
     assert_bit_equal(kc, okc, "k_cache after store")
     assert_bit_equal(vc, ovc, "v_cache after store")

@@ -94,12 +94,12 @@ def test_decode_shared_prefix_equals_private_copies(pa):
     assert_bit_equal(a, b, "shared prefix vs private copies")
 
 
-@pytest.mark.parametrize("part", ["64", "128", "512", "4096"])
-def test_decode_partition_size_does_not_change_result(pa, part, monkeypatch):
+@pytest.mark.parametrize("part,stages", [(64, 3), (128, 2), (512, 0), (4096, 3)])
+def test_decode_partition_size_does_not_change_result(pa, part, stages):
+    # the split-K plan overridden through pa_decode_ex's options: the same attention
     st = inputs.make_decode([1, 700, 2049, 5000], num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=256,
                             dtype=torch.bfloat16, seed=53)
-    monkeypatch.setenv("PA_DECODE_PARTITION", part)
-    check_decode(pa, st)
+    check_decode(pa, st, options=pa.DecodeOptions(partition=part, stages=stages))
 
 
 def test_decode_identical_keys_mean_of_v(pa):
