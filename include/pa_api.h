@@ -261,9 +261,16 @@ PA_API int pa_store_decode_ex(const void *k, const void *v, int64_t k_row_stride
  * allocates nothing.
  *   - A shape whose pa_decode_workspace_bytes(...) exceeds 8 MiB is rejected
  *     with PA_ERR_UNSUPPORTED (see pa_last_error) before any CUDA call.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Set-up: CUDA loads modules lazily by default, so the 8 MiB array (and
+ *     the decode kernels' code) would be placed in device memory only at the
+ *     first call on a device.  Call pa_decode_static_workspace once with
+ *     batch == 0 (the other pointers may be NULL) on each device, with that
+ *     device current, BEFORE reserving the KV pool and before any stream
+ *     capture: that call looks up the array's device address
+ *     (cudaGetSymbolAddress), loads every kernel this entry point launches,
+ *     and computes nothing.  Later calls take no device memory.  The address
+ *     is cached per device with the id of its CUDA context, so after a device
+ *     reset the next call looks it up again (and places the array again).
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents.  Each call writes every scratch element it later reads, so
  *     nothing needs clearing.  Calls that overlap on the GPU (unordered

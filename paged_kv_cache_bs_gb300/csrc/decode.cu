@@ -678,6 +678,31 @@ static int resident_ctas(int stages, int head_dim, bool fp8) {
 // is slightly ahead.
 static int stages_for(int32_t block_size) { return block_size < kTile ? 2 : 3; }
 
+// Loads every partition and merge kernel of the 16-bit pools into the current context (CUDA loads
+// kernels lazily, at first use, by default), so that later launches load no code.
+cudaError_t preload_decode_kernels() {
+    cudaFuncAttributes fa;
+    const void *kernels[] = {
+        reinterpret_cast<const void *>(decode_partition_kernel<__nv_bfloat16, 128, 3, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__nv_bfloat16, 128, 2, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__nv_bfloat16, 64, 3, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__nv_bfloat16, 64, 2, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__half, 128, 3, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__half, 128, 2, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__half, 64, 3, false>),
+        reinterpret_cast<const void *>(decode_partition_kernel<__half, 64, 2, false>),
+        reinterpret_cast<const void *>(decode_combine_kernel<__nv_bfloat16, 128>),
+        reinterpret_cast<const void *>(decode_combine_kernel<__nv_bfloat16, 64>),
+        reinterpret_cast<const void *>(decode_combine_kernel<__half, 128>),
+        reinterpret_cast<const void *>(decode_combine_kernel<__half, 64>),
+    };
+    for (const void *k : kernels) {
+        const cudaError_t e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                        int32_t max_blocks_per_seq, int32_t block_size, bool fp8, const pa_decode_options *opt) {
     DecodePlan pl{};

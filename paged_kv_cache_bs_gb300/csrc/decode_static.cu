@@ -11,8 +11,18 @@
 //
 // The kernels are the ones pa_decode launches; this file only supplies their
 // workspace.  Host code cannot use the array's name as a device address, so
-// the address is looked up with cudaGetSymbolAddress once per device (on the
-// first call made with that device current) and cached.
+// the address is looked up with cudaGetSymbolAddress, with the device current,
+// and cached per device together with the unique id of the context it belongs
+// to: after a device reset the next call sees a new context and looks the
+// address up again.
+//
+// Under CUDA's default lazy module loading, the array is placed in device
+// memory only when its module is first used, i.e. at the first call on a
+// device.  A call with batch == 0 is the set-up call: it places the array and
+// loads every kernel this entry point can launch, and computes nothing, so a
+// caller can take the 8 MiB (and the kernels' code) before it gives the rest
+// of the device memory to its KV pool.
+#include <cuda.h>
 #include <stdio.h>
 
 #include <mutex>
@@ -27,23 +37,53 @@ constexpr int kMaxDevices = 64;
 // The split-K partials of one call.  Every call uses the same array.
 static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long *);
 
-// Device address of g_decode_scratch on the current device (set-up on first use).
+struct Slot {
+    unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+    void *ptr;
+};
+
+std::mutex g_mu;
+Slot g_slot[kMaxDevices] = {};
+
+template <typename F> F driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(p);
+}
+
+// Unique id of the current context (ids are never reused within a process), or 0.
+unsigned long long current_context_id() {
+    static const CtxGetCurrent get_current = driver_fn<CtxGetCurrent>("cuCtxGetCurrent");
+    static const CtxGetId get_id = driver_fn<CtxGetId>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_decode_scratch on the current device (looked up once per context).
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // 0 before the device's primary context exists; then the lookup below creates it
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!id || g_slot[dev].ctx_id != id || !g_slot[dev].ptr) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
+        g_slot[dev] = Slot{current_context_id(), p};
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_slot[dev].ptr;
     return cudaSuccess;
 }
 
@@ -51,6 +91,7 @@ cudaError_t scratch_address(void **out) {
 
 namespace pa {
 int set_last_error(int code, const char *msg);
+cudaError_t preload_decode_kernels();
 }
 
 extern "C" PA_API int pa_decode_static_workspace(
@@ -70,10 +111,11 @@ extern "C" PA_API int pa_decode_static_workspace(
         return pa::set_last_error(PA_ERR_UNSUPPORTED, msg);
     }
     void *scratch = nullptr;
-    const cudaError_t e = scratch_address(&scratch);
+    cudaError_t e = scratch_address(&scratch);
+    if (e == cudaSuccess && batch == 0) e = pa::preload_decode_kernels();  // the set-up call
     if (e != cudaSuccess) {
         char msg[256];
-        snprintf(msg, sizeof msg, "pa_decode_static_workspace: cudaGetSymbolAddress failed: %s",
+        snprintf(msg, sizeof msg, "pa_decode_static_workspace: set-up of the static scratch failed: %s",
                  cudaGetErrorString(e));
         return pa::set_last_error(PA_ERR_CUDA, msg);
     }

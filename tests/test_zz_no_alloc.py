@@ -4,22 +4,29 @@ An engine that handed nearly all free device memory to its KV pool, or a
 plugin whose host framework owns every device allocation, cannot cudaMalloc a
 per-call workspace; this entry point uses the library's own static device
 scratch instead.  The test calls it through the C ABI (ctypes, no binding
-code) and checks its output against pa_decode with a caller workspace, on two
-calls in a row with different shapes and dtypes (the second call runs over
-the scratch the first one left behind).  It also checks that an oversized
-shape is refused before anything runs.
+code) and checks its output against pa_decode with a caller workspace, bit for
+bit (the same kernels and plan), on two calls in a row with different shapes
+and dtypes (the second call runs over the scratch the first one left behind).
+It checks, in a fresh process, that the set-up call (batch 0) is where the
+8 MiB is taken and that later calls take no device memory, and that an
+oversized shape is refused before anything runs.
 
 This file is named to be collected last, and it passes alone in a fresh
 process as well as after the other tests.
 """
 
 import ctypes
+import json
+import os
+import subprocess
+import sys
+import textwrap
 
 import pytest
 import torch
 
 from tests import inputs
-from tests.gpu_cases import TOL, max_err
+from tests.gpu_cases import assert_bit_equal
 
 pytestmark = pytest.mark.gpu
 
@@ -60,8 +67,47 @@ def test_static_workspace_matches_caller_workspace(pa):
         rc = _call(pa, f, st, q, kc, vc, bt, cl, out)
         assert rc == 0, pa.library().pa_last_error()
         torch.cuda.synchronize()
-        err = max_err(out, ref.cpu().float())
-        assert err <= TOL[q.dtype], f"static-workspace decode differs from pa_decode by {err}"
+        assert_bit_equal(out, ref, "static-workspace decode vs pa_decode")
+
+
+_FRESH = textwrap.dedent("""
+    import ctypes, json, sys, torch
+    sys.path.insert(0, sys.argv[1])
+    import paged_kv_cache_bs_gb300 as pa
+    from tests import inputs
+    from tests.test_zz_no_alloc import _entry, _call, _device_step
+    f = _entry(pa.library())
+    st = inputs.qwen3_0p6b_decode()
+    q, kc, vc, bt, cl = _device_step(pa, st)     # every tensor of the test is allocated here
+    out = torch.empty_like(q)
+    torch.cuda.synchronize()
+    free = [torch.cuda.mem_get_info()[0]]
+    n, bs, hkv, d = kc.shape
+    rc0 = f(None, q.stride(0), None, None, None, bt.shape[1], None, 0, q.shape[1], hkv, d, n, bs,
+            ctypes.c_float(st.scale), None, pa.PA_BF16, None, None)                  # the set-up call
+    torch.cuda.synchronize()
+    free.append(torch.cuda.mem_get_info()[0])
+    rcs = []
+    for _ in range(2):
+        rcs.append(_call(pa, f, st, q, kc, vc, bt, cl, out))
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
+    print(json.dumps({"rc": [rc0] + rcs, "free": free}))
+""")
+
+
+def test_static_workspace_set_up_takes_the_scratch_and_calls_take_nothing():
+    # a fresh process with CUDA's default lazy loading: the library's modules are not loaded yet
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    r = subprocess.run([sys.executable, "-c", _FRESH, root], capture_output=True, text=True, timeout=600, env=env,
+                       cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["rc"] == [0, 0, 0]
+    f0, f1, f2, f3 = res["free"]
+    assert f0 - f1 >= 8 << 20, f"the set-up call took {f0 - f1} bytes, expected the 8 MiB scratch"
+    assert f1 == f2 == f3, f"decode calls after the set-up took device memory: free {f1} -> {f2} -> {f3}"
 
 
 def test_static_workspace_rejects_oversized_shapes(pa):
