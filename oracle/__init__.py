@@ -5,8 +5,10 @@ Only ``tests/``, ``__graft_entry__.smoke`` and the CPU-baseline leg of
 never touch it, and it never touches them: the two share no code.
 
 ``oracle.c`` is plain single-threaded fp32 C built with ``-O2 -fno-fast-math``.
-This module compiles it (``build``) and wraps its three entry points for
-torch CPU tensors.  Parity is pinned by ``tests/test_oracle_pins.py`` against
+This module compiles it (``build``) and wraps its entry points for torch CPU
+tensors.  ``build_omp`` / ``load_omp`` give the same source built with
+``-fopenmp`` (its independent rows spread over the host cores, each row's
+arithmetic unchanged): the all-core CPU baseline of the benchmark.  Parity is pinned by ``tests/test_oracle_pins.py`` against
 the pages' worked examples, closed forms, brute force and library attention.
 """
 
@@ -21,6 +23,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
+LIB_OMP = os.path.join(HERE, "liboracle_omp.so")
 
 F16, BF16 = 0, 1
 _DT = {torch.float16: F16, torch.bfloat16: BF16}
@@ -28,15 +31,21 @@ _DT = {torch.float16: F16, torch.bfloat16: BF16}
 _lib = None
 
 
-def build(src: str = SRC, out: str = LIB) -> str:
-    """Compile the oracle (or a variant source) into a shared library."""
+def build(src: str = SRC, out: str = LIB, openmp: bool = False) -> str:
+    """Compile the oracle (or a variant source) into a shared library (with ``openmp``: the
+    multi-threaded build of the same source)."""
     if src == SRC and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
     tmp = out + ".tmp"
-    subprocess.run(["gcc", "-O2", "-fno-fast-math", "-std=c11", "-shared", "-fPIC", src, "-o", tmp, "-lm"],
+    omp = ["-fopenmp"] if openmp else []
+    subprocess.run(["gcc", "-O2", "-fno-fast-math", "-std=c11", *omp, "-shared", "-fPIC", src, "-o", tmp, "-lm"],
                    check=True)
     os.replace(tmp, out)
     return out
+
+
+def build_omp() -> str:
+    return build(SRC, LIB_OMP, openmp=True)
 
 
 def _declare(lib):
@@ -70,6 +79,17 @@ def load(path: str | None = None):
     if _lib is None:
         _lib = _declare(ctypes.CDLL(build()))
     return _lib
+
+
+_lib_omp = None
+
+
+def load_omp():
+    """The OpenMP build of the oracle (building it first if needed); pass it as ``lib=``."""
+    global _lib_omp
+    if _lib_omp is None:
+        _lib_omp = _declare(ctypes.CDLL(build_omp()))
+    return _lib_omp
 
 
 def _ptr(t):

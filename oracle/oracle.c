@@ -3,8 +3,13 @@
  * library never links, includes or calls this file, and only the tests, the
  * smoke check and the benchmark's CPU-baseline leg load it.
  *
- * Plain, slow, single-threaded, fp32 (the precision the problem statement
- * fixes for the reference computation), written straight from the pages:
+ * Plain, slow, fp32 (the precision the problem statement fixes for the
+ * reference computation), written straight from the pages.  Built as usual it
+ * is single-threaded.  Built with -fopenmp (only for the benchmark's all-core
+ * CPU baseline) the independent rows of the work -- the gathered positions of
+ * one sequence, and the (query row, head) attention rows -- are spread over
+ * the host cores; each row's arithmetic and its order are the same either way,
+ * so both builds give bit-identical results.
  *
  *   store   - "Inference engine: inside nano-vLLM", section "Attention in
  *             nano-vLLM" (store_kvcache): token t's K and V rows go to cache
@@ -32,6 +37,29 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads of the parallel regions below, and the calling thread's index (1 and
+ * 0 in the usual single-threaded build). */
+static int n_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static int thread_id(void)
+{
+#ifdef _OPENMP
+    return omp_get_thread_num();
+#else
+    return 0;
+#endif
+}
 
 #define OR_F16 0
 #define OR_BF16 1
@@ -94,20 +122,34 @@ int oracle_store_kv(const uint16_t *k, const uint16_t *v, int64_t k_row_stride, 
 
 /* --------------------------------------------------------------- gather */
 
+/* Physical page of logical block `logical` of a sequence's table, or -1 when
+ * the table has no valid page there (past its end, -1 padding, or an id
+ * outside the pool). */
+static int32_t page_of(const int32_t *table, int32_t table_len, int32_t logical, int32_t num_blocks)
+{
+    if (logical >= table_len)
+        return -1;
+    int32_t page = table[logical];
+    if (page < 0 || page >= num_blocks)
+        return -1;
+    return page;
+}
+
 /* Copies logical positions [0, n) of one sequence out of the pool into
- * dense fp32 buffers kc/vc of shape [n, H_kv, D]. */
+ * dense fp32 buffers kc/vc of shape [n, H_kv, D].  Every page the context
+ * needs is checked first; then the rows are copied (independent rows). */
 static int gather(const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *table,
                   int32_t table_len, int32_t n, int32_t num_kv_heads, int32_t head_dim,
                   int32_t num_blocks, int32_t block_size, int dtype, float *kc, float *vc)
 {
     const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int32_t j = 0; j < n; j += block_size)
+        if (page_of(table, table_len, j / block_size, num_blocks) < 0)
+            return -2;
+#pragma omp parallel for schedule(static)
     for (int32_t j = 0; j < n; ++j) {
-        int32_t logical = j / block_size;
-        if (logical >= table_len)
-            return -2;
-        int32_t page = table[logical];
-        if (page < 0 || page >= num_blocks)
-            return -2;
+        const int32_t logical = j / block_size;
+        const int32_t page = page_of(table, table_len, logical, num_blocks);
         int64_t r = (int64_t)page * block_size + j % block_size;
         for (int64_t e = 0; e < row; ++e) {
             kc[j * row + e] = to_float(k_cache[r * row + e], dtype);
@@ -179,21 +221,27 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
         if (context_lens[b] > max_len)
             max_len = context_lens[b];
     }
+    const int nt = n_threads();
     float *kc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
     float *vc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
-    float *s = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1));
-    float *qh = malloc(sizeof(float) * (size_t)head_dim);
+    float *s = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * nt);   /* per thread */
+    float *qh = malloc(sizeof(float) * (size_t)head_dim * nt);                  /* per thread */
     float *res = malloc(sizeof(float) * (size_t)batch * num_q_heads * head_dim + 1);
     int rc = (kc && vc && s && qh && res) ? 0 : -5;
     for (int32_t b = 0; b < batch && !rc; ++b) {
         int32_t n = context_lens[b];
         rc = gather(k_cache, v_cache, block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq,
                     n, num_kv_heads, head_dim, num_blocks, block_size, dtype, kc, vc);
-        for (int32_t h = 0; h < num_q_heads && !rc; ++h) {
+        if (rc)
+            break;
+#pragma omp parallel for schedule(static)
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            const int t = thread_id();
+            float *qt = qh + (int64_t)t * head_dim;
             const uint16_t *qb = q + ((int64_t)b * num_q_heads + h) * head_dim;
             for (int32_t d = 0; d < head_dim; ++d)
-                qh[d] = to_float(qb[d], dtype);
-            attend(qh, kc, vc, n, h / group, num_kv_heads, head_dim, scale, s,
+                qt[d] = to_float(qb[d], dtype);
+            attend(qt, kc, vc, n, h / group, num_kv_heads, head_dim, scale, s + (int64_t)t * (max_len ? max_len : 1),
                    res + ((int64_t)b * num_q_heads + h) * head_dim);
         }
     }
@@ -228,10 +276,11 @@ int oracle_prefill_paged(const uint16_t *q, const uint16_t *k, const uint16_t *v
         if (lk > max_k)
             max_k = lk;
     }
+    const int nt = n_threads();
     float *kc = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1) * row);
     float *vc = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1) * row);
-    float *s = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1));
-    float *qh = malloc(sizeof(float) * (size_t)head_dim);
+    float *s = malloc(sizeof(float) * (size_t)(max_k ? max_k : 1) * nt);   /* per thread */
+    float *qh = malloc(sizeof(float) * (size_t)head_dim * nt);             /* per thread */
     float *res = malloc(sizeof(float) * (size_t)total_q * num_q_heads * head_dim + 1);
     int rc = (kc && vc && s && qh && res) ? 0 : -5;
     for (int32_t i = 0; i < num_seqs && !rc; ++i) {
@@ -248,14 +297,19 @@ int oracle_prefill_paged(const uint16_t *q, const uint16_t *k, const uint16_t *v
                 kc[(prefix + r) * row + e] = to_float(k[(q0 + r) * row + e], dtype);
                 vc[(prefix + r) * row + e] = to_float(v[(q0 + r) * row + e], dtype);
             }
-        for (int32_t r = 0; r < lq && !rc; ++r)
-            for (int32_t h = 0; h < num_q_heads; ++h) {
-                const uint16_t *qr = q + ((int64_t)(q0 + r) * num_q_heads + h) * head_dim;
-                for (int32_t d = 0; d < head_dim; ++d)
-                    qh[d] = to_float(qr[d], dtype);
-                attend(qh, kc, vc, prefix + r + 1, h / group, num_kv_heads, head_dim, scale, s,
-                       res + ((int64_t)(q0 + r) * num_q_heads + h) * head_dim);
-            }
+        if (rc)
+            break;
+#pragma omp parallel for schedule(dynamic, 4)
+        for (int64_t rh = 0; rh < (int64_t)lq * num_q_heads; ++rh) {   /* query row r, head h */
+            const int32_t r = (int32_t)(rh / num_q_heads), h = (int32_t)(rh % num_q_heads);
+            const int t = thread_id();
+            float *qt = qh + (int64_t)t * head_dim;
+            const uint16_t *qr = q + ((int64_t)(q0 + r) * num_q_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                qt[d] = to_float(qr[d], dtype);
+            attend(qt, kc, vc, prefix + r + 1, h / group, num_kv_heads, head_dim, scale,
+                   s + (int64_t)t * (max_k ? max_k : 1), res + ((int64_t)(q0 + r) * num_q_heads + h) * head_dim);
+        }
     }
     if (!rc)
         memcpy(out, res, sizeof(float) * (size_t)total_q * num_q_heads * head_dim);
@@ -406,32 +460,40 @@ int oracle_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *
         if (context_lens[b] > max_len)
             max_len = context_lens[b];
     }
+    const int nt = n_threads();
     float *kc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
     float *vc = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * row);
-    float *s = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1));
-    float *qh = malloc(sizeof(float) * (size_t)head_dim);
+    float *s = malloc(sizeof(float) * (size_t)(max_len ? max_len : 1) * nt);   /* per thread */
+    float *qh = malloc(sizeof(float) * (size_t)head_dim * nt);                  /* per thread */
     float *res = malloc(sizeof(float) * (size_t)batch * num_q_heads * head_dim + 1);
     int rc = (kc && vc && s && qh && res) ? 0 : -5;
     for (int32_t b = 0; b < batch && !rc; ++b) {
         const int32_t n = context_lens[b];
         const int32_t *table = block_tables + (int64_t)b * max_blocks_per_seq;
-        for (int32_t j = 0; j < n && !rc; ++j) {
-            const int32_t logical = j / block_size;
-            if (logical >= max_blocks_per_seq || table[logical] < 0 || table[logical] >= num_blocks) {
+        for (int32_t j = 0; j < n; j += block_size)
+            if (page_of(table, max_blocks_per_seq, j / block_size, num_blocks) < 0) {
                 rc = -2;
                 break;
             }
-            const int64_t r = (int64_t)table[logical] * block_size + j % block_size;
+        if (rc)
+            break;
+#pragma omp parallel for schedule(static)
+        for (int32_t j = 0; j < n; ++j) {
+            const int32_t page = page_of(table, max_blocks_per_seq, j / block_size, num_blocks);
+            const int64_t r = (int64_t)page * block_size + j % block_size;
             for (int64_t e = 0; e < row; ++e) {
                 kc[j * row + e] = e4m3_to_float(k_cache[r * row + e]) * k_scale;
                 vc[j * row + e] = e4m3_to_float(v_cache[r * row + e]) * v_scale;
             }
         }
-        for (int32_t h = 0; h < num_q_heads && !rc; ++h) {
+#pragma omp parallel for schedule(static)
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            const int t = thread_id();
+            float *qt = qh + (int64_t)t * head_dim;
             const uint16_t *qb = q + ((int64_t)b * num_q_heads + h) * head_dim;
             for (int32_t d = 0; d < head_dim; ++d)
-                qh[d] = to_float(qb[d], dtype);
-            attend(qh, kc, vc, n, h / group, num_kv_heads, head_dim, scale, s,
+                qt[d] = to_float(qb[d], dtype);
+            attend(qt, kc, vc, n, h / group, num_kv_heads, head_dim, scale, s + (int64_t)t * (max_len ? max_len : 1),
                    res + ((int64_t)b * num_q_heads + h) * head_dim);
         }
     }

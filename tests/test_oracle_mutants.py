@@ -11,7 +11,7 @@ import oracle
 from tests.test_oracle_pins import PINS
 
 MUTANTS = {
-    "gqa_head_map_modulo": ("attend(qh, kc, vc, n, h / group,", "attend(qh, kc, vc, n, h % num_kv_heads,"),
+    "gqa_head_map_modulo": ("attend(qt, kc, vc, n, h / group,", "attend(qt, kc, vc, n, h % num_kv_heads,"),
     "page_offset_dropped": ("(int64_t)page * block_size + j % block_size", "(int64_t)page * block_size"),
     "logical_not_physical_page": ("int64_t r = (int64_t)page * block_size", "int64_t r = (int64_t)logical * block_size"),
     "scale_dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
@@ -19,8 +19,8 @@ MUTANTS = {
     "exp_sign_flipped": ("s[j] = expf(s[j] - m);", "s[j] = expf(m - s[j]);"),
     "v_gathered_from_k": ("vc[j * row + e] = to_float(v_cache[r * row + e], dtype);",
                           "vc[j * row + e] = to_float(k_cache[r * row + e], dtype);"),
-    "causal_top_left": ("attend(qh, kc, vc, prefix + r + 1,", "attend(qh, kc, vc, r + 1,"),
-    "causal_off_by_one": ("attend(qh, kc, vc, prefix + r + 1,", "attend(qh, kc, vc, prefix + r + (r > 0),"),
+    "causal_top_left": ("attend(qt, kc, vc, prefix + r + 1,", "attend(qt, kc, vc, r + 1,"),
+    "causal_off_by_one": ("attend(qt, kc, vc, prefix + r + 1,", "attend(qt, kc, vc, prefix + r + (r > 0),"),
     "chunk_rows_ignore_seq_offset": ("to_float(k[(q0 + r) * row + e], dtype)", "to_float(k[(r) * row + e], dtype)"),
     "store_v_from_k": ("v_cache[s * row + e] = v[t * v_row_stride + e];", "v_cache[s * row + e] = k[t * k_row_stride + e];"),
     "store_ignores_row_stride": ("k_cache[s * row + e] = k[t * k_row_stride + e];", "k_cache[s * row + e] = k[t * row + e];"),
@@ -39,8 +39,8 @@ MUTANTS = {
                                    "float_to_e4m3(to_float(k[t * k_row_stride + e], dtype) * k_scale)"),
     "fp8_decode_drops_v_scale": ("vc[j * row + e] = e4m3_to_float(v_cache[r * row + e]) * v_scale;",
                                  "vc[j * row + e] = e4m3_to_float(v_cache[r * row + e]);"),
-    "minus_one_block_read_as_block_0": ("if (page < 0 || page >= num_blocks)\n            return -2;",
-                                        "if (page >= num_blocks)\n            return -2;\n        if (page < 0) page = 0;"),
+    "minus_one_block_read_as_block_0": ("if (page < 0 || page >= num_blocks)\n        return -1;",
+                                        "if (page >= num_blocks)\n        return -1;\n    if (page < 0) page = 0;"),
 }
 
 
