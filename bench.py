@@ -2,20 +2,26 @@
 """Benchmark of the paged-KV hot path on GB300.
 
 One step = one pass of the layer's hot path over one batch of synthetic input
-resident in HBM: ``pa_store_kv`` of the step's new K/V rows, then the
-attention call(s) of that step (``pa_decode``; the mixed chunked-prefill
-workload also runs ``pa_prefill_paged``).  Every benchmarked workload reads
-more than 4x the 129 MB L2 of KV per step, streamed in the same order each
-step, so each step starts cold without any flush; a workload with less than
-twice the L2 of KV is flushed between steps by a 256 MB write, outside the
-timed events.  (A write
+resident in HBM: the store of the step's new K/V rows, then the attention
+call(s) of that step (decode; the mixed chunked-prefill workload also runs
+the chunked prefill).  Every decode workload reads more than 4x the 129 MB L2
+of KV per step, streamed in the same order each step, so each step starts cold
+without any flush; a workload with less than twice the L2 of KV is flushed
+between steps by reading a 256 MB buffer, outside the timed events.  (A write
 flush leaves the L2 full of dirty lines whose write-back then lands inside the
 next step, an artefact a real multi-layer step does not have.)
 
-Prints ONE JSON line.  ``value`` = algorithmic KV bytes of the step's decode
-attention (sum of context lengths x 2 x H_kv x D x 2 bytes) / step time.
+Prints ONE JSON line.  The headline workload (default: the Qwen3-8B-like
+decode whose sequences share a 512-token prefix in groups of 8, the largest
+decode workload) gives ``value`` = K+V bytes DRAM must supply per step (each
+physical page once) / step time; ``value_logical`` counts every sequence's
+context.  Unless ``--no-configs``, the same run then times every other
+workload (tiny decode, the Qwen3-0.6B-like decode over 16-bit and E4M3 pools,
+long-context decode, the mixed chunked-prefill step, the 16384-token store
+and the sampler) and reports each under ``configs``, with its own roofline,
+clocks and CPU baselines.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-configs]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
@@ -46,7 +52,10 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the 
 # host has enqueued the whole step before the GPU reaches it: the events then
 # time the kernels, not the host's launch latency.
 PRE_STEP_SPIN_CYCLES = 400_000
-DEFAULT_WORKLOAD = "qwen3_0p6b_decode"
+DEFAULT_WORKLOAD = "qwen3_8b_shared_decode"
+# the other workloads a default run reports under "configs", in this order
+SUB_CONFIGS = ["tiny_decode", "qwen3_0p6b_decode", "long_context_decode", "mixed_chunked_prefill",
+               "qwen3_0p6b_decode_fp8", "store_stress", "sampler_qwen3_vocab"]
 
 # DRAM bytes (read + write) of the dominant kernel per launch, from one ncu
 # capture of the current kernels on that workload; a workload missing here
@@ -98,8 +107,14 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_CONFIG))
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
+                    help="budget of the single-threaded oracle baseline (headline workload)")
+    ap.add_argument("--cpu-all-seconds", type=float, default=3.0,
+                    help="budget of the all-core (OpenMP) oracle baseline (headline workload)")
+    ap.add_argument("--sub-cpu-seconds", type=float, default=2.0,
+                    help="budget of each oracle baseline of the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the chosen workload only")
     ap.add_argument("--split-sms", type=int, default=96,
                     help="mixed chunked-prefill step: SMs of the prefill's partition (0: no SM split)")
     ap.add_argument("--unfused", action="store_true",
@@ -164,6 +179,18 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads
 
+_INPUTS: dict = {}
+
+
+def workload_inputs(name: str):
+    """The workload's seeded synthetic inputs, generated once per run (the timed device
+    copies, the end-to-end path and the CPU baselines all read the same objects, which
+    nothing mutates: every consumer copies what it writes)."""
+    if name not in _INPUTS:
+        from tests import inputs
+        _INPUTS[name] = inputs.WORKLOADS[name]()
+    return _INPUTS[name]
+
 class L2Flush:
     """Evicts the L2 between timed steps by READING a 256 MB buffer (a sum into one float):
     a write flush would leave ~129 MB of dirty lines whose write-back lands in the next
@@ -212,11 +239,10 @@ class DecodeWorkload:
     all inputs resident on the device."""
 
     def __init__(self, name: str, dev: torch.device, fused: bool = True):
-        from tests import inputs
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
         self.name = name
-        self.st = st = inputs.WORKLOADS[name]()
+        self.st = st = workload_inputs(name)
         p = st.pool
         self.dev = dev
         self.kc, self.vc = p.k_cache.to(dev), p.v_cache.to(dev)
@@ -260,30 +286,36 @@ class DecodeWorkload:
     def make_runner(self, zero_copy: bool):
         from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
         st, fs = self.st, getattr(self, "fs", None)
-        runner = DecodeGraphRunner(self.kc, self.vc, st.num_q_heads, st.batch, st.block_tables.shape[1],
-                                   st.scale, st.q.dtype, k_scale=fs.k_scale if fs else None,
-                                   v_scale=fs.v_scale if fs else None, zero_copy=zero_copy)
-        runner.set_inputs(st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables)
-        return runner
+        return DecodeGraphRunner(self.kc, self.vc, st.num_q_heads, st.batch, st.block_tables.shape[1],
+                                 st.scale, st.q.dtype, k_scale=fs.k_scale if fs else None,
+                                 v_scale=fs.v_scale if fs else None, zero_copy=zero_copy)
+
+    @staticmethod
+    def runner_args(st):
+        return st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables
 
     def e2e_buffers(self):
         if self.fused:
             # the engine's decode path: one CUDA graph per padded batch size holding the fused store +
-            # decode, whose kernels read the step's packed inputs from pinned host memory and write the
-            # output into pinned host memory (captured here, untimed)
+            # decode (captured here, untimed); a step is DecodeGraphRunner.step() from the caller's host
+            # tensors, alternating between this step and the next one over the same pool
+            from tests import inputs
             st = self.st
             self.runner = self.make_runner(zero_copy=True)
-            self.e2e_path = ("DecodeGraphRunner (zero copy): CUDA-graph replay of the fused store + decode, its "
-                             "kernels reading the step's packed inputs from pinned host memory and writing the "
-                             "output into pinned host memory over NVLink-C2C, then a stream sync; host wall clock")
+            self.e2e_inputs = [self.runner_args(st), self.runner_args(inputs.next_decode_step(st, seed=4242))]
+            self.e2e_path = ("DecodeGraphRunner.step() from the caller's host tensors, alternating two seeded "
+                             "decode steps over the same pool: the step's inputs copied into the pinned staging, "
+                             "CUDA-graph replay of the fused store + decode whose kernels read that staging and "
+                             "write the output into pinned host memory over NVLink-C2C, stream sync; host wall "
+                             "clock")
             return None, None, self.runner.h2d_bytes(st.batch), self.runner.d2h_bytes(st.batch)
         pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         return pinned, out_host, pinned.numel(), out_host.numel() * out_host.element_size()
 
-    def e2e_step(self, pinned, out_host):
+    def e2e_step(self, pinned, out_host, i: int = 0):
         if self.fused:
-            self.runner.replay(self.st.batch)
+            self.runner.step(*self.e2e_inputs[i % 2])
             return
         self.inputs.copy_(pinned, non_blocking=True)   # the step's inputs, one copy
         for _, fn in self.phases:
@@ -297,11 +329,10 @@ class Fp8DecodeWorkload(DecodeWorkload):
     fused=False pa_store_kv_fp8 then pa_decode_fp8."""
 
     def __init__(self, name: str, dev: torch.device, fused: bool = True):
-        from tests import inputs
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
         self.name = name
-        fs = inputs.WORKLOADS[name]()
+        fs = workload_inputs(name)
         self.fs, self.st = fs, fs.step
         st = fs.step
         p = st.pool
@@ -351,13 +382,12 @@ class MixedWorkload(DecodeWorkload):
     their cached prefixes, decode of the other sequences."""
 
     def __init__(self, name: str, dev: torch.device, split_sms: int = 0):
-        from tests import inputs
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
         self.name = name
         # the whole step in one call, the prefill and the decode side by side on disjoint SM sets
         self.split = pa.SmSplit(split_sms) if split_sms else None
-        m = inputs.WORKLOADS[name]()
+        m = workload_inputs(name)
         self.st = st = m.decode
         pf = m.prefill
         self.pf = pf
@@ -407,7 +437,7 @@ class MixedWorkload(DecodeWorkload):
                              "outputs, stream sync; host wall clock")
         return pinned, outs, pinned.numel(), outs.numel() * outs.element_size()
 
-    def e2e_step(self, pinned, out_host):
+    def e2e_step(self, pinned, out_host, i: int = 0):
         self.inputs.copy_(pinned, non_blocking=True)   # the step's inputs, one copy
         if self.split is not None:
             self.split_step()
@@ -449,10 +479,11 @@ def max_over_ranks(x: float, world: int, dev) -> float:
     return float(t.item())
 
 
+# ------------------------------------------------------------ CPU baselines
+
 def _decode_part(name: str):
     """The decode step of a workload (the decode rows of the mixed step)."""
-    from tests import inputs
-    st = inputs.WORKLOADS[name]()
+    st = workload_inputs(name)
     return st.decode if hasattr(st, "decode") else st
 
 
@@ -497,6 +528,102 @@ def cpu_baseline(name: str, seconds: float):
             "sample": f"store + decode of {n} sequences (round robin over the {st.batch} of the workload) "
                       f"({done_bytes / 1e6:.1f} MB of KV), single-threaded C oracle, "
                       f"{os.cpu_count()} host cores present"}
+
+
+def cpu_baseline_all_cores(name: str, seconds: float):
+    """The same oracle source built with OpenMP (bit-identical results), on all host cores:
+    decode of 8 sequences per call, round robin over the batch, until the budget is spent
+    (the store of the step's rows is done once, before the timing)."""
+    import oracle
+    lib = oracle.load_omp()
+    st = _decode_part(name)
+    fp8 = hasattr(st, "step")
+    if fp8:
+        fs, st = st, st.step
+        kc, vc = fs.k_cache.clone(), fs.v_cache.clone()
+        oracle.store_kv_fp8(st.k_new, st.v_new, kc, vc, st.slot_mapping, fs.k_scale, fs.v_scale)
+        row = 2 * st.pool.num_kv_heads * st.pool.head_dim
+    else:
+        kc, vc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+        oracle.store_kv(st.k_new, st.v_new, kc, vc, st.slot_mapping)
+        row = 2 * st.pool.num_kv_heads * st.pool.head_dim * st.q.element_size()
+    chunk, B = 8, st.batch
+    done_bytes, n, t_total = 0, 0, 0.0
+    while t_total < seconds:
+        b0 = (n * chunk) % B
+        sl = slice(b0, min(b0 + chunk, B))
+        t0 = time.perf_counter()
+        if fp8:
+            oracle.decode_fp8(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale, fs.k_scale,
+                              fs.v_scale, lib=lib)
+        else:
+            oracle.decode(st.q[sl], kc, vc, st.block_tables[sl], st.context_lens[sl], st.scale, lib=lib)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(st.context_lens[sl].sum()) * row
+        n += 1
+    threads = lib.oracle_num_threads()
+    return {"value": done_bytes / t_total / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle (OpenMP build)",
+            "sample": f"decode of {n} batches of up to {chunk} sequences (round robin over the {B} of the "
+                      f"workload, {done_bytes / 1e6:.1f} MB of KV), {threads} threads over (query head) rows "
+                      f"and gathered positions, {os.cpu_count()} host cores present"}
+
+
+def decode_cpu_baselines(name: str, single_s: float, all_s: float):
+    """Single-threaded oracle baseline with the all-core figure beside it."""
+    base = cpu_baseline(name, single_s)
+    base["all_cores"] = cpu_baseline_all_cores(name, all_s)
+    return base
+
+
+def prefill_cpu_baselines(single_s: float, all_s: float):
+    """The oracle's chunked prefill of the mixed workload on the host, in TFLOP/s of the
+    kernel's algorithmic work (masked work excluded): single-threaded on 16-row windows
+    of the chunks (round robin), and the OpenMP build on whole chunks (round robin)."""
+    import oracle
+    m = workload_inputs("mixed_chunked_prefill")
+    st = m.prefill
+    okc, ovc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+    oracle.store_kv(m.k_new, m.v_new, okc, ovc, m.slot_mapping)
+    cq, ck = st.cu_seqlens_q.tolist(), st.cu_seqlens_k.tolist()
+    S, H, D = len(cq) - 1, st.num_q_heads, st.q.shape[2]
+
+    def window(i, r0, r1, lib=None):
+        lq, lk = cq[i + 1] - cq[i], ck[i + 1] - ck[i]
+        P = lk - lq
+        rows = slice(cq[i] + r0, cq[i] + r1)
+        t0 = time.perf_counter()
+        oracle.prefill_paged(st.q[rows], st.k_new[rows], st.v_new[rows], okc, ovc,
+                             torch.tensor([0, r1 - r0], dtype=torch.int32),
+                             torch.tensor([0, P + r1], dtype=torch.int32), st.block_tables[i:i + 1], st.scale,
+                             lib=lib)
+        dt = time.perf_counter() - t0
+        return dt, 4 * D * H * sum(P + r + 1 for r in range(r0, r1))
+
+    out = {}
+    for kind, budget in (("single", single_s), ("all", all_s)):
+        lib = oracle.load_omp() if kind == "all" else None
+        t_total, flops, n = 0.0, 0, 0
+        while t_total < budget:
+            i = n % S
+            lq = cq[i + 1] - cq[i]
+            if kind == "single":
+                r0 = (16 * (n // S)) % max(lq - 15, 1)
+                dt, f = window(i, r0, min(r0 + 16, lq))
+            else:
+                dt, f = window(i, 0, lq, lib)
+            t_total += dt
+            flops += f
+            n += 1
+        out[kind] = (flops / t_total / 1e12, n, flops)
+    threads = oracle.load_omp().oracle_num_threads()
+    v1, n1, f1 = out["single"]
+    va, na, fa = out["all"]
+    return {"value": v1, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n1} 16-row windows of the 8 chunks (round robin), {f1 / 1e9:.1f} GFLOP, single-threaded "
+                      f"C oracle, {os.cpu_count()} host cores present",
+            "all_cores": {"value": va, "unit": "TFLOP/s", "cores": threads, "kind": "oracle (OpenMP build)",
+                          "sample": f"{na} whole 512-row chunks (round robin), {fa / 1e9:.1f} GFLOP, {threads} "
+                                    f"threads over (query row, head) rows"}}
 
 
 def run_reference(args, world, rank):
@@ -602,10 +729,11 @@ def sampler_cpu_baseline(seconds: float):
     nbytes = n * logits.shape[1] * logits.element_size()
     return {"value": nbytes / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n} rows of the workload sampled one at a time (noise drawn outside the timing), "
-                      f"single-threaded C oracle, {os.cpu_count()} host cores present"}
+                      f"single-threaded C oracle (the sampler oracle has no multi-threaded build), "
+                      f"{os.cpu_count()} host cores present"}
 
 
-def run_sampler(args, world, rank, local):
+def measure_sampler(name, args, world, rank, local, cpu_s):
     """pa_sample on 64 rows of a 151936-token vocabulary, in-kernel noise, a new offset every step."""
     import paged_kv_cache_bs_gb300 as pa
     dev = torch.device("cuda", local)
@@ -652,38 +780,32 @@ def run_sampler(args, world, rank, local):
         e2e_s += time.perf_counter() - t0
     e2e_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
     if rank != 0:
-        return
+        return None
     peaks, peak_kind = measured_peaks()
     sm_mhz = clk.get("sm_mhz") or 2070.0
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     issue_peak = ISSUE_PER_SM_PER_CLK * sms * sm_mhz * 1e6
-    if SAMPLER_INSTRUCTIONS_PER_CALL:
-        achieved = SAMPLER_INSTRUCTIONS_PER_CALL / (ms / 1e3)
-        roof = {"bound": "alu", "kernel": "sample_kernel (Philox4x32-10 + two logf per entry, issue-bound)",
-                "achieved": achieved, "peak": issue_peak, "unit": "warp-instr/s", "frac": achieved / issue_peak,
-                "peak_source": f"derived: {ISSUE_PER_SM_PER_CLK} warp instructions/clock/SM x {sms} SMs x "
-                               f"{sm_mhz:.0f} MHz sampled", "traffic": SAMPLER_TRAFFIC_PER_CALL,
-                "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
-    else:
-        roof = {"bound": "alu", "kernel": "sample_kernel", "achieved": None, "peak": issue_peak,
-                "unit": "warp-instr/s", "frac": None, "traffic": None,
-                "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
-    line = {
+    achieved = SAMPLER_INSTRUCTIONS_PER_CALL / (ms / 1e3)
+    roof = {"bound": "alu", "kernel": "sample_kernel (Philox4x32-10 + two logf per entry, issue-bound)",
+            "achieved": achieved, "peak": issue_peak, "unit": "warp-instr/s", "frac": achieved / issue_peak,
+            "peak_source": f"derived: {ISSUE_PER_SM_PER_CLK} warp instructions/clock/SM x {sms} SMs x "
+                           f"{sm_mhz:.0f} MHz sampled", "traffic": SAMPLER_TRAFFIC_PER_CALL,
+            "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    return {
         "metric": SAMPLER_METRIC, "value": world * nbytes / (ms_max / 1e3) / 1e9, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+        "config": {"workload": name, **WORKLOAD_CONFIG[name],
                    "l2": "flushed (256 MB read) between steps, outside the timed events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "rows_per_s": world * B / (ms_max / 1e3),
         "roofline": roof,
-        "cpu_baseline": sampler_cpu_baseline(args.cpu_seconds) if world == 1 and not args.no_cpu_baseline else None,
+        "cpu_baseline": sampler_cpu_baseline(cpu_s) if world == 1 and cpu_s > 0 else None,
         "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": nbytes + B * 4, "d2h_bytes_per_step": B * 4, "ms_per_step": e2e_ms},
         "gpu_launches": K,
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
 
 
 def _store_inputs():
@@ -692,7 +814,7 @@ def _store_inputs():
 
 
 def store_cpu_baseline(seconds: float):
-    """The oracle's store single-threaded on this host, token by token (the whole 16384 once it fits)."""
+    """The oracle's store single-threaded on this host, token by token."""
     import oracle
     k, v, kc, vc, slots = _store_inputs()
     row = k.shape[1] * k.shape[2] * k.element_size()
@@ -704,11 +826,11 @@ def store_cpu_baseline(seconds: float):
         t_total += time.perf_counter() - t0
         n += 1
     return {"value": 4 * row * n / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} tokens of the workload stored one at a time, single-threaded C oracle, "
-                      f"{os.cpu_count()} host cores present"}
+            "sample": f"{n} tokens of the workload stored one at a time, single-threaded C oracle (the store "
+                      f"oracle has no multi-threaded build), {os.cpu_count()} host cores present"}
 
 
-def run_store(args, world, rank, local):
+def measure_store(name, args, world, rank, local, cpu_s):
     """pa_store_kv of 16384 tokens (the engine's max batched tokens) into distinct random slots."""
     import paged_kv_cache_bs_gb300 as pa
     dev = torch.device("cuda", local)
@@ -756,21 +878,21 @@ def run_store(args, world, rank, local):
         e2e_s += time.perf_counter() - t0
     e2e_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
     if rank != 0:
-        return
+        return None
     peaks, peak_kind = measured_peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
-    line = {
+    return {
         "metric": STORE_METRIC, "value": world * nbytes / (ms_max / 1e3) / 1e9, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_max, "ms_per_step_median": statistics.median(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+        "config": {"workload": name, **WORKLOAD_CONFIG[name],
                    "l2": "flushed (256 MB read) between steps, outside the timed events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": world * T / (ms_max / 1e3),
         "roofline": {"bound": "hbm", "kernel": "store_kv_kernel (one warp per token, 16-byte vectors)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "peak_source": f"{peak_kind} (hbm_gbs)", "traffic": STORE_TRAFFIC_PER_CALL},
-        "cpu_baseline": store_cpu_baseline(args.cpu_seconds) if world == 1 and not args.no_cpu_baseline else None,
+        "cpu_baseline": store_cpu_baseline(cpu_s) if world == 1 and cpu_s > 0 else None,
         "e2e": {"value": world * nbytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": 2 * T * row + 4 * T, "d2h_bytes_per_step": 0, "ms_per_step": e2e_ms,
                 "path": "H2D copies of the new K/V rows and slots from pinned memory, pa_store_kv, stream sync; "
@@ -778,22 +900,20 @@ def run_store(args, world, rank, local):
         "gpu_launches": K,
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
-    if args.workload == "sampler_qwen3_vocab":
-        return run_sampler(args, world, rank, local)
-    if args.workload == "store_stress":
-        return run_store(args, world, rank, local)
+def measure_attention(name, args, world, rank, local, cpu_s, cpu_all_s):
+    """A decode or mixed chunked-prefill workload: the device-resident timed steps, the
+    mixed step on SM partitions, the end-to-end step through the public API, the roofline
+    of the dominant kernel and the CPU baselines."""
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    if args.workload == "mixed_chunked_prefill":
-        w = MixedWorkload(args.workload, dev, split_sms=args.split_sms)
-    elif args.workload.endswith("_fp8"):
-        w = Fp8DecodeWorkload(args.workload, dev, fused=not args.unfused)
+    if name == "mixed_chunked_prefill":
+        w = MixedWorkload(name, dev, split_sms=args.split_sms)
+    elif name.endswith("_fp8"):
+        w = Fp8DecodeWorkload(name, dev, fused=not args.unfused)
     else:
-        w = DecodeWorkload(args.workload, dev, fused=not args.unfused)
+        w = DecodeWorkload(name, dev, fused=not args.unfused)
     flush_needed = w.kv_unique_bytes < 2 * L2_BYTES
     flush = L2Flush(dev, flush_needed)
     stream = torch.cuda.current_stream(dev)
@@ -828,7 +948,7 @@ def run_ours(args, world, rank, local):
     barrier(world, local)
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
-    phase_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j, (name, _) in enumerate(w.phases)}
+    phase_ms = {pn: sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j, (pn, _) in enumerate(w.phases)}
     step_ms = sum(phase_ms.values())
     step_ms_median = statistics.median(e[0].elapsed_time(e[nph]) for e in ev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
@@ -861,12 +981,12 @@ def run_ours(args, world, rank, local):
         step_ms_max = max_over_ranks(split_ms, world, dev)
         step_ms_median = statistics.median(split_times)
 
-    # ---- end to end through the public API, as a caller sees it: host wall
-    # clock from the H2D copies of the step's inputs (pinned host memory) to the
-    # result back in host memory, launch overheads and the final sync included.
+    # ---- end to end through the public API, as a caller sees it: host wall clock from the
+    # step's inputs in host memory to its result back in host memory, launch overheads and
+    # the final sync included.
     pinned, out_host, h2d, d2h = w.e2e_buffers()
-    for _ in range(args.warmup):
-        w.e2e_step(pinned, out_host)
+    for i in range(args.warmup):
+        w.e2e_step(pinned, out_host, i)
     torch.cuda.synchronize(dev)
     Ke = min(K, 500)
     barrier(world, local)
@@ -875,50 +995,58 @@ def run_ours(args, world, rank, local):
         between_steps()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        w.e2e_step(pinned, out_host)
+        w.e2e_step(pinned, out_host, i)
         stream.synchronize()
         e2e_s += time.perf_counter() - t0
     barrier(world, local)
     e2e_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
-    # the same step with the graph's copy-engine transfers instead of zero-copy operands (context)
-    e2e_copy_ms = None
+    # breakdown of the graph runner's step: the replay alone (inputs already staged), and the
+    # step with the graph's copy-engine transfers instead of zero-copy operands
+    e2e_replay_ms = e2e_copy_ms = None
     if getattr(w, "runner", None) is not None:
+        w.runner.set_inputs(*w.e2e_inputs[0])
+        e2e_s = 0.0
+        for i in range(Ke):
+            between_steps()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            w.runner.replay(w.st.batch)
+            stream.synchronize()
+            e2e_s += time.perf_counter() - t0
+        e2e_replay_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
         rc = w.make_runner(zero_copy=False)
-        for _ in range(args.warmup):
-            rc.replay(w.st.batch)
+        for i in range(args.warmup):
+            rc.step(*w.e2e_inputs[i % 2])
         torch.cuda.synchronize(dev)
         e2e_s = 0.0
         for i in range(Ke):
             between_steps()
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
-            rc.replay(w.st.batch)
-            stream.synchronize()
+            rc.step(*w.e2e_inputs[i % 2])
             e2e_s += time.perf_counter() - t0
         e2e_copy_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
         del rc
 
     peaks, peak_kind = measured_peaks()
-    value = world * w.kv_bytes / (step_ms_max / 1e3) / 1e9
+    # bytes DRAM must supply per step: each physical page once (pages shared by several
+    # sequences are counted once; for unshared workloads this equals the logical KV bytes)
+    value = world * w.kv_unique_bytes / (step_ms_max / 1e3) / 1e9
     if rank != 0:
-        return
+        return None
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+    if world == 1 and cpu_s > 0:
+        cpu = decode_cpu_baselines(name, cpu_s, cpu_all_s)
     decode_gbs = w.kv_bytes / (dec_ms_avg / 1e3) / 1e9
+    unique_gbs = w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9
     dominant = max(phase_ms, key=phase_ms.get)
     if dominant == "prefill":
         achieved = w.prefill_flops / (phase_ms["prefill"] / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": "prefill_kernel (tcgen05, bf16, fp32 accumulate)", "achieved": achieved,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
-                "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
-                "peak_source": f"{peak_kind} (bf16_tflops_sustained; timed inside a repeated step)",
-                "traffic": TRAFFIC_PER_CALL.get(args.workload)}
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peak_kind} (bf16_tflops, burst: the kernel is timed by its own events)",
+                "traffic": PREFILL_TRAFFIC_PER_CALL.get(name)}
     else:
-        # bytes DRAM must supply: each physical page once (pages shared by several sequences
-        # are counted once; for unshared workloads this equals the logical KV bytes)
-        unique_gbs = w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9
         f8 = isinstance(w, Fp8DecodeWorkload)
         kern = ("pa_store_decode_fp8 (E4M3 store fused into the split-K partition kernel + merge)"
                 if f8 and "store+decode" in phase_ms else
@@ -929,16 +1057,25 @@ def run_ours(args, world, rank, local):
                 "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": unique_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} (hbm_gbs)",
                 "frac_of_nominal": unique_gbs / NOMINAL_HBM_GBS,
-                "traffic": TRAFFIC_PER_CALL.get(args.workload)}
+                "traffic": TRAFFIC_PER_CALL.get(name)}
+    e2e = {"value": world * w.kv_unique_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "path": w.e2e_path}
+    if e2e_replay_ms is not None:
+        e2e["breakdown"] = {"ms_per_step_replay_only": e2e_replay_ms,
+                            "ms_per_step_with_copy_engine": e2e_copy_ms,
+                            "note": "replay only: the graph replayed with the inputs already in the pinned "
+                                    "staging; with copy engine: step() of a runner whose graph copies the "
+                                    "inputs to and the output from device buffers"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms_max, "ms_per_step_median": step_ms_median, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": WORKLOAD_CONFIG[args.workload]["dtype"], "data": "synthetic",
-        "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload],
+        "scaling": "weak", "vs_baseline": None, "dtype": WORKLOAD_CONFIG[name]["dtype"], "data": "synthetic",
+        "config": {"workload": name, **WORKLOAD_CONFIG[name],
                    "l2": ("flushed (256 MB read) between steps, outside the timed events" if flush_needed else
                           f"not flushed: inputs larger than L2 ({w.kv_unique_bytes / 2**20:.0f} MiB of KV per step "
                           f"vs 129 MB L2, read in the same order every step)"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "value_logical": world * w.kv_bytes / (step_ms_max / 1e3) / 1e9,
         "tokens_per_s": world * w.batch / (step_ms_max / 1e3),
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "phase_ms": phase_ms,
@@ -948,16 +1085,14 @@ def run_ours(args, world, rank, local):
                                  "partitions at once; phase_ms times the three calls one after the other"}}
            if split_ms is not None else {}),
         "decode_gbs": decode_gbs,
-        "decode_unique_gbs": w.kv_unique_bytes / (dec_ms_avg / 1e3) / 1e9,
+        "decode_unique_gbs": unique_gbs,
         "kv_unique_bytes_per_step": w.kv_unique_bytes,
         "store_gbs": w.store_bytes / (store_ms / 1e3) / 1e9 if store_ms else None,
         "store_fused_into_decode": "store+decode" in phase_ms,
         "kv_bytes_per_step": w.kv_bytes,
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * w.kv_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "path": w.e2e_path,
-                **({"ms_per_step_with_copy_engine": e2e_copy_ms} if e2e_copy_ms is not None else {})},
+        "e2e": e2e,
         "gpu_launches": K * w.launches_per_step,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
@@ -968,11 +1103,45 @@ def run_ours(args, world, rank, local):
         line["prefill_flops_per_step"] = w.prefill_flops
         line["roofline_prefill"] = {
             "bound": "tensor", "kernel": "prefill_kernel (tcgen05, bf16 in, fp32 accumulate)", "achieved": tf,
-            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops_sustained"],
-            "frac_of_burst_peak": tf / peaks["bf16_tflops"],
-            "peak_source": f"{peak_kind} (bf16_tflops_sustained; timed inside a repeated step)",
-            "traffic": PREFILL_TRAFFIC_PER_CALL.get(args.workload)}
-    print(json.dumps(line), flush=True)
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+            "frac_of_sustained_peak": tf / peaks["bf16_tflops_sustained"],
+            "peak_source": f"{peak_kind} (bf16_tflops, burst: the kernel is timed by its own events)",
+            "traffic": PREFILL_TRAFFIC_PER_CALL.get(name)}
+        if world == 1 and cpu_s > 0:
+            line["cpu_baseline_prefill"] = prefill_cpu_baselines(cpu_s, cpu_all_s)
+    del w
+    torch.cuda.empty_cache()
+    return line
+
+
+def measure(name, args, world, rank, local, cpu_s, cpu_all_s):
+    try:
+        if name == "sampler_qwen3_vocab":
+            return measure_sampler(name, args, world, rank, local, cpu_s)
+        if name == "store_stress":
+            return measure_store(name, args, world, rank, local, cpu_s)
+        return measure_attention(name, args, world, rank, local, cpu_s, cpu_all_s)
+    finally:
+        _INPUTS.pop(name, None)
+
+
+def run_ours(args, world, rank, local):
+    cpu_s = 0.0 if args.no_cpu_baseline else args.cpu_seconds
+    cpu_all_s = 0.0 if args.no_cpu_baseline else args.cpu_all_seconds
+    line = measure(args.workload, args, world, rank, local, cpu_s, cpu_all_s)
+    if not args.no_configs:
+        sub_s = 0.0 if args.no_cpu_baseline else args.sub_cpu_seconds
+        configs = {}
+        for name in SUB_CONFIGS:
+            if name == args.workload:
+                continue
+            rec = measure(name, args, world, rank, local, sub_s, sub_s)
+            if rec is not None:
+                configs[name] = rec
+        if line is not None:
+            line["configs"] = configs
+    if line is not None:
+        print(json.dumps(line), flush=True)
 
 
 def main():

@@ -279,6 +279,22 @@ def _decode_from_pool(pool: Pool, ctx: list[int], num_q_heads: int, gen, scale=N
                       scale if scale is not None else 1.0 / math.sqrt(d))
 
 
+def next_decode_step(st: DecodeStep, seed: int) -> DecodeStep:
+    """The decode step after ``st`` over the same pool and block tables: each sequence
+    gains one token while its last allocated page has room (else keeps its length),
+    with new random q and new K/V rows stored at the slot of its new last position."""
+    p = st.pool
+    gen = torch.Generator().manual_seed(seed)
+    ctx = [L + 1 if 0 < L < len(t) * p.block_size else L for t, L in zip(p.tables, st.context_lens.tolist())]
+    B, hkv, d = len(ctx), p.num_kv_heads, p.head_dim
+    q = torch.randn(B, st.num_q_heads, d, generator=gen).to(st.q.dtype)
+    k_new = torch.randn(B, hkv, d, generator=gen).to(st.q.dtype)
+    v_new = torch.randn(B, hkv, d, generator=gen).to(st.q.dtype)
+    slots = [decode_slot(t, p.block_size, L) if L > 0 else -1 for t, L in zip(p.tables, ctx)]
+    return DecodeStep(p, st.num_q_heads, q, k_new, v_new, torch.tensor(slots, dtype=torch.int32),
+                      st.block_tables.clone(), torch.tensor(ctx, dtype=torch.int32), st.scale)
+
+
 def make_decode(ctx: list[int], *, num_q_heads: int, num_kv_heads: int, head_dim: int,
                 block_size: int, dtype: torch.dtype, seed: int, num_blocks: int | None = None,
                 share_groups: int = 0, share_tokens: int = 0, scale=None) -> DecodeStep:
