@@ -96,6 +96,43 @@ PA_API int pa_bm_prefill_inputs(const pa_bm *bm, const int64_t *seq_ids, const i
                                 int32_t max_blocks, int32_t *slot_mapping, int32_t *cu_seqlens_q,
                                 int32_t *cu_seqlens_k, int32_t *block_tables);
 
+/*
+ * pa_prefix_groups -- the shared-prefix groups of a decode batch, the input
+ * of the prefix-sharing decode (pa_decode_options of pa_api.h).
+ *
+ * With prefix caching, sequences with a common prompt prefix point at the
+ * same physical pages ("nano-vLLM Part 2", section 2.5: prompt B's table
+ * [0, 3, 4, 5] starts with A's page 0; "How vLLM works", prefix caching).
+ * The pages define the sharing, not a grouping of a decode batch; this
+ * library's rule:
+ *   1. a sequence whose context length L is 0 or at most block_size holds no
+ *      complete page and is never grouped;
+ *   2. the others are grouped by the first entry of their block table, groups
+ *      in the order their first member appears in the batch, members in batch
+ *      order;
+ *   3. a group of two or more shares its first n pages: the number of leading
+ *      table entries equal across all members, but at most (L - 1) /
+ *      block_size for each member (the page holding a sequence's newest token,
+ *      the one a decode step writes, is never shared; only complete pages are,
+ *      section 2.4);
+ *   4. groups with n < max(min_shared_pages, 1) are dropped, singletons too.
+ *   block_tables  host int32 [batch, max_blocks] row-major, -1 padded.
+ *   context_lens  host int32 [batch], each in [0, max_blocks * block_size].
+ *   group_offsets host int32 [batch / 2 + 1] at least (out): the members of
+ *                 group g are group_seqs[group_offsets[g] .. group_offsets[g+1]).
+ *   group_seqs    host int32 [batch] (out).
+ *   prefix_lens   host int32 [batch] (out): n * block_size for a member of a
+ *                 group, 0 for every other sequence.
+ *   *num_groups, *max_group_size, *max_prefix_len (out): the host sizes the
+ *                 decode options need.
+ * Errors: INVALID_ARG for null pointers, negative sizes, a context length
+ * outside the table.
+ */
+PA_API int pa_prefix_groups(const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
+                            int32_t batch, int32_t block_size, int32_t min_shared_pages, int32_t *group_offsets,
+                            int32_t *group_seqs, int32_t *prefix_lens, int32_t *num_groups, int32_t *max_group_size,
+                            int32_t *max_prefix_len);
+
 #ifdef __cplusplus
 }
 #endif

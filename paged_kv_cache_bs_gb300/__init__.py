@@ -171,6 +171,26 @@ def store_kv(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     _check("pa_store_kv", rc)
 
 
+class PrefixGroups:
+    """Shared-prefix groups of a decode batch (``pa_prefix_groups``): the members of group g are
+    ``group_seqs[group_offsets[g]:group_offsets[g + 1]]``; ``prefix_lens[b]`` tokens at the start
+    of sequence b's context are read once for its whole group (0: not grouped).  int32 tensors,
+    on the host as computed, on the device for a decode call (:meth:`to`)."""
+
+    def __init__(self, group_offsets: torch.Tensor, group_seqs: torch.Tensor, prefix_lens: torch.Tensor,
+                 max_group_size: int, max_prefix_len: int):
+        self.group_offsets, self.group_seqs, self.prefix_lens = group_offsets, group_seqs, prefix_lens
+        self.max_group_size, self.max_prefix_len = int(max_group_size), int(max_prefix_len)
+
+    @property
+    def num_groups(self) -> int:
+        return self.group_offsets.numel() - 1
+
+    def to(self, device) -> "PrefixGroups":
+        return PrefixGroups(self.group_offsets.to(device), self.group_seqs.to(device), self.prefix_lens.to(device),
+                            self.max_group_size, self.max_prefix_len)
+
+
 class DecodeOptions:
     """Optional settings of :func:`decode` / :func:`store_decode` (``pa_decode_options``).
 

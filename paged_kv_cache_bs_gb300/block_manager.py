@@ -13,7 +13,7 @@ import ctypes
 
 import torch
 
-from . import _lib, PagedAttentionError
+from . import _lib, PagedAttentionError, PrefixGroups
 
 _p, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -33,6 +33,8 @@ for _name, _args in (("pa_bm_add_sequence", [_p, _i64, _I32P, _i32]), ("pa_bm_ap
                      ("pa_bm_prefill_inputs", [_p, _I64P, _I32P, _i32, _i32, _I32P, _I32P, _I32P, _I32P])):
     getattr(_lib, _name).restype = ctypes.c_int
     getattr(_lib, _name).argtypes = _args
+_lib.pa_prefix_groups.restype = ctypes.c_int
+_lib.pa_prefix_groups.argtypes = [_I32P, _i32, _I32P, _i32, _i32, _i32, _I32P, _I32P, _I32P, _I32P, _I32P, _I32P]
 for _name in ("pa_bm_seq_len", "pa_bm_num_cached_tokens"):
     getattr(_lib, _name).restype = ctypes.c_int64
     getattr(_lib, _name).argtypes = [_p, _i64]
@@ -141,3 +143,25 @@ class BlockManager:
 
 
 __all__ = ["BlockManager"]
+
+
+def prefix_groups(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int,
+                  min_shared_pages: int = 1) -> PrefixGroups:
+    """``pa_prefix_groups``: the shared-prefix groups of a decode batch from its host block
+    tables ([B, max_blocks] int32, -1 padded) and context lengths ([B] int32), as host int32
+    tensors (``.to(device)`` for the decode call)."""
+    bt = block_tables.to(torch.int32).contiguous()
+    cl = context_lens.to(torch.int32).contiguous()
+    if bt.device.type != "cpu" or cl.device.type != "cpu" or bt.dim() != 2 or cl.numel() != bt.shape[0]:
+        raise ValueError("block_tables [B, max_blocks] and context_lens [B] must be host tensors")
+    B = bt.shape[0]
+    off = torch.zeros(B // 2 + 1, dtype=torch.int32)
+    seqs = torch.zeros(max(B, 1), dtype=torch.int32)
+    pre = torch.zeros(max(B, 1), dtype=torch.int32)
+    n, big, longest = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    rc = _lib.pa_prefix_groups(_i32buf(bt), bt.shape[1], _i32buf(cl), B, block_size, min_shared_pages, _i32buf(off),
+                               _i32buf(seqs), _i32buf(pre), ctypes.byref(n), ctypes.byref(big), ctypes.byref(longest))
+    if rc != 0:
+        raise PagedAttentionError("pa_prefix_groups", rc)
+    g = n.value
+    return PrefixGroups(off[:g + 1].clone(), seqs[:int(off[g])].clone(), pre[:B].clone(), big.value, longest.value)

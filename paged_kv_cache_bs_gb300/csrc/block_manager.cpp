@@ -378,4 +378,61 @@ int pa_bm_prefill_inputs(const pa_bm *bm, const int64_t *seq_ids, const int32_t 
     return PA_OK;
 }
 
+int pa_prefix_groups(const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens, int32_t batch,
+                     int32_t block_size, int32_t min_shared_pages, int32_t *group_offsets, int32_t *group_seqs,
+                     int32_t *prefix_lens, int32_t *num_groups, int32_t *max_group_size, int32_t *max_prefix_len) {
+    if (batch < 0 || max_blocks <= 0 || block_size <= 0 || !group_offsets || !num_groups || !max_group_size ||
+        !max_prefix_len || (batch > 0 && (!block_tables || !context_lens || !group_seqs || !prefix_lens)))
+        return fail(PA_ERR_INVALID_ARG, "bad prefix-group arguments");
+    const int64_t cap_tokens = static_cast<int64_t>(max_blocks) * block_size;
+    for (int32_t b = 0; b < batch; ++b)
+        if (context_lens[b] < 0 || context_lens[b] > cap_tokens)
+            return fail(PA_ERR_INVALID_ARG, "context length %lld of sequence %lld is outside the table",
+                        context_lens[b], b);
+    const int32_t min_pages = min_shared_pages > 1 ? min_shared_pages : 1;
+    // candidates keyed by the first page of their table, groups in order of first appearance
+    std::unordered_map<int32_t, size_t> slot_of_page;
+    std::vector<std::vector<int32_t>> cand;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t complete = (context_lens[b] - 1) / block_size;  // pages before the newest token's page
+        if (context_lens[b] <= 0 || complete < 1) continue;
+        const int32_t first = block_tables[static_cast<int64_t>(b) * max_blocks];
+        auto it = slot_of_page.find(first);
+        if (it == slot_of_page.end()) {
+            slot_of_page.emplace(first, cand.size());
+            cand.emplace_back(1, b);
+        } else {
+            cand[it->second].push_back(b);
+        }
+    }
+    for (int32_t b = 0; b < batch; ++b) prefix_lens[b] = 0;
+    int32_t groups = 0, members = 0, largest = 0, longest = 0;
+    group_offsets[0] = 0;
+    for (const std::vector<int32_t> &m : cand) {
+        if (m.size() < 2) continue;
+        int32_t pages = INT32_MAX;
+        for (int32_t b : m) pages = std::min(pages, (context_lens[b] - 1) / block_size);
+        const int32_t *lead = block_tables + static_cast<int64_t>(m[0]) * max_blocks;
+        int32_t n = 0;
+        for (; n < pages; ++n) {
+            bool same = true;
+            for (size_t i = 1; i < m.size() && same; ++i)
+                same = block_tables[static_cast<int64_t>(m[i]) * max_blocks + n] == lead[n];
+            if (!same) break;
+        }
+        if (n < min_pages) continue;
+        for (int32_t b : m) {
+            group_seqs[members++] = b;
+            prefix_lens[b] = n * block_size;
+        }
+        group_offsets[++groups] = members;
+        largest = std::max(largest, static_cast<int32_t>(m.size()));
+        longest = std::max(longest, n * block_size);
+    }
+    *num_groups = groups;
+    *max_group_size = largest;
+    *max_prefix_len = longest;
+    return PA_OK;
+}
+
 }  // extern "C"

@@ -8,6 +8,7 @@ import os
 import random
 
 import pytest
+import torch
 
 from oracle.block_manager import OracleBlockManager
 
@@ -187,3 +188,51 @@ def test_native_rejects_misuse(native):
     bm.allocate(0, 0)
     with pytest.raises(PagedAttentionError):
         bm.postprocess(0, 9)                    # more tokens than the sequence has
+
+
+# ------------------------------------------------------------- prefix groups
+
+def _pg_native(tables, ctx, bs, min_pages=1):
+    from paged_kv_cache_bs_gb300.block_manager import prefix_groups as native
+    width = max([len(t) for t in tables] + [1])
+    bt = torch.tensor([list(t) + [-1] * (width - len(t)) for t in tables] or [[-1]], dtype=torch.int32)[:len(tables)]
+    g = native(bt.reshape(len(tables), width), torch.tensor(ctx, dtype=torch.int32), bs, min_pages)
+    return g.group_offsets.tolist(), g.group_seqs.tolist(), g.prefix_lens.tolist(), g
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_native_prefix_groups_equal_the_oracle(seed):
+    import random
+    from oracle.prefix_groups import prefix_groups as ref
+    from tests.test_prefix_groups import _built_batch
+    rng = random.Random(seed)
+    bs = rng.choice([1, 4, 16, 256])
+    if seed % 2:
+        tables, ctx, _ = _built_batch(rng, bs)
+    else:   # random tables over a small page alphabet: accidental equal entries are common
+        B = rng.randint(0, 30)
+        ctx = [rng.choice([0, rng.randint(1, 9 * bs)]) for _ in range(B)]
+        tables = [[rng.randint(0, 4) for _ in range(-(-L // bs))] for L in ctx]
+    width = max([-(-L // bs) for L in ctx] + [1])
+    tables = [list(t) + [-1] * (width - len(t)) for t in tables]
+    min_pages = rng.choice([1, 1, 2, 3])
+    off, seqs, pre, g = _pg_native(tables, ctx, bs, min_pages)
+    assert (off, seqs, pre) == ref(tables, ctx, bs, min_pages)
+    sizes = [off[i + 1] - off[i] for i in range(len(off) - 1)]
+    assert g.max_group_size == max(sizes, default=0) and g.max_prefix_len == max(pre, default=0)
+
+
+def test_native_prefix_groups_pages_example():
+    import json
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "prefix_groups_example.json")))
+    ctx = [gold["context_lens"]["A"]["printed"], gold["context_lens"]["B"]["derived"]]
+    off, seqs, pre, _ = _pg_native(gold["block_tables"]["printed"], ctx, gold["block_size"])
+    e = gold["expect"]
+    assert (off, seqs, pre) == (e["group_offsets"], e["group_seqs"], e["prefix_lens"])
+
+
+def test_native_prefix_groups_rejects_bad_lengths():
+    import paged_kv_cache_bs_gb300 as pa
+    from paged_kv_cache_bs_gb300.block_manager import prefix_groups as native
+    with pytest.raises(pa.PagedAttentionError):
+        native(torch.zeros(2, 3, dtype=torch.int32), torch.tensor([5, 13], dtype=torch.int32), 4)  # 13 > 3 * 4
