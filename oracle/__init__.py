@@ -68,6 +68,8 @@ def _declare(lib):
     lib.oracle_sample.restype = ci
     lib.oracle_half_to_float.argtypes = [ctypes.c_uint16, ci]
     lib.oracle_half_to_float.restype = f32
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ci
     return lib
 
 

@@ -95,6 +95,9 @@ static float to_float(uint16_t h, int dtype)
 
 float oracle_half_to_float(uint16_t bits, int dtype) { return to_float(bits, dtype); }
 
+/* Threads the parallel regions use (1 in the single-threaded build). */
+int oracle_num_threads(void) { return n_threads(); }
+
 /* ---------------------------------------------------------------- store */
 
 int oracle_store_kv(const uint16_t *k, const uint16_t *v, int64_t k_row_stride, int64_t v_row_stride,
