@@ -96,6 +96,7 @@ enum {
     PA_FLAG_TIMEOUT = 8,
     PA_FLAG_INTERNAL = 16,
     PA_FLAG_BAD_VALUE = 32, /* a value outside its domain (pa_sample: temperature <= 1e-10) */
+    PA_FLAG_BAD_GROUP = 64, /* a shared-prefix descriptor breaking its rules (pa_decode_options) */
 };
 
 /* Message describing the calling thread's last failed call ("" if none). */
@@ -206,21 +207,61 @@ PA_API int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, i
 /*
  * pa_decode_options -- optional settings of pa_decode_ex / pa_store_decode_ex.
  * Zero-initialise it and set only what you need; a NULL pointer or an
- * all-zero struct gives exactly pa_decode / pa_store_decode.  Host memory,
- * read during the call only.
- *   partition     tokens per split-K context partition, overriding the
- *                 library's plan (0: the plan).  A multiple of 64 in
- *                 [64, 2^20]; it is lowered to a multiple of 64 that keeps a
- *                 partition within 256 pages of the block table.  The result
- *                 is the same attention up to the fp32 rounding of the
- *                 log-sum-exp merge.
- *   stages        TMA ring depth of the partition kernel over a 16-bit pool,
- *                 2 or 3 (0: the plan); ignored over an E4M3 pool.
- * Use: tuning and tests; the plan needs no help for ordinary shapes.
+ * all-zero struct gives exactly pa_decode / pa_store_decode.  The struct is
+ * host memory, read during the call only; the arrays it points to are device
+ * memory (or pinned host memory, like the per-step operands), read by the
+ * kernels.
+ *
+ * Split-K plan overrides (tuning and tests; the plan needs no help for
+ * ordinary shapes):
+ *   partition     tokens per split-K context partition (0: the plan).  A
+ *                 multiple of 64 in [64, 2^20]; it is lowered to a multiple of
+ *                 64 that keeps a partition within 256 pages of the block
+ *                 table.  The result is the same attention up to the fp32
+ *                 rounding of the log-sum-exp merge.
+ *   stages        TMA ring depth of the partition kernel, 2 or 3 (0: the plan).
+ *
+ * Shared prefixes (prefix caching: sequences whose block tables begin with the
+ * same physical pages, "nano-vLLM Part 2: Block Tables, KV Cache, and the Path
+ * to the GPU", section 2.5; "How vLLM works", prefix caching).  Each shared
+ * page is then read from memory once per group and kv head for all the group's
+ * query heads, instead of once per sequence; the result is the same attention
+ * (up to the fp32 rounding of the merge).  pa_prefix_groups
+ * (pa_block_manager.h) derives the descriptor from the host block tables.
+ *   num_groups      number of groups (0: no sharing; the fields below unused).
+ *   max_group_size  host: the most sequences in one group (>= 1).
+ *   max_prefix_len  host: the longest prefix_lens entry, tokens (>= 1).
+ *   prefix_partition  tokens per partition of a shared prefix (0: the plan;
+ *                   else a multiple of 64 in [64, 16384]).
+ *   group_offsets   int32 [num_groups + 1], non-decreasing from 0: the members
+ *                   of group g are group_seqs[group_offsets[g] ..
+ *                   group_offsets[g + 1]).
+ *   group_seqs      int32 [batch] (entries past group_offsets[num_groups]
+ *                   unused): sequence indices in [0, batch), each at most once;
+ *                   every group_offsets entry is at most batch.
+ *   prefix_lens     int32 [batch]: the number of leading context tokens of
+ *                   sequence b its group's pages hold (0 for a sequence in no
+ *                   group).  For a member: a multiple of block_size, the same
+ *                   for every member of the group, below context_lens[b]
+ *                   (the token a decode step stores is never shared), at most
+ *                   max_prefix_len, and the first prefix_lens[b] / block_size
+ *                   block-table entries equal across the group.
+ * A descriptor breaking these rules sets PA_FLAG_BAD_GROUP where a kernel sees
+ * it (outputs of the sequences involved are then unspecified; nothing faults);
+ * a sequence with prefix_lens[b] > 0 that is in no group gets an unspecified
+ * output without a flag.  Supported for 16-bit pools (pa_decode_ex,
+ * pa_store_decode_ex).
  */
 typedef struct pa_decode_options {
     int32_t partition;
     int32_t stages;
+    int32_t num_groups;
+    int32_t max_group_size;
+    int32_t max_prefix_len;
+    int32_t prefix_partition;
+    const int32_t *group_offsets;
+    const int32_t *group_seqs;
+    const int32_t *prefix_lens;
 } pa_decode_options;
 
 /* Workspace bytes of pa_decode_ex / pa_store_decode_ex with these options

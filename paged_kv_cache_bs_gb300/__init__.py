@@ -56,7 +56,9 @@ _lib.pa_store_decode.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _
 
 class _Options(ctypes.Structure):
     """Mirror of pa_decode_options."""
-    _fields_ = [("partition", _i32), ("stages", _i32)]
+    _fields_ = [("partition", _i32), ("stages", _i32), ("num_groups", _i32), ("max_group_size", _i32),
+                ("max_prefix_len", _i32), ("prefix_partition", _i32), ("group_offsets", _p), ("group_seqs", _p),
+                ("prefix_lens", _p)]
 
 
 _opt_p = ctypes.POINTER(_Options)
@@ -101,6 +103,7 @@ PA_F16, PA_BF16, PA_F32, PA_E4M3 = 0, 1, 2, 3
 _FP8_POOL = (torch.uint8, torch.float8_e4m3fn)  # E4M3 codes, one byte per element
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_INTERNAL, FLAG_BAD_VALUE = 1, 2, 4, 8, 16, 32
+FLAG_BAD_GROUP = 64
 
 
 class PagedAttentionError(RuntimeError):
@@ -173,7 +176,8 @@ def store_kv(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: t
 
 class PrefixGroups:
     """Shared-prefix groups of a decode batch (``pa_prefix_groups``): the members of group g are
-    ``group_seqs[group_offsets[g]:group_offsets[g + 1]]``; ``prefix_lens[b]`` tokens at the start
+    ``group_seqs[group_offsets[g]:group_offsets[g + 1]]`` (``group_seqs`` has room for the whole
+    batch; entries past the last offset are unused); ``prefix_lens[b]`` tokens at the start
     of sequence b's context are read once for its whole group (0: not grouped).  int32 tensors,
     on the host as computed, on the device for a decode call (:meth:`to`)."""
 
@@ -195,13 +199,27 @@ class DecodeOptions:
     """Optional settings of :func:`decode` / :func:`store_decode` (``pa_decode_options``).
 
     ``partition``: tokens per split-K partition (a multiple of 64; 0 = the library's plan).
-    ``stages``: TMA ring depth of the partition kernel, 2 or 3 (0 = the plan)."""
+    ``stages``: TMA ring depth of the partition kernel, 2 or 3 (0 = the plan).
+    ``groups``: shared-prefix groups (:class:`PrefixGroups` on the call's device, or in pinned
+    host memory): each group's shared pages are read once for all its sequences.
+    ``prefix_partition``: tokens per partition of a shared prefix (0 = the plan)."""
 
-    def __init__(self, partition: int = 0, stages: int = 0):
+    def __init__(self, partition: int = 0, stages: int = 0, groups: PrefixGroups | None = None,
+                 prefix_partition: int = 0):
         self.partition, self.stages = int(partition), int(stages)
+        self.groups, self.prefix_partition = groups, int(prefix_partition)
 
     def _c(self) -> _Options:
-        return _Options(self.partition, self.stages)
+        g = self.groups
+        if g is None or g.num_groups == 0:
+            return _Options(self.partition, self.stages, 0, 0, 0, self.prefix_partition, None, None, None)
+        for name in ("group_offsets", "group_seqs", "prefix_lens"):
+            t = getattr(g, name)
+            if t.dtype != torch.int32 or not t.is_contiguous():
+                raise ValueError(f"groups.{name} must be contiguous int32")
+        return _Options(self.partition, self.stages, g.num_groups, max(g.max_group_size, 1),
+                        max(g.max_prefix_len, 1), self.prefix_partition, g.group_offsets.data_ptr(),
+                        g.group_seqs.data_ptr(), g.prefix_lens.data_ptr())
 
 
 def _opts(options: DecodeOptions | None):

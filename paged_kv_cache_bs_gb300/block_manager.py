@@ -164,4 +164,5 @@ def prefix_groups(block_tables: torch.Tensor, context_lens: torch.Tensor, block_
     if rc != 0:
         raise PagedAttentionError("pa_prefix_groups", rc)
     g = n.value
-    return PrefixGroups(off[:g + 1].clone(), seqs[:int(off[g])].clone(), pre[:B].clone(), big.value, longest.value)
+    # group_seqs keeps room for B entries (the decode call reads it within [0, batch))
+    return PrefixGroups(off[:g + 1].clone(), seqs[:max(B, 1)].clone(), pre[:B].clone(), big.value, longest.value)

@@ -38,6 +38,8 @@
 //     launch overlaps the kernel before it.
 #include <math.h>
 
+#include <algorithm>
+
 #include <type_traits>
 
 #include "tc_common.cuh"
@@ -61,6 +63,10 @@ constexpr int kMinPartition = 128;
 // workload (64 sequences, context U[128, 4096]): 4 waves (1024-token partitions) beat 8 (512)
 // by 1.4 % on the bf16 pool and by 9 % on the E4M3 pool, whose CTAs stream half the bytes.
 constexpr int kTargetWaves = 4;
+// Tokens per prefix partition of a shared-prefix CTA (its four warps each stream every tile
+// of the partition for their own query rows): short enough that the prefix CTAs, about four
+// times a private CTA's work per tile, do not trail the last wave.
+constexpr int kPrefixPartition = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
@@ -78,8 +84,8 @@ struct DecodeArgs {
     int32_t log2_bs;
     float scale_log2;
     void *out;
-    float *ws_o;     // [B][H_q][max_parts][D]  unnormalised partial outputs
-    float2 *ws_ml;   // [B][H_q][max_parts]     (reference max, sum), log2 domain
+    float *ws_o;     // [B][H_q][slots][D]  unnormalised partial outputs
+    float2 *ws_ml;   // [B][H_q][slots]     (reference max, sum), log2 domain
     int32_t partition;
     int32_t max_parts;
     int32_t *err_flag;
@@ -91,6 +97,17 @@ struct DecodeArgs {
     void *k_cache_w;
     void *v_cache_w;
     float k_scale, v_scale;  // E4M3 pool: K = code * k_scale, V = code * v_scale (1 for 16-bit pools)
+    int32_t batch;
+    // shared prefixes: the first prefix_ctas z indices of the grid are prefix CTAs (0: none)
+    int32_t prefix_ctas;
+    int32_t group_ctas;      // prefix CTAs per group: ceil(largest group / seqs_per_cta)
+    int32_t seqs_per_cta;    // members one prefix CTA serves: 32 query rows / group
+    const int32_t *group_offsets;
+    const int32_t *group_seqs;
+    const int32_t *prefix_lens;  // [batch], or null
+    int32_t pre_partition;   // tokens per prefix partition
+    int32_t pre_parts;       // workspace slots of prefix partials, before the private partitions'
+    int32_t slots;           // workspace slots per (sequence, q head): pre_parts + max_parts
 };
 
 // Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
@@ -187,6 +204,26 @@ __device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t codes) {
     return out;
 }
 
+// One consumer lane's share of the online softmax of two query columns (N indices
+// 2*(lane%4) and +1 of the warp's m16n8 tiles): the unnormalised O^T fragments, the
+// running maxima m, the exponent references mu (m, or 0 while m = -inf) and the sums l.
+template <int D> struct Acc {
+    float o[D / 16][4];
+    float m0, m1, l0, l1, mu0, mu1;
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = mu0 = mu1 = 0.f;
+    }
+};
+
+// K and V fragments of 16 tokens of a stage (F8: V kept as byte-permuted codes).
+template <int D, bool F8> struct Frags {
+    uint32_t kf[D / 16][4];
+    uint32_t vf[F8 ? D / 32 : D / 16][4];
+};
+
 // F8: the pool holds E4M3 codes (one byte per element, D = 128).  K and V are
 // widened to fp16 in registers (exactly: every E4M3 value is an fp16 value)
 // and the warp MMAs run in fp16, q converted once.  ldmatrix moves 16-bit
@@ -198,6 +235,430 @@ __device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t codes) {
 // permutation splits them by d, and row m = lane / 4 of block mt holds
 // d = 16 mt + 2m, row m + 8 holds d = 16 mt + 2m + 1.  V stays in codes until
 // its MMA (fewer live registers).
+template <int D, int kSlices, bool F8>
+__device__ __forceinline__ void load_frags(Frags<D, F8> &f, uint32_t kb, uint32_t vb, int wrow, int lane, int lbr) {
+    const int rk = wrow + (lane & 7) + ((lane >> 3) & 1) * 8, ck = lane >> 4;
+    if constexpr (F8) {
+        // one x4 load covers two 16-byte d chunks of the warp's 16 tokens
+#pragma unroll
+        for (int kp = 0; kp < D / 32; ++kp) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4(kb + tile_off<kSlices>(rk, kp * 2 + ck, lbr), r0, r1, r2, r3);
+            f.kf[2 * kp][0] = e4m3x2_lo(r0);
+            f.kf[2 * kp][1] = e4m3x2_lo(r1);
+            f.kf[2 * kp][2] = e4m3x2_hi(r0);
+            f.kf[2 * kp][3] = e4m3x2_hi(r1);
+            f.kf[2 * kp + 1][0] = e4m3x2_lo(r2);
+            f.kf[2 * kp + 1][1] = e4m3x2_lo(r3);
+            f.kf[2 * kp + 1][2] = e4m3x2_hi(r2);
+            f.kf[2 * kp + 1][3] = e4m3x2_hi(r3);
+            ldmatrix_x4_trans(vb + tile_off<kSlices>(rk, kp * 2 + ck, lbr), r0, r1, r2, r3);
+            // bytes (token 2j, d 2m), (2j, 2m+1), (2j+1, 2m), (2j+1, 2m+1) -> split by d:
+            // bytes 0-1 are tokens 2j, 2j+1 of d 2m, bytes 2-3 those of d 2m+1
+            f.vf[kp][0] = __byte_perm(r0, 0, 0x3120);
+            f.vf[kp][1] = __byte_perm(r1, 0, 0x3120);
+            f.vf[kp][2] = __byte_perm(r2, 0, 0x3120);
+            f.vf[kp][3] = __byte_perm(r3, 0, 0x3120);
+        }
+    } else {
+        const int rv = wrow + (lane & 7) + (lane >> 4) * 8, cv = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+            ldmatrix_x4(kb + tile_off<kSlices>(rk, ks * 2 + ck, lbr), f.kf[ks][0], f.kf[ks][1], f.kf[ks][2], f.kf[ks][3]);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+            ldmatrix_x4_trans(vb + tile_off<kSlices>(rv, mt * 2 + cv, lbr), f.vf[mt][0], f.vf[mt][1], f.vf[mt][2],
+                              f.vf[mt][3]);
+    }
+}
+
+// The online-softmax step over 16 tokens whose first is context position `tok`: S^T = K Q^T,
+// P = exp2(S - mu), O^T += V^T P^T.  Token j counts for column 0 (1) of this lane when
+// j < lim0 (lim1); V rows at or past `end` may hold anything (NaN) and are zeroed.
+template <typename MT, int D, bool F8>
+__device__ __forceinline__ void attend16(Frags<D, F8> &f, Acc<D> &s, const uint32_t (&qb)[D / 16][2], float scale_log2,
+                                         int tok, int end, int lim0, int lim1, int lane) {
+    constexpr int kKSteps = D / 16;
+    // S^T (16 tokens x 8 columns) = K (16 x D) . Q^T (D x 8), independent chains
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < kKSteps; ks += 2) {
+        Mma<MT>::run(sa, f.kf[ks][0], f.kf[ks][1], f.kf[ks][2], f.kf[ks][3], qb[ks][0], qb[ks][1]);
+        Mma<MT>::run(sb, f.kf[ks + 1][0], f.kf[ks + 1][1], f.kf[ks + 1][2], f.kf[ks + 1][3], qb[ks + 1][0],
+                     qb[ks + 1][1]);
+    }
+    // lane holds tokens lane/4 (s0, s1) and lane/4 + 8 (s2, s3) for columns 2*(lane%4), +1
+    float s0 = (sa[0] + sb[0]) * scale_log2, s1 = (sa[1] + sb[1]) * scale_log2;
+    float s2 = (sa[2] + sb[2]) * scale_log2, s3 = (sa[3] + sb[3]) * scale_log2;
+    if (tok + 16 > min(lim0, lim1)) {  // some of these tokens are past a column's context
+        const int j0 = tok + (lane >> 2);
+        if (j0 >= lim0) s0 = -INFINITY;
+        if (j0 >= lim1) s1 = -INFINITY;
+        if (j0 + 8 >= lim0) s2 = -INFINITY;
+        if (j0 + 8 >= lim1) s3 = -INFINITY;
+    }
+    if (tok + 16 > end) {
+        // V rows past the end: zero them in the fragments, whose tokens are 2*(lane%4) + {0, 1}
+        // (regs 0, 1) and + 8 (regs 2, 3)
+        const int jt = tok + (lane & 3) * 2;
+        if constexpr (F8) {  // codes: bytes 0, 2 are token 2j (+8 in regs 1, 3), bytes 1, 3 token 2j+1
+            const uint32_t lo = (jt < end ? 0x00FF00FFu : 0u) | (jt + 1 < end ? 0xFF00FF00u : 0u);
+            const uint32_t hi = (jt + 8 < end ? 0x00FF00FFu : 0u) | (jt + 9 < end ? 0xFF00FF00u : 0u);
+#pragma unroll
+            for (int kp = 0; kp < kKSteps / 2; ++kp) {
+                f.vf[kp][0] &= lo;
+                f.vf[kp][1] &= hi;
+                f.vf[kp][2] &= lo;
+                f.vf[kp][3] &= hi;
+            }
+        } else {
+            const uint32_t lo = (jt < end ? 0xFFFFu : 0u) | (jt + 1 < end ? 0xFFFF0000u : 0u);
+            const uint32_t hi = (jt + 8 < end ? 0xFFFFu : 0u) | (jt + 9 < end ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < kKSteps; ++mt) {
+                f.vf[mt][0] &= lo;
+                f.vf[mt][1] &= lo;
+                f.vf[mt][2] &= hi;
+                f.vf[mt][3] &= hi;
+            }
+        }
+    }
+    // move the reference maximum only when a score exceeds it by more than 2^8
+    const bool grow = fmaxf(s0, s2) > s.m0 + kRescaleThreshold || fmaxf(s1, s3) > s.m1 + kRescaleThreshold;
+    if (__any_sync(0xffffffffu, grow)) {
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        mx0 = warp_max_xor(mx0, 4);
+        mx1 = warp_max_xor(mx1, 4);
+        mx0 = warp_max_xor(mx0, 8);
+        mx1 = warp_max_xor(mx1, 8);
+        mx0 = warp_max_xor(mx0, 16);
+        mx1 = warp_max_xor(mx1, 16);
+        const float mn0 = fmaxf(s.m0, mx0), mn1 = fmaxf(s.m1, mx1);
+        const float nu0 = mn0 == -INFINITY ? 0.f : mn0;  // all masked so far: keep exp2 finite
+        const float nu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float c0 = tc::ex2_approx(s.mu0 - nu0), c1 = tc::ex2_approx(s.mu1 - nu1);
+        s.l0 *= c0;
+        s.l1 *= c1;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            s.o[mt][0] *= c0;
+            s.o[mt][1] *= c1;
+            s.o[mt][2] *= c0;
+            s.o[mt][3] *= c1;
+        }
+        s.m0 = mn0;
+        s.m1 = mn1;
+        s.mu0 = nu0;
+        s.mu1 = nu1;
+    }
+    const float p0 = tc::ex2_approx(s0 - s.mu0), p1 = tc::ex2_approx(s1 - s.mu1);
+    const float p2 = tc::ex2_approx(s2 - s.mu0), p3 = tc::ex2_approx(s3 - s.mu1);
+    s.l0 += p0 + p2;
+    s.l1 += p1 + p3;
+    // P^T as the B operand (16 tokens x 8 columns): transpose the two 8x8 halves
+    const uint32_t pb0 = movmatrix_trans(Dt<MT>::pack(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(Dt<MT>::pack(p2, p3));
+    // O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 x 8)
+    if constexpr (F8) {
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            const uint32_t pa = f.vf[mt >> 1][(mt & 1) * 2], pc = f.vf[mt >> 1][(mt & 1) * 2 + 1];
+            Mma<MT>::run(s.o[mt], e4m3x2_lo(pa), e4m3x2_hi(pa), e4m3x2_lo(pc), e4m3x2_hi(pc), pb0, pb1);
+        }
+    } else {
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt)
+            Mma<MT>::run(s.o[mt], f.vf[mt][0], f.vf[mt][1], f.vf[mt][2], f.vf[mt][3], pb0, pb1);
+    }
+}
+
+// The producer thread's loop: each 64-token tile of context positions [start, end) into the
+// ring, one TMA box per page (or per 64 rows of a longer page) and kv-head row slice.  bt_s
+// holds the physical pages of logical pages first_page, first_page + 1, ...  Returns the tiles
+// started (a wait that gave up stops the loop, flagged).
+template <int D, int ST, bool F8>
+__device__ __forceinline__ int produce_tiles(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                             const CUtensorMap *tm_k_tail, const CUtensorMap *tm_v_tail,
+                                             const DecodeArgs &a, int g, int start, int end, int first_page,
+                                             const int32_t *bt_s, uint32_t ring, uint32_t bars,
+                                             volatile int *abort_s) {
+    using S = Shape<D, ST, F8>;
+    constexpr int kStages = ST;
+    const int ntiles = (end - start + kTile - 1) / kTile;
+    const int box_rows = min(1 << a.log2_bs, kTile);
+    const int bs_mask = (1 << a.log2_bs) - 1;
+    int issued = 0;
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages &&
+            !tc::mbar_wait_or_abort(bars + 8 * (kStages + s), ((t / kStages) - 1) & 1, kWaitCycles, abort_s)) {
+            raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
+            break;
+        }
+        const int tile_start = start + t * kTile;
+        const int valid = min(kTile, end - tile_start);
+        const uint32_t full = bars + 8 * s;
+        const uint32_t kdst = ring + s * S::kStageBytes;
+        const uint32_t vdst = kdst + S::kTileBytes;
+        if (valid < kTile && box_rows == kTile) {
+            // the context ends inside this tile of one page: fetch it in 16-row boxes up to the
+            // end instead of a whole 64-row box (rows past the end are masked either way)
+            constexpr int kTailRows = 16;
+            const int nsub = (valid + kTailRows - 1) / kTailRows;
+            tc::mbar_arrive_expect_tx(full, nsub * kTailRows * S::kRowBytes * 2);
+            const int y0 = (bt_s[(tile_start >> a.log2_bs) - first_page] << a.log2_bs) + (tile_start & bs_mask);
+            for (int i = 0; i < nsub; ++i) {
+#pragma unroll
+                for (int h = 0; h < S::kSlices; ++h) {
+                    const int x = g * D + h * (F8 ? 128 : 64);  // elements: 128 bytes per slice
+                    const uint32_t off = h * (kTile * 128) + i * kTailRows * 128;
+                    tc::tma_load_2d(kdst + off, tm_k_tail, x, y0 + i * kTailRows, full);
+                    tc::tma_load_2d(vdst + off, tm_v_tail, x, y0 + i * kTailRows, full);
+                }
+            }
+            issued = t + 1;
+            continue;
+        }
+        const int nbox = (valid + box_rows - 1) / box_rows;
+        tc::mbar_arrive_expect_tx(full, nbox * box_rows * S::kRowBytes * 2);
+        for (int i = 0; i < nbox; ++i) {
+            const int j = tile_start + i * box_rows;
+            const int y = (bt_s[(j >> a.log2_bs) - first_page] << a.log2_bs) + (j & bs_mask);
+            const uint32_t box_off = i * box_rows * 128 * S::kSlices;
+            if constexpr (S::kSlices == 1) {
+                const int x = g * D;  // elements: one 128-byte slice holds the kv head's row
+                tc::tma_load_2d(kdst + box_off, tm_k, x, y, full);
+                tc::tma_load_2d(vdst + box_off, tm_v, x, y, full);
+            } else {
+                // both 128-byte slices of the kv head's rows in one 3-D box, slice by slice
+                tc::tma_load_3d(kdst + box_off, tm_k, 0, y, g * S::kSlices, full);
+                tc::tma_load_3d(vdst + box_off, tm_v, 0, y, g * S::kSlices, full);
+            }
+        }
+        issued = t + 1;
+    }
+    return issued;
+}
+
+// After a wait gave up: let every load this CTA started land before the CTA leaves.
+template <int ST> __device__ __forceinline__ void drain(uint32_t bars, int issued) {
+    for (int s = 0; s < ST && s < issued; ++s) {
+        const int t_last = s + ST * ((issued - 1 - s) / ST);
+        tc::mbar_wait(bars + 8 * s, (t_last / ST) & 1, kWaitCycles);
+    }
+}
+
+// Loads the block-table entries of logical pages [first_page, first_page + span) of
+// `table` (a sequence's row) into registers, one memory round trip for the CTA.
+constexpr int kPerThread = (kMaxTablePages + kThreads - 1) / kThreads;
+__device__ __forceinline__ void prefetch_table(int (&pg)[kPerThread], const int32_t *table, int first_page, int span,
+                                               int tid) {
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int i = tid + k * kThreads;
+        pg[k] = i < span ? table[first_page + i] : 0;
+    }
+}
+
+// Stores the first npages prefetched entries into the shared slice, a bad id flagged and
+// read as page 0.
+__device__ __forceinline__ void publish_table(const int (&pg)[kPerThread], int32_t *bt_s, int npages,
+                                              const DecodeArgs &a, int tid) {
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int i = tid + k * kThreads;
+        if (i < npages) {
+            int p = pg[k];
+            if (p < 0 || p >= a.num_blocks) {
+                raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
+                p = 0;
+            }
+            bt_s[i] = p;
+        }
+    }
+}
+
+// Tokens at the start of sequence b's context that its group's prefix CTAs read (0: not
+// grouped), clamped to what the workspace holds; a length that is no whole number of pages
+// or not below the context is flagged (the descriptor is the caller's).
+__device__ __forceinline__ int shared_prefix(const DecodeArgs &a, int b, int L, bool flag) {
+    if (!a.prefix_lens) return 0;
+    const int P = a.prefix_lens[b];
+    if (P <= 0) return 0;
+    if (flag && ((P & ((1 << a.log2_bs) - 1)) || P >= L)) raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
+    return min(P, min(a.pre_parts * a.pre_partition, a.max_blocks << a.log2_bs));
+}
+
+// The prefix role of the partition kernel: one CTA per (group chunk, kv head, prefix
+// partition) streams the group's shared pages once for up to 32 query rows -- the G heads of
+// up to 32 / G member sequences -- and writes each row's softmax partial to the workspace.
+// Warp w owns rows 8w .. 8w+7 (the N dimension of its MMAs) and walks every 16-token slice of
+// each tile; row r is head r % G of the chunk's member r / G.
+template <typename T, int D, int ST>
+__device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                                 const CUtensorMap *tm_k_tail, const CUtensorMap *tm_v_tail,
+                                                 const DecodeArgs &a, uint8_t *smem) {
+    using S = Shape<D, ST, false>;
+    constexpr int kStages = ST;
+    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t bars = smem_u32(smem + S::kBarOff);
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
+    const int pp = blockIdx.x, g = blockIdx.y;
+    const int gi = blockIdx.z / a.group_ctas, chunk = blockIdx.z % a.group_ctas;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    const int off0 = a.group_offsets[gi], off1 = a.group_offsets[gi + 1];
+    if (off0 < 0 || off1 > a.batch || off0 > off1) {  // group_seqs has room for batch entries
+        if (tid == 0 && pp == 0 && g == 0 && chunk == 0) raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
+        return;
+    }
+    const int m0 = off0 + chunk * a.seqs_per_cta;
+    const int nm = min(a.seqs_per_cta, off1 - m0);  // members of this chunk
+    if (nm <= 0) return;
+    const int leader = a.group_seqs[off0];
+    const int start = pp * a.pre_partition;
+    const int first_page = start >> a.log2_bs;
+    const int span = min(a.max_blocks, ((start + a.pre_partition - 1) >> a.log2_bs) + 1) - first_page;
+    int pg_pre[kPerThread];
+    if (leader >= 0 && leader < a.batch)
+        prefetch_table(pg_pre, a.block_tables + static_cast<int64_t>(leader) * a.max_blocks, first_page, span, tid);
+    if (leader < 0 || leader >= a.batch) {
+        if (tid == 0 && pp == 0 && g == 0) raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
+        return;
+    }
+    const int Ll = max(context_len(a, leader), 0);
+    const int P = shared_prefix(a, leader, Ll, false);
+    const int end = min(start + a.pre_partition, P);
+    if (start >= end) return;
+    const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;
+
+    publish_table(pg_pre, bt_s, npages, a, tid);
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(bars + 8 * s, 1);
+            tc::mbar_init(bars + 8 * (kStages + s), kConsumerWarps);
+        }
+        *abort_s = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tc::prefetch_tmap(tm_k);
+        tc::prefetch_tmap(tm_v);
+    }
+    __syncthreads();  // table slice, barriers ready
+
+    Acc<D> acc;
+    acc.init();
+    int issued = 0;
+    const int ntiles = (end - start + kTile - 1) / kTile;
+    // this lane's two columns (rows rc0, rc0 + 1) and its B-operand row rq: member sequences
+    // and their context limits (loaded by the consumers while the first tile is in flight)
+    const int G = a.group;
+    const int rc0 = 8 * warp + 2 * (lane & 3), rq = 8 * warp + (lane >> 2);
+    int b0 = -1, b1 = -1;
+    if (warp == kProducerWarp) {
+        if (lane == 0)
+            issued = produce_tiles<D, ST, false>(tm_k, tm_v, tm_k_tail, tm_v_tail, a, g, start, end, first_page, bt_s,
+                                                 ring, bars, abort_s);
+    } else {
+        auto member = [&](int r) -> int {
+            const int mi = r / G;
+            if (mi >= nm) return -1;
+            const int b = a.group_seqs[m0 + mi];
+            return (b >= 0 && b < a.batch) ? b : -1;
+        };
+        b0 = member(rc0);
+        b1 = member(rc0 + 1);
+        const int bq = member(rq);
+        const int lim0 = b0 >= 0 ? min(P, max(context_len(a, b0), 0)) : 0;
+        const int lim1 = b1 >= 0 ? min(P, max(context_len(a, b1), 0)) : 0;
+        // query fragments (B operand of S^T = K Q^T): row rq's head
+        uint32_t qb[D / 16][2];
+        const int dq = (lane & 3) * 2;
+        const T *qrow = bq >= 0 ? static_cast<const T *>(a.q) + static_cast<int64_t>(bq) * a.q_row_stride +
+                                      static_cast<int64_t>(g * G + rq % G) * D
+                                : nullptr;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            if (qrow) {
+                qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + dq);
+                qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + dq);
+            } else {
+                qb[ks][0] = qb[ks][1] = 0u;
+            }
+        }
+        const int lbr = min(a.log2_bs, 6);
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % kStages;
+            const bool ok = tc::mbar_wait_or_abort(bars + 8 * s, (t / kStages) & 1, kWaitCycles, abort_s);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
+                break;
+            }
+            const uint32_t kb = ring + s * S::kStageBytes;
+            const uint32_t vb = kb + S::kTileBytes;
+            const int tile_start = start + t * kTile;
+#pragma unroll 1
+            for (int u = 0; u < kTile / 16; ++u) {
+                if (tile_start + 16 * u >= end) break;
+                Frags<D, false> f;
+                load_frags<D, S::kSlices, false>(f, kb, vb, 16 * u, lane, lbr);
+                attend16<T, D, false>(f, acc, qb, a.scale_log2, tile_start + 16 * u, end, lim0, lim1, lane);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bars + 8 * (kStages + s));  // stage free for the next tile
+        }
+    }
+    // the caller's descriptor: every member of the chunk shares the leader's pages of this
+    // partition (checked once, by the first kv head's CTAs), reads the same prefix and has
+    // tokens after it
+    if (g == 0) {
+        for (int i = tid; i < nm * npages; i += kThreads) {
+            const int b = a.group_seqs[m0 + i / npages];
+            if (b < 0 || b >= a.batch ||
+                a.block_tables[static_cast<int64_t>(b) * a.max_blocks + first_page + i % npages] != bt_s[i % npages])
+                raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
+        }
+        if (pp == 0 && tid < nm) {
+            const int b = a.group_seqs[m0 + tid];
+            if (b < 0 || b >= a.batch || a.prefix_lens[b] != a.prefix_lens[leader] || context_len(a, b) <= P)
+                raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
+        }
+    }
+    __syncthreads();
+    if (*abort_s) {
+        if (warp == kProducerWarp && lane == 0) drain<ST>(bars, issued);
+        return;
+    }
+    if (warp >= kConsumerWarps) return;
+    // each warp writes its own rows' partials: (reference max, sum) and the unnormalised O
+    acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 4);
+    acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 4);
+    acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 8);
+    acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 8);
+    acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 16);
+    acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 16);
+    const int dr = lane >> 2;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int b = c ? b1 : b0;
+        if (b < 0) continue;
+        const int hq = g * G + (rc0 + c) % G;
+        const int64_t idx = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.slots + pp;
+        float *o = a.ws_o + idx * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            o[mt * 16 + dr] = acc.o[mt][c];
+            o[mt * 16 + dr + 8] = acc.o[mt][c + 2];
+        }
+        if (dr == 0) {
+            const float m = c ? acc.m1 : acc.m0;
+            a.ws_ml[idx] = make_float2(m == -INFINITY ? -INFINITY : (c ? acc.mu1 : acc.mu0), c ? acc.l1 : acc.l0);
+        }
+    }
+}
+
 template <typename T, int D, int ST, bool F8>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -208,66 +669,64 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     constexpr int kStages = ST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
-    const uint32_t ring = smem_u32(smem);
-    const uint32_t bars = smem_u32(smem + S::kBarOff);  // full[s] at 8s, empty[s] at 8(kStages + s)
-    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
-
-    const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // Launched as a programmatic dependent of the previous kernel on the stream (the store
     // of this step): wait for it to finish before reading the cache, and let the merge
     // kernel be launched right away (it waits for this grid itself).
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    if constexpr (!F8) {
+        if (blockIdx.z < a.prefix_ctas) {  // the first z indices: shared-prefix CTAs
+            prefix_partition<T, D, ST>(&tm_k, &tm_v, &tm_k_tail, &tm_v_tail, a, smem);
+            return;
+        }
+    }
+    int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t bars = smem_u32(smem + S::kBarOff);  // full[s] at 8s, empty[s] at 8(kStages + s)
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
+
+    const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z - a.prefix_ctas;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // The block-table entries this partition can touch are loaded together with the context
     // length (one memory round trip before the first TMA instead of two); entries past the
     // context are loaded (they lie inside the table's row) but never used.
-    const int start = p * a.partition;
-    const int first_page = start >> a.log2_bs;
-    const int span = min(a.max_blocks, ((start + a.partition - 1) >> a.log2_bs) + 1) - first_page;
-    constexpr int kPerThread = (kMaxTablePages + kThreads - 1) / kThreads;
+    const int part_start = p * a.partition;
+    const int first_page = part_start >> a.log2_bs;
+    const int span = min(a.max_blocks, ((part_start + a.partition - 1) >> a.log2_bs) + 1) - first_page;
     int pg_pre[kPerThread];
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-        const int i = tid + k * kThreads;
-        pg_pre[k] = i < span ? a.block_tables[static_cast<int64_t>(b) * a.max_blocks + first_page + i] : 0;
-    }
+    prefetch_table(pg_pre, a.block_tables + static_cast<int64_t>(b) * a.max_blocks, first_page, span, tid);
     int L = context_len(a, b);
     if (L < 0) {
         if (p == 0 && tid == 0) raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
         L = 0;
     }
+    // a shared prefix [0, ps) is read by the group's prefix CTAs: this partition covers the
+    // rest of [part_start, part_start + partition)
+    const int P = shared_prefix(a, b, L, p == 0 && g == 0 && tid == 0);
+    const int ps = min(P, L);
+    const int start = max(part_start, ps);
     T *out = static_cast<T *>(a.out);
-    if (start >= L) {
-        if (p == 0) {  // empty context (e.g. a padding row): zero output, no page read
+    if (start >= min(part_start + a.partition, L)) {
+        if (p == 0 && L == 0) {  // empty context (e.g. a padding row): zero output, no page read
             for (int i = tid; i < a.group * D; i += kThreads)
                 out[(static_cast<int64_t>(b) * a.num_q_heads + g * a.group + i / D) * D + i % D] =
                     Dt<T>::from_float(0.f);
-            if (a.slot_mapping && g == 0 && tid == 0 && a.slot_mapping[b] != -1)
-                raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);  // a new token needs a context position
         }
+        // a new token needs a context position outside the shared prefix
+        if (a.slot_mapping && g == 0 && tid == 0 && (L == 0 ? p == 0 : (L - 1) / a.partition == p) &&
+            a.slot_mapping[b] != -1)
+            raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);
         return;
     }
-    const int end = min(L, start + a.partition);
-    const int nparts = (L + a.partition - 1) / a.partition;
+    const int end = min(L, part_start + a.partition);
+    // this sequence's partials: its prefix partitions, then its private partitions
+    const bool direct = P == 0 && (L + a.partition - 1) / a.partition == 1;
     const int ntiles = (end - start + kTile - 1) / kTile;
 
     // block-table slice of this partition, validated once (a bad id is flagged and read as page 0)
     const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;  // <= span
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-        const int i = tid + k * kThreads;
-        if (i < npages) {
-            int pg = pg_pre[k];
-            if (pg < 0 || pg >= a.num_blocks) {
-                raise_flag(a.err_flag, PA_FLAG_BAD_BLOCK);
-                pg = 0;
-            }
-            bt_s[i] = pg;
-        }
-    }
+    publish_table(pg_pre, bt_s, npages, a, tid);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(bars + 8 * s, 1);
@@ -314,73 +773,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     }
     __syncthreads();  // table slice, barriers ready
 
-    float o[S::kKSteps][4];
-#pragma unroll
-    for (int mt = 0; mt < S::kKSteps; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*(lane%4) and +1
-    float mu0 = 0.f, mu1 = 0.f;                                 // exponent references (m, or 0 while m = -inf)
-    int issued = 0;                                             // tiles the producer started
+    Acc<D> acc;
+    acc.init();
+    int issued = 0;  // tiles the producer started
 
     if (warp == kProducerWarp) {
         if (a.slot_mapping && end == L) store_new_row<T, D, F8>(a, b, g, L, lane);
-        if (lane == 0) {
-            const int box_rows = min(1 << a.log2_bs, kTile);
-            const int bs_mask = (1 << a.log2_bs) - 1;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % kStages;
-                if (t >= kStages &&
-                    !tc::mbar_wait_or_abort(bars + 8 * (kStages + s), ((t / kStages) - 1) & 1, kWaitCycles, abort_s)) {
-                    raise_flag(a.err_flag, PA_FLAG_TIMEOUT);
-                    break;
-                }
-                const int tile_start = start + t * kTile;
-                const int valid = min(kTile, end - tile_start);
-                const uint32_t full = bars + 8 * s;
-                const uint32_t kdst = ring + s * S::kStageBytes;
-                const uint32_t vdst = kdst + S::kTileBytes;
-                if (valid < kTile && box_rows == kTile) {
-                    // the context ends inside this tile of one page: fetch it in 16-row boxes up to the
-                    // end instead of a whole 64-row box (rows past the end are masked either way)
-                    constexpr int kTailRows = 16;
-                    const int nsub = (valid + kTailRows - 1) / kTailRows;
-                    tc::mbar_arrive_expect_tx(full, nsub * kTailRows * S::kRowBytes * 2);
-                    const int y0 = (bt_s[(tile_start >> a.log2_bs) - first_page] << a.log2_bs) + (tile_start & bs_mask);
-                    for (int i = 0; i < nsub; ++i) {
-#pragma unroll
-                        for (int h = 0; h < S::kSlices; ++h) {
-                            const int x = g * D + h * (F8 ? 128 : 64);  // elements: 128 bytes per slice
-                            const uint32_t off = h * (kTile * 128) + i * kTailRows * 128;
-                            tc::tma_load_2d(kdst + off, &tm_k_tail, x, y0 + i * kTailRows, full);
-                            tc::tma_load_2d(vdst + off, &tm_v_tail, x, y0 + i * kTailRows, full);
-                        }
-                    }
-                    issued = t + 1;
-                    continue;
-                }
-                const int nbox = (valid + box_rows - 1) / box_rows;
-                tc::mbar_arrive_expect_tx(full, nbox * box_rows * S::kRowBytes * 2);
-                for (int i = 0; i < nbox; ++i) {
-                    const int j = tile_start + i * box_rows;
-                    const int y = (bt_s[(j >> a.log2_bs) - first_page] << a.log2_bs) + (j & bs_mask);
-                    const uint32_t box_off = i * box_rows * 128 * S::kSlices;
-                    if constexpr (S::kSlices == 1) {
-                        const int x = g * D;  // elements: one 128-byte slice holds the kv head's row
-                        tc::tma_load_2d(kdst + box_off, &tm_k, x, y, full);
-                        tc::tma_load_2d(vdst + box_off, &tm_v, x, y, full);
-                    } else {
-                        // both 128-byte slices of the kv head's rows in one 3-D box, slice by slice
-                        tc::tma_load_3d(kdst + box_off, &tm_k, 0, y, g * S::kSlices, full);
-                        tc::tma_load_3d(vdst + box_off, &tm_v, 0, y, g * S::kSlices, full);
-                    }
-                }
-                issued = t + 1;
-            }
-        }
+        if (lane == 0)
+            issued = produce_tiles<D, ST, F8>(&tm_k, &tm_v, &tm_k_tail, &tm_v_tail, a, g, start, end, first_page, bt_s,
+                                              ring, bars, abort_s);
     } else {
-        const int wrow = warp * 16;
         const int lbr = min(a.log2_bs, 6);  // log2 of the rows of one TMA box (at most the 64-row tile)
-        const int rk = wrow + (lane & 7) + ((lane >> 3) & 1) * 8, ck = lane >> 4;
-        const int rv = wrow + (lane & 7) + (lane >> 4) * 8, cv = (lane >> 3) & 1;
+        const int wrow = warp * 16;
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kStages;
             const bool ok = tc::mbar_wait_or_abort(bars + 8 * s, (t / kStages) & 1, kWaitCycles, abort_s);
@@ -390,139 +794,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
             }
             const uint32_t kb = ring + s * S::kStageBytes;
             const uint32_t vb = kb + S::kTileBytes;
-            uint32_t kf[S::kKSteps][4];
-            uint32_t vf[F8 ? S::kKSteps / 2 : S::kKSteps][4];  // F8: byte-permuted codes, widened at the MMA
-            if constexpr (F8) {
-                // one x4 load covers two 16-byte d chunks of the warp's 16 tokens
-#pragma unroll
-                for (int kp = 0; kp < S::kKSteps / 2; ++kp) {
-                    uint32_t r0, r1, r2, r3;
-                    ldmatrix_x4(kb + tile_off<S::kSlices>(rk, kp * 2 + ck, lbr), r0, r1, r2, r3);
-                    kf[2 * kp][0] = e4m3x2_lo(r0);
-                    kf[2 * kp][1] = e4m3x2_lo(r1);
-                    kf[2 * kp][2] = e4m3x2_hi(r0);
-                    kf[2 * kp][3] = e4m3x2_hi(r1);
-                    kf[2 * kp + 1][0] = e4m3x2_lo(r2);
-                    kf[2 * kp + 1][1] = e4m3x2_lo(r3);
-                    kf[2 * kp + 1][2] = e4m3x2_hi(r2);
-                    kf[2 * kp + 1][3] = e4m3x2_hi(r3);
-                    ldmatrix_x4_trans(vb + tile_off<S::kSlices>(rk, kp * 2 + ck, lbr), r0, r1, r2, r3);
-                    // bytes (token 2j, d 2m), (2j, 2m+1), (2j+1, 2m), (2j+1, 2m+1) -> split by d:
-                    // bytes 0-1 are tokens 2j, 2j+1 of d 2m, bytes 2-3 those of d 2m+1
-                    vf[kp][0] = __byte_perm(r0, 0, 0x3120);
-                    vf[kp][1] = __byte_perm(r1, 0, 0x3120);
-                    vf[kp][2] = __byte_perm(r2, 0, 0x3120);
-                    vf[kp][3] = __byte_perm(r3, 0, 0x3120);
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < S::kKSteps; ++ks)
-                    ldmatrix_x4(kb + tile_off<S::kSlices>(rk, ks * 2 + ck, lbr), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
-#pragma unroll
-                for (int mt = 0; mt < S::kKSteps; ++mt)
-                    ldmatrix_x4_trans(vb + tile_off<S::kSlices>(rv, mt * 2 + cv, lbr), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
-            }
+            Frags<D, F8> f;
+            load_frags<D, S::kSlices, F8>(f, kb, vb, wrow, lane, lbr);
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bars + 8 * (kStages + s));  // stage free for the next tile
-
-            // S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8), independent chains
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < S::kKSteps; ks += 2) {
-                Mma<MT>::run(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qb[ks][0], qb[ks][1]);
-                Mma<MT>::run(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3], qb[ks + 1][0],
-                             qb[ks + 1][1]);
-            }
-            // lane holds tokens lane/4 (s0, s1) and lane/4 + 8 (s2, s3) for heads 2*(lane%4), +1
-            float s0 = (sa[0] + sb[0]) * a.scale_log2, s1 = (sa[1] + sb[1]) * a.scale_log2;
-            float s2 = (sa[2] + sb[2]) * a.scale_log2, s3 = (sa[3] + sb[3]) * a.scale_log2;
-            const int tile_start = start + t * kTile;
-            if (tile_start + kTile > end) {  // last tile, partly past the context
-                const int j0 = tile_start + wrow + (lane >> 2);
-                if (j0 >= end) s0 = s1 = -INFINITY;
-                if (j0 + 8 >= end) s2 = s3 = -INFINITY;
-                // V rows past the end may hold anything (NaN): zero them in the fragments,
-                // whose tokens are 2*(lane%4) + {0, 1} (regs 0, 1) and + 8 (regs 2, 3)
-                const int jt = tile_start + wrow + (lane & 3) * 2;
-                if constexpr (F8) {  // codes: bytes 0, 2 are token 2j (+8 in regs 1, 3), bytes 1, 3 token 2j+1
-                    const uint32_t lo = (jt < end ? 0x00FF00FFu : 0u) | (jt + 1 < end ? 0xFF00FF00u : 0u);
-                    const uint32_t hi = (jt + 8 < end ? 0x00FF00FFu : 0u) | (jt + 9 < end ? 0xFF00FF00u : 0u);
-#pragma unroll
-                    for (int kp = 0; kp < S::kKSteps / 2; ++kp) {
-                        vf[kp][0] &= lo;
-                        vf[kp][1] &= hi;
-                        vf[kp][2] &= lo;
-                        vf[kp][3] &= hi;
-                    }
-                } else {
-                    const uint32_t lo = (jt < end ? 0xFFFFu : 0u) | (jt + 1 < end ? 0xFFFF0000u : 0u);
-                    const uint32_t hi = (jt + 8 < end ? 0xFFFFu : 0u) | (jt + 9 < end ? 0xFFFF0000u : 0u);
-#pragma unroll
-                    for (int mt = 0; mt < S::kKSteps; ++mt) {
-                        vf[mt][0] &= lo;
-                        vf[mt][1] &= lo;
-                        vf[mt][2] &= hi;
-                        vf[mt][3] &= hi;
-                    }
-                }
-            }
-            // move the reference maximum only when a score exceeds it by more than 2^8
-            const bool grow = fmaxf(s0, s2) > m0 + kRescaleThreshold || fmaxf(s1, s3) > m1 + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, grow)) {
-                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-                mx0 = warp_max_xor(mx0, 4);
-                mx1 = warp_max_xor(mx1, 4);
-                mx0 = warp_max_xor(mx0, 8);
-                mx1 = warp_max_xor(mx1, 8);
-                mx0 = warp_max_xor(mx0, 16);
-                mx1 = warp_max_xor(mx1, 16);
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float nu0 = mn0 == -INFINITY ? 0.f : mn0;  // all masked so far: keep exp2 finite
-                const float nu1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float c0 = tc::ex2_approx(mu0 - nu0), c1 = tc::ex2_approx(mu1 - nu1);
-                l0 *= c0;
-                l1 *= c1;
-#pragma unroll
-                for (int mt = 0; mt < S::kKSteps; ++mt) {
-                    o[mt][0] *= c0;
-                    o[mt][1] *= c1;
-                    o[mt][2] *= c0;
-                    o[mt][3] *= c1;
-                }
-                m0 = mn0;
-                m1 = mn1;
-                mu0 = nu0;
-                mu1 = nu1;
-            }
-            const float p0 = tc::ex2_approx(s0 - mu0), p1 = tc::ex2_approx(s1 - mu1);
-            const float p2 = tc::ex2_approx(s2 - mu0), p3 = tc::ex2_approx(s3 - mu1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // P^T as the B operand (16 tokens x 8 heads): transpose the two 8x8 halves
-            const uint32_t pb0 = movmatrix_trans(Dt<MT>::pack(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(Dt<MT>::pack(p2, p3));
-            // O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 x 8)
-            if constexpr (F8) {
-#pragma unroll
-                for (int mt = 0; mt < S::kKSteps; ++mt) {
-                    const uint32_t pa = vf[mt >> 1][(mt & 1) * 2], pc = vf[mt >> 1][(mt & 1) * 2 + 1];
-                    Mma<MT>::run(o[mt], e4m3x2_lo(pa), e4m3x2_hi(pa), e4m3x2_lo(pc), e4m3x2_hi(pc), pb0, pb1);
-                }
-            } else {
-#pragma unroll
-                for (int mt = 0; mt < S::kKSteps; ++mt)
-                    Mma<MT>::run(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
-            }
+            attend16<MT, D, F8>(f, acc, qb, a.scale_log2, start + t * kTile + wrow, end, end, end, lane);
         }
     }
     __syncthreads();
     if (*abort_s) {
         // a wait gave up (flagged above): let every load this CTA started land, then leave
-        if (warp == kProducerWarp && lane == 0)
-            for (int s = 0; s < kStages && s < issued; ++s) {
-                const int t_last = s + kStages * ((issued - 1 - s) / kStages);
-                tc::mbar_wait(bars + 8 * s, (t_last / kStages) & 1, kWaitCycles);
-            }
+        if (warp == kProducerWarp && lane == 0) drain<ST>(bars, issued);
         return;
     }
 
@@ -531,12 +813,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     float *mm = mo + kConsumerWarps * 8 * D;        // [warp][head 8]  reference max
     float *ml = mm + kConsumerWarps * 8;            // [warp][head 8]  sum
     if (warp < kConsumerWarps) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 4);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 4);
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 8);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 8);
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 16);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 16);
         const int h0 = (lane & 3) * 2;
         const int dr = lane >> 2;
         // the two d of this lane's O^T fragment rows (see the F8 permutation above)
@@ -544,16 +826,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
         float *w = mo + warp * 8 * D;
 #pragma unroll
         for (int mt = 0; mt < S::kKSteps; ++mt) {
-            w[h0 * D + mt * 16 + d_lo] = o[mt][0];
-            w[(h0 + 1) * D + mt * 16 + d_lo] = o[mt][1];
-            w[h0 * D + mt * 16 + d_hi] = o[mt][2];
-            w[(h0 + 1) * D + mt * 16 + d_hi] = o[mt][3];
+            w[h0 * D + mt * 16 + d_lo] = acc.o[mt][0];
+            w[(h0 + 1) * D + mt * 16 + d_lo] = acc.o[mt][1];
+            w[h0 * D + mt * 16 + d_hi] = acc.o[mt][2];
+            w[(h0 + 1) * D + mt * 16 + d_hi] = acc.o[mt][3];
         }
         if (lane < 4) {  // a warp whose tokens were all masked has m = -inf and sum 0: weight 0 below
-            mm[warp * 8 + h0] = m0 == -INFINITY ? -INFINITY : mu0;
-            mm[warp * 8 + h0 + 1] = m1 == -INFINITY ? -INFINITY : mu1;
-            ml[warp * 8 + h0] = l0;
-            ml[warp * 8 + h0 + 1] = l1;
+            mm[warp * 8 + h0] = acc.m0 == -INFINITY ? -INFINITY : acc.mu0;
+            mm[warp * 8 + h0 + 1] = acc.m1 == -INFINITY ? -INFINITY : acc.mu1;
+            ml[warp * 8 + h0] = acc.l0;
+            ml[warp * 8 + h0 + 1] = acc.l1;
         }
     }
     __syncthreads();
@@ -563,50 +845,58 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + h]);
-        float acc = 0.f, sum = 0.f;
+        float accv = 0.f, sum = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
             const float wt = exp2f(mm[w * 8 + h] - M);  // a warp with no token has max -inf: weight 0
-            acc += mo[(w * 8 + h) * D + d] * wt;
+            accv += mo[(w * 8 + h) * D + d] * wt;
             sum += ml[w * 8 + h] * wt;
         }
-        if constexpr (F8) acc *= a.v_scale;
+        if constexpr (F8) accv *= a.v_scale;
         const int hq = g * a.group + h;
-        if (nparts == 1) {
-            out[(static_cast<int64_t>(b) * a.num_q_heads + hq) * D + d] = Dt<T>::from_float(acc / sum);
+        if (direct) {
+            out[(static_cast<int64_t>(b) * a.num_q_heads + hq) * D + d] = Dt<T>::from_float(accv / sum);
         } else {
-            const int64_t idx = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.max_parts + p;
-            a.ws_o[idx * D + d] = acc;
+            const int64_t idx = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.slots + a.pre_parts + p;
+            a.ws_o[idx * D + d] = accv;
             if (d == 0) a.ws_ml[idx] = make_float2(M, sum);
         }
     }
 }
 
-// Log-sum-exp merge of the partitions of sequences that have more than one.
-// The partials are loaded eight partitions at a time and folded in with an
-// online maximum: one memory round trip per eight partitions.
+// Log-sum-exp merge of the partials of sequences that have more than one: the prefix
+// partitions' (slots [0, prefix partitions)) and the private partitions' (slot pre_parts + p
+// for partition p).  The partials are loaded eight at a time and folded in with an online
+// maximum: one memory round trip per eight partials.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
     constexpr int kBatch = 8;
     const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-    // context_lens is an input of the call: this grid launches only after every partition
-    // CTA has passed its own wait on the previous kernel, so it may be read before the wait
+    // context_lens and prefix_lens are inputs of the call: this grid launches only after every
+    // partition CTA has passed its own wait on the previous kernel, so they may be read before
+    // the wait
     const int L = max(context_len(a, b), 0);
-    const int np = (L + a.partition - 1) / a.partition;
-    if (np <= 1) return;
+    const int P = shared_prefix(a, b, L, false);
+    const int ps = min(P, L);
+    const int npre = P > 0 ? (P + a.pre_partition - 1) / a.pre_partition : 0;
+    const int p_lo = ps / a.partition, p_hi = ps < L ? (L + a.partition - 1) / a.partition : p_lo;
+    const int n = npre + (p_hi - p_lo);
+    if (npre == 0 && p_hi - p_lo <= 1) return;  // written by its only partition
     // launched early (programmatic dependent launch): wait until the partition grid has
     // finished and its partials are visible
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    const int64_t base = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.max_parts;
+    const int64_t base = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.slots;
     float M = -INFINITY, acc = 0.f, sum = 0.f;
-    for (int p0 = 0; p0 < np; p0 += kBatch) {
+    for (int i0 = 0; i0 < n; i0 += kBatch) {
         float2 ml[kBatch];
         float o[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            if (p0 + j < np) {
-                ml[j] = a.ws_ml[base + p0 + j];
-                o[j] = a.ws_o[(base + p0 + j) * D + d];
+            const int i = i0 + j;
+            if (i < n) {
+                const int64_t slot = base + (i < npre ? i : a.pre_parts + p_lo + (i - npre));
+                ml[j] = a.ws_ml[slot];
+                o[j] = a.ws_o[slot * D + d];
             } else {
                 ml[j] = make_float2(-INFINITY, 0.f);
                 o[j] = 0.f;
@@ -729,7 +1019,25 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     if (part < kTile) part = kTile;
     pl.partition = static_cast<int>(part);
     pl.max_parts = static_cast<int>(cap > 0 ? (cap + part - 1) / part : 1);
-    const size_t n = static_cast<size_t>(batch) * num_q_heads * pl.max_parts;
+    // shared prefixes: one CTA per (group chunk, kv head, prefix partition) in front of the grid
+    if (opt && opt->num_groups > 0) {
+        const int64_t lim = (kMaxTablePages - 1) * static_cast<int64_t>(block_size);
+        int64_t pre = opt->prefix_partition ? opt->prefix_partition
+                                            : std::min<int64_t>((opt->max_prefix_len + kTile - 1) / kTile * kTile,
+                                                                kPrefixPartition);
+        while (pre > lim) pre = (pre / 2 + kTile - 1) / kTile * kTile;
+        pl.pre_partition = static_cast<int>(std::max<int64_t>(pre, kTile));
+        pl.pre_parts = (opt->max_prefix_len + pl.pre_partition - 1) / pl.pre_partition;
+        pl.seqs_per_cta = kConsumerWarps * 8 / (num_q_heads / num_kv_heads);
+        pl.group_ctas = (opt->max_group_size + pl.seqs_per_cta - 1) / pl.seqs_per_cta;
+        pl.prefix_ctas = static_cast<int64_t>(opt->num_groups) * pl.group_ctas;
+    } else {
+        pl.pre_partition = kTile;
+        pl.pre_parts = pl.seqs_per_cta = pl.group_ctas = 0;
+        pl.prefix_ctas = 0;
+    }
+    pl.slots = pl.pre_parts + pl.max_parts;
+    const size_t n = static_cast<size_t>(batch) * num_q_heads * pl.slots;
     const size_t ml_bytes = (n * sizeof(float2) + 255) / 256 * 256;
     pl.ws_bytes = ml_bytes + n * head_dim * sizeof(float);
     return pl;
@@ -740,7 +1048,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
                           const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
-                          const FusedStore *fused, const Fp8Scales *fp8) {
+                          const FusedStore *fused, const Fp8Scales *fp8, const pa_decode_options *opt) {
     if (batch == 0) return cudaSuccess;
     DecodeArgs a;
     a.q = q;
@@ -757,12 +1065,23 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.k_scale = fp8 ? fp8->k_scale : 1.f;
     a.v_scale = fp8 ? fp8->v_scale : 1.f;
     a.out = out;
-    const size_t n = static_cast<size_t>(batch) * num_q_heads * plan.max_parts;
+    const size_t n = static_cast<size_t>(batch) * num_q_heads * plan.slots;
     const size_t ml_bytes = (n * sizeof(float2) + 255) / 256 * 256;
     a.ws_ml = static_cast<float2 *>(workspace);
     a.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + ml_bytes);
     a.partition = plan.partition;
     a.max_parts = plan.max_parts;
+    a.batch = batch;
+    const bool groups = plan.prefix_ctas > 0 && opt;
+    a.prefix_ctas = groups ? static_cast<int32_t>(plan.prefix_ctas) : 0;
+    a.group_ctas = plan.group_ctas;
+    a.seqs_per_cta = plan.seqs_per_cta;
+    a.group_offsets = groups ? opt->group_offsets : nullptr;
+    a.group_seqs = groups ? opt->group_seqs : nullptr;
+    a.prefix_lens = groups ? opt->prefix_lens : nullptr;
+    a.pre_partition = plan.pre_partition;
+    a.pre_parts = groups ? plan.pre_parts : 0;
+    a.slots = plan.slots;
     a.err_flag = err_flag;
     a.slot_mapping = fused ? fused->slot_mapping : nullptr;
     a.k_new = fused ? fused->k : nullptr;
@@ -800,7 +1119,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(a.max_parts, a.num_kv_heads, batch);
+        cfg.gridDim = dim3(std::max(a.max_parts, a.pre_parts), a.num_kv_heads, a.prefix_ctas + batch);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
@@ -808,7 +1127,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
         cfg.numAttrs = 1;
         err = cudaLaunchKernelEx(&cfg, kern_part, tm_k, tm_v, tm_k_tail, tm_v_tail, a);
         if (err != cudaSuccess) return err;
-        if (a.max_parts > 1) {
+        if (a.max_parts > 1 || a.prefix_ctas > 0) {
             cfg.gridDim = dim3(a.num_q_heads, batch);
             cfg.blockDim = dim3(d);
             cfg.dynamicSmemBytes = 0;

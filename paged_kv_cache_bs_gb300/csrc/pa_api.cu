@@ -77,6 +77,18 @@ int check_options(const pa_decode_options *opt) {
                     opt->partition);
     if (opt->stages && opt->stages != 2 && opt->stages != 3)
         return fail(PA_ERR_INVALID_ARG, "options.stages %d must be 0, 2 or 3", opt->stages);
+    if (opt->num_groups < 0) return fail(PA_ERR_INVALID_ARG, "options.num_groups %d is negative", opt->num_groups);
+    if (opt->num_groups > 0) {
+        if (!opt->group_offsets || !opt->group_seqs || !opt->prefix_lens)
+            return fail(PA_ERR_INVALID_ARG, "options: group_offsets, group_seqs and prefix_lens are required");
+        if (opt->max_group_size < 1 || opt->max_prefix_len < 1)
+            return fail(PA_ERR_INVALID_ARG, "options: max_group_size %d and max_prefix_len %d must be positive",
+                        opt->max_group_size, opt->max_prefix_len);
+        if (opt->prefix_partition &&
+            (opt->prefix_partition < 64 || opt->prefix_partition % 64 || opt->prefix_partition > 16384))
+            return fail(PA_ERR_INVALID_ARG, "options.prefix_partition %d must be 0 or a multiple of 64 in [64, 16384]",
+                        opt->prefix_partition);
+    }
     return PA_OK;
 }
 
@@ -111,8 +123,17 @@ int check_decode(const void *q, int64_t q_row_stride, const void *k_cache, const
     if (!aligned(q, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 2) ||
         !aligned(workspace, 256))
         return fail(PA_ERR_INVALID_ARG, "alignment: q 4 B, caches 16 B, out 2 B, workspace 256 B");
+    if (opt && opt->num_groups > 0) {
+        if (fp8) return fail(PA_ERR_UNSUPPORTED, "shared-prefix groups need a 16-bit pool");
+        if (opt->max_prefix_len > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+            return fail(PA_ERR_INVALID_ARG, "options.max_prefix_len %d is longer than a block table",
+                        opt->max_prefix_len);
+    }
     *plan = pa::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
                             fp8 != nullptr, opt);
+    if (plan->prefix_ctas + batch > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "batch %d plus %lld shared-prefix CTAs per kv head exceed 65535", batch,
+                    (long long)plan->prefix_ctas);
     if (workspace_bytes < plan->ws_bytes)
         return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
                     plan->ws_bytes);
@@ -214,7 +235,7 @@ int store_decode(const void *k, const void *v, int64_t k_row_stride, int64_t v_r
     return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                          context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
                                          block_size, scale, out, workspace, plan, dtype, err_flag,
-                                         static_cast<cudaStream_t>(stream), &fused, fp8),
+                                         static_cast<cudaStream_t>(stream), &fused, fp8, opt),
                        fp8 ? "pa_store_decode_fp8 launch" : "pa_store_decode launch");
 }
 
@@ -287,7 +308,7 @@ int pa_decode_ex(const void *q, int64_t q_row_stride, const void *k_cache, const
     return cuda_status(pa::launch_decode(q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                          context_lens, batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
                                          block_size, scale, out, workspace, plan, dtype, err_flag,
-                                         static_cast<cudaStream_t>(stream)),
+                                         static_cast<cudaStream_t>(stream), nullptr, nullptr, options),
                        "pa_decode launch");
 }
 

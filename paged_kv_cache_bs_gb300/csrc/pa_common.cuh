@@ -134,6 +134,13 @@ struct DecodePlan {
     int stages;         // ring depth of the partition kernel (2 or 3)
     int partition;      // tokens per split-K partition (multiple of the tile)
     int max_parts;      // partitions per sequence at the maximum context
+    // shared prefixes (pa_decode_options groups; all 0 without)
+    int pre_partition;  // tokens per prefix partition
+    int pre_parts;      // prefix partitions at the longest shared prefix
+    int seqs_per_cta;   // member sequences one prefix CTA serves
+    int group_ctas;     // prefix CTAs per group and (kv head, prefix partition)
+    int64_t prefix_ctas;  // num_groups * group_ctas
+    int slots;          // workspace partials per (sequence, q head): pre_parts + max_parts
     size_t ws_bytes;    // workspace bytes
 };
 // The E4M3 pool of the fp8 calls: K = code * k_scale, V = code * v_scale.
@@ -158,7 +165,8 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                           int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t num_blocks, int32_t block_size, float scale, void *out, void *workspace,
                           const DecodePlan &plan, pa_dtype dtype, int32_t *err_flag, cudaStream_t stream,
-                          const FusedStore *fused = nullptr, const Fp8Scales *fp8 = nullptr);
+                          const FusedStore *fused = nullptr, const Fp8Scales *fp8 = nullptr,
+                          const pa_decode_options *opt = nullptr);
 cudaError_t launch_sample(const void *logits, int64_t row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
                           const float *temperatures, const float *noise, uint64_t seed, uint64_t offset,
                           int32_t *tokens, int32_t *err_flag, cudaStream_t stream);

@@ -279,6 +279,23 @@ def _decode_from_pool(pool: Pool, ctx: list[int], num_q_heads: int, gen, scale=N
                       scale if scale is not None else 1.0 / math.sqrt(d))
 
 
+def make_decode_shared(seqs: list[tuple[int, int, int]], *, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                       block_size: int, dtype: torch.dtype, seed: int, num_blocks: int | None = None) -> DecodeStep:
+    """Decode step over sequences given as (context length, share group or -1, shared tokens):
+    the members of a share group point at the same physical pages for their first shared
+    tokens (whole pages, below every member's context length); -1 shares nothing."""
+    gen = torch.Generator().manual_seed(seed)
+    specs = []
+    for L, grp, share in seqs:
+        if L == 0:
+            specs.append(SeqSpec(0, 0))
+        else:
+            specs.append(SeqSpec(L - 1, 1, grp, share if grp >= 0 else 0))
+    pool = build_pool(specs, block_size=block_size, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                      dtype=dtype, gen=gen, num_blocks=num_blocks)
+    return _decode_from_pool(pool, [L for L, _, _ in seqs], num_q_heads, gen)
+
+
 def next_decode_step(st: DecodeStep, seed: int) -> DecodeStep:
     """The decode step after ``st`` over the same pool and block tables: each sequence
     gains one token while its last allocated page has room (else keeps its length),

@@ -197,7 +197,7 @@ def _pg_native(tables, ctx, bs, min_pages=1):
     width = max([len(t) for t in tables] + [1])
     bt = torch.tensor([list(t) + [-1] * (width - len(t)) for t in tables] or [[-1]], dtype=torch.int32)[:len(tables)]
     g = native(bt.reshape(len(tables), width), torch.tensor(ctx, dtype=torch.int32), bs, min_pages)
-    return g.group_offsets.tolist(), g.group_seqs.tolist(), g.prefix_lens.tolist(), g
+    return g.group_offsets.tolist(), g.group_seqs[:g.group_offsets[-1]].tolist(), g.prefix_lens.tolist(), g
 
 
 @pytest.mark.parametrize("seed", range(40))
