@@ -54,6 +54,8 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the 
 PRE_STEP_SPIN_CYCLES = 400_000
 DEFAULT_WORKLOAD = "qwen3_8b_shared_decode"
 # the other workloads a default run reports under "configs", in this order
+# workloads whose sequences share prefix pages: decoded with their shared-prefix groups
+SHARED_PREFIX_WORKLOADS = {"qwen3_8b_shared_decode"}
 SUB_CONFIGS = ["tiny_decode", "qwen3_0p6b_decode", "long_context_decode", "mixed_chunked_prefill",
                "qwen3_0p6b_decode_fp8", "store_stress", "sampler_qwen3_vocab"]
 
@@ -238,6 +240,9 @@ class DecodeWorkload:
     """A decode step (store of one token per sequence + paged decode) with
     all inputs resident on the device."""
 
+    groups = None    # shared-prefix groups (host), for workloads whose sequences share pages
+    options = None   # the decode options carrying them (device)
+
     def __init__(self, name: str, dev: torch.device, fused: bool = True):
         import paged_kv_cache_bs_gb300 as pa
         self.pa = pa
@@ -248,9 +253,23 @@ class DecodeWorkload:
         self.kc, self.vc = p.k_cache.to(dev), p.v_cache.to(dev)
         self.host = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "slot_mapping": st.slot_mapping,
                      "block_tables": st.block_tables, "context_lens": st.context_lens}
+        # sequences sharing prefix pages: their groups, derived on the host from the block tables
+        # (pa_prefix_groups), are one more input of the step, and each shared page is read once
+        self.groups = None
+        if name in SHARED_PREFIX_WORKLOADS:
+            from paged_kv_cache_bs_gb300.block_manager import prefix_groups
+            self.groups = prefix_groups(st.block_tables, st.context_lens, p.block_size)
+            self.host.update(group_offsets=self.groups.group_offsets, group_seqs=self.groups.group_seqs,
+                             prefix_lens=self.groups.prefix_lens)
         self.inputs, self.d, self.layout = pack_inputs(self.host, dev)
+        self.options = None
+        if self.groups is not None:
+            g = self.groups
+            self.options = pa.DecodeOptions(groups=pa.PrefixGroups(self.d["group_offsets"], self.d["group_seqs"],
+                                                                   self.d["prefix_lens"], g.max_group_size,
+                                                                   g.max_prefix_len))
         self.out = torch.empty_like(self.d["q"])
-        self.ws = pa.alloc_decode_workspace(self.d["q"], self.kc, self.d["block_tables"])
+        self.ws = pa.alloc_decode_workspace(self.d["q"], self.kc, self.d["block_tables"], self.options)
         self.kv_bytes = st.kv_bytes()
         # each physical row counted once (differs when sequences share prefix pages)
         self.kv_unique_bytes = st.unique_kv_bytes() if name == "qwen3_8b_shared_decode" else self.kv_bytes
@@ -260,6 +279,7 @@ class DecodeWorkload:
         self.prefill_flops = 0
         self.fused = fused
         if fused:   # one call: pa_store_decode (store fused into the partition kernel) + merge kernel
+            # (with shared prefixes: the prefix grid, then the sequences' grid, which merges)
             self.launches_per_step = 2
             self.phases = [("store+decode", self.store_and_attend)]
         else:
@@ -273,26 +293,33 @@ class DecodeWorkload:
     def attend(self):
         d = self.d
         self.pa.decode(d["q"], self.kc, self.vc, d["block_tables"], d["context_lens"], self.st.scale,
-                       out=self.out, workspace=self.ws)
+                       out=self.out, workspace=self.ws, options=self.options)
 
     def store_and_attend(self):
         d = self.d
         self.pa.store_decode(d["k_new"], d["v_new"], d["slot_mapping"], d["q"], self.kc, self.vc, d["block_tables"],
-                             d["context_lens"], self.st.scale, out=self.out, workspace=self.ws)
+                             d["context_lens"], self.st.scale, out=self.out, workspace=self.ws, options=self.options)
 
     e2e_path = ("one packed H2D copy of the step's inputs from pinned memory, the step's calls, "
                 "D2H of the output, stream sync; host wall clock")
 
     def make_runner(self, zero_copy: bool):
         from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
-        st, fs = self.st, getattr(self, "fs", None)
+        st, fs, g = self.st, getattr(self, "fs", None), getattr(self, "groups", None)
+        caps = (g.num_groups, g.max_group_size, g.max_prefix_len) if g is not None else None
         return DecodeGraphRunner(self.kc, self.vc, st.num_q_heads, st.batch, st.block_tables.shape[1],
                                  st.scale, st.q.dtype, k_scale=fs.k_scale if fs else None,
-                                 v_scale=fs.v_scale if fs else None, zero_copy=zero_copy)
+                                 v_scale=fs.v_scale if fs else None, zero_copy=zero_copy, group_caps=caps)
 
     @staticmethod
     def runner_args(st):
         return st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables
+
+    def runner_step(self, runner, args):
+        """DecodeGraphRunner.step from a step's host tensors; for workloads that share prefix
+        pages the runner derives the groups from the staged block tables (pa_prefix_groups),
+        every step, as a caller's step would."""
+        return runner.step(*args, share_prefixes=self.groups is not None)
 
     def e2e_buffers(self):
         if self.fused:
@@ -307,7 +334,8 @@ class DecodeWorkload:
                              "decode steps over the same pool: the step's inputs copied into the pinned staging, "
                              "CUDA-graph replay of the fused store + decode whose kernels read that staging and "
                              "write the output into pinned host memory over NVLink-C2C, stream sync; host wall "
-                             "clock")
+                             "clock" + ("; the shared-prefix groups derived from the staged block tables "
+                                        "(pa_prefix_groups, C++) every step" if self.groups is not None else ""))
             return None, None, self.runner.h2d_bytes(st.batch), self.runner.d2h_bytes(st.batch)
         pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
@@ -315,7 +343,7 @@ class DecodeWorkload:
 
     def e2e_step(self, pinned, out_host, i: int = 0):
         if self.fused:
-            self.runner.step(*self.e2e_inputs[i % 2])
+            self.runner_step(self.runner, self.e2e_inputs[i % 2])
             return
         self.inputs.copy_(pinned, non_blocking=True)   # the step's inputs, one copy
         for _, fn in self.phases:
@@ -1004,7 +1032,7 @@ def measure_attention(name, args, world, rank, local, cpu_s, cpu_all_s):
     # step with the graph's copy-engine transfers instead of zero-copy operands
     e2e_replay_ms = e2e_copy_ms = None
     if getattr(w, "runner", None) is not None:
-        w.runner.set_inputs(*w.e2e_inputs[0])
+        w.runner_step(w.runner, w.e2e_inputs[0])
         e2e_s = 0.0
         for i in range(Ke):
             between_steps()
@@ -1016,14 +1044,14 @@ def measure_attention(name, args, world, rank, local, cpu_s, cpu_all_s):
         e2e_replay_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
         rc = w.make_runner(zero_copy=False)
         for i in range(args.warmup):
-            rc.step(*w.e2e_inputs[i % 2])
+            w.runner_step(rc, w.e2e_inputs[i % 2])
         torch.cuda.synchronize(dev)
         e2e_s = 0.0
         for i in range(Ke):
             between_steps()
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
-            rc.step(*w.e2e_inputs[i % 2])
+            w.runner_step(rc, w.e2e_inputs[i % 2])
             e2e_s += time.perf_counter() - t0
         e2e_copy_ms = max_over_ranks(e2e_s * 1e3 / Ke, world, dev)
         del rc
@@ -1051,7 +1079,10 @@ def measure_attention(name, args, world, rank, local, cpu_s, cpu_all_s):
         kern = ("pa_store_decode_fp8 (E4M3 store fused into the split-K partition kernel + merge)"
                 if f8 and "store+decode" in phase_ms else
                 "pa_decode_fp8 (E4M3 split-K partitions + merge)" if f8 else
-                "pa_store_decode (store fused into the split-K partition kernel + merge)"
+                ("pa_store_decode_ex with shared-prefix groups (the groups' shared pages read once by a prefix "
+                 "grid; the sequences' grid stores, attends over the private pages and folds in the prefix "
+                 "partials)" if w.options is not None else
+                 "pa_store_decode (store fused into the split-K partition kernel + merge)")
                 if "store+decode" in phase_ms else "pa_decode (split-K partitions + merge)")
         roof = {"bound": "hbm", "kernel": kern, "achieved": unique_gbs,
                 "achieved_logical": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",

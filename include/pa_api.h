@@ -251,6 +251,7 @@ PA_API int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, i
  * a sequence with prefix_lens[b] > 0 that is in no group gets an unspecified
  * output without a flag.  Supported for 16-bit pools (pa_decode_ex,
  * pa_store_decode_ex).
+
  */
 typedef struct pa_decode_options {
     int32_t partition;

@@ -63,10 +63,10 @@ constexpr int kMinPartition = 128;
 // workload (64 sequences, context U[128, 4096]): 4 waves (1024-token partitions) beat 8 (512)
 // by 1.4 % on the bf16 pool and by 9 % on the E4M3 pool, whose CTAs stream half the bytes.
 constexpr int kTargetWaves = 4;
-// Tokens per prefix partition of a shared-prefix CTA (its four warps each stream every tile
-// of the partition for their own query rows): short enough that the prefix CTAs, about four
-// times a private CTA's work per tile, do not trail the last wave.
-constexpr int kPrefixPartition = 256;
+// Tokens per partition of a shared prefix (one CTA per group chunk, kv head and partition):
+// measured on the Qwen3-8B-like shared-prefix decode, one 512-token partition per prefix
+// (149.5 us) beats two of 256 (155.6 us) and four of 128.
+constexpr int kPrefixPartition = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
@@ -108,6 +108,10 @@ struct DecodeArgs {
     int32_t pre_partition;   // tokens per prefix partition
     int32_t pre_parts;       // workspace slots of prefix partials, before the private partitions'
     int32_t slots;           // workspace slots per (sequence, q head): pre_parts + max_parts
+    // 1: wait for the previous kernel before reading the cache.  0 (the sequences' grid after the
+    // prefix grid): that grid already waited before letting this one launch, and each CTA waits
+    // for it (griddepcontrol.wait) before it reads the prefix partials and before it exits
+    int32_t wait_at_start;
 };
 
 // Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
@@ -449,24 +453,27 @@ template <int ST> __device__ __forceinline__ void drain(uint32_t bars, int issue
 }
 
 // Loads the block-table entries of logical pages [first_page, first_page + span) of
-// `table` (a sequence's row) into registers, one memory round trip for the CTA.
-constexpr int kPerThread = (kMaxTablePages + kThreads - 1) / kThreads;
-__device__ __forceinline__ void prefetch_table(int (&pg)[kPerThread], const int32_t *table, int first_page, int span,
-                                               int tid) {
+// `table` (a sequence's row) into registers, one memory round trip for the CTA of NT threads.
+template <int NT> constexpr int per_thread() { return (kMaxTablePages + NT - 1) / NT; }
+constexpr int kPerThread = per_thread<kThreads>();
+template <int NT>
+__device__ __forceinline__ void prefetch_table(int (&pg)[per_thread<NT>()], const int32_t *table, int first_page,
+                                               int span, int tid) {
 #pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-        const int i = tid + k * kThreads;
+    for (int k = 0; k < per_thread<NT>(); ++k) {
+        const int i = tid + k * NT;
         pg[k] = i < span ? table[first_page + i] : 0;
     }
 }
 
 // Stores the first npages prefetched entries into the shared slice, a bad id flagged and
 // read as page 0.
-__device__ __forceinline__ void publish_table(const int (&pg)[kPerThread], int32_t *bt_s, int npages,
+template <int NT>
+__device__ __forceinline__ void publish_table(const int (&pg)[per_thread<NT>()], int32_t *bt_s, int npages,
                                               const DecodeArgs &a, int tid) {
 #pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-        const int i = tid + k * kThreads;
+    for (int k = 0; k < per_thread<NT>(); ++k) {
+        const int i = tid + k * NT;
         if (i < npages) {
             int p = pg[k];
             if (p < 0 || p >= a.num_blocks) {
@@ -489,17 +496,61 @@ __device__ __forceinline__ int shared_prefix(const DecodeArgs &a, int b, int L, 
     return min(P, min(a.pre_parts * a.pre_partition, a.max_blocks << a.log2_bs));
 }
 
-// The prefix role of the partition kernel: one CTA per (group chunk, kv head, prefix
-// partition) streams the group's shared pages once for up to 32 query rows -- the G heads of
-// up to 32 / G member sequences -- and writes each row's softmax partial to the workspace.
-// Warp w owns rows 8w .. 8w+7 (the N dimension of its MMAs) and walks every 16-token slice of
-// each tile; row r is head r % G of the chunk's member r / G.
+// Partials of sequence b's output (per q head): its prefix partitions, then its private
+// partitions [p_lo, p_hi) (slots pre_parts + p).  Every kernel that writes or merges them
+// derives the same numbers from the same inputs.
+struct PartialSet {
+    int npre, p_lo, p_hi;
+    __device__ __forceinline__ int count() const { return npre + p_hi - p_lo; }
+    __device__ __forceinline__ int slot(int i, int pre_parts) const {
+        return i < npre ? i : pre_parts + p_lo + (i - npre);
+    }
+};
+__device__ __forceinline__ PartialSet partial_set(const DecodeArgs &a, int b) {
+    const int L = max(context_len(a, b), 0);
+    const int P = shared_prefix(a, b, L, false);
+    const int ps = min(P, L);
+    PartialSet r;
+    r.npre = P > 0 ? (P + a.pre_partition - 1) / a.pre_partition : 0;
+    r.p_lo = ps / a.partition;
+    r.p_hi = ps < L ? (L + a.partition - 1) / a.partition : r.p_lo;
+    return r;
+}
+
+// The shared-prefix kernel: one CTA per (group chunk, kv head, prefix partition) streams the
+// group's shared pages once for up to 32 query rows -- the G heads of up to 32 / G member
+// sequences -- and writes each row's softmax partial to the workspace.  Row r is head r % G of
+// the chunk's member r / G.  Rows come in four groups of 8 (the N dimension of the MMAs); two
+// consumer warps own each row group and split every 64-token tile between them (32 tokens
+// each), then merge their states through shared memory.
+// Sequence of member mi of a prefix chunk whose members start at group_seqs[m0] (nm of them),
+// or -1 past the chunk or for an index outside the batch.
+__device__ __forceinline__ int group_member(const DecodeArgs &a, int m0, int nm, int mi) {
+    if (mi >= nm) return -1;
+    const int b = a.group_seqs[m0 + mi];
+    return (b >= 0 && b < a.batch) ? b : -1;
+}
+
+// Consumer warps of the shared-prefix kernel: 4 (one per row group, walking every 16-token slice
+// of a tile) or 8 (two per row group, half a tile each, merged at the end).  Measured on the
+// Qwen3-8B-like shared-prefix decode: 4 warps with a 2-stage ring, one partition per prefix,
+// 149.5 us per step; 8 warps 154.4 us; 3 stages 151.6 us.
+constexpr int kPrefixConsumerWarps = 4;
+constexpr int kPrefixStages = 2;  // ring depth
+constexpr int kPrefixProducerWarp = kPrefixConsumerWarps;
+constexpr int kPrefixThreads = (kPrefixConsumerWarps + 1) * 32;
+constexpr int kPrefixRows = 32;  // query rows of one prefix CTA
+
 template <typename T, int D, int ST>
-__device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                                 const CUtensorMap *tm_k_tail, const CUtensorMap *tm_v_tail,
-                                                 const DecodeArgs &a, uint8_t *smem) {
+__global__ void __launch_bounds__(kPrefixThreads, ctas_per_sm<kPrefixStages>())
+    decode_prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_k_tail, const __grid_constant__ CUtensorMap tm_v_tail,
+                         const DecodeArgs a) {
     using S = Shape<D, ST, false>;
     constexpr int kStages = ST;
+    constexpr int kPerT = per_thread<kPrefixThreads>();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
     const uint32_t ring = smem_u32(smem);
     const uint32_t bars = smem_u32(smem + S::kBarOff);
@@ -507,6 +558,10 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const 
     const int pp = blockIdx.x, g = blockIdx.y;
     const int gi = blockIdx.z / a.group_ctas, chunk = blockIdx.z % a.group_ctas;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the previous kernel on the stream (this step's store) first; the sequences' grid may
+    // launch once every prefix CTA is past this point
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     const int off0 = a.group_offsets[gi], off1 = a.group_offsets[gi + 1];
     if (off0 < 0 || off1 > a.batch || off0 > off1) {  // group_seqs has room for batch entries
@@ -517,34 +572,34 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const 
     const int nm = min(a.seqs_per_cta, off1 - m0);  // members of this chunk
     if (nm <= 0) return;
     const int leader = a.group_seqs[off0];
-    const int start = pp * a.pre_partition;
-    const int first_page = start >> a.log2_bs;
-    const int span = min(a.max_blocks, ((start + a.pre_partition - 1) >> a.log2_bs) + 1) - first_page;
-    int pg_pre[kPerThread];
-    if (leader >= 0 && leader < a.batch)
-        prefetch_table(pg_pre, a.block_tables + static_cast<int64_t>(leader) * a.max_blocks, first_page, span, tid);
     if (leader < 0 || leader >= a.batch) {
         if (tid == 0 && pp == 0 && g == 0) raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
         return;
     }
+    const int start = pp * a.pre_partition;
+    const int first_page = start >> a.log2_bs;
+    const int span = min(a.max_blocks, ((start + a.pre_partition - 1) >> a.log2_bs) + 1) - first_page;
+    int pg_pre[kPerT];
+    prefetch_table<kPrefixThreads>(pg_pre, a.block_tables + static_cast<int64_t>(leader) * a.max_blocks, first_page,
+                                   span, tid);
     const int Ll = max(context_len(a, leader), 0);
     const int P = shared_prefix(a, leader, Ll, false);
     const int end = min(start + a.pre_partition, P);
     if (start >= end) return;
     const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;
 
-    publish_table(pg_pre, bt_s, npages, a, tid);
+    publish_table<kPrefixThreads>(pg_pre, bt_s, npages, a, tid);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(bars + 8 * s, 1);
-            tc::mbar_init(bars + 8 * (kStages + s), kConsumerWarps);
+            tc::mbar_init(bars + 8 * (kStages + s), kPrefixConsumerWarps);
         }
         *abort_s = 0;
         tc::mbar_fence_init();
     }
-    if (warp == kProducerWarp && lane == 0) {
-        tc::prefetch_tmap(tm_k);
-        tc::prefetch_tmap(tm_v);
+    if (warp == kPrefixProducerWarp && lane == 0) {
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
     }
     __syncthreads();  // table slice, barriers ready
 
@@ -552,25 +607,23 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const 
     acc.init();
     int issued = 0;
     const int ntiles = (end - start + kTile - 1) / kTile;
-    // this lane's two columns (rows rc0, rc0 + 1) and its B-operand row rq: member sequences
-    // and their context limits (loaded by the consumers while the first tile is in flight)
+    // this warp's row group rg and tile half hh; this lane's two columns (rows rc0, rc0 + 1) and
+    // its B-operand row rq: member sequences and their context limits (loaded while the first
+    // tile is in flight)
     const int G = a.group;
-    const int rc0 = 8 * warp + 2 * (lane & 3), rq = 8 * warp + (lane >> 2);
+    constexpr int kSplit = kPrefixConsumerWarps / 4;         // warps sharing a row group
+    constexpr int kSubPerWarp = (kTile / 16) / kSplit;        // 16-token slices per warp and tile
+    const int rg = warp / kSplit, hh = warp % kSplit;
+    const int rc0 = 8 * rg + 2 * (lane & 3), rq = 8 * rg + (lane >> 2);
     int b0 = -1, b1 = -1;
-    if (warp == kProducerWarp) {
+    if (warp == kPrefixProducerWarp) {
         if (lane == 0)
-            issued = produce_tiles<D, ST, false>(tm_k, tm_v, tm_k_tail, tm_v_tail, a, g, start, end, first_page, bt_s,
-                                                 ring, bars, abort_s);
+            issued = produce_tiles<D, ST, false>(&tm_k, &tm_v, &tm_k_tail, &tm_v_tail, a, g, start, end, first_page,
+                                                 bt_s, ring, bars, abort_s);
     } else {
-        auto member = [&](int r) -> int {
-            const int mi = r / G;
-            if (mi >= nm) return -1;
-            const int b = a.group_seqs[m0 + mi];
-            return (b >= 0 && b < a.batch) ? b : -1;
-        };
-        b0 = member(rc0);
-        b1 = member(rc0 + 1);
-        const int bq = member(rq);
+        b0 = group_member(a, m0, nm, rc0 / G);
+        b1 = group_member(a, m0, nm, (rc0 + 1) / G);
+        const int bq = group_member(a, m0, nm, rq / G);
         const int lim0 = b0 >= 0 ? min(P, max(context_len(a, b0), 0)) : 0;
         const int lim1 = b1 >= 0 ? min(P, max(context_len(a, b1), 0)) : 0;
         // query fragments (B operand of S^T = K Q^T): row rq's head
@@ -600,7 +653,7 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const 
             const uint32_t vb = kb + S::kTileBytes;
             const int tile_start = start + t * kTile;
 #pragma unroll 1
-            for (int u = 0; u < kTile / 16; ++u) {
+            for (int u = kSubPerWarp * hh; u < kSubPerWarp * (hh + 1); ++u) {
                 if (tile_start + 16 * u >= end) break;
                 Frags<D, false> f;
                 load_frags<D, S::kSlices, false>(f, kb, vb, 16 * u, lane, lbr);
@@ -614,7 +667,7 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const 
     // partition (checked once, by the first kv head's CTAs), reads the same prefix and has
     // tokens after it
     if (g == 0) {
-        for (int i = tid; i < nm * npages; i += kThreads) {
+        for (int i = tid; i < nm * npages; i += kPrefixThreads) {
             const int b = a.group_seqs[m0 + i / npages];
             if (b < 0 || b >= a.batch ||
                 a.block_tables[static_cast<int64_t>(b) * a.max_blocks + first_page + i % npages] != bt_s[i % npages])
@@ -628,34 +681,53 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap *tm_k, const 
     }
     __syncthreads();
     if (*abort_s) {
-        if (warp == kProducerWarp && lane == 0) drain<ST>(bars, issued);
+        if (warp == kPrefixProducerWarp && lane == 0) drain<ST>(bars, issued);
         return;
     }
-    if (warp >= kConsumerWarps) return;
-    // each warp writes its own rows' partials: (reference max, sum) and the unnormalised O
-    acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 4);
-    acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 4);
-    acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 8);
-    acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 8);
-    acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 16);
-    acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 16);
+    // the two warps of a row group hold the same columns in the same lanes: the second warp
+    // hands its state over through shared memory (the ring is free), the first merges and writes
+    constexpr int kStateFloats = (D / 16) * 4 + 4;  // O fragments, then (m0, m1, l0, l1)
+    float *xs = reinterpret_cast<float *>(smem) + (rg * 32 + lane) * kStateFloats;
+    if (warp < kPrefixConsumerWarps) {
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 4);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 4);
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 8);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 8);
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, 16);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, 16);
+        if (kSplit == 2 && hh == 1) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xs[mt * 4 + e] = acc.o[mt][e];
+            xs[(D / 16) * 4 + 0] = acc.m0 == -INFINITY ? -INFINITY : acc.mu0;
+            xs[(D / 16) * 4 + 1] = acc.m1 == -INFINITY ? -INFINITY : acc.mu1;
+            xs[(D / 16) * 4 + 2] = acc.l0;
+            xs[(D / 16) * 4 + 3] = acc.l1;
+        }
+    }
+    __syncthreads();
+    if (warp >= kPrefixConsumerWarps || hh == 1) return;
     const int dr = lane >> 2;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int b = c ? b1 : b0;
         if (b < 0) continue;
+        const float ma = (c ? acc.m1 : acc.m0) == -INFINITY ? -INFINITY : (c ? acc.mu1 : acc.mu0);
+        const float mb = kSplit == 2 ? xs[(D / 16) * 4 + c] : -INFINITY;
+        const float M = fmaxf(ma, mb);
+        const float wa = M == -INFINITY ? 0.f : exp2f(ma - M), wb = M == -INFINITY ? 0.f : exp2f(mb - M);
         const int hq = g * G + (rc0 + c) % G;
         const int64_t idx = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.slots + pp;
         float *o = a.ws_o + idx * D;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-            o[mt * 16 + dr] = acc.o[mt][c];
-            o[mt * 16 + dr + 8] = acc.o[mt][c + 2];
+            const float x0 = kSplit == 2 ? xs[mt * 4 + c] * wb : 0.f, x1 = kSplit == 2 ? xs[mt * 4 + c + 2] * wb : 0.f;
+            o[mt * 16 + dr] = acc.o[mt][c] * wa + x0;
+            o[mt * 16 + dr + 8] = acc.o[mt][c + 2] * wa + x1;
         }
-        if (dr == 0) {
-            const float m = c ? acc.m1 : acc.m0;
-            a.ws_ml[idx] = make_float2(m == -INFINITY ? -INFINITY : (c ? acc.mu1 : acc.mu0), c ? acc.l1 : acc.l0);
-        }
+        if (dr == 0)
+            a.ws_ml[idx] = make_float2(M, (c ? acc.l1 : acc.l0) * wa + (kSplit == 2 ? xs[(D / 16) * 4 + 2 + c] * wb : 0.f));
     }
 }
 
@@ -670,22 +742,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Launched as a programmatic dependent of the previous kernel on the stream (the store
-    // of this step): wait for it to finish before reading the cache, and let the merge
+    // of this step, or the shared-prefix grid): wait for it to finish before reading the cache
+    // (after a shared-prefix grid the wait comes later, see wait_at_start), then let the next
     // kernel be launched right away (it waits for this grid itself).
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (a.wait_at_start) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    if constexpr (!F8) {
-        if (blockIdx.z < a.prefix_ctas) {  // the first z indices: shared-prefix CTAs
-            prefix_partition<T, D, ST>(&tm_k, &tm_v, &tm_k_tail, &tm_v_tail, a, smem);
-            return;
-        }
-    }
     int32_t *bt_s = reinterpret_cast<int32_t *>(smem + S::kTableOff);
     const uint32_t ring = smem_u32(smem);
     const uint32_t bars = smem_u32(smem + S::kBarOff);  // full[s] at 8s, empty[s] at 8(kStages + s)
     volatile int *abort_s = reinterpret_cast<volatile int *>(smem + S::kAbortOff);
 
-    const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z - a.prefix_ctas;
+    const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // The block-table entries this partition can touch are loaded together with the context
@@ -695,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     const int first_page = part_start >> a.log2_bs;
     const int span = min(a.max_blocks, ((part_start + a.partition - 1) >> a.log2_bs) + 1) - first_page;
     int pg_pre[kPerThread];
-    prefetch_table(pg_pre, a.block_tables + static_cast<int64_t>(b) * a.max_blocks, first_page, span, tid);
+    prefetch_table<kThreads>(pg_pre, a.block_tables + static_cast<int64_t>(b) * a.max_blocks, first_page, span, tid);
     int L = context_len(a, b);
     if (L < 0) {
         if (p == 0 && tid == 0) raise_flag(a.err_flag, PA_FLAG_BAD_LENGTH);
@@ -717,16 +784,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
         if (a.slot_mapping && g == 0 && tid == 0 && (L == 0 ? p == 0 : (L - 1) / a.partition == p) &&
             a.slot_mapping[b] != -1)
             raise_flag(a.err_flag, PA_FLAG_BAD_SLOT);
+        if (!a.wait_at_start) asm volatile("griddepcontrol.wait;\n" ::: "memory");
         return;
     }
     const int end = min(L, part_start + a.partition);
-    // this sequence's partials: its prefix partitions, then its private partitions
-    const bool direct = P == 0 && (L + a.partition - 1) / a.partition == 1;
+    // this sequence's partials: its prefix partitions (the prefix grid's), then its private
+    // partitions; with one private partition this CTA writes the output, folding in the
+    // prefix partials, else the merge kernel merges them all
+    const int npre = P > 0 ? (P + a.pre_partition - 1) / a.pre_partition : 0;
+    const bool direct = (L + a.partition - 1) / a.partition - ps / a.partition == 1;
     const int ntiles = (end - start + kTile - 1) / kTile;
 
     // block-table slice of this partition, validated once (a bad id is flagged and read as page 0)
     const int npages = ((end - 1) >> a.log2_bs) - first_page + 1;  // <= span
-    publish_table(pg_pre, bt_s, npages, a, tid);
+    publish_table<kThreads>(pg_pre, bt_s, npages, a, tid);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(bars + 8 * s, 1);
@@ -805,6 +876,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     if (*abort_s) {
         // a wait gave up (flagged above): let every load this CTA started land, then leave
         if (warp == kProducerWarp && lane == 0) drain<ST>(bars, issued);
+        if (!a.wait_at_start) asm volatile("griddepcontrol.wait;\n" ::: "memory");
         return;
     }
 
@@ -839,6 +911,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
         }
     }
     __syncthreads();
+    // the prefix partials are complete once the prefix grid has finished
+    if (direct && npre > 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     for (int i = tid; i < a.group * D; i += kThreads) {
         const int h = i / D, d = i % D;
@@ -854,6 +928,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
         }
         if constexpr (F8) accv *= a.v_scale;
         const int hq = g * a.group + h;
+        if (direct && npre > 0) {  // fold in the prefix partitions' partials, loaded together
+            const int64_t base = (static_cast<int64_t>(b) * a.num_q_heads + hq) * a.slots;
+            for (int k0 = 0; k0 < npre; k0 += 4) {
+                float2 pml[4];
+                float po[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    pml[j] = k0 + j < npre ? __ldcg(a.ws_ml + base + k0 + j) : make_float2(-INFINITY, 0.f);
+                    po[j] = k0 + j < npre ? __ldcg(a.ws_o + (base + k0 + j) * D + d) : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float Mn = fmaxf(M, pml[j].x);
+                    if (Mn == -INFINITY) continue;
+                    const float cold = exp2f(M - Mn), cnew = exp2f(pml[j].x - Mn);
+                    accv = accv * cold + po[j] * cnew;
+                    sum = sum * cold + pml[j].y * cnew;
+                    M = Mn;
+                }
+            }
+        }
         if (direct) {
             out[(static_cast<int64_t>(b) * a.num_q_heads + hq) * D + d] = Dt<T>::from_float(accv / sum);
         } else {
@@ -862,12 +957,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
             if (d == 0) a.ws_ml[idx] = make_float2(M, sum);
         }
     }
+    if (!a.wait_at_start) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
-// Log-sum-exp merge of the partials of sequences that have more than one: the prefix
-// partitions' (slots [0, prefix partitions)) and the private partitions' (slot pre_parts + p
-// for partition p).  The partials are loaded eight at a time and folded in with an online
-// maximum: one memory round trip per eight partials.
+// Log-sum-exp merge of the partials of sequences whose context spans several private partitions:
+// the prefix partitions' partials (slots [0, prefix partitions)) and the private partitions'
+// (slot pre_parts + p for partition p).  One block per (q head, sequence), one thread per d; the
+// partials are loaded eight at a time and folded in with an online maximum: one memory round
+// trip per eight partials.  (A wider layout -- float4 chunks of several heads per thread, fewer
+// blocks -- measured slower: its larger blocks, resident early beside the partition grid's last
+// wave, slowed that wave.)
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
     constexpr int kBatch = 8;
@@ -875,13 +974,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
     // context_lens and prefix_lens are inputs of the call: this grid launches only after every
     // partition CTA has passed its own wait on the previous kernel, so they may be read before
     // the wait
-    const int L = max(context_len(a, b), 0);
-    const int P = shared_prefix(a, b, L, false);
-    const int ps = min(P, L);
-    const int npre = P > 0 ? (P + a.pre_partition - 1) / a.pre_partition : 0;
-    const int p_lo = ps / a.partition, p_hi = ps < L ? (L + a.partition - 1) / a.partition : p_lo;
-    const int n = npre + (p_hi - p_lo);
-    if (npre == 0 && p_hi - p_lo <= 1) return;  // written by its only partition
+    const PartialSet ps = partial_set(a, b);
+    const int npriv = ps.p_hi - ps.p_lo, n = ps.count();
+    if (npriv == 1 || n == 0) return;  // written by its only private partition (prefix partials folded in)
     // launched early (programmatic dependent launch): wait until the partition grid has
     // finished and its partials are visible
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -892,9 +987,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
         float o[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            const int i = i0 + j;
-            if (i < n) {
-                const int64_t slot = base + (i < npre ? i : a.pre_parts + p_lo + (i - npre));
+            if (i0 + j < n) {
+                const int64_t slot = base + ps.slot(i0 + j, a.pre_parts);
                 ml[j] = a.ws_ml[slot];
                 o[j] = a.ws_o[slot * D + d];
             } else {
@@ -931,6 +1025,16 @@ template <typename T, int D, int ST, bool F8 = false> cudaError_t prepare_partit
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(decode_partition_kernel<T, D, ST, F8>,
                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
+// The shared-prefix kernel's shared-memory opt-in.
+template <typename T, int D> cudaError_t prepare_prefix_kernel() {
+    cudaError_t e = cudaFuncSetAttribute(decode_prefix_kernel<T, D, kPrefixStages>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Shape<D, kPrefixStages>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(decode_prefix_kernel<T, D, kPrefixStages>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
 }
 
@@ -1028,7 +1132,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
         while (pre > lim) pre = (pre / 2 + kTile - 1) / kTile * kTile;
         pl.pre_partition = static_cast<int>(std::max<int64_t>(pre, kTile));
         pl.pre_parts = (opt->max_prefix_len + pl.pre_partition - 1) / pl.pre_partition;
-        pl.seqs_per_cta = kConsumerWarps * 8 / (num_q_heads / num_kv_heads);
+            pl.seqs_per_cta = kPrefixRows / (num_q_heads / num_kv_heads);
         pl.group_ctas = (opt->max_group_size + pl.seqs_per_cta - 1) / pl.seqs_per_cta;
         pl.prefix_ctas = static_cast<int64_t>(opt->num_groups) * pl.group_ctas;
     } else {
@@ -1082,6 +1186,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.pre_partition = plan.pre_partition;
     a.pre_parts = groups ? plan.pre_parts : 0;
     a.slots = plan.slots;
+    a.wait_at_start = 1;
     a.err_flag = err_flag;
     a.slot_mapping = fused ? fused->slot_mapping : nullptr;
     a.k_new = fused ? fused->k : nullptr;
@@ -1112,22 +1217,36 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
                                                 make_tmap_rows(&tm_v_tail, v_cache, pool, cols, rows, 16));
     if (!maps_ok || !tails_ok) return cudaErrorInvalidValue;
 
-    auto run = [&](auto kern_part, auto kern_comb, auto prepare, int smem, int d) -> cudaError_t {
+    auto run = [&](auto kern_part, auto kern_comb, auto prepare, int smem, int d, auto kern_pre, auto prepare_pre,
+                   int smem_pre) -> cudaError_t {
         cudaError_t err = prepare();
         if (err != cudaSuccess) return err;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(std::max(a.max_parts, a.pre_parts), a.num_kv_heads, a.prefix_ctas + batch);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        if (a.prefix_ctas > 0) {
+            // the shared-prefix CTAs first, then the sequences' CTAs as its programmatic dependent
+            err = prepare_pre();
+            if (err != cudaSuccess) return err;
+            cfg.gridDim = dim3(a.pre_parts, a.num_kv_heads, a.prefix_ctas);
+            cfg.blockDim = dim3(kPrefixThreads);
+            cfg.dynamicSmemBytes = smem_pre;
+            err = cudaLaunchKernelEx(&cfg, kern_pre, tm_k, tm_v, tm_k_tail, tm_v_tail, a);
+            if (err != cudaSuccess) return err;
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            a.wait_at_start = 0;
+        }
+        cfg.gridDim = dim3(a.max_parts, a.num_kv_heads, batch);
         err = cudaLaunchKernelEx(&cfg, kern_part, tm_k, tm_v, tm_k_tail, tm_v_tail, a);
         if (err != cudaSuccess) return err;
-        if (a.max_parts > 1 || a.prefix_ctas > 0) {
+        if (a.max_parts > 1) {
             cfg.gridDim = dim3(a.num_q_heads, batch);
             cfg.blockDim = dim3(d);
             cfg.dynamicSmemBytes = 0;
@@ -1137,10 +1256,14 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     };
 #define PA_DECODE_RUN(T, D, ST)                                                                                  \
     run(decode_partition_kernel<T, D, ST, false>, decode_combine_kernel<T, D>,                                 \
-        prepare_partition_kernel<T, D, ST, false>, Shape<D, ST>::kSmemBytes, D)
-#define PA_DECODE_RUN_F8(T)                                                                                      \
+        prepare_partition_kernel<T, D, ST, false>, Shape<D, ST>::kSmemBytes, D,                                 \
+        decode_prefix_kernel<T, D, kPrefixStages>, prepare_prefix_kernel<T, D>,                                 \
+        Shape<D, kPrefixStages>::kSmemBytes)
+#define PA_DECODE_RUN_F8(T)  /* no shared-prefix grid over an E4M3 pool */                                    \
     run(decode_partition_kernel<T, 128, kF8Stages, true>, decode_combine_kernel<T, 128>,                       \
-        prepare_partition_kernel<T, 128, kF8Stages, true>, Shape<128, kF8Stages, true>::kSmemBytes, 128)
+        prepare_partition_kernel<T, 128, kF8Stages, true>, Shape<128, kF8Stages, true>::kSmemBytes, 128,       \
+        decode_prefix_kernel<T, 128, kPrefixStages>, prepare_prefix_kernel<T, 128>,                             \
+        Shape<128, kPrefixStages>::kSmemBytes)
     const bool bf = dtype == PA_BF16, d128 = head_dim == 128, deep = plan.stages == 3;
     cudaError_t e;
     if (fp8)  // head_dim 128, checked by the caller

@@ -23,10 +23,13 @@ only: every step of the path runs in the library's kernels.
 
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
-from . import (_fp8_pool, _FP8_POOL, decode_fp8_workspace_bytes, decode_workspace_bytes, store_decode,
-               store_decode_fp8)
+from . import (_fp8_pool, _FP8_POOL, _lib, DecodeOptions, PagedAttentionError, PrefixGroups,
+               decode_fp8_workspace_bytes, decode_workspace_bytes, store_decode, store_decode_fp8)
+from . import block_manager as _bm  # declares pa_prefix_groups
 
 
 def graph_batch_sizes(max_batch: int) -> list[int]:
@@ -51,13 +54,16 @@ class DecodeGraphRunner:
     ``torch.float8_e4m3fn`` with ``k_scale`` and ``v_scale`` given).  ``dtype``: the type of q,
     the new K/V rows and the output.  ``zero_copy``: the kernels read the step's inputs from, and
     write its output to, the pinned staging (default), or the graph copies them to and from
-    device buffers.  Steps are issued on the current stream of the pool's device; one runner
-    serves one step at a time.
+    device buffers.  ``group_caps``: (groups, members per group, prefix tokens) -- the largest
+    shared-prefix groups a step may pass (:class:`PrefixGroups`, 16-bit pools); the graphs are
+    captured for them (unused groups are empty and cost a CTA exit each).  Steps are issued on
+    the current stream of the pool's device; one runner serves one step at a time.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_q_heads: int, max_batch: int,
                  max_blocks_per_seq: int, scale: float, dtype: torch.dtype = torch.bfloat16,
-                 k_scale: float | None = None, v_scale: float | None = None, zero_copy: bool = True):
+                 k_scale: float | None = None, v_scale: float | None = None, zero_copy: bool = True,
+                 group_caps: tuple[int, int, int] | None = None):
         self.fp8 = k_cache.dtype in _FP8_POOL
         if self.fp8:
             if k_scale is None or v_scale is None:
@@ -70,6 +76,9 @@ class DecodeGraphRunner:
         self.scale, self.k_scale, self.v_scale = float(scale), k_scale, v_scale
         self.dtype = dtype
         self.zero_copy = zero_copy
+        if group_caps is not None and (self.fp8 or min(group_caps) < 1):
+            raise ValueError("group_caps: positive (groups, members, prefix tokens), 16-bit pools only")
+        self.group_caps = group_caps
         self.sizes = graph_batch_sizes(max_batch)
         dev = k_cache.device
         esz = torch.empty(0, dtype=dtype).element_size()
@@ -85,7 +94,11 @@ class DecodeGraphRunner:
             self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
             self.dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
         ws_fn = decode_fp8_workspace_bytes if self.fp8 else decode_workspace_bytes
-        ws = max(ws_fn(b, num_q_heads, hkv, d, max_blocks_per_seq, bs) for b in self.sizes)
+        if group_caps is not None:
+            ws = max(decode_workspace_bytes(b, num_q_heads, hkv, d, max_blocks_per_seq, bs, self._options(b, None))
+                     for b in self.sizes)
+        else:
+            ws = max(ws_fn(b, num_q_heads, hkv, d, max_blocks_per_seq, bs) for b in self.sizes)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
         self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
         self._capture()
@@ -99,6 +112,11 @@ class DecodeGraphRunner:
                   ("slot_mapping", (b,), torch.int32, 4 * b),
                   ("context_lens", (b,), torch.int32, 4 * b),
                   ("block_tables", (b, mb), torch.int32, 4 * b * mb)]
+        if self.group_caps is not None:
+            ng = self.group_caps[0]
+            fields += [("group_offsets", (ng + 1,), torch.int32, 4 * (ng + 1)),
+                       ("group_seqs", (b,), torch.int32, 4 * b),
+                       ("prefix_lens", (b,), torch.int32, 4 * b)]
         lay, off = {}, 0
         for name, shape, dt, nbytes in fields:
             lay[name] = (off, shape, dt, nbytes)
@@ -119,6 +137,17 @@ class DecodeGraphRunner:
         n = b * self.num_q_heads * self.head_dim
         return buf.view(self.dtype)[:n].view(b, self.num_q_heads, self.head_dim)
 
+    def _options(self, b: int, views: dict | None) -> DecodeOptions | None:
+        """The decode options of bucket b: the staged groups at their captured capacities."""
+        if self.group_caps is None:
+            return None
+        ng, members, prefix = self.group_caps
+        if views is None:  # sizing only
+            z = torch.zeros(max(b, ng + 1), dtype=torch.int32)
+            return DecodeOptions(groups=PrefixGroups(z[:ng + 1], z[:b], z[:b], members, prefix))
+        return DecodeOptions(groups=PrefixGroups(views["group_offsets"], views["group_seqs"], views["prefix_lens"],
+                                                 members, prefix))
+
     # ----------------------------------------------------------------- capture
     def _launch(self, b: int) -> None:
         lay = self._layout[b]
@@ -135,7 +164,8 @@ class DecodeGraphRunner:
                              out=out, workspace=self.workspace)
         else:
             store_decode(v["k_new"], v["v_new"], v["slot_mapping"], v["q"], self.k_cache, self.v_cache,
-                         v["block_tables"], v["context_lens"], self.scale, out=out, workspace=self.workspace)
+                         v["block_tables"], v["context_lens"], self.scale, out=out, workspace=self.workspace,
+                         options=self._options(b, v))
         if not self.zero_copy:
             self._out_view(self.host_out, b).copy_(out, non_blocking=True)
 
@@ -145,6 +175,9 @@ class DecodeGraphRunner:
             h = self._views(self.host_in, b)
             h["slot_mapping"].fill_(-1)
             h["context_lens"].zero_()
+            if self.group_caps is not None:  # empty groups, no shared prefix
+                h["group_offsets"].zero_()
+                h["prefix_lens"].zero_()
         stream = torch.cuda.Stream(device=self.k_cache.device)
         stream.wait_stream(torch.cuda.current_stream(self.k_cache.device))
         with torch.cuda.stream(stream):
@@ -170,21 +203,78 @@ class DecodeGraphRunner:
         ``batch``, or use :meth:`set_inputs`)."""
         return self._views(self.host_in, self.bucket(batch))
 
-    def set_inputs(self, q, k_new, v_new, slot_mapping, context_lens, block_tables) -> int:
+    def set_inputs(self, q, k_new, v_new, slot_mapping, context_lens, block_tables,
+                   groups: PrefixGroups | None = None, share_prefixes: bool = False) -> int:
         """Copy one step's host tensors into the pinned staging of its bucket and pad the rest
-        (slot -1, context length 0).  Returns the bucket size."""
+        (slot -1, context length 0; groups past the step's are empty).  The shared-prefix groups
+        are ``groups``, or with ``share_prefixes`` derived by ``pa_prefix_groups`` from the staged
+        block tables, written straight into the staging.  Returns the bucket size."""
         batch = q.shape[0]
         b = self.bucket(batch)
         h = self._views(self.host_in, b)
+        if share_prefixes:
+            if self.group_caps is None:
+                raise ValueError("this runner was built without group_caps")
+            self._stage_tables(h, batch, context_lens, block_tables)
+            self._derive_groups(h, batch)
+        elif self.group_caps is not None:
+            ng, members, prefix = self.group_caps
+            h["prefix_lens"].zero_()
+            if groups is None or groups.num_groups == 0:
+                h["group_offsets"].zero_()
+            else:
+                if groups.num_groups > ng or groups.max_group_size > members or groups.max_prefix_len > prefix:
+                    raise ValueError(f"groups ({groups.num_groups}, {groups.max_group_size}, {groups.max_prefix_len}) "
+                                     f"exceed the captured capacities {self.group_caps}")
+                g = groups.num_groups
+                off = groups.group_offsets
+                h["group_offsets"][:g + 1].copy_(off)
+                h["group_offsets"][g + 1:].fill_(int(off[g]))
+                n = int(off[g])
+                h["group_seqs"][:n].copy_(groups.group_seqs[:n])
+                h["prefix_lens"][:batch].copy_(groups.prefix_lens[:batch])
+        elif groups is not None and groups.num_groups:
+            raise ValueError("this runner was built without group_caps")
         h["q"][:batch].copy_(q)
         h["k_new"][:batch].copy_(k_new)
         h["v_new"][:batch].copy_(v_new)
         h["slot_mapping"].fill_(-1)
         h["slot_mapping"][:batch].copy_(slot_mapping)
+        if not share_prefixes:
+            self._stage_tables(h, batch, context_lens, block_tables)
+        return b
+
+    @staticmethod
+    def _stage_tables(h: dict, batch: int, context_lens, block_tables) -> None:
         h["context_lens"].zero_()
         h["context_lens"][:batch].copy_(context_lens)
         h["block_tables"][:batch, :block_tables.shape[1]].copy_(block_tables)
-        return b
+
+    def _derive_groups(self, h: dict, batch: int) -> None:
+        """pa_prefix_groups over the staged tables and lengths, into the staged group fields."""
+        ng, members, prefix = self.group_caps
+        n, big, longest = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        i32 = lambda t: ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+        h["prefix_lens"].zero_()
+        # room for the largest possible output, which may exceed the captured groups: counted below
+        off = self._group_offsets_scratch(batch)
+        rc = _lib.pa_prefix_groups(i32(h["block_tables"]), self.max_blocks, i32(h["context_lens"]), batch,
+                                   self.k_cache.shape[1], 1, i32(off), i32(h["group_seqs"]), i32(h["prefix_lens"]),
+                                   ctypes.byref(n), ctypes.byref(big), ctypes.byref(longest))
+        if rc != 0:
+            raise PagedAttentionError("pa_prefix_groups", rc)
+        if n.value > ng or big.value > members or longest.value > prefix:
+            raise ValueError(f"the step's groups ({n.value}, {big.value}, {longest.value}) exceed the captured "
+                             f"capacities {self.group_caps}")
+        g = h["group_offsets"]
+        g[:n.value + 1].copy_(off[:n.value + 1])
+        g[n.value + 1:].fill_(int(off[n.value]))
+
+    def _group_offsets_scratch(self, batch: int) -> torch.Tensor:
+        need = batch // 2 + 1
+        if getattr(self, "_off_scratch", None) is None or self._off_scratch.numel() < need:
+            self._off_scratch = torch.zeros(need, dtype=torch.int32)
+        return self._off_scratch
 
     def replay(self, batch: int) -> torch.Tensor:
         """Replay the bucket's graph (inputs from the pinned staging) on the current stream; the
@@ -193,9 +283,11 @@ class DecodeGraphRunner:
         self.graphs[b].replay()
         return self._out_view(self.host_out, b)[:batch]
 
-    def step(self, q, k_new, v_new, slot_mapping, context_lens, block_tables) -> torch.Tensor:
-        """One decode step from host tensors to the host output [batch, H_q, D] (synchronises)."""
-        self.set_inputs(q, k_new, v_new, slot_mapping, context_lens, block_tables)
+    def step(self, q, k_new, v_new, slot_mapping, context_lens, block_tables,
+             groups: PrefixGroups | None = None, share_prefixes: bool = False) -> torch.Tensor:
+        """One decode step from host tensors to the host output [batch, H_q, D] (synchronises);
+        groups as :meth:`set_inputs`."""
+        self.set_inputs(q, k_new, v_new, slot_mapping, context_lens, block_tables, groups, share_prefixes)
         out = self.replay(q.shape[0])
         torch.cuda.current_stream(self.k_cache.device).synchronize()
         return out

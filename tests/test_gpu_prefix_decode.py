@@ -138,3 +138,4 @@ def test_shared_prefix_bad_descriptors_are_flagged_not_fatal(pa):
 def inputs_groups(pa, g, prefix_lens):
     return pa.DecodeOptions(groups=pa.PrefixGroups(g.group_offsets, g.group_seqs, prefix_lens, g.max_group_size,
                                                    max(g.max_prefix_len, int(prefix_lens.max()))))
+

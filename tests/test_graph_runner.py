@@ -77,3 +77,36 @@ def test_runner_equals_eager_step(pa, fp8, zero_copy):
         oracle.store_kv(st.k_new, st.v_new, okc, ovc, st.slot_mapping)
         ref = oracle.decode(st.q, okc, ovc, st.block_tables, st.context_lens, st.scale)
     assert max_err(got, ref) <= TOL[st.q.dtype]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("zero_copy", [True, False])
+def test_runner_with_shared_prefix_groups(pa, zero_copy):
+    # a runner captured for shared-prefix groups: steps with their groups (fewer than the capacity,
+    # and none at all) replayed from the staging, each against the oracle
+    from paged_kv_cache_bs_gb300.block_manager import prefix_groups
+    from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
+    seqs = [(600 + 37 * i, i // 6, 512) for i in range(18)] + [(90 + i, -1, 0) for i in range(5)]
+    st = inputs.make_decode_shared(seqs, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                   dtype=torch.bfloat16, seed=181)
+    kc, vc = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    runner = DecodeGraphRunner(kc, vc, 32, 24, st.block_tables.shape[1], st.scale, torch.bfloat16,
+                               zero_copy=zero_copy, group_caps=(4, 8, 1024))
+    okc, ovc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+    steps = [st, inputs.next_decode_step(st, seed=182)]
+    for i, s in enumerate(steps * 3):
+        # the groups passed in, none (plain decode), or derived by the runner from the staged tables
+        g = prefix_groups(s.block_tables, s.context_lens, 16) if i < 2 else None
+        if g is not None:
+            assert g.num_groups == 3
+        got = runner.step(s.q, s.k_new, s.v_new, s.slot_mapping, s.context_lens, s.block_tables, groups=g,
+                          share_prefixes=i >= 4)
+        if i >= 4:
+            assert int(runner.host_inputs(s.q.shape[0])["group_offsets"][3]) == 18
+        oracle.store_kv(s.k_new, s.v_new, okc, ovc, s.slot_mapping)
+        ref = oracle.decode(s.q, okc, ovc, s.block_tables, s.context_lens, s.scale)
+        assert max_err(got, ref) <= TOL[torch.bfloat16], f"step {i}"
+    with pytest.raises(ValueError):
+        big = prefix_groups(st.block_tables, st.context_lens, 16)
+        runner.set_inputs(st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables,
+                          groups=pa.PrefixGroups(big.group_offsets, big.group_seqs, big.prefix_lens, 9, 512))
