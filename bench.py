@@ -66,7 +66,9 @@ TRAFFIC_PER_CALL = {
     "qwen3_0p6b_decode": 575_843_072 + 4_158_720,       # decode_partition_kernel (store fused)
     "qwen3_0p6b_decode_fp8": 288_197_120 + 4_085_248,   # decode_partition_kernel, E4M3 pool (store fused)
     "long_context_decode": 536_962_560 + 3_218_944,     # decode_partition_kernel (store fused)
-    "qwen3_8b_shared_decode": 869_801_728 + 5_674_752,  # decode_partition_kernel (store fused; L2 absorbs shared pages)
+    # both grids of the step with shared-prefix groups: decode_partition_kernel (sequences; store fused)
+    # + decode_prefix_kernel (each group's shared pages once)
+    "qwen3_8b_shared_decode": 805_121_536 + 2_861_056 + 69_261_056 + 66_304,
 }
 PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 119_218_432 + 13_745_408}  # prefill_kernel (ncu, current code)
 # store_kv_kernel on store_stress: DRAM read + write inside the launch (the L2 holds most written
