@@ -421,9 +421,12 @@ PA_API int pa_store_decode_fp8(const void *k, const void *v, int64_t k_row_strid
  *   out           [total_q, num_q_heads, head_dim] contiguous, written.
  * Buffers q, k, v, k_cache, v_cache must be 16-byte aligned (TMA); scale must
  * be positive (the kernel takes the row maximum of the unscaled scores).
- * QK^T and PV run on the tensor cores (tcgen05, accumulators in TMEM), one
- * CTA per 128 query rows of one head; K/V tiles of 128 keys come through the
- * block table by TMA.
+ * QK^T and PV run on the tensor cores (tcgen05, accumulators in TMEM); a work
+ * item is 128 query rows of two query heads of one GQA group (one head without
+ * GQA), and K/V tiles of 128 keys come through the block table by TMA.  The
+ * grid is persistent: one CTA per SM of the device, each working through its
+ * share of the items (dealt out longest first) with the K/V stream running on
+ * from one item into the next.
  */
 PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache,
                      const void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
@@ -431,6 +434,28 @@ PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const v
                      const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_q_heads,
                      int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                      float scale, void *out, pa_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
+ * pa_prefill_paged_ex -- pa_prefill_paged with launch options (opt may be
+ * NULL: the defaults, which is pa_prefill_paged).
+ *   max_ctas  0: one CTA per SM of the device.  Otherwise the kernel occupies
+ *             at most max_ctas SMs (1 <= max_ctas <= 65535): pass the SM count
+ *             of the partition when `stream` belongs to a green context with
+ *             fewer SMs than the device, or to leave SMs to concurrent work.
+ *             The results do not depend on it, bit for bit: an item is
+ *             computed the same way whichever CTA takes it.
+ * PA_ERR_INVALID_ARG for a max_ctas outside that range.
+ */
+typedef struct pa_prefill_options {
+    int32_t max_ctas;
+} pa_prefill_options;
+PA_API int pa_prefill_paged_ex(const void *q, const void *k, const void *v, const void *k_cache,
+                               const void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                               int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                               float scale, void *out, pa_dtype dtype, int32_t *err_flag,
+                               const pa_prefill_options *opt, void *stream);
 
 /*
  * pa_selftest_wait_timeout -- a diagnostic with no counterpart on the pages:

@@ -99,6 +99,14 @@ _lib.pa_prefill_paged.restype = ctypes.c_int
 _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _i32, _i32, _i32, _i32,
                                   _i32, _i32, _f32, _p, ctypes.c_int, _p, _p]
 
+
+class _PrefillOptions(ctypes.Structure):
+    _fields_ = [("max_ctas", ctypes.c_int32)]
+
+
+_lib.pa_prefill_paged_ex.restype = ctypes.c_int
+_lib.pa_prefill_paged_ex.argtypes = _lib.pa_prefill_paged.argtypes[:-1] + [ctypes.POINTER(_PrefillOptions), _p]
+
 PA_F16, PA_BF16, PA_F32, PA_E4M3 = 0, 1, 2, 3
 _FP8_POOL = (torch.uint8, torch.float8_e4m3fn)  # E4M3 codes, one byte per element
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
@@ -328,8 +336,11 @@ def store_decode(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q
 def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | None, k_cache: torch.Tensor,
                   v_cache: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                   max_seqlen_q: int, max_seqlen_k: int, block_tables: torch.Tensor | None, scale: float,
-                  out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None) -> torch.Tensor:
-    """Causal varlen prefill over a paged prefix: q [Tq, H_q, D] -> out [Tq, H_q, D]."""
+                  out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+                  max_ctas: int = 0) -> torch.Tensor:
+    """Causal varlen prefill over a paged prefix: q [Tq, H_q, D] -> out [Tq, H_q, D].
+    ``max_ctas`` > 0 caps the persistent grid (``pa_prefill_paged_ex``), e.g. at the SM count of
+    a green-context partition."""
     n, bs, hkv, d = _cache_shape(k_cache, v_cache)
     tq, hq = q.shape[0], q.shape[1]
     if not q.is_contiguous():
@@ -344,11 +355,17 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
             raise ValueError(f"{name} must be contiguous")
     if out is None:
         out = torch.empty(tq, hq, d, dtype=q.dtype, device=q.device)
-    rc = _lib.pa_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
-                               _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, tq, int(max_seqlen_q), int(max_seqlen_k),
-                               _ptr(block_tables), block_tables.shape[1] if block_tables is not None else 0,
-                               hq, hkv, d, n, bs, float(scale), _ptr(out), _dtype(q), _ptr(err_flag), _stream(q))
-    _check("pa_prefill_paged", rc)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            cu_seqlens_q.numel() - 1, tq, int(max_seqlen_q), int(max_seqlen_k), _ptr(block_tables),
+            block_tables.shape[1] if block_tables is not None else 0, hq, hkv, d, n, bs, float(scale), _ptr(out),
+            _dtype(q), _ptr(err_flag))
+    if max_ctas:
+        opt = _PrefillOptions(int(max_ctas))
+        rc = _lib.pa_prefill_paged_ex(*args, ctypes.byref(opt), _stream(q))
+        _check("pa_prefill_paged_ex", rc)
+    else:
+        rc = _lib.pa_prefill_paged(*args, _stream(q))
+        _check("pa_prefill_paged", rc)
     return out
 
 

@@ -390,6 +390,10 @@ int check_prefill(const void *q, const void *k, const void *v, const void *k_cac
         return fail(PA_ERR_INVALID_ARG, "sizes: num_seqs %d, total_q %d, max_seqlen_q %d, max_seqlen_k %d", num_seqs,
                     total_q, max_seqlen_q, max_seqlen_k);
     if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PA_OK;
+    // work items: (sequence, 128-row q tile, query head pair), counted in 32-bit in the kernel
+    if (static_cast<int64_t>(num_seqs) * ((max_seqlen_q + 127) / 128) * num_q_heads >= (1LL << 31))
+        return fail(PA_ERR_INVALID_ARG, "num_seqs %d x max_seqlen_q %d x num_q_heads %d is too large", num_seqs,
+                    max_seqlen_q, num_q_heads);
     if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !out)
         return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
     if (!block_tables && (!k || !v)) return fail(PA_ERR_INVALID_ARG, "k and v are required without block_tables");
@@ -409,12 +413,15 @@ int check_prefill(const void *q, const void *k, const void *v, const void *k_cac
 
 extern "C" {
 
-int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
-                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
-                     int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
-                     int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                     int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
-                     int32_t *err_flag, void *stream) {
+int pa_prefill_paged_ex(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                        int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
+                        int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
+                        int32_t *err_flag, const pa_prefill_options *opt, void *stream) {
+    const int32_t max_ctas = opt ? opt->max_ctas : 0;
+    if (max_ctas < 0 || max_ctas > 65535)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_paged_ex: max_ctas %d is not in [0, 65535]", max_ctas);
     bool work = false;
     const int rc = check_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
                                  max_seqlen_q, max_seqlen_k, block_tables, max_blocks_per_seq, num_q_heads,
@@ -428,9 +435,21 @@ int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_
     const cudaError_t e = pa::launch_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs,
                                              total_q, max_seqlen_q, block_tables, max_blocks_per_seq, num_q_heads,
                                              num_kv_heads, head_dim, num_blocks, block_size, scale, out, dtype,
-                                             err_flag, static_cast<cudaStream_t>(stream), &why);
+                                             err_flag, max_ctas, static_cast<cudaStream_t>(stream), &why);
     if (why) return fail(PA_ERR_CUDA, "pa_prefill_paged: %s", why);
     return cuda_status(e, "pa_prefill_paged launch");
+}
+
+int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_cache, const void *v_cache,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                     int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
+                     int32_t *err_flag, void *stream) {
+    return pa_prefill_paged_ex(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
+                               max_seqlen_q, max_seqlen_k, block_tables, max_blocks_per_seq, num_q_heads,
+                               num_kv_heads, head_dim, num_blocks, block_size, scale, out, dtype, err_flag, nullptr,
+                               stream);
 }
 
 int pa_sample(const void *logits, int64_t logits_row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
@@ -507,7 +526,7 @@ int pa_mixed_step(const void *k, const void *v, int64_t k_row_stride, int64_t v_
         e = pa::launch_prefill(prefill_q, nullptr, nullptr, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
                                num_prefill_seqs, total_prefill_q, max_seqlen_q, prefill_block_tables,
                                prefill_max_blocks, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
-                               prefill_out, dtype, err_flag, s_prefill, &why);
+                               prefill_out, dtype, err_flag, both ? pa::split_sms(split, 0) : 0, s_prefill, &why);
         if (why) return fail(PA_ERR_CUDA, "pa_mixed_step: %s", why);
     }
     if (e == cudaSuccess && decode)

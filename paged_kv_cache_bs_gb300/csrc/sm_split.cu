@@ -104,6 +104,7 @@ void release(pa_sm_split *s) {
 }  // namespace
 
 cudaStream_t split_stream(const pa_sm_split *s, int i) { return s->stream[i]; }
+int split_sms(const pa_sm_split *s, int i) { return s->sms[i]; }
 int split_device(const pa_sm_split *s) { return s->device; }
 
 cudaError_t split_fork(const pa_sm_split *s, cudaStream_t from) {

@@ -138,6 +138,24 @@ def test_prefill_validation(lib):
     assert call(q=ctypes.c_void_p((1 << 20) + 8)) == -1   # TMA needs 16-byte alignment
     assert call(scale=0.0) == -1 and call(scale=-0.1) == -1
     assert call(S=0) == 0 and call(tq=0) == 0
+    # (sequence, q tile, head pair) work items are counted in 32 bits
+    assert call(S=65535, tq=1 << 30, mq=1 << 20, mk=1 << 20) == -1
+
+
+def test_prefill_ex_validation(lib):
+    import paged_kv_cache_bs_gb300 as pa
+    Opt = pa._PrefillOptions  # the binding's mirror of pa_prefill_options
+    f = lib.pa_prefill_paged_ex
+
+    def call(opt, **kw):
+        a = dict(S=8, tq=4096, mq=512, mk=4096, kc=FAKE)
+        a.update(kw)
+        return f(FAKE, FAKE, FAKE, a["kc"], FAKE, FAKE, FAKE, a["S"], a["tq"], a["mq"], a["mk"], FAKE, 16, 32, 8, 128,
+                 600, 256, ctypes.c_float(0.088), FAKE, 1, None, opt, None)
+    assert call(ctypes.byref(Opt(-1))) == -1
+    assert call(ctypes.byref(Opt(65536))) == -1
+    assert call(ctypes.byref(Opt(4)), kc=None) == -1          # the usual checks still apply
+    assert call(ctypes.byref(Opt(4)), S=0) == 0 and call(None, S=0) == 0
 
 
 def test_store_decode_validation(lib):

@@ -119,6 +119,77 @@ def test_prefill_mixed_workload_every_row(pa):
     print(f"mixed workload prefill, all {cq[-1]} rows (prefixes {prefixes}): max|err| {max(errs):.2e}")
 
 
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 8), (8, 1, 256), (4, 4, 16)])
+def test_prefill_row_seeing_one_key_returns_its_value_row(pa, hq, hkv, bs):
+    # The first query row of a fresh prompt sees one key, its own: weight 1, so the output is that
+    # token's value row for every head of the group, bit for bit (the row maximum, the exponent and
+    # the sum must agree exactly; any column of the 128-key tile leaking into the maximum shows).
+    chunk = [1, 64, 128, 129, 300, 7]
+    st, _ = inputs.make_prefill([0] * len(chunk), chunk, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                                block_size=bs, dtype=torch.bfloat16, seed=96 + bs)
+    out, _, _ = run_prefill_gpu(pa, st)
+    out = out.cpu()
+    for r in st.cu_seqlens_q[:-1].tolist():
+        expect = st.v_new[r].repeat_interleave(hq // hkv, dim=0)
+        assert_bit_equal(out[r], expect, f"row {r}")
+
+
+@pytest.mark.parametrize("max_ctas", [1, 3, 16])
+def test_prefill_few_ctas_many_items_each(pa, max_ctas):
+    # the persistent grid capped at a few CTAs: each works through many items, so the K/V stream
+    # runs across item boundaries (short and long items, chunks of 1 row to several tiles, an empty
+    # chunk, block sizes below the tile); results equal the oracle and, bit for bit, the full grid
+    prefix = [0, 5, 300, 1000, 77, 2000, 0]
+    chunk = [7, 200, 1, 129, 300, 0, 260]
+    st, _ = inputs.make_prefill(prefix, chunk, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=64,
+                                dtype=torch.bfloat16, seed=94 + max_ctas)
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    pa.store_kv(st.k_new.cuda(), st.v_new.cuda(), kc, vc, st.slot_mapping.cuda())
+    args = (st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(), st.max_seqlen_q,
+            st.max_seqlen_k, st.block_tables.cuda(), st.scale)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    few = pa.prefill_paged(*args, err_flag=flag, max_ctas=max_ctas)
+    full = pa.prefill_paged(*args)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    assert_bit_equal(few, full, f"max_ctas {max_ctas} vs the full grid")
+    okc, ovc = oracle_after_store(st)
+    ref = oracle.prefill_paged(st.q, st.k_new, st.v_new, okc, ovc, st.cu_seqlens_q, st.cu_seqlens_k,
+                               st.block_tables, st.scale)
+    assert max_err(few, ref) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype,head_dim,hq,hkv", [(torch.float16, 64, 4, 4), (torch.bfloat16, 128, 8, 1)])
+def test_prefill_one_cta_without_gqa_pairs_and_packed_keys(pa, dtype, head_dim, hq, hkv):
+    # one CTA for every item: heads one per item without GQA (hq == hkv), two per item with it;
+    # keys from the packed rows (no block table)
+    st, _ = inputs.make_prefill([0, 0, 0], [11, 300, 129], num_q_heads=hq, num_kv_heads=hkv, head_dim=head_dim,
+                                block_size=16, dtype=dtype, seed=95 + hq)
+    out = pa.prefill_paged(st.q.cuda(), st.k_new.cuda(), st.v_new.cuda(), st.pool.k_cache.cuda(),
+                           st.pool.v_cache.cuda(), st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(), st.max_seqlen_q,
+                           st.max_seqlen_k, None, st.scale, max_ctas=1)
+    torch.cuda.synchronize()
+    ref = oracle.prefill_paged(st.q, st.k_new, st.v_new, st.pool.k_cache, st.pool.v_cache, st.cu_seqlens_q,
+                               st.cu_seqlens_k, None, st.scale)
+    assert max_err(out, ref) <= TOL[dtype]
+
+
+def test_prefill_mixed_workload_capped_grid_bit_equal(pa):
+    # the full mixed workload on 40 CTAs (about 13 items each) equals the default grid bit for bit
+    m = inputs.mixed_chunked_prefill()
+    st = m.prefill
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    pa.store_kv(m.k_new.cuda(), m.v_new.cuda(), kc, vc, m.slot_mapping.cuda())
+    args = (st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(), st.max_seqlen_q,
+            st.max_seqlen_k, st.block_tables.cuda(), st.scale)
+    a = pa.prefill_paged(*args, max_ctas=40)
+    b = pa.prefill_paged(*args)
+    torch.cuda.synchronize()
+    assert_bit_equal(a, b, "40 CTAs vs the full grid")
+
+
 def test_prefill_bad_metadata_is_flagged_not_fatal(pa):
     st, _ = inputs.make_prefill([40, 40], [30, 30], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
                                 dtype=torch.bfloat16, seed=93)
