@@ -331,11 +331,14 @@ class DecodeWorkload:
             from tests import inputs
             st = self.st
             self.runner = self.make_runner(zero_copy=True)
-            self.e2e_inputs = [self.runner_args(st), self.runner_args(inputs.next_decode_step(st, seed=4242))]
-            self.e2e_path = ("DecodeGraphRunner.step() from the caller's host tensors, alternating two seeded "
-                             "decode steps over the same pool: the step's inputs copied into the pinned staging, "
-                             "CUDA-graph replay of the fused store + decode whose kernels read that staging and "
-                             "write the output into pinned host memory over NVLink-C2C, stream sync; host wall "
+            # the caller's step inputs in page-locked host memory (allocated once, outside the timing)
+            pin = lambda args: tuple(t.contiguous().pin_memory() for t in args)  # noqa: E731
+            self.e2e_inputs = [pin(self.runner_args(st)), pin(self.runner_args(inputs.next_decode_step(st, seed=4242)))]
+            self.e2e_path = ("DecodeGraphRunner.step() from the caller's page-locked host tensors, alternating two "
+                             "seeded decode steps over the same pool: slot mapping, context lengths and block tables "
+                             "copied into the pinned staging, CUDA-graph replay whose first kernel (pa_copy_segments) "
+                             "pulls q and the new K/V rows from the caller's tensors over NVLink-C2C, then the fused "
+                             "store + decode writing the output into pinned host memory, stream sync; host wall "
                              "clock" + ("; the shared-prefix groups derived from the staged block tables "
                                         "(pa_prefix_groups, C++) every step" if self.groups is not None else ""))
             return None, None, self.runner.h2d_bytes(st.batch), self.runner.d2h_bytes(st.batch)

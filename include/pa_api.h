@@ -458,6 +458,28 @@ PA_API int pa_prefill_paged_ex(const void *q, const void *k, const void *v, cons
                                const pa_prefill_options *opt, void *stream);
 
 /*
+ * pa_copy_segments -- `count` copies (0 <= count <= 64) in one kernel on `stream`.
+ * The list `segments` is read when the kernel runs, from device memory or
+ * page-locked host memory (cudaHostAlloc / cudaMallocHost), and each src / dst
+ * is a device-accessible address (device memory, or page-locked host memory
+ * through its host pointer).  So a CUDA graph that begins with this call reads
+ * a new step's inputs where the caller left them once the caller rewrites the
+ * list: the step's inputs need no host-side copy into the graph's staging, and
+ * all SMs pull them over the CPU-GPU link at once.  Segments must not overlap
+ * one another's destinations; the copy uses 16-byte accesses where both
+ * addresses are 16-byte aligned.  The pages describe no such call (the
+ * library's way of feeding the decode step of "Inference engine: inside
+ * nano-vLLM", section "Attention in nano-vLLM", from host buffers).
+ * PA_ERR_INVALID_ARG for a count outside [0, 64] or a null list with count > 0.
+ */
+typedef struct pa_copy_segment {
+    const void *src;
+    void *dst;
+    uint64_t bytes;
+} pa_copy_segment;
+PA_API int pa_copy_segments(const pa_copy_segment *segments, int32_t count, void *stream);
+
+/*
  * pa_selftest_wait_timeout -- a diagnostic with no counterpart on the pages:
  * shows on a live GPU that the library's bounded waits end with a status
  * instead of a hang.  Launches one thread on `stream` that waits on an

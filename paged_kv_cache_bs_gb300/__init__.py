@@ -107,6 +107,14 @@ class _PrefillOptions(ctypes.Structure):
 _lib.pa_prefill_paged_ex.restype = ctypes.c_int
 _lib.pa_prefill_paged_ex.argtypes = _lib.pa_prefill_paged.argtypes[:-1] + [ctypes.POINTER(_PrefillOptions), _p]
 
+class CopySegment(ctypes.Structure):
+    """Mirror of pa_copy_segment."""
+    _fields_ = [("src", _p), ("dst", _p), ("bytes", ctypes.c_uint64)]
+
+
+_lib.pa_copy_segments.restype = ctypes.c_int
+_lib.pa_copy_segments.argtypes = [_p, _i32, _p]
+
 PA_F16, PA_BF16, PA_F32, PA_E4M3 = 0, 1, 2, 3
 _FP8_POOL = (torch.uint8, torch.float8_e4m3fn)  # E4M3 codes, one byte per element
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
@@ -369,6 +377,16 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     return out
 
 
+def copy_segments(segments_ptr: int, count: int, stream: int | None = None) -> None:
+    """``pa_copy_segments``: ``count`` copies in one kernel, the :class:`CopySegment` list at
+    address ``segments_ptr`` (page-locked host or device memory) read when the kernel runs;
+    ``stream`` is a raw stream handle (default: the current stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check("pa_copy_segments", _lib.pa_copy_segments(ctypes.c_void_p(segments_ptr), int(count),
+                                                       ctypes.c_void_p(stream)))
+
+
 def selftest_wait_timeout(err_flag: torch.Tensor, max_cycles: int = 2_000_000) -> None:
     """``pa_selftest_wait_timeout``: a bounded wait that nothing satisfies gives up after
     ``max_cycles`` and ORs FLAG_TIMEOUT into ``err_flag`` (a CUDA int32 tensor)."""
@@ -568,7 +586,7 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
     return out
 
 
-__all__ = ["store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
+__all__ = ["copy_segments", "CopySegment", "store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
            "store_decode_fp8", "mixed_step", "SmSplit",
            "decode_workspace_bytes", "decode_fp8_workspace_bytes", "alloc_decode_workspace", "library",
            "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "PA_E4M3", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",

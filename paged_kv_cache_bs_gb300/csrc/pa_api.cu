@@ -452,6 +452,23 @@ int pa_prefill_paged(const void *q, const void *k, const void *v, const void *k_
                                stream);
 }
 
+int pa_copy_segments(const pa_copy_segment *segments, int32_t count, void *stream) {
+    if (count < 0 || count > 64 || (count > 0 && !segments))
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_segments: count %d (0..64) with a segment list", count);
+    if (count == 0) {
+        g_err[0] = '\0';
+        return PA_OK;
+    }
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (!sms[dev] && (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                      sms[dev] <= 0))
+        sms[dev] = 148;
+    return cuda_status(pa::launch_copy_segments(segments, count, 2 * sms[dev], static_cast<cudaStream_t>(stream)),
+                       "pa_copy_segments launch");
+}
+
 int pa_sample(const void *logits, int64_t logits_row_stride, int32_t batch, int32_t vocab, pa_dtype dtype,
               const float *temperatures, const float *noise, uint64_t seed, uint64_t offset, int32_t *tokens,
               int32_t *err_flag, void *stream) {

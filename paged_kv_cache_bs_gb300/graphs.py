@@ -10,13 +10,18 @@ the output.
 
 Here one graph holds the whole step of one attention layer.  By default
 (``zero_copy=True``) it is the fused store + decode (``pa_store_decode``, or
-``pa_store_decode_fp8`` over an E4M3 pool) with its small per-step operands in
-pinned host memory: the kernels read q, the new K/V rows, the slot mapping,
-context lengths and block tables from the pinned staging and write the output
-into pinned memory directly over the CPU-GPU link (NVLink-C2C on a Grace-based
-GB300), so the step has no copy-engine transfer, whose start-up latency is
-longer than the transfer of these few hundred KB.  With ``zero_copy=False``
-the graph holds a host-to-device copy of the packed inputs, the fused call on
+``pa_store_decode_fp8`` over an E4M3 pool) with its per-step operands in host
+memory, read over the CPU-GPU link (NVLink-C2C on a Grace-based GB300): the
+kernels read the slot mapping, context lengths and block tables from the
+pinned staging and write the output into pinned memory directly, so the step
+has no copy-engine transfer, whose start-up latency is longer than the
+transfer of these few MB.  q and the new K/V rows come one of two ways, each
+bucket holding a graph for both: when the caller's tensors are page-locked,
+the graph begins with ``pa_copy_segments``, which pulls them with all SMs into
+device buffers from where they are (their addresses written into a pinned
+segment list each step: no host-side copy); otherwise they are copied into the
+pinned staging and the kernels read them there.  With ``zero_copy=False`` the
+graph holds a host-to-device copy of the packed inputs, the fused call on
 device buffers and a device-to-host copy of the output.  Argument marshalling
 only: every step of the path runs in the library's kernels.
 """
@@ -27,7 +32,7 @@ import ctypes
 
 import torch
 
-from . import (_fp8_pool, _FP8_POOL, _lib, DecodeOptions, PagedAttentionError, PrefixGroups,
+from . import (_fp8_pool, _FP8_POOL, _lib, CopySegment, DecodeOptions, PagedAttentionError, PrefixGroups,
                decode_fp8_workspace_bytes, decode_workspace_bytes, store_decode, store_decode_fp8)
 from . import block_manager as _bm  # declares pa_prefix_groups
 
@@ -45,6 +50,15 @@ def graph_batch_sizes(max_batch: int) -> list[int]:
 
 def _align(n: int) -> int:
     return (n + 255) // 256 * 256
+
+
+def _copy_rows(dst: torch.Tensor, src: torch.Tensor, rows: int) -> None:
+    """dst[:rows] = src: one memmove for a contiguous host int32 source (no torch dispatch, no
+    wake-up of torch's copy threads for these few KB), else a torch copy."""
+    if src.device.type == "cpu" and src.dtype == dst.dtype and src.is_contiguous():
+        ctypes.memmove(dst.data_ptr(), src.data_ptr(), rows * dst[0].numel() * dst.element_size())
+    else:
+        dst[:rows].copy_(src)
 
 
 class DecodeGraphRunner:
@@ -84,12 +98,22 @@ class DecodeGraphRunner:
         esz = torch.empty(0, dtype=dtype).element_size()
         # per-bucket packed layout (the same in pinned host memory and on the device)
         self._layout = {b: self._pack_layout(b, esz) for b in self.sizes}
+        self._staged_views, self._staged_out, self._ptr_cache = {}, {}, {}
+        self._group_out = (ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32())
         in_bytes = max(lay["_bytes"] for lay in self._layout.values())
         out_bytes = max(self.sizes) * num_q_heads * d * esz
         self.host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
         self.host_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
+        # the step's q and new K/V rows: device buffers the graph's first kernel fills from the
+        # caller's page-locked tensors (zero_copy); the list of its three copies is pinned
+        self._qkv_names = ("q", "k_new", "v_new")
         if zero_copy:
             self.dev_in = self.dev_out = None
+            lay = self._layout[max(self.sizes)]
+            self._qkv_dev = torch.zeros(sum(lay[n][3] for n in self._qkv_names) + 512, dtype=torch.uint8, device=dev)
+            self._seg_buf = torch.zeros(3 * ctypes.sizeof(CopySegment), dtype=torch.uint8).pin_memory()
+            self._segs = (CopySegment * 3).from_address(self._seg_buf.data_ptr())
+            self._qkv_views = {}
         else:
             self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
             self.dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
@@ -100,7 +124,11 @@ class DecodeGraphRunner:
         else:
             ws = max(ws_fn(b, num_q_heads, hkv, d, max_blocks_per_seq, bs) for b in self.sizes)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+        # per bucket: the graph whose kernels read q and the new rows from the pinned staging, and
+        # (zero_copy) the one that first pulls them from the caller's page-locked tensors
         self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
+        self._gather_graphs: dict[int, torch.cuda.CUDAGraph] = {}
+        self._use_gather: dict[int, bool] = {}
         self._capture()
 
     # ------------------------------------------------------------------ layout
@@ -149,10 +177,40 @@ class DecodeGraphRunner:
                                                  members, prefix))
 
     # ----------------------------------------------------------------- capture
-    def _launch(self, b: int) -> None:
+    def _dev_qkv(self, b: int) -> dict:
+        """Device views of bucket b's q, k_new and v_new (zero_copy)."""
+        views = self._qkv_views.get(b)
+        if views is None:
+            lay, off, views = self._layout[b], 0, {}
+            for n in self._qkv_names:
+                _, shape, dt, nbytes = lay[n]
+                views[n] = self._qkv_dev[off:off + nbytes].view(dt).view(shape)
+                off = _align(off + nbytes)
+            self._qkv_views[b] = views
+        return views
+
+    def _point_segments(self, b: int, batch: int, sources) -> None:
+        """The segment list of a step: source i (a host tensor's address, or the staging's) to
+        bucket b's device buffer, ``batch`` rows."""
+        dev = self._dev_qkv(b)
+        for i, (n, src) in enumerate(zip(self._qkv_names, sources)):
+            seg = self._segs[i]
+            seg.src = src
+            seg.dst = dev[n].data_ptr()
+            seg.bytes = batch * dev[n][0].numel() * dev[n].element_size()
+
+    def _launch(self, b: int, gather: bool = False) -> None:
         lay = self._layout[b]
         if self.zero_copy:
-            v = self._views(self.host_in, b)
+            v = dict(self._views(self.host_in, b))
+            if gather:
+                # capture with the list pointing at the staging (valid memory); steps rewrite it
+                self._point_segments(b, b, [v[n].data_ptr() for n in self._qkv_names])
+                rc = _lib.pa_copy_segments(ctypes.c_void_p(self._seg_buf.data_ptr()), 3,
+                                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                if rc != 0:
+                    raise PagedAttentionError("pa_copy_segments", rc)
+                v.update(self._dev_qkv(b))
             out = self._out_view(self.host_out, b)
         else:
             self.dev_in[:lay["_bytes"]].copy_(self.host_in[:lay["_bytes"]], non_blocking=True)
@@ -180,15 +238,18 @@ class DecodeGraphRunner:
                 h["prefix_lens"].zero_()
         stream = torch.cuda.Stream(device=self.k_cache.device)
         stream.wait_stream(torch.cuda.current_stream(self.k_cache.device))
+        modes = (False, True) if self.zero_copy else (False,)
         with torch.cuda.stream(stream):
             for b in self.sizes:  # warm-up: function attributes and tensor maps are set outside capture
-                self._launch(b)
+                for m in modes:
+                    self._launch(b, m)
         stream.synchronize()
         for b in reversed(self.sizes):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                self._launch(b)
-            self.graphs[b] = g
+            for m in modes:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    self._launch(b, m)
+                (self._gather_graphs if m else self.graphs)[b] = g
         torch.cuda.current_stream(self.k_cache.device).wait_stream(stream)
 
     # -------------------------------------------------------------------- step
@@ -203,6 +264,13 @@ class DecodeGraphRunner:
         ``batch``, or use :meth:`set_inputs`)."""
         return self._views(self.host_in, self.bucket(batch))
 
+    def _staged(self, b: int) -> dict:
+        """The pinned staging views of bucket b (built once: the step path reuses them)."""
+        views = self._staged_views.get(b)
+        if views is None:
+            views = self._staged_views[b] = self._views(self.host_in, b)
+        return views
+
     def set_inputs(self, q, k_new, v_new, slot_mapping, context_lens, block_tables,
                    groups: PrefixGroups | None = None, share_prefixes: bool = False) -> int:
         """Copy one step's host tensors into the pinned staging of its bucket and pad the rest
@@ -211,7 +279,7 @@ class DecodeGraphRunner:
         block tables, written straight into the staging.  Returns the bucket size."""
         batch = q.shape[0]
         b = self.bucket(batch)
-        h = self._views(self.host_in, b)
+        h = self._staged(b)
         if share_prefixes:
             if self.group_caps is None:
                 raise ValueError("this runner was built without group_caps")
@@ -235,29 +303,44 @@ class DecodeGraphRunner:
                 h["prefix_lens"][:batch].copy_(groups.prefix_lens[:batch])
         elif groups is not None and groups.num_groups:
             raise ValueError("this runner was built without group_caps")
-        h["q"][:batch].copy_(q)
-        h["k_new"][:batch].copy_(k_new)
-        h["v_new"][:batch].copy_(v_new)
-        h["slot_mapping"].fill_(-1)
-        h["slot_mapping"][:batch].copy_(slot_mapping)
+        qkv = (q, k_new, v_new)
+        gather = self.zero_copy and all(t.dtype == self.dtype and t.is_contiguous() and t.shape[1:] == h[n].shape[1:]
+                                        and t.is_pinned() for n, t in zip(self._qkv_names, qkv))
+        self._use_gather[b] = gather
+        if gather:
+            # page-locked tensors: the graph's first kernel reads them where they are
+            self._point_segments(b, batch, [t.data_ptr() for t in qkv])
+        else:
+            h["q"][:batch].copy_(q)
+            h["k_new"][:batch].copy_(k_new)
+            h["v_new"][:batch].copy_(v_new)
+        _copy_rows(h["slot_mapping"], slot_mapping, batch)
+        if batch < b:
+            h["slot_mapping"][batch:].fill_(-1)
         if not share_prefixes:
             self._stage_tables(h, batch, context_lens, block_tables)
         return b
 
     @staticmethod
     def _stage_tables(h: dict, batch: int, context_lens, block_tables) -> None:
-        h["context_lens"].zero_()
-        h["context_lens"][:batch].copy_(context_lens)
-        h["block_tables"][:batch, :block_tables.shape[1]].copy_(block_tables)
+        _copy_rows(h["context_lens"], context_lens, batch)
+        if batch < h["context_lens"].shape[0]:
+            h["context_lens"][batch:].zero_()
+        if block_tables.shape[1] == h["block_tables"].shape[1]:
+            _copy_rows(h["block_tables"], block_tables, batch)
+        else:
+            h["block_tables"][:batch, :block_tables.shape[1]].copy_(block_tables)
 
     def _derive_groups(self, h: dict, batch: int) -> None:
-        """pa_prefix_groups over the staged tables and lengths, into the staged group fields."""
+        """pa_prefix_groups over the staged tables and lengths, into the staged group fields
+        (prefix_lens of the step's rows written by the call itself)."""
         ng, members, prefix = self.group_caps
-        n, big, longest = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-        i32 = lambda t: ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_int32))  # noqa: E731
-        h["prefix_lens"].zero_()
+        n, big, longest = self._group_out
+        if batch < h["prefix_lens"].shape[0]:
+            h["prefix_lens"][batch:].zero_()
         # room for the largest possible output, which may exceed the captured groups: counted below
         off = self._group_offsets_scratch(batch)
+        i32 = self._i32_ptr
         rc = _lib.pa_prefix_groups(i32(h["block_tables"]), self.max_blocks, i32(h["context_lens"]), batch,
                                    self.k_cache.shape[1], 1, i32(off), i32(h["group_seqs"]), i32(h["prefix_lens"]),
                                    ctypes.byref(n), ctypes.byref(big), ctypes.byref(longest))
@@ -267,8 +350,17 @@ class DecodeGraphRunner:
             raise ValueError(f"the step's groups ({n.value}, {big.value}, {longest.value}) exceed the captured "
                              f"capacities {self.group_caps}")
         g = h["group_offsets"]
-        g[:n.value + 1].copy_(off[:n.value + 1])
-        g[n.value + 1:].fill_(int(off[n.value]))
+        cnt = n.value + 1
+        ctypes.memmove(g.data_ptr(), off.data_ptr(), 4 * cnt)
+        if cnt < g.shape[0]:
+            g[cnt:].fill_(int(off[n.value]))
+
+    def _i32_ptr(self, t: torch.Tensor):
+        """ctypes int32 pointer of a staging view (cached by address)."""
+        p = self._ptr_cache.get(t.data_ptr())
+        if p is None:
+            p = self._ptr_cache[t.data_ptr()] = ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_int32))
+        return p
 
     def _group_offsets_scratch(self, batch: int) -> torch.Tensor:
         need = batch // 2 + 1
@@ -280,8 +372,11 @@ class DecodeGraphRunner:
         """Replay the bucket's graph (inputs from the pinned staging) on the current stream; the
         returned pinned host view of the output is valid once that stream has synchronised."""
         b = self.bucket(batch)
-        self.graphs[b].replay()
-        return self._out_view(self.host_out, b)[:batch]
+        (self._gather_graphs if self._use_gather.get(b) else self.graphs)[b].replay()
+        out = self._staged_out.get(b)
+        if out is None:
+            out = self._staged_out[b] = self._out_view(self.host_out, b)
+        return out[:batch]
 
     def step(self, q, k_new, v_new, slot_mapping, context_lens, block_tables,
              groups: PrefixGroups | None = None, share_prefixes: bool = False) -> torch.Tensor:

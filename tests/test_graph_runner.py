@@ -66,6 +66,13 @@ def test_runner_equals_eager_step(pa, fp8, zero_copy):
                           st.block_tables[sl])
         assert got.shape == ref.shape
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"batch {batch}: output differs"
+        if zero_copy:
+            # the caller's page-locked tensors, read in place by the graph's first kernel (the step is
+            # stored again: the same rows into the same slots)
+            pinned = [t[sl].contiguous().pin_memory() for t in (st.q, st.k_new, st.v_new, st.slot_mapping,
+                                                               st.context_lens, st.block_tables)]
+            got = runner.step(*pinned).clone()
+            assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"batch {batch}: pinned inputs"
         bits = (lambda t: t.cpu().view(torch.uint8))  # noqa: E731  (NaN sentinels compare by bits)
         assert torch.equal(bits(kc), bits(kc2)) and torch.equal(bits(vc), bits(vc2)), f"batch {batch}: pool differs"
     # and the replayed step against the oracle on the real rows
