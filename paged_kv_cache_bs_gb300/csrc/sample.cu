@@ -125,9 +125,8 @@ template <> struct Vec8<__half> {
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
-            v[2 * j] = f.x;
-            v[2 * j + 1] = f.y;
+            v[2 * j] = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j] & 0xFFFFu)));
+            v[2 * j + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j] >> 16)));
         }
     }
     static __device__ __forceinline__ float one(const __half *p) { return __half2float(*p); }
@@ -202,8 +201,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
                 e = noise[i];
             } else {
                 const uint4 r = philox4x32_10(make_uint4(i >> 2, b, a.off_lo, a.off_hi), keys);
-                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-                e = exp1_scaled(w[i & 3]);
+                const int q = i & 3;
+                e = exp1_scaled(q == 0 ? r.x : q == 1 ? r.y : q == 2 ? r.z : r.w);
             }
             visit(i, Vec8<T>::one(row + i), e, min_noise);
         }

@@ -51,6 +51,28 @@ def test_decode_block_sizes(pa, bs):
     check_decode(pa, st)
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("hq,hkv,head_dim,bs", [(32, 8, 128, 16), (8, 1, 64, 256), (4, 4, 128, 8)])
+def test_decode_context_of_one_returns_its_value_row(pa, dtype, hq, hkv, head_dim, bs):
+    # A context of one token (the one this step stores) has weight 1: the output is that token's value
+    # row for every query head of its group, bit for bit, through pa_decode and the fused store + decode
+    # (the row maximum, the exponent and the sum must agree exactly).
+    ctx = [1, 1, 37, 1, 300, 1]
+    st = inputs.make_decode(ctx, num_q_heads=hq, num_kv_heads=hkv, head_dim=head_dim, block_size=bs,
+                            dtype=dtype, seed=52 + hq + bs)
+    out, _, _ = run_decode_gpu(pa, st)
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    fused = pa.store_decode(st.k_new.cuda(), st.v_new.cuda(), st.slot_mapping.cuda(), st.q.cuda(), kc, vc,
+                            st.block_tables.cuda(), st.context_lens.cuda(), st.scale)
+    torch.cuda.synchronize()
+    for b, L in enumerate(ctx):
+        if L == 1:
+            expect = st.v_new[b].repeat_interleave(hq // hkv, dim=0)
+            assert_bit_equal(out[b], expect, f"sequence {b}")
+            assert_bit_equal(fused[b], expect, f"sequence {b}, fused")
+
+
 def test_decode_empty_context_rows_are_zero(pa):
     st = inputs.make_decode([0, 5, 0, 70], num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
                             dtype=torch.float16, seed=50)
