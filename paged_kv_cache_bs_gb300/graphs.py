@@ -276,7 +276,10 @@ class DecodeGraphRunner:
         """Copy one step's host tensors into the pinned staging of its bucket and pad the rest
         (slot -1, context length 0; groups past the step's are empty).  The shared-prefix groups
         are ``groups``, or with ``share_prefixes`` derived by ``pa_prefix_groups`` from the staged
-        block tables, written straight into the staging.  Returns the bucket size."""
+        block tables, written straight into the staging.  With ``zero_copy`` and page-locked,
+        contiguous q / k_new / v_new of the runner's dtype, those three are not copied: the next
+        :meth:`replay` reads them where they are, so keep them unchanged until its stream has
+        completed (:meth:`step` synchronises).  Returns the bucket size."""
         batch = q.shape[0]
         b = self.bucket(batch)
         h = self._staged(b)
