@@ -390,43 +390,54 @@ int pa_prefix_groups(const int32_t *block_tables, int32_t max_blocks, const int3
             return fail(PA_ERR_INVALID_ARG, "context length %lld of sequence %lld is outside the table",
                         context_lens[b], b);
     const int32_t min_pages = min_shared_pages > 1 ? min_shared_pages : 1;
-    // candidates keyed by the first page of their table, groups in order of first appearance
-    std::unordered_map<int32_t, size_t> slot_of_page;
-    std::vector<std::vector<int32_t>> cand;
+    // candidates keyed by the first page of their table, groups in order of first appearance,
+    // members in batch order (a counting sort); the buffers are reused from call to call
+    thread_local std::unordered_map<int32_t, int32_t> slot_of_page;
+    thread_local std::vector<int32_t> cand_of, count, first, members_of;
+    slot_of_page.clear();
+    cand_of.assign(static_cast<size_t>(batch), -1);
+    count.clear();
+    int32_t eligible = 0;
     for (int32_t b = 0; b < batch; ++b) {
         const int32_t complete = (context_lens[b] - 1) / block_size;  // pages before the newest token's page
         if (context_lens[b] <= 0 || complete < 1) continue;
-        const int32_t first = block_tables[static_cast<int64_t>(b) * max_blocks];
-        auto it = slot_of_page.find(first);
-        if (it == slot_of_page.end()) {
-            slot_of_page.emplace(first, cand.size());
-            cand.emplace_back(1, b);
-        } else {
-            cand[it->second].push_back(b);
-        }
+        const int32_t page0 = block_tables[static_cast<int64_t>(b) * max_blocks];
+        const auto ins = slot_of_page.try_emplace(page0, static_cast<int32_t>(count.size()));
+        if (ins.second) count.push_back(0);
+        cand_of[b] = ins.first->second;
+        ++count[cand_of[b]];
+        ++eligible;
     }
+    const int32_t ncand = static_cast<int32_t>(count.size());
+    first.assign(static_cast<size_t>(ncand) + 1, 0);
+    for (int32_t c = 0; c < ncand; ++c) first[c + 1] = first[c] + count[c];
+    members_of.resize(static_cast<size_t>(eligible));
+    for (int32_t c = 0; c < ncand; ++c) count[c] = first[c];  // next free position of candidate c
+    for (int32_t b = 0; b < batch; ++b)
+        if (cand_of[b] >= 0) members_of[count[cand_of[b]]++] = b;
     for (int32_t b = 0; b < batch; ++b) prefix_lens[b] = 0;
     int32_t groups = 0, members = 0, largest = 0, longest = 0;
     group_offsets[0] = 0;
-    for (const std::vector<int32_t> &m : cand) {
-        if (m.size() < 2) continue;
-        int32_t pages = INT32_MAX;
-        for (int32_t b : m) pages = std::min(pages, (context_lens[b] - 1) / block_size);
+    for (int32_t c = 0; c < ncand; ++c) {
+        const int32_t *m = members_of.data() + first[c];
+        const int32_t size = first[c + 1] - first[c];
+        if (size < 2) continue;
+        int32_t n = INT32_MAX;  // leading table entries equal across the members, within every cap
+        for (int32_t i = 0; i < size; ++i) n = std::min(n, (context_lens[m[i]] - 1) / block_size);
         const int32_t *lead = block_tables + static_cast<int64_t>(m[0]) * max_blocks;
-        int32_t n = 0;
-        for (; n < pages; ++n) {
-            bool same = true;
-            for (size_t i = 1; i < m.size() && same; ++i)
-                same = block_tables[static_cast<int64_t>(m[i]) * max_blocks + n] == lead[n];
-            if (!same) break;
+        for (int32_t i = 1; i < size && n > 0; ++i) {
+            const int32_t *row = block_tables + static_cast<int64_t>(m[i]) * max_blocks;
+            int32_t k = 0;
+            while (k < n && row[k] == lead[k]) ++k;
+            n = k;
         }
         if (n < min_pages) continue;
-        for (int32_t b : m) {
-            group_seqs[members++] = b;
-            prefix_lens[b] = n * block_size;
+        for (int32_t i = 0; i < size; ++i) {
+            group_seqs[members++] = m[i];
+            prefix_lens[m[i]] = n * block_size;
         }
         group_offsets[++groups] = members;
-        largest = std::max(largest, static_cast<int32_t>(m.size()));
+        largest = std::max(largest, size);
         longest = std::max(longest, n * block_size);
     }
     *num_groups = groups;
