@@ -363,6 +363,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         if (!ok) break;
                     }
                     load(cur, &maps.v, sb + S::kOffV + (u & 1) * S::kTile, bar_st(u), t, vpage);
+                    // the K and V boxes of the item's tile t + 2 into L2 now: the first copy of a tile
+                    // then finds it there instead of waiting on HBM (one box per tile)
+                    if (paged && one_box && t + 2 < cur.nkt) {
+                        const int jp = (t + 2) * kBN;
+                        const int y = (page_of(cur, jp >> a.log2_bs) << a.log2_bs) + (jp & ((1 << a.log2_bs) - 1));
+                        const int x = (cur.h0 / a.group) * D;
+                        for (int hf = 0; hf < S::kHalves; ++hf) {
+                            tc::tma_prefetch_2d(&maps.k, x + hf * 64, y);
+                            tc::tma_prefetch_2d(&maps.v, x + hf * 64, y);
+                        }
+                    }
                     const uint32_t kdst = sb + S::kOffK + ((u + 1) & 1) * S::kTile;
                     if (t + 1 < cur.nkt)
                         load(cur, &maps.k, kdst, bar_st(u), t + 1, kpage);
