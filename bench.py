@@ -70,7 +70,7 @@ TRAFFIC_PER_CALL = {
     # + decode_prefix_kernel (each group's shared pages once)
     "qwen3_8b_shared_decode": 805_121_536 + 2_861_056 + 69_261_056 + 66_304,
 }
-PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 126_675_712 + 13_154_816}  # prefill_kernel (ncu, current code)
+PREFILL_TRAFFIC_PER_CALL = {"mixed_chunked_prefill": 126_953_728 + 13_033_728}  # prefill_kernel (ncu, current code)
 # store_kv_kernel on store_stress: DRAM read + write inside the launch (the L2 holds most written
 # rows as dirty lines until after the launch, so this is below the algorithmic 134,217,728 B)
 STORE_TRAFFIC_PER_CALL = 67_182_848 + 15_672_576
