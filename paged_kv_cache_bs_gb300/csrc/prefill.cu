@@ -32,7 +32,8 @@
 //     swizzle the MMA descriptors expect; K/V tiles are double-buffered and
 //     fetched page by page through the block table (one box per page when a
 //     page is shorter than the tile); stage t = {V_t, K_(t+1)} is refilled
-//     once the MMAs of step t-2 are done.
+//     once the MMAs of step t-2 are done, and the tile two ahead is brought
+//     into L2 meanwhile (its first copy then needs no trip to HBM).
 //   * S = Q K^T: 128x128x16 tcgen05.mma steps, fp32 accumulator in TMEM.
 //   * Softmax: each thread owns one row; it loads its S row from TMEM, masks
 //     (causal, bottom-right aligned, and past the context), and exponentiates
