@@ -119,7 +119,7 @@ def parse_args():
                     help="budget of each oracle baseline of the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="time the chosen workload only")
-    ap.add_argument("--split-sms", type=int, default=96,
+    ap.add_argument("--split-sms", type=int, default=88,
                     help="mixed chunked-prefill step: SMs of the prefill's partition (0: no SM split)")
     ap.add_argument("--unfused", action="store_true",
                     help="decode workloads: time pa_store_kv + pa_decode as two calls instead of pa_store_decode")
