@@ -336,11 +336,12 @@ class DecodeWorkload:
             self.e2e_inputs = [pin(self.runner_args(st)), pin(self.runner_args(inputs.next_decode_step(st, seed=4242)))]
             self.e2e_path = ("DecodeGraphRunner.step() from the caller's page-locked host tensors, alternating two "
                              "seeded decode steps over the same pool: slot mapping, context lengths and block tables "
-                             "copied into the pinned staging, CUDA-graph replay whose first kernel (pa_copy_segments) "
+                             "written into the pinned staging by one native call (pa_stage_decode_step, C++), "
+                             "CUDA-graph replay whose first kernel (pa_copy_segments) "
                              "pulls q and the new K/V rows from the caller's tensors over NVLink-C2C, then the fused "
                              "store + decode writing the output into pinned host memory, stream sync; host wall "
                              "clock" + ("; the shared-prefix groups derived from the staged block tables "
-                                        "(pa_prefix_groups, C++) every step" if self.groups is not None else ""))
+                                        "inside that call every step" if self.groups is not None else ""))
             return None, None, self.runner.h2d_bytes(st.batch), self.runner.d2h_bytes(st.batch)
         pinned = pinned_inputs(self.host, self.layout, self.inputs.numel())
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()

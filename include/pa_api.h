@@ -480,6 +480,77 @@ typedef struct pa_copy_segment {
 PA_API int pa_copy_segments(const pa_copy_segment *segments, int32_t count, void *stream);
 
 /*
+ * pa_decode_staging -- one bucket of a captured decode step (a CUDA graph of
+ * pa_store_decode_ex, optionally preceded by pa_copy_segments): the host
+ * arrays its kernels read when it is replayed, all page-locked and owned by
+ * the caller.  The pages record one graph per padded decode batch size and
+ * have a step write its slot mapping, context lengths and block tables into
+ * the graph's fixed buffers, padding the unused rows ("nano-vLLM Part 2",
+ * section 4.2); this struct names those buffers for one bucket.
+ *   rows            the bucket: rows of every per-sequence array (> 0).
+ *   max_blocks      columns of block_tables (> 0).
+ *   block_size      tokens per page of the pool (> 0).
+ *   slot_mapping    int32 [rows]; context_lens int32 [rows];
+ *   block_tables    int32 [rows, max_blocks] row-major.
+ *   max_groups, max_group_size, max_prefix_len: the shared-prefix capacities
+ *                   the graph was captured for (pa_decode_options), 0 when it
+ *                   holds no groups, in which case the three group arrays are
+ *                   NULL:
+ *   group_offsets   int32 [max_groups + 1]; group_seqs int32 [rows];
+ *   prefix_lens     int32 [rows].
+ *   segments        the gather list the graph's pa_copy_segments reads, or
+ *                   NULL; num_segments (0..4) entries whose dst the caller
+ *                   set; segment_row_bytes[i] the bytes of one row of
+ *                   segment i (a sequence's q, or its new K or V rows).
+ */
+typedef struct pa_decode_staging {
+    int32_t rows;
+    int32_t max_blocks;
+    int32_t block_size;
+    int32_t *slot_mapping;
+    int32_t *context_lens;
+    int32_t *block_tables;
+    int32_t max_groups;
+    int32_t max_group_size;
+    int32_t max_prefix_len;
+    int32_t *group_offsets;
+    int32_t *group_seqs;
+    int32_t *prefix_lens;
+    pa_copy_segment *segments;
+    int32_t num_segments;
+    uint64_t segment_row_bytes[4];
+} pa_decode_staging;
+
+/* shared-prefix groups of a staged step (the `groups` argument below) */
+#define PA_STAGE_NO_GROUPS 0     /* no sharing: every group empty, every prefix_lens 0 */
+#define PA_STAGE_DERIVE_GROUPS 1 /* pa_prefix_groups over the staged tables (min_shared_pages 1) */
+#define PA_STAGE_KEEP_GROUPS 2   /* the group arrays are left as they are (the caller writes them) */
+
+/*
+ * pa_stage_decode_step -- writes one decode step of `batch` sequences into a
+ * bucket's staging, on the host, with no GPU call: slot_mapping, context_lens
+ * and the first table_cols columns of block_tables into the first `batch`
+ * rows (the other columns of those rows -1); rows batch..rows-1 padded (slot
+ * -1, context length 0, table row untouched: a context of 0 reads no page);
+ * the groups as `groups` says, unused group entries empty; and, when
+ * `sources` is not NULL, segment i pointed at sources[i] for batch *
+ * segment_row_bytes[i] bytes (the caller's page-locked q / new K / new V).
+ *   batch           in [0, st->rows].
+ *   slot_mapping    host int32 [batch]; context_lens host int32 [batch], each
+ *                   in [0, table_cols * block_size].
+ *   block_tables    host int32 [batch, table_cols] row-major, table_cols in
+ *                   [1, st->max_blocks].
+ * Derived groups larger than the captured capacities are an error: the
+ * graph's launch shape could not cover them.  Errors: PA_ERR_INVALID_ARG for
+ * null pointers, sizes out of range, a context length outside the table, a
+ * groups mode the staging cannot hold, derived groups beyond the
+ * capacities; the staging's contents are then unspecified.
+ */
+PA_API int pa_stage_decode_step(const pa_decode_staging *st, int32_t batch, const int32_t *slot_mapping,
+                                const int32_t *context_lens, const int32_t *block_tables, int32_t table_cols,
+                                int32_t groups, const void *const *sources);
+
+/*
  * pa_selftest_wait_timeout -- a diagnostic with no counterpart on the pages:
  * shows on a live GPU that the library's bounded waits end with a status
  * instead of a hang.  Launches one thread on `stream` that waits on an

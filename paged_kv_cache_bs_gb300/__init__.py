@@ -115,6 +115,20 @@ class CopySegment(ctypes.Structure):
 _lib.pa_copy_segments.restype = ctypes.c_int
 _lib.pa_copy_segments.argtypes = [_p, _i32, _p]
 
+
+class DecodeStaging(ctypes.Structure):
+    """Mirror of pa_decode_staging (the host arrays of one captured decode bucket)."""
+    _fields_ = [("rows", _i32), ("max_blocks", _i32), ("block_size", _i32),
+                ("slot_mapping", _p), ("context_lens", _p), ("block_tables", _p),
+                ("max_groups", _i32), ("max_group_size", _i32), ("max_prefix_len", _i32),
+                ("group_offsets", _p), ("group_seqs", _p), ("prefix_lens", _p),
+                ("segments", _p), ("num_segments", _i32), ("segment_row_bytes", ctypes.c_uint64 * 4)]
+
+
+STAGE_NO_GROUPS, STAGE_DERIVE_GROUPS, STAGE_KEEP_GROUPS = 0, 1, 2
+_lib.pa_stage_decode_step.restype = ctypes.c_int
+_lib.pa_stage_decode_step.argtypes = [_p, _i32, _p, _p, _p, _i32, _i32, _p]
+
 PA_F16, PA_BF16, PA_F32, PA_E4M3 = 0, 1, 2, 3
 _FP8_POOL = (torch.uint8, torch.float8_e4m3fn)  # E4M3 codes, one byte per element
 _DTYPES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
@@ -387,6 +401,26 @@ def copy_segments(segments_ptr: int, count: int, stream: int | None = None) -> N
                                                        ctypes.c_void_p(stream)))
 
 
+def stage_decode_step(staging: DecodeStaging, slot_mapping: torch.Tensor, context_lens: torch.Tensor,
+                      block_tables: torch.Tensor, groups: int = STAGE_NO_GROUPS, sources=None) -> None:
+    """``pa_stage_decode_step``: one decode step's metadata (contiguous host int32 tensors, batch =
+    ``slot_mapping.numel()``) into the pinned arrays ``staging`` names, rows past the batch padded;
+    ``groups`` one of the STAGE_* modes; ``sources`` None or the addresses of the step's q and new
+    K / V rows for the staging's gather list.  Host only."""
+    batch = slot_mapping.numel()
+    for name, t in (("slot_mapping", slot_mapping), ("context_lens", context_lens), ("block_tables", block_tables)):
+        if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host int32 tensor")
+    if context_lens.numel() != batch or block_tables.dim() != 2 or block_tables.shape[0] != batch:
+        raise ValueError(f"context_lens and block_tables must hold {batch} rows")
+    src = None
+    if sources is not None:
+        src = (ctypes.c_void_p * max(len(sources), 1))(*sources)
+    _check("pa_stage_decode_step", _lib.pa_stage_decode_step(
+        ctypes.addressof(staging), batch, slot_mapping.data_ptr(), context_lens.data_ptr(), block_tables.data_ptr(),
+        block_tables.shape[1], int(groups), None if src is None else ctypes.addressof(src)))
+
+
 def selftest_wait_timeout(err_flag: torch.Tensor, max_cycles: int = 2_000_000) -> None:
     """``pa_selftest_wait_timeout``: a bounded wait that nothing satisfies gives up after
     ``max_cycles`` and ORs FLAG_TIMEOUT into ``err_flag`` (a CUDA int32 tensor)."""
@@ -586,7 +620,8 @@ def sample(logits: torch.Tensor, temperatures: torch.Tensor, noise: torch.Tensor
     return out
 
 
-__all__ = ["copy_segments", "CopySegment", "store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
+__all__ = ["copy_segments", "CopySegment", "stage_decode_step", "DecodeStaging", "STAGE_NO_GROUPS", "STAGE_DERIVE_GROUPS",
+           "STAGE_KEEP_GROUPS", "store_kv", "decode", "store_decode", "prefill_paged", "sample", "store_kv_fp8", "decode_fp8",
            "store_decode_fp8", "mixed_step", "SmSplit",
            "decode_workspace_bytes", "decode_fp8_workspace_bytes", "alloc_decode_workspace", "library",
            "PagedAttentionError", "LIB_PATH", "PA_F16", "PA_BF16", "PA_F32", "PA_E4M3", "FLAG_BAD_SLOT", "FLAG_BAD_BLOCK",

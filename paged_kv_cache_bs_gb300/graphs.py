@@ -28,13 +28,14 @@ only: every step of the path runs in the library's kernels.
 
 from __future__ import annotations
 
+import bisect
 import ctypes
 
 import torch
 
-from . import (_fp8_pool, _FP8_POOL, _lib, CopySegment, DecodeOptions, PagedAttentionError, PrefixGroups,
-               decode_fp8_workspace_bytes, decode_workspace_bytes, store_decode, store_decode_fp8)
-from . import block_manager as _bm  # declares pa_prefix_groups
+from . import (_fp8_pool, _FP8_POOL, _lib, CopySegment, DecodeOptions, DecodeStaging, PagedAttentionError,
+               PrefixGroups, STAGE_DERIVE_GROUPS, STAGE_KEEP_GROUPS, STAGE_NO_GROUPS, decode_fp8_workspace_bytes,
+               decode_workspace_bytes, store_decode, store_decode_fp8)
 
 
 def graph_batch_sizes(max_batch: int) -> list[int]:
@@ -52,13 +53,11 @@ def _align(n: int) -> int:
     return (n + 255) // 256 * 256
 
 
-def _copy_rows(dst: torch.Tensor, src: torch.Tensor, rows: int) -> None:
-    """dst[:rows] = src: one memmove for a contiguous host int32 source (no torch dispatch, no
-    wake-up of torch's copy threads for these few KB), else a torch copy."""
-    if src.device.type == "cpu" and src.dtype == dst.dtype and src.is_contiguous():
-        ctypes.memmove(dst.data_ptr(), src.data_ptr(), rows * dst[0].numel() * dst.element_size())
-    else:
-        dst[:rows].copy_(src)
+def _host_i32(t: torch.Tensor) -> torch.Tensor:
+    """t as a contiguous host int32 tensor (itself when it already is one)."""
+    if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        t = t.to("cpu", torch.int32).contiguous()
+    return t
 
 
 class DecodeGraphRunner:
@@ -98,8 +97,7 @@ class DecodeGraphRunner:
         esz = torch.empty(0, dtype=dtype).element_size()
         # per-bucket packed layout (the same in pinned host memory and on the device)
         self._layout = {b: self._pack_layout(b, esz) for b in self.sizes}
-        self._staged_views, self._staged_out, self._ptr_cache = {}, {}, {}
-        self._group_out = (ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32())
+        self._staged_views, self._staged_out = {}, {}
         in_bytes = max(lay["_bytes"] for lay in self._layout.values())
         out_bytes = max(self.sizes) * num_q_heads * d * esz
         self.host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
@@ -111,8 +109,8 @@ class DecodeGraphRunner:
             self.dev_in = self.dev_out = None
             lay = self._layout[max(self.sizes)]
             self._qkv_dev = torch.zeros(sum(lay[n][3] for n in self._qkv_names) + 512, dtype=torch.uint8, device=dev)
-            self._seg_buf = torch.zeros(3 * ctypes.sizeof(CopySegment), dtype=torch.uint8).pin_memory()
-            self._segs = (CopySegment * 3).from_address(self._seg_buf.data_ptr())
+            # one list per bucket: its destinations are fixed, a step rewrites sources and sizes
+            self._seg_buf = torch.zeros(3 * len(self.sizes) * ctypes.sizeof(CopySegment), dtype=torch.uint8).pin_memory()
             self._qkv_views = {}
         else:
             self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
@@ -124,6 +122,12 @@ class DecodeGraphRunner:
         else:
             ws = max(ws_fn(b, num_q_heads, hkv, d, max_blocks_per_seq, bs) for b in self.sizes)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+        # per bucket: the pa_decode_staging a step's metadata are written into (one native call)
+        self._stagings = {b: self._make_staging(b) for b in self.sizes}
+        self._staging_addr = {b: ctypes.addressof(st) for b, st in self._stagings.items()}
+        self._sources = (ctypes.c_void_p * 3)()
+        self._sources_addr = ctypes.addressof(self._sources)
+        self._row_shapes = ((num_q_heads, d), (hkv, d), (hkv, d))  # a row of q, k_new, v_new
         # per bucket: the graph whose kernels read q and the new rows from the pinned staging, and
         # (zero_copy) the one that first pulls them from the caller's page-locked tensors
         self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
@@ -189,15 +193,39 @@ class DecodeGraphRunner:
             self._qkv_views[b] = views
         return views
 
+    def _segments_ptr(self, b: int) -> int:
+        """Address of bucket b's gather list (three CopySegments in pinned memory)."""
+        return self._seg_buf.data_ptr() + 3 * self.sizes.index(b) * ctypes.sizeof(CopySegment)
+
     def _point_segments(self, b: int, batch: int, sources) -> None:
-        """The segment list of a step: source i (a host tensor's address, or the staging's) to
-        bucket b's device buffer, ``batch`` rows."""
+        """Bucket b's gather list: source i (a host tensor's address, or the staging's) to the
+        bucket's device buffer, ``batch`` rows."""
         dev = self._dev_qkv(b)
+        segs = (CopySegment * 3).from_address(self._segments_ptr(b))
         for i, (n, src) in enumerate(zip(self._qkv_names, sources)):
-            seg = self._segs[i]
-            seg.src = src
-            seg.dst = dev[n].data_ptr()
-            seg.bytes = batch * dev[n][0].numel() * dev[n].element_size()
+            segs[i].src = src
+            segs[i].dst = dev[n].data_ptr()
+            segs[i].bytes = batch * dev[n][0].numel() * dev[n].element_size()
+
+    def _make_staging(self, b: int) -> DecodeStaging:
+        """The pa_decode_staging of bucket b over its pinned views (and gather list)."""
+        h = self._staged(b)
+        st = DecodeStaging(rows=b, max_blocks=self.max_blocks, block_size=self.k_cache.shape[1],
+                           slot_mapping=h["slot_mapping"].data_ptr(), context_lens=h["context_lens"].data_ptr(),
+                           block_tables=h["block_tables"].data_ptr())
+        if self.group_caps is not None:
+            st.max_groups, st.max_group_size, st.max_prefix_len = self.group_caps
+            st.group_offsets = h["group_offsets"].data_ptr()
+            st.group_seqs = h["group_seqs"].data_ptr()
+            st.prefix_lens = h["prefix_lens"].data_ptr()
+        if self.zero_copy:
+            dev = self._dev_qkv(b)
+            self._point_segments(b, b, [h[n].data_ptr() for n in self._qkv_names])
+            st.segments = self._segments_ptr(b)
+            st.num_segments = 3
+            for i, n in enumerate(self._qkv_names):
+                st.segment_row_bytes[i] = dev[n][0].numel() * dev[n].element_size()
+        return st
 
     def _launch(self, b: int, gather: bool = False) -> None:
         lay = self._layout[b]
@@ -206,7 +234,7 @@ class DecodeGraphRunner:
             if gather:
                 # capture with the list pointing at the staging (valid memory); steps rewrite it
                 self._point_segments(b, b, [v[n].data_ptr() for n in self._qkv_names])
-                rc = _lib.pa_copy_segments(ctypes.c_void_p(self._seg_buf.data_ptr()), 3,
+                rc = _lib.pa_copy_segments(ctypes.c_void_p(self._segments_ptr(b)), 3,
                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
                 if rc != 0:
                     raise PagedAttentionError("pa_copy_segments", rc)
@@ -254,10 +282,10 @@ class DecodeGraphRunner:
 
     # -------------------------------------------------------------------- step
     def bucket(self, batch: int) -> int:
-        for b in self.sizes:
-            if b >= batch:
-                return b
-        raise ValueError(f"batch {batch} exceeds the largest captured size {self.sizes[-1]}")
+        i = bisect.bisect_left(self.sizes, batch)
+        if i == len(self.sizes):
+            raise ValueError(f"batch {batch} exceeds the largest captured size {self.sizes[-1]}")
+        return self.sizes[i]
 
     def host_inputs(self, batch: int) -> dict:
         """Pinned host views of the step inputs for a batch (the bucket's rows; fill the first
@@ -273,103 +301,70 @@ class DecodeGraphRunner:
 
     def set_inputs(self, q, k_new, v_new, slot_mapping, context_lens, block_tables,
                    groups: PrefixGroups | None = None, share_prefixes: bool = False) -> int:
-        """Copy one step's host tensors into the pinned staging of its bucket and pad the rest
+        """Write one step's host tensors into the pinned staging of its bucket and pad the rest
         (slot -1, context length 0; groups past the step's are empty).  The shared-prefix groups
         are ``groups``, or with ``share_prefixes`` derived by ``pa_prefix_groups`` from the staged
-        block tables, written straight into the staging.  With ``zero_copy`` and page-locked,
-        contiguous q / k_new / v_new of the runner's dtype, those three are not copied: the next
-        :meth:`replay` reads them where they are, so keep them unchanged until its stream has
-        completed (:meth:`step` synchronises).  Returns the bucket size."""
+        block tables.  The metadata, the groups and the gather list go by one native call,
+        ``pa_stage_decode_step``.  With ``zero_copy`` and page-locked, contiguous q / k_new / v_new
+        of the runner's dtype, those three are not copied: the next :meth:`replay` reads them where
+        they are, so keep them unchanged until its stream has completed (:meth:`step`
+        synchronises).  Returns the bucket size."""
         batch = q.shape[0]
         b = self.bucket(batch)
-        h = self._staged(b)
         if share_prefixes:
             if self.group_caps is None:
                 raise ValueError("this runner was built without group_caps")
-            self._stage_tables(h, batch, context_lens, block_tables)
-            self._derive_groups(h, batch)
-        elif self.group_caps is not None:
-            ng, members, prefix = self.group_caps
-            h["prefix_lens"].zero_()
-            if groups is None or groups.num_groups == 0:
-                h["group_offsets"].zero_()
-            else:
-                if groups.num_groups > ng or groups.max_group_size > members or groups.max_prefix_len > prefix:
-                    raise ValueError(f"groups ({groups.num_groups}, {groups.max_group_size}, {groups.max_prefix_len}) "
-                                     f"exceed the captured capacities {self.group_caps}")
-                g = groups.num_groups
-                off = groups.group_offsets
-                h["group_offsets"][:g + 1].copy_(off)
-                h["group_offsets"][g + 1:].fill_(int(off[g]))
-                n = int(off[g])
-                h["group_seqs"][:n].copy_(groups.group_seqs[:n])
-                h["prefix_lens"][:batch].copy_(groups.prefix_lens[:batch])
+            mode = STAGE_DERIVE_GROUPS
         elif groups is not None and groups.num_groups:
-            raise ValueError("this runner was built without group_caps")
-        qkv = (q, k_new, v_new)
-        gather = self.zero_copy and all(t.dtype == self.dtype and t.is_contiguous() and t.shape[1:] == h[n].shape[1:]
-                                        and t.is_pinned() for n, t in zip(self._qkv_names, qkv))
+            if self.group_caps is None:
+                raise ValueError("this runner was built without group_caps")
+            self._stage_groups(b, batch, groups)
+            mode = STAGE_KEEP_GROUPS
+        else:
+            mode = STAGE_NO_GROUPS
+        slot_mapping, context_lens, block_tables = (_host_i32(slot_mapping), _host_i32(context_lens),
+                                                    _host_i32(block_tables))
+        if (slot_mapping.numel() != batch or context_lens.numel() != batch or block_tables.dim() != 2
+                or block_tables.shape[0] != batch):
+            raise ValueError(f"slot_mapping {tuple(slot_mapping.shape)}, context_lens {tuple(context_lens.shape)} "
+                             f"and block_tables {tuple(block_tables.shape)} must hold {batch} rows")
+        dt, shapes = self.dtype, self._row_shapes
+        gather = self.zero_copy and all(t.dtype == dt and t.shape[1:] == shp and t.is_contiguous() and t.is_pinned()
+                                        for t, shp in zip((q, k_new, v_new), shapes))
         self._use_gather[b] = gather
         if gather:
             # page-locked tensors: the graph's first kernel reads them where they are
-            self._point_segments(b, batch, [t.data_ptr() for t in qkv])
+            src = self._sources
+            src[0], src[1], src[2] = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+            sources = self._sources_addr
         else:
+            h = self._staged(b)
             h["q"][:batch].copy_(q)
             h["k_new"][:batch].copy_(k_new)
             h["v_new"][:batch].copy_(v_new)
-        _copy_rows(h["slot_mapping"], slot_mapping, batch)
-        if batch < b:
-            h["slot_mapping"][batch:].fill_(-1)
-        if not share_prefixes:
-            self._stage_tables(h, batch, context_lens, block_tables)
+            sources = None
+        rc = _lib.pa_stage_decode_step(self._staging_addr[b], batch, slot_mapping.data_ptr(),
+                                       context_lens.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                                       mode, sources)
+        if rc != 0:
+            raise PagedAttentionError("pa_stage_decode_step", rc)
         return b
 
-    @staticmethod
-    def _stage_tables(h: dict, batch: int, context_lens, block_tables) -> None:
-        _copy_rows(h["context_lens"], context_lens, batch)
-        if batch < h["context_lens"].shape[0]:
-            h["context_lens"][batch:].zero_()
-        if block_tables.shape[1] == h["block_tables"].shape[1]:
-            _copy_rows(h["block_tables"], block_tables, batch)
-        else:
-            h["block_tables"][:batch, :block_tables.shape[1]].copy_(block_tables)
-
-    def _derive_groups(self, h: dict, batch: int) -> None:
-        """pa_prefix_groups over the staged tables and lengths, into the staged group fields
-        (prefix_lens of the step's rows written by the call itself)."""
+    def _stage_groups(self, b: int, batch: int, groups: PrefixGroups) -> None:
+        """Caller-given groups into bucket b's staged group fields, unused entries empty."""
         ng, members, prefix = self.group_caps
-        n, big, longest = self._group_out
-        if batch < h["prefix_lens"].shape[0]:
-            h["prefix_lens"][batch:].zero_()
-        # room for the largest possible output, which may exceed the captured groups: counted below
-        off = self._group_offsets_scratch(batch)
-        i32 = self._i32_ptr
-        rc = _lib.pa_prefix_groups(i32(h["block_tables"]), self.max_blocks, i32(h["context_lens"]), batch,
-                                   self.k_cache.shape[1], 1, i32(off), i32(h["group_seqs"]), i32(h["prefix_lens"]),
-                                   ctypes.byref(n), ctypes.byref(big), ctypes.byref(longest))
-        if rc != 0:
-            raise PagedAttentionError("pa_prefix_groups", rc)
-        if n.value > ng or big.value > members or longest.value > prefix:
-            raise ValueError(f"the step's groups ({n.value}, {big.value}, {longest.value}) exceed the captured "
-                             f"capacities {self.group_caps}")
-        g = h["group_offsets"]
-        cnt = n.value + 1
-        ctypes.memmove(g.data_ptr(), off.data_ptr(), 4 * cnt)
-        if cnt < g.shape[0]:
-            g[cnt:].fill_(int(off[n.value]))
-
-    def _i32_ptr(self, t: torch.Tensor):
-        """ctypes int32 pointer of a staging view (cached by address)."""
-        p = self._ptr_cache.get(t.data_ptr())
-        if p is None:
-            p = self._ptr_cache[t.data_ptr()] = ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_int32))
-        return p
-
-    def _group_offsets_scratch(self, batch: int) -> torch.Tensor:
-        need = batch // 2 + 1
-        if getattr(self, "_off_scratch", None) is None or self._off_scratch.numel() < need:
-            self._off_scratch = torch.zeros(need, dtype=torch.int32)
-        return self._off_scratch
+        if groups.num_groups > ng or groups.max_group_size > members or groups.max_prefix_len > prefix:
+            raise ValueError(f"groups ({groups.num_groups}, {groups.max_group_size}, {groups.max_prefix_len}) "
+                             f"exceed the captured capacities {self.group_caps}")
+        h = self._staged(b)
+        g = groups.num_groups
+        off = groups.group_offsets
+        h["group_offsets"][:g + 1].copy_(off)
+        h["group_offsets"][g + 1:].fill_(int(off[g]))
+        n = int(off[g])
+        h["group_seqs"][:n].copy_(groups.group_seqs[:n])
+        h["prefix_lens"].zero_()
+        h["prefix_lens"][:batch].copy_(groups.prefix_lens[:batch])
 
     def replay(self, batch: int) -> torch.Tensor:
         """Replay the bucket's graph (inputs from the pinned staging) on the current stream; the
