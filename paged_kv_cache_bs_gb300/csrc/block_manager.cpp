@@ -127,6 +127,60 @@ const Sequence *find(const pa_bm *bm, int64_t id) {
     const auto it = bm->seqs.find(id);
     return it == bm->seqs.end() ? nullptr : &it->second;
 }
+// Leading entries equal in rows a and b, at most n: 8-entry blocks compared whole first (an OR
+// of XORs, which the compiler turns into vector code), then entry by entry.
+int32_t common_prefix(const int32_t *a, const int32_t *b, int32_t n) {
+    int32_t k = 0;
+    for (; k + 8 <= n; k += 8) {
+        uint32_t diff = 0;
+        for (int j = 0; j < 8; ++j) diff |= static_cast<uint32_t>(a[k + j] ^ b[k + j]);
+        if (diff) break;
+    }
+    while (k < n && a[k] == b[k]) ++k;
+    return k;
+}
+
+// Open-addressing map from a page id to an int32 value (-1: absent), linear probing over a
+// power-of-two table at most half full.  A slot belongs to the current call when its stamp is
+// the call's generation, so starting a call clears nothing.
+class PageSlots {
+  public:
+    void reset(int32_t max_keys) {
+        size_t cap = 16;
+        int bits = 4;
+        while (cap < 2 * static_cast<size_t>(max_keys)) cap <<= 1, ++bits;
+        if (cap > keys_.size()) {
+            bits_ = bits;
+            keys_.assign(cap, 0);
+            vals_.assign(cap, -1);
+            stamps_.assign(cap, 0);
+            gen_ = 0;
+        }
+        if (++gen_ == 0) {  // the stamps wrapped: clear them once
+            std::fill(stamps_.begin(), stamps_.end(), 0u);
+            gen_ = 1;
+        }
+    }
+    int32_t &find_or_add(int32_t key) {
+        const size_t mask = keys_.size() - 1;
+        // multiplicative hashing (Knuth): the top bits of the id times 2^32 / golden ratio
+        size_t i = (static_cast<uint32_t>(key) * 2654435769u) >> (32 - bits_);
+        while (stamps_[i] == gen_ && keys_[i] != key) i = (i + 1) & mask;
+        if (stamps_[i] != gen_) {
+            stamps_[i] = gen_;
+            keys_[i] = key;
+            vals_[i] = -1;
+        }
+        return vals_[i];
+    }
+
+  private:
+    std::vector<int32_t> keys_, vals_;
+    std::vector<uint32_t> stamps_;
+    uint32_t gen_ = 0;
+    int bits_ = 0;
+};
+
 int no_seq(int64_t id) { return fail(PA_ERR_INVALID_ARG, "no sequence %lld in this block manager", id); }
 
 }  // namespace
@@ -392,20 +446,29 @@ int pa_prefix_groups(const int32_t *block_tables, int32_t max_blocks, const int3
     const int32_t min_pages = min_shared_pages > 1 ? min_shared_pages : 1;
     // candidates keyed by the first page of their table, groups in order of first appearance,
     // members in batch order (a counting sort); the buffers are reused from call to call
-    thread_local std::unordered_map<int32_t, int32_t> slot_of_page;
-    thread_local std::vector<int32_t> cand_of, count, first, members_of;
-    slot_of_page.clear();
+    thread_local PageSlots slot_of_page;
+    thread_local std::vector<int32_t> cand_of, pages_of, count, first, members_of;
+    slot_of_page.reset(batch);
     cand_of.assign(static_cast<size_t>(batch), -1);
+    pages_of.resize(static_cast<size_t>(batch));
     count.clear();
+    const bool pow2 = (block_size & (block_size - 1)) == 0;
+    const int shift = pow2 ? __builtin_ctz(static_cast<unsigned>(block_size)) : 0;
     int32_t eligible = 0;
     for (int32_t b = 0; b < batch; ++b) {
-        const int32_t complete = (context_lens[b] - 1) / block_size;  // pages before the newest token's page
-        if (context_lens[b] <= 0 || complete < 1) continue;
-        const int32_t page0 = block_tables[static_cast<int64_t>(b) * max_blocks];
-        const auto ins = slot_of_page.try_emplace(page0, static_cast<int32_t>(count.size()));
-        if (ins.second) count.push_back(0);
-        cand_of[b] = ins.first->second;
-        ++count[cand_of[b]];
+        const int32_t len = context_lens[b];
+        if (len <= 0) continue;
+        // pages before the newest token's page
+        const int32_t complete = pow2 ? (len - 1) >> shift : (len - 1) / block_size;
+        if (complete < 1) continue;
+        pages_of[b] = complete;
+        int32_t &c = slot_of_page.find_or_add(block_tables[static_cast<int64_t>(b) * max_blocks]);
+        if (c < 0) {
+            c = static_cast<int32_t>(count.size());
+            count.push_back(0);
+        }
+        cand_of[b] = c;
+        ++count[c];
         ++eligible;
     }
     const int32_t ncand = static_cast<int32_t>(count.size());
@@ -423,14 +486,10 @@ int pa_prefix_groups(const int32_t *block_tables, int32_t max_blocks, const int3
         const int32_t size = first[c + 1] - first[c];
         if (size < 2) continue;
         int32_t n = INT32_MAX;  // leading table entries equal across the members, within every cap
-        for (int32_t i = 0; i < size; ++i) n = std::min(n, (context_lens[m[i]] - 1) / block_size);
+        for (int32_t i = 0; i < size; ++i) n = std::min(n, pages_of[m[i]]);
         const int32_t *lead = block_tables + static_cast<int64_t>(m[0]) * max_blocks;
-        for (int32_t i = 1; i < size && n > 0; ++i) {
-            const int32_t *row = block_tables + static_cast<int64_t>(m[i]) * max_blocks;
-            int32_t k = 0;
-            while (k < n && row[k] == lead[k]) ++k;
-            n = k;
-        }
+        for (int32_t i = 1; i < size && n > 0; ++i)
+            n = common_prefix(lead, block_tables + static_cast<int64_t>(m[i]) * max_blocks, n);
         if (n < min_pages) continue;
         for (int32_t i = 0; i < size; ++i) {
             group_seqs[members++] = m[i];

@@ -22,8 +22,10 @@ device buffers from where they are (their addresses written into a pinned
 segment list each step: no host-side copy); otherwise they are copied into the
 pinned staging and the kernels read them there.  With ``zero_copy=False`` the
 graph holds a host-to-device copy of the packed inputs, the fused call on
-device buffers and a device-to-host copy of the output.  Argument marshalling
-only: every step of the path runs in the library's kernels.
+device buffers and a device-to-host copy of the output.  A step's host side is
+one native call (``pa_stage_decode_step``: metadata rows, padding, shared-prefix
+groups, gather list) and one ``cuGraphLaunch``.  Argument marshalling only:
+every step of the path runs in the library's kernels.
 """
 
 from __future__ import annotations
@@ -51,6 +53,23 @@ def graph_batch_sizes(max_batch: int) -> list[int]:
 
 def _align(n: int) -> int:
     return (n + 255) // 256 * 256
+
+
+_cu_graph_launch = None
+
+
+def _graph_launch(graph_exec: int, stream: int) -> None:
+    """cuGraphLaunch of an instantiated graph on a stream.  torch's ``CUDAGraph.replay`` first
+    refreshes the captured random-generator state with two small fill kernels; the runner's
+    graphs draw no random numbers, so they are launched directly."""
+    global _cu_graph_launch
+    if _cu_graph_launch is None:
+        f = ctypes.CDLL("libcuda.so.1").cuGraphLaunch
+        f.argtypes, f.restype = [ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int
+        _cu_graph_launch = f
+    rc = _cu_graph_launch(graph_exec, stream)
+    if rc != 0:
+        raise RuntimeError(f"cuGraphLaunch failed with CUresult {rc}")
 
 
 def _host_i32(t: torch.Tensor) -> torch.Tensor:
@@ -133,6 +152,8 @@ class DecodeGraphRunner:
         self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
         self._gather_graphs: dict[int, torch.cuda.CUDAGraph] = {}
         self._use_gather: dict[int, bool] = {}
+        self._execs: dict[tuple[int, bool], int] = {}  # (bucket, gather) -> the instantiated graph
+        self._device_index = dev.index if dev.index is not None else torch.cuda.current_device()
         self._capture()
 
     # ------------------------------------------------------------------ layout
@@ -278,6 +299,7 @@ class DecodeGraphRunner:
                 with torch.cuda.graph(g, stream=stream):
                     self._launch(b, m)
                 (self._gather_graphs if m else self.graphs)[b] = g
+                self._execs[(b, m)] = g.raw_cuda_graph_exec()
         torch.cuda.current_stream(self.k_cache.device).wait_stream(stream)
 
     # -------------------------------------------------------------------- step
@@ -370,11 +392,12 @@ class DecodeGraphRunner:
         """Replay the bucket's graph (inputs from the pinned staging) on the current stream; the
         returned pinned host view of the output is valid once that stream has synchronised."""
         b = self.bucket(batch)
-        (self._gather_graphs if self._use_gather.get(b) else self.graphs)[b].replay()
-        out = self._staged_out.get(b)
-        if out is None:
-            out = self._staged_out[b] = self._out_view(self.host_out, b)
-        return out[:batch]
+        _graph_launch(self._execs[(b, self._use_gather.get(b, False))],
+                      torch._C._cuda_getCurrentRawStream(self._device_index))
+        out = self._staged_out.get(batch)
+        if out is None:  # the first `batch` rows of the bucket's output, one view per batch size
+            out = self._staged_out[batch] = self._out_view(self.host_out, b)[:batch]
+        return out
 
     def step(self, q, k_new, v_new, slot_mapping, context_lens, block_tables,
              groups: PrefixGroups | None = None, share_prefixes: bool = False) -> torch.Tensor:

@@ -206,7 +206,7 @@ def test_native_prefix_groups_equal_the_oracle(seed):
     from oracle.prefix_groups import prefix_groups as ref
     from tests.test_prefix_groups import _built_batch
     rng = random.Random(seed)
-    bs = rng.choice([1, 4, 16, 256])
+    bs = rng.choice([1, 3, 4, 12, 16, 256])  # any positive block size, powers of two or not
     if seed % 2:
         tables, ctx, _ = _built_batch(rng, bs)
     else:   # random tables over a small page alphabet: accidental equal entries are common
@@ -220,6 +220,26 @@ def test_native_prefix_groups_equal_the_oracle(seed):
     assert (off, seqs, pre) == ref(tables, ctx, bs, min_pages)
     sizes = [off[i + 1] - off[i] for i in range(len(off) - 1)]
     assert g.max_group_size == max(sizes, default=0) and g.max_prefix_len == max(pre, default=0)
+
+
+@pytest.mark.parametrize("batch", [600, 5, 2000, 64])
+def test_native_prefix_groups_many_candidates(batch):
+    # first pages that differ only in high bits, or only in low bits, many of them, and batches
+    # of changing size one after the other (the native lookup table is reused between calls)
+    import random
+    from oracle.prefix_groups import prefix_groups as ref
+    rng = random.Random(batch)
+    bs = 4
+    starts = [k << 20 for k in range(40)] + [k for k in range(40)] + [rng.randrange(2**31) for _ in range(40)]
+    tables, ctx = [], []
+    for b in range(batch):
+        p0 = rng.choice(starts)
+        L = rng.randint(1, 6 * bs)
+        tables.append([p0] + [rng.choice([p0 + 1, p0 + 2]) for _ in range(5)])
+        ctx.append(L)
+    off, seqs, pre, _ = _pg_native(tables, ctx, bs)
+    assert (off, seqs, pre) == ref(tables, ctx, bs)
+    assert len(off) > 2 or batch < 64  # several groups in the larger batches
 
 
 def test_native_prefix_groups_pages_example():
