@@ -117,3 +117,30 @@ def test_runner_with_shared_prefix_groups(pa, zero_copy):
         big = prefix_groups(st.block_tables, st.context_lens, 16)
         runner.set_inputs(st.q, st.k_new, st.v_new, st.slot_mapping, st.context_lens, st.block_tables,
                           groups=pa.PrefixGroups(big.group_offsets, big.group_seqs, big.prefix_lens, 9, 512))
+
+
+@pytest.mark.gpu
+def test_runner_with_tables_narrower_than_its_width(pa):
+    # the runner is captured for wider tables than the steps pass: the staged rows are padded with
+    # -1 past the step's columns (no stale entry from an earlier, wider step is ever in reach), and
+    # steps of several batch sizes alternate with the derived shared-prefix groups
+    from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
+    seqs = [(300 + 41 * i, i // 4, 256) for i in range(12)] + [(40 + i, -1, 0) for i in range(4)]
+    st = inputs.make_decode_shared(seqs, num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
+                                   dtype=torch.bfloat16, seed=191)
+    width = st.block_tables.shape[1]
+    kc, vc = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    runner = DecodeGraphRunner(kc, vc, 16, 16, width + 7, st.scale, torch.bfloat16, group_caps=(4, 8, 512))
+    okc, ovc = st.pool.k_cache.clone(), st.pool.v_cache.clone()
+    # a first step with garbage in the extra columns of the staging
+    runner.host_inputs(16)["block_tables"].fill_(12345)
+    for i, s in enumerate([st, inputs.next_decode_step(st, seed=192)]):
+        for share in (True, False):
+            got = runner.step(s.q, s.k_new, s.v_new, s.slot_mapping, s.context_lens, s.block_tables,
+                              share_prefixes=share).clone()
+            staged = runner.host_inputs(16)["block_tables"]
+            assert (staged[:, width:] == -1).all()
+            if share:
+                oracle.store_kv(s.k_new, s.v_new, okc, ovc, s.slot_mapping)
+            ref = oracle.decode(s.q, okc, ovc, s.block_tables, s.context_lens, s.scale)
+            assert max_err(got, ref) <= TOL[torch.bfloat16], f"step {i} share {share}"
