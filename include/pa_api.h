@@ -11,7 +11,19 @@
  * plus the decode step's store fused into decode (pa_store_decode), the same
  * store and decode over an FP8 pool (pa_store_kv_fp8, pa_decode_fp8,
  * pa_store_decode_fp8) and the
- * sampler that turns the step's logits into tokens (pa_sample).
+ * sampler that turns the step's logits into tokens (pa_sample).  Around them:
+ *
+ *   pa_decode_ex, pa_store_decode_ex   decode options: split-K plan overrides
+ *                     and shared-prefix groups (read each shared page once)
+ *   pa_decode_static_workspace  decode for callers that cannot allocate
+ *   pa_prefill_paged_ex  prefill with a cap on its persistent grid
+ *   pa_sm_split_*, pa_mixed_step  a mixed step's prefill and decode at once
+ *                     on disjoint SM partitions
+ *   pa_copy_segments, pa_stage_decode_step  the device and host halves of a
+ *                     captured decode step fed from the caller's host buffers
+ *   pa_selftest_wait_timeout  shows the kernels' bounded waits ending
+ * and, in pa_block_manager.h, the host-side page directory (pa_bm_*) and the
+ * shared-prefix grouping of a decode batch (pa_prefix_groups).
  *
  * Conventions shared by every call
  *   - All tensor arguments are DEVICE pointers to caller-owned memory; the
