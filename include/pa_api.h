@@ -107,7 +107,8 @@ enum {
     PA_FLAG_BAD_LENGTH = 4,
     PA_FLAG_TIMEOUT = 8,
     PA_FLAG_INTERNAL = 16,
-    PA_FLAG_BAD_VALUE = 32, /* a value outside its domain (pa_sample: temperature <= 1e-10) */
+    PA_FLAG_BAD_VALUE = 32, /* a value outside its domain (pa_sample: temperature <= 1e-10; an unaligned
+                               address in pa_decode_options.operands) */
     PA_FLAG_BAD_GROUP = 64, /* a shared-prefix descriptor breaking its rules (pa_decode_options) */
 };
 
@@ -263,7 +264,23 @@ PA_API int pa_store_decode(const void *k, const void *v, int64_t k_row_stride, i
  * a sequence with prefix_lens[b] > 0 that is in no group gets an unspecified
  * output without a flag.  Supported for 16-bit pools (pa_decode_ex,
  * pa_store_decode_ex).
-
+ *
+ * Operands read at run time (an extension with no counterpart on the pages;
+ * it serves the captured decode step of "nano-vLLM Part 2", section 4.2, whose
+ * graph has fixed arguments):
+ *   operands      NULL, or three addresses {q, k, v} in device-readable memory
+ *                 (device memory, or page-locked host memory from cudaHostAlloc /
+ *                 cudaMallocHost), read by the kernels when they run in place of
+ *                 the call's q, k and v arguments (pa_decode_ex reads only
+ *                 entry 0).  Each address must hold a tensor of the shape,
+ *                 element type and row stride the call's own arguments
+ *                 describe, device-accessible (device or page-locked host
+ *                 memory) and 16-byte aligned; a CTA that reads an unaligned
+ *                 one sets PA_FLAG_BAD_VALUE and skips its work (the outputs
+ *                 are then unspecified).  A CUDA graph of the call is then pointed at a new
+ *                 step's buffers by rewriting the three addresses between
+ *                 replays; the call's own q, k and v must still be valid
+ *                 addresses (they are checked, not read).
  */
 typedef struct pa_decode_options {
     int32_t partition;
@@ -275,6 +292,7 @@ typedef struct pa_decode_options {
     const int32_t *group_offsets;
     const int32_t *group_seqs;
     const int32_t *prefix_lens;
+    const void *const *operands;
 } pa_decode_options;
 
 /* Workspace bytes of pa_decode_ex / pa_store_decode_ex with these options
@@ -514,6 +532,8 @@ PA_API int pa_copy_segments(const pa_copy_segment *segments, int32_t count, void
  *                   NULL; num_segments (0..4) entries whose dst the caller
  *                   set; segment_row_bytes[i] the bytes of one row of
  *                   segment i (a sequence's q, or its new K or V rows).
+ *   operands        the graph's pa_decode_options operands array (three
+ *                   entries: q, k, v), or NULL.
  */
 typedef struct pa_decode_staging {
     int32_t rows;
@@ -531,6 +551,7 @@ typedef struct pa_decode_staging {
     pa_copy_segment *segments;
     int32_t num_segments;
     uint64_t segment_row_bytes[4];
+    const void **operands;
 } pa_decode_staging;
 
 /* shared-prefix groups of a staged step (the `groups` argument below) */
@@ -546,7 +567,9 @@ typedef struct pa_decode_staging {
  * -1, context length 0, table row untouched: a context of 0 reads no page);
  * the groups as `groups` says, unused group entries empty; and, when
  * `sources` is not NULL, segment i pointed at sources[i] for batch *
- * segment_row_bytes[i] bytes (the caller's page-locked q / new K / new V).
+ * segment_row_bytes[i] bytes and the operands array set to sources[0..2]
+ * (the caller's page-locked q / new K / new V), for whichever of the two the
+ * staging holds.
  *   batch           in [0, st->rows].
  *   slot_mapping    host int32 [batch]; context_lens host int32 [batch], each
  *                   in [0, table_cols * block_size].

@@ -58,7 +58,7 @@ class _Options(ctypes.Structure):
     """Mirror of pa_decode_options."""
     _fields_ = [("partition", _i32), ("stages", _i32), ("num_groups", _i32), ("max_group_size", _i32),
                 ("max_prefix_len", _i32), ("prefix_partition", _i32), ("group_offsets", _p), ("group_seqs", _p),
-                ("prefix_lens", _p)]
+                ("prefix_lens", _p), ("operands", _p)]
 
 
 _opt_p = ctypes.POINTER(_Options)
@@ -122,7 +122,8 @@ class DecodeStaging(ctypes.Structure):
                 ("slot_mapping", _p), ("context_lens", _p), ("block_tables", _p),
                 ("max_groups", _i32), ("max_group_size", _i32), ("max_prefix_len", _i32),
                 ("group_offsets", _p), ("group_seqs", _p), ("prefix_lens", _p),
-                ("segments", _p), ("num_segments", _i32), ("segment_row_bytes", ctypes.c_uint64 * 4)]
+                ("segments", _p), ("num_segments", _i32), ("segment_row_bytes", ctypes.c_uint64 * 4),
+                ("operands", _p)]
 
 
 STAGE_NO_GROUPS, STAGE_DERIVE_GROUPS, STAGE_KEEP_GROUPS = 0, 1, 2
@@ -232,24 +233,29 @@ class DecodeOptions:
     ``stages``: TMA ring depth of the partition kernel, 2 or 3 (0 = the plan).
     ``groups``: shared-prefix groups (:class:`PrefixGroups` on the call's device, or in pinned
     host memory): each group's shared pages are read once for all its sequences.
-    ``prefix_partition``: tokens per partition of a shared prefix (0 = the plan)."""
+    ``prefix_partition``: tokens per partition of a shared prefix (0 = the plan).
+    ``operands``: the address of three pointers {q, k, v} in device-readable memory (page-locked
+    host or device), read by the kernels when they run in place of the call's q, k and v (0 = the
+    call's own)."""
 
     def __init__(self, partition: int = 0, stages: int = 0, groups: PrefixGroups | None = None,
-                 prefix_partition: int = 0):
+                 prefix_partition: int = 0, operands: int = 0):
         self.partition, self.stages = int(partition), int(stages)
         self.groups, self.prefix_partition = groups, int(prefix_partition)
+        self.operands = int(operands)
 
     def _c(self) -> _Options:
         g = self.groups
+        ops = self.operands or None
         if g is None or g.num_groups == 0:
-            return _Options(self.partition, self.stages, 0, 0, 0, self.prefix_partition, None, None, None)
+            return _Options(self.partition, self.stages, 0, 0, 0, self.prefix_partition, None, None, None, ops)
         for name in ("group_offsets", "group_seqs", "prefix_lens"):
             t = getattr(g, name)
             if t.dtype != torch.int32 or not t.is_contiguous():
                 raise ValueError(f"groups.{name} must be contiguous int32")
         return _Options(self.partition, self.stages, g.num_groups, max(g.max_group_size, 1),
                         max(g.max_prefix_len, 1), self.prefix_partition, g.group_offsets.data_ptr(),
-                        g.group_seqs.data_ptr(), g.prefix_lens.data_ptr())
+                        g.group_seqs.data_ptr(), g.prefix_lens.data_ptr(), ops)
 
 
 def _opts(options: DecodeOptions | None):

@@ -112,6 +112,9 @@ struct DecodeArgs {
     // prefix grid): that grid already waited before letting this one launch, and each CTA waits
     // for it (griddepcontrol.wait) before it reads the prefix partials and before it exits
     int32_t wait_at_start;
+    // null, or three addresses {q, k_new, v_new} read when the kernels run, in place of the
+    // fields above (a captured graph pointed at a new step's buffers between replays)
+    const void *const *operands;
 };
 
 // Shared memory: the ring (each tile = D/64 slices of 64 rows x 128 bytes,
@@ -150,7 +153,8 @@ __device__ __forceinline__ int context_len(const DecodeArgs &a, int b) {
 // reads that slice, and the proxy fence makes the plain stores visible to the
 // TMA loads this warp issues next.
 template <typename T, int D, bool F8>
-__device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g, int L, int lane) {
+__device__ __forceinline__ void store_new_row(const DecodeArgs &a, const void *k_new, const void *v_new, int b, int g,
+                                              int L, int lane) {
     constexpr int kChunks = D / 8;  // 8-element (16-byte) chunks of one head's new row
     const bool is_v = lane >= kChunks;
     const int ci = is_v ? lane - kChunks : lane;
@@ -162,7 +166,7 @@ __device__ __forceinline__ void store_new_row(const DecodeArgs &a, int b, int g,
     const int pg = a.block_tables[static_cast<int64_t>(b) * a.max_blocks + (j >> a.log2_bs)];
     uint4 raw = make_uint4(0u, 0u, 0u, 0u);
     if (lane < 2 * kChunks)
-        raw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(is_v ? a.v_new : a.k_new) +
+        raw = *reinterpret_cast<const uint4 *>(static_cast<const T *>(is_v ? v_new : k_new) +
                                                b * (is_v ? a.v_new_stride : a.k_new_stride) + g * D + ci * 8);
     if (slot == -1) return;
     const int64_t expect =
@@ -568,6 +572,11 @@ __global__ void __launch_bounds__(kPrefixThreads, ctas_per_sm<kPrefixStages>())
         if (tid == 0 && pp == 0 && g == 0 && chunk == 0) raise_flag(a.err_flag, PA_FLAG_BAD_GROUP);
         return;
     }
+    const void *q_src = a.operands ? a.operands[0] : a.q;  // the step's q (see DecodeArgs::operands)
+    if (reinterpret_cast<uintptr_t>(q_src) & 15) {  // flagged by the sequences' grid as well
+        if (tid == 0) raise_flag(a.err_flag, PA_FLAG_BAD_VALUE);
+        return;
+    }
     const int m0 = off0 + chunk * a.seqs_per_cta;
     const int nm = min(a.seqs_per_cta, off1 - m0);  // members of this chunk
     if (nm <= 0) return;
@@ -629,7 +638,7 @@ __global__ void __launch_bounds__(kPrefixThreads, ctas_per_sm<kPrefixStages>())
         // query fragments (B operand of S^T = K Q^T): row rq's head
         uint32_t qb[D / 16][2];
         const int dq = (lane & 3) * 2;
-        const T *qrow = bq >= 0 ? static_cast<const T *>(a.q) + static_cast<int64_t>(bq) * a.q_row_stride +
+        const T *qrow = bq >= 0 ? static_cast<const T *>(q_src) + static_cast<int64_t>(bq) * a.q_row_stride +
                                       static_cast<int64_t>(g * G + rq % G) * D
                                 : nullptr;
 #pragma unroll
@@ -754,6 +763,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
 
     const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the step's q and new rows: the call's, or the addresses the operands array holds now
+    // (loaded with the length and the table below, one round trip)
+    const void *q_src = a.q, *k_src = a.k_new, *v_src = a.v_new;
+    if (a.operands) {
+        q_src = a.operands[0];
+        if (a.slot_mapping) {
+            k_src = a.operands[1];
+            v_src = a.operands[2];
+        }
+        // every access below is a 4- or 16-byte vector: an unaligned address is flagged and the
+        // CTA leaves (the same decision in every thread, before any barrier)
+        if ((reinterpret_cast<uintptr_t>(q_src) | reinterpret_cast<uintptr_t>(k_src) |
+             reinterpret_cast<uintptr_t>(v_src)) & 15) {
+            if (tid == 0) raise_flag(a.err_flag, PA_FLAG_BAD_VALUE);
+            if (!a.wait_at_start) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            return;
+        }
+    }
 
     // The block-table entries this partition can touch are loaded together with the context
     // length (one memory round trip before the first TMA instead of two); entries past the
@@ -815,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     uint32_t qb[S::kKSteps][2];
     if constexpr (F8) {  // fp16, contraction index d = 16 ks + 4j + {0..3} (see the F8 note above)
         const int hq = lane >> 2, j = lane & 3;
-        const T *qrow = static_cast<const T *>(a.q) + static_cast<int64_t>(b) * a.q_row_stride +
+        const T *qrow = static_cast<const T *>(q_src) + static_cast<int64_t>(b) * a.q_row_stride +
                         static_cast<int64_t>(g * a.group + hq) * D;
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) {
@@ -830,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     } else {
         const int hq = lane >> 2;
         const int dq = (lane & 3) * 2;
-        const T *qrow = static_cast<const T *>(a.q) + static_cast<int64_t>(b) * a.q_row_stride +
+        const T *qrow = static_cast<const T *>(q_src) + static_cast<int64_t>(b) * a.q_row_stride +
                         static_cast<int64_t>(g * a.group + hq) * D;
 #pragma unroll
         for (int ks = 0; ks < S::kKSteps; ++ks) {
@@ -849,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<ST, F8>())
     int issued = 0;  // tiles the producer started
 
     if (warp == kProducerWarp) {
-        if (a.slot_mapping && end == L) store_new_row<T, D, F8>(a, b, g, L, lane);
+        if (a.slot_mapping && end == L) store_new_row<T, D, F8>(a, k_src, v_src, b, g, L, lane);
         if (lane == 0)
             issued = produce_tiles<D, ST, F8>(&tm_k, &tm_v, &tm_k_tail, &tm_v_tail, a, g, start, end, first_page, bt_s,
                                               ring, bars, abort_s);
@@ -1195,6 +1222,7 @@ cudaError_t launch_decode(const void *q, int64_t q_row_stride, const void *k_cac
     a.v_new_stride = fused ? fused->v_row_stride : 0;
     a.k_cache_w = const_cast<void *>(k_cache);
     a.v_cache_w = const_cast<void *>(v_cache);
+    a.operands = opt ? opt->operands : nullptr;
 
     // the pool as [num_blocks * block_size rows, H_kv * D columns]; one box = min(block_size, 64)
     // rows (a box never crosses a page) of one kv head's row: 128 bytes (E4M3 codes, or 16-bit at

@@ -3,8 +3,9 @@
 // the GPU", section 4.2: a decode step writes its slot mapping, context
 // lengths and block tables into the fixed buffers of the graph recorded for
 // its padded batch size and pads the rows past the batch.  Doing that, the
-// shared-prefix grouping and the gather list in one call keeps a step's host
-// work to plain memory copies.  Plain C++, no GPU.
+// shared-prefix grouping and the addresses of the caller's buffers (a gather
+// list, or the decode's operands array) in one call keeps a step's host work to
+// plain memory copies.  Plain C++, no GPU.
 #include <stdio.h>
 #include <string.h>
 
@@ -50,8 +51,10 @@ int pa_stage_decode_step(const pa_decode_staging *st, int32_t batch, const int32
     if (groups != PA_STAGE_NO_GROUPS && groups != PA_STAGE_DERIVE_GROUPS && groups != PA_STAGE_KEEP_GROUPS)
         return fail("unknown groups mode %lld", groups);
     if (groups == PA_STAGE_DERIVE_GROUPS && !has_groups) return fail("this staging holds no shared-prefix groups");
-    if (sources && (!st->segments || st->num_segments < 0 || st->num_segments > 4))
-        return fail("this staging holds no gather list");
+    if (sources && !st->operands && !st->segments)
+        return fail("this staging holds neither a gather list nor an operands array");
+    if (sources && st->segments && (st->num_segments < 0 || st->num_segments > 4))
+        return fail("num_segments %lld outside [0, 4]", st->num_segments);
     const int64_t cap = static_cast<int64_t>(table_cols) * st->block_size;
     for (int32_t b = 0; b < batch; ++b)
         if (context_lens[b] < 0 || context_lens[b] > cap)
@@ -93,12 +96,14 @@ int pa_stage_decode_step(const pa_decode_staging *st, int32_t batch, const int32
         fill(st->prefix_lens + batch, pad, 0);
     }
 
-    if (sources) {
+    if (sources && st->segments) {
         for (int32_t i = 0; i < st->num_segments; ++i) {
             st->segments[i].src = sources[i];
             st->segments[i].bytes = static_cast<uint64_t>(batch) * st->segment_row_bytes[i];
         }
     }
+    if (sources && st->operands)
+        for (int i = 0; i < 3; ++i) st->operands[i] = sources[i];
     return PA_OK;
 }
 

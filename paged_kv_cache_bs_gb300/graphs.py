@@ -17,14 +17,16 @@ pinned staging and write the output into pinned memory directly, so the step
 has no copy-engine transfer, whose start-up latency is longer than the
 transfer of these few MB.  q and the new K/V rows come one of two ways, each
 bucket holding a graph for both: when the caller's tensors are page-locked,
-the graph begins with ``pa_copy_segments``, which pulls them with all SMs into
-device buffers from where they are (their addresses written into a pinned
-segment list each step: no host-side copy); otherwise they are copied into the
-pinned staging and the kernels read them there.  With ``zero_copy=False`` the
+they are read where they are -- over a 16-bit pool by the kernels themselves,
+which take the three addresses from a pinned array (the decode options'
+``operands``) rewritten each step, over an E4M3 pool by a first kernel,
+``pa_copy_segments``, that pulls them with all SMs into device buffers from a
+pinned list of the three copies; otherwise they are copied into the pinned
+staging and the kernels read them there.  With ``zero_copy=False`` the
 graph holds a host-to-device copy of the packed inputs, the fused call on
 device buffers and a device-to-host copy of the output.  A step's host side is
 one native call (``pa_stage_decode_step``: metadata rows, padding, shared-prefix
-groups, gather list) and one ``cuGraphLaunch``.  Argument marshalling only:
+groups, the addresses of the caller's buffers) and one ``cuGraphLaunch``.  Argument marshalling only:
 every step of the path runs in the library's kernels.
 """
 
@@ -121,16 +123,23 @@ class DecodeGraphRunner:
         out_bytes = max(self.sizes) * num_q_heads * d * esz
         self.host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
         self.host_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
-        # the step's q and new K/V rows: device buffers the graph's first kernel fills from the
-        # caller's page-locked tensors (zero_copy); the list of its three copies is pinned
+        # zero_copy: the step's q and new K/V rows are read where the caller left them when they are
+        # page-locked -- over a 16-bit pool by the kernels themselves through a pinned array of
+        # their three addresses (the decode options' operands), over an E4M3 pool (whose calls
+        # take no options) by a first kernel that gathers them into device buffers, from a pinned
+        # list of the three copies (one list per bucket: its destinations are fixed)
         self._qkv_names = ("q", "k_new", "v_new")
+        self._operands = None
         if zero_copy:
             self.dev_in = self.dev_out = None
-            lay = self._layout[max(self.sizes)]
-            self._qkv_dev = torch.zeros(sum(lay[n][3] for n in self._qkv_names) + 512, dtype=torch.uint8, device=dev)
-            # one list per bucket: its destinations are fixed, a step rewrites sources and sizes
-            self._seg_buf = torch.zeros(3 * len(self.sizes) * ctypes.sizeof(CopySegment), dtype=torch.uint8).pin_memory()
-            self._qkv_views = {}
+            self._operands = torch.zeros(3, dtype=torch.int64).pin_memory()
+            if self.fp8:
+                lay = self._layout[max(self.sizes)]
+                self._qkv_dev = torch.zeros(sum(lay[n][3] for n in self._qkv_names) + 512, dtype=torch.uint8,
+                                            device=dev)
+                self._seg_buf = torch.zeros(3 * len(self.sizes) * ctypes.sizeof(CopySegment),
+                                            dtype=torch.uint8).pin_memory()
+                self._qkv_views = {}
         else:
             self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
             self.dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
@@ -150,9 +159,9 @@ class DecodeGraphRunner:
         # per bucket: the graph whose kernels read q and the new rows from the pinned staging, and
         # (zero_copy) the one that first pulls them from the caller's page-locked tensors
         self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
-        self._gather_graphs: dict[int, torch.cuda.CUDAGraph] = {}
-        self._use_gather: dict[int, bool] = {}
-        self._execs: dict[tuple[int, bool], int] = {}  # (bucket, gather) -> the instantiated graph
+        self._inplace_graphs: dict[int, torch.cuda.CUDAGraph] = {}
+        self._use_inplace: dict[int, bool] = {}
+        self._execs: dict[tuple[int, bool], int] = {}  # (bucket, in place) -> the instantiated graph
         self._device_index = dev.index if dev.index is not None else torch.cuda.current_device()
         self._capture()
 
@@ -190,16 +199,17 @@ class DecodeGraphRunner:
         n = b * self.num_q_heads * self.head_dim
         return buf.view(self.dtype)[:n].view(b, self.num_q_heads, self.head_dim)
 
-    def _options(self, b: int, views: dict | None) -> DecodeOptions | None:
-        """The decode options of bucket b: the staged groups at their captured capacities."""
+    def _options(self, b: int, views: dict | None, operands: int = 0) -> DecodeOptions | None:
+        """The decode options of bucket b: the staged groups at their captured capacities, and the
+        operands array when the kernels read the caller's q and new rows in place."""
         if self.group_caps is None:
-            return None
+            return DecodeOptions(operands=operands) if operands else None
         ng, members, prefix = self.group_caps
         if views is None:  # sizing only
             z = torch.zeros(max(b, ng + 1), dtype=torch.int32)
             return DecodeOptions(groups=PrefixGroups(z[:ng + 1], z[:b], z[:b], members, prefix))
         return DecodeOptions(groups=PrefixGroups(views["group_offsets"], views["group_seqs"], views["prefix_lens"],
-                                                 members, prefix))
+                                                 members, prefix), operands=operands)
 
     # ----------------------------------------------------------------- capture
     def _dev_qkv(self, b: int) -> dict:
@@ -229,7 +239,8 @@ class DecodeGraphRunner:
             segs[i].bytes = batch * dev[n][0].numel() * dev[n].element_size()
 
     def _make_staging(self, b: int) -> DecodeStaging:
-        """The pa_decode_staging of bucket b over its pinned views (and gather list)."""
+        """The pa_decode_staging of bucket b over its pinned views (and its gather list, or the
+        operands array)."""
         h = self._staged(b)
         st = DecodeStaging(rows=b, max_blocks=self.max_blocks, block_size=self.k_cache.shape[1],
                            slot_mapping=h["slot_mapping"].data_ptr(), context_lens=h["context_lens"].data_ptr(),
@@ -239,20 +250,23 @@ class DecodeGraphRunner:
             st.group_offsets = h["group_offsets"].data_ptr()
             st.group_seqs = h["group_seqs"].data_ptr()
             st.prefix_lens = h["prefix_lens"].data_ptr()
-        if self.zero_copy:
+        if self.zero_copy and self.fp8:
             dev = self._dev_qkv(b)
             self._point_segments(b, b, [h[n].data_ptr() for n in self._qkv_names])
             st.segments = self._segments_ptr(b)
             st.num_segments = 3
             for i, n in enumerate(self._qkv_names):
                 st.segment_row_bytes[i] = dev[n][0].numel() * dev[n].element_size()
+        elif self.zero_copy:
+            st.operands = self._operands.data_ptr()
         return st
 
-    def _launch(self, b: int, gather: bool = False) -> None:
+    def _launch(self, b: int, inplace: bool = False) -> None:
         lay = self._layout[b]
+        operands = 0
         if self.zero_copy:
             v = dict(self._views(self.host_in, b))
-            if gather:
+            if inplace and self.fp8:
                 # capture with the list pointing at the staging (valid memory); steps rewrite it
                 self._point_segments(b, b, [v[n].data_ptr() for n in self._qkv_names])
                 rc = _lib.pa_copy_segments(ctypes.c_void_p(self._segments_ptr(b)), 3,
@@ -260,6 +274,12 @@ class DecodeGraphRunner:
                 if rc != 0:
                     raise PagedAttentionError("pa_copy_segments", rc)
                 v.update(self._dev_qkv(b))
+            elif inplace:
+                # the kernels read q and the new rows through the operands array: captured (and
+                # warmed up) pointing at the staging's own, valid memory; steps rewrite it
+                for i, n in enumerate(self._qkv_names):
+                    self._operands[i] = v[n].data_ptr()
+                operands = self._operands.data_ptr()
             out = self._out_view(self.host_out, b)
         else:
             self.dev_in[:lay["_bytes"]].copy_(self.host_in[:lay["_bytes"]], non_blocking=True)
@@ -272,7 +292,7 @@ class DecodeGraphRunner:
         else:
             store_decode(v["k_new"], v["v_new"], v["slot_mapping"], v["q"], self.k_cache, self.v_cache,
                          v["block_tables"], v["context_lens"], self.scale, out=out, workspace=self.workspace,
-                         options=self._options(b, v))
+                         options=self._options(b, v, operands))
         if not self.zero_copy:
             self._out_view(self.host_out, b).copy_(out, non_blocking=True)
 
@@ -298,7 +318,7 @@ class DecodeGraphRunner:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     self._launch(b, m)
-                (self._gather_graphs if m else self.graphs)[b] = g
+                (self._inplace_graphs if m else self.graphs)[b] = g
                 self._execs[(b, m)] = g.raw_cuda_graph_exec()
         torch.cuda.current_stream(self.k_cache.device).wait_stream(stream)
 
@@ -326,11 +346,11 @@ class DecodeGraphRunner:
         """Write one step's host tensors into the pinned staging of its bucket and pad the rest
         (slot -1, context length 0; groups past the step's are empty).  The shared-prefix groups
         are ``groups``, or with ``share_prefixes`` derived by ``pa_prefix_groups`` from the staged
-        block tables.  The metadata, the groups and the gather list go by one native call,
-        ``pa_stage_decode_step``.  With ``zero_copy`` and page-locked, contiguous q / k_new / v_new
-        of the runner's dtype, those three are not copied: the next :meth:`replay` reads them where
-        they are, so keep them unchanged until its stream has completed (:meth:`step`
-        synchronises).  Returns the bucket size."""
+        block tables.  The metadata, the groups and the addresses of the caller's buffers go by one
+        native call, ``pa_stage_decode_step``.  With ``zero_copy`` and page-locked, contiguous,
+        16-byte aligned q / k_new / v_new of the runner's dtype, those three are not copied: the
+        next :meth:`replay` reads them where they are, so keep them unchanged until its stream has
+        completed (:meth:`step` synchronises).  Returns the bucket size."""
         batch = q.shape[0]
         b = self.bucket(batch)
         if share_prefixes:
@@ -351,11 +371,12 @@ class DecodeGraphRunner:
             raise ValueError(f"slot_mapping {tuple(slot_mapping.shape)}, context_lens {tuple(context_lens.shape)} "
                              f"and block_tables {tuple(block_tables.shape)} must hold {batch} rows")
         dt, shapes = self.dtype, self._row_shapes
-        gather = self.zero_copy and all(t.dtype == dt and t.shape[1:] == shp and t.is_contiguous() and t.is_pinned()
-                                        for t, shp in zip((q, k_new, v_new), shapes))
-        self._use_gather[b] = gather
-        if gather:
-            # page-locked tensors: the graph's first kernel reads them where they are
+        inplace = self.zero_copy and all(t.dtype == dt and t.shape[1:] == shp and t.data_ptr() % 16 == 0
+                                         and t.is_contiguous() and t.is_pinned()
+                                         for t, shp in zip((q, k_new, v_new), shapes))
+        self._use_inplace[b] = inplace
+        if inplace:
+            # page-locked tensors: the graph reads them where they are
             src = self._sources
             src[0], src[1], src[2] = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
             sources = self._sources_addr
@@ -392,7 +413,7 @@ class DecodeGraphRunner:
         """Replay the bucket's graph (inputs from the pinned staging) on the current stream; the
         returned pinned host view of the output is valid once that stream has synchronised."""
         b = self.bucket(batch)
-        _graph_launch(self._execs[(b, self._use_gather.get(b, False))],
+        _graph_launch(self._execs[(b, self._use_inplace.get(b, False))],
                       torch._C._cuda_getCurrentRawStream(self._device_index))
         out = self._staged_out.get(batch)
         if out is None:  # the first `batch` rows of the bucket's output, one view per batch size

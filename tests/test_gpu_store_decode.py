@@ -112,3 +112,42 @@ def test_store_decode_with_pinned_host_operands(pa, fp8):
     assert torch.equal(bits(kc_h), bits(kc_d)) and torch.equal(bits(vc_h), bits(vc_d)), "pool differs"
     with pytest.raises(ValueError):
         call(dict(ops), kc_h, vc_h, None)  # pageable host tensors
+
+
+@pytest.mark.parametrize("where", ["device", "pinned"])
+@pytest.mark.parametrize("grouped", [False, True])
+def test_store_decode_operands_read_at_run_time(pa, where, grouped):
+    """pa_decode_options.operands: the kernels take q and the new K/V rows from an array of three
+    addresses read when they run.  The call's own q / k / v point at a zero-filled decoy: output and
+    pool are bit-identical to the call that passes the real tensors, with and without shared-prefix
+    groups, for operands in device or page-locked host memory."""
+    from paged_kv_cache_bs_gb300.block_manager import prefix_groups
+    seqs = [(500 + 29 * i, i // 5, 256) for i in range(15)] + [(70 + 3 * i, -1, 0) for i in range(6)]
+    st = inputs.make_decode_shared(seqs, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                                   dtype=torch.bfloat16, seed=211)
+    groups = prefix_groups(st.block_tables, st.context_lens, 16).to("cuda") if grouped else None
+    real = dict(k=st.k_new, v=st.v_new, q=st.q)
+    real = {n: (t.cuda() if where == "device" else t.pin_memory()) for n, t in real.items()}
+    decoy = {n: torch.zeros_like(t, device="cuda") for n, t in real.items()}
+    sm, bt, cl = st.slot_mapping.cuda(), st.block_tables.cuda(), st.context_lens.cuda()
+    kc_a, vc_a = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    ref = pa.store_decode(real["k"], real["v"], sm, real["q"], kc_a, vc_a, bt, cl, st.scale,
+                          options=pa.DecodeOptions(groups=groups) if grouped else None)
+    ops = torch.tensor([real["q"].data_ptr(), real["k"].data_ptr(), real["v"].data_ptr()],
+                       dtype=torch.int64).pin_memory()
+    kc_b, vc_b = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pa.store_decode(decoy["k"], decoy["v"], sm, decoy["q"], kc_b, vc_b, bt, cl, st.scale, err_flag=flag,
+                          options=pa.DecodeOptions(groups=groups, operands=ops.data_ptr()))
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    assert_bit_equal(got, ref, "output through the operands array")
+    bits = (lambda t: t.cpu().view(torch.uint8))  # noqa: E731
+    assert torch.equal(bits(kc_b), bits(kc_a)) and torch.equal(bits(vc_b), bits(vc_a)), "pool differs"
+    # an unaligned address is flagged before any access through it (no load is issued from it)
+    ops[0] = real["q"].data_ptr() + 2
+    kc_c, vc_c = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    pa.store_decode(decoy["k"], decoy["v"], sm, decoy["q"], kc_c, vc_c, bt, cl, st.scale, err_flag=flag,
+                    options=pa.DecodeOptions(groups=groups, operands=ops.data_ptr()))
+    torch.cuda.synchronize()
+    assert int(flag.item()) & pa.FLAG_BAD_VALUE

@@ -1,8 +1,8 @@
 """pa_stage_decode_step on the host (no GPU): a decode step's slot mapping, context lengths and
 block tables written into a captured bucket's staging with the rows past the batch padded
 ("nano-vLLM Part 2: Block Tables, KV Cache, and the Path to the GPU", section 4.2), the
-shared-prefix groups staged as their mode says, and the gather list pointed at the caller's
-buffers.  The staging arrays here are ordinary host tensors: the call never touches a GPU."""
+shared-prefix groups staged as their mode says, and the gather list or the decode's operands
+array pointed at the caller's buffers.  The staging arrays here are ordinary host tensors: the call never touches a GPU."""
 
 import ctypes
 import random
@@ -126,6 +126,21 @@ def test_gather_list_pointed_at_sources(pa_host):
     assert s.segs[0].bytes == 5 * 256
 
 
+def test_operands_array_pointed_at_sources(pa_host):
+    s = Staging(pa_host)
+    ops = torch.zeros(3, dtype=torch.int64)
+    s.st.operands = ops.data_ptr()
+    pa_host.stage_decode_step(s.st, *step(4, seed=9), sources=[0xA000, 0xB010, 0xC020])
+    assert ops.tolist() == [0xA000, 0xB010, 0xC020]
+    pa_host.stage_decode_step(s.st, *step(4, seed=9))  # no sources: left as it is
+    assert ops.tolist() == [0xA000, 0xB010, 0xC020]
+    # with both a gather list and an operands array, both are written
+    s = Staging(pa_host, segments=True)
+    s.st.operands = ops.data_ptr()
+    pa_host.stage_decode_step(s.st, *step(2, seed=10), sources=[0x1, 0x2, 0x3])
+    assert ops.tolist() == [1, 2, 3] and s.segs[2].src == 3
+
+
 def test_invalid_arguments_rejected_before_any_write(pa_host):
     s = Staging(pa_host, caps=(4, 8, 160))
     slot, ctx, tables = step(4, seed=8)
@@ -140,7 +155,7 @@ def test_invalid_arguments_rejected_before_any_write(pa_host):
     assert call(batch=-1) == -1
     assert call(cols=0) == -1 and call(cols=MAX_BLOCKS + 1) == -1
     assert call(mode=3) == -1
-    assert call(sources=ctypes.addressof((ctypes.c_void_p * 3)())) == -1  # no gather list in this staging
+    assert call(sources=ctypes.addressof((ctypes.c_void_p * 3)())) == -1  # no gather list or operands array
     assert call(staging=None) == -1
     bad = ctx.clone()
     bad[2] = MAX_BLOCKS * BS + 1
