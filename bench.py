@@ -337,13 +337,10 @@ class DecodeWorkload:
             self.e2e_path = ("DecodeGraphRunner.step() from the caller's page-locked host tensors, alternating two "
                              "seeded decode steps over the same pool: slot mapping, context lengths and block tables "
                              "written into the pinned staging by one native call (pa_stage_decode_step, C++), "
-                             + ("CUDA-graph replay whose first kernel (pa_copy_segments) pulls q and the new K/V rows "
-                                "from the caller's tensors over NVLink-C2C, then the fused store + decode"
-                                if self.runner.fp8 else
-                                "CUDA-graph replay of the fused store + decode, whose kernels read q and the new K/V "
-                                "rows from the caller's tensors over NVLink-C2C (their addresses in a pinned operands "
-                                "array the same call writes)")
-                             + " writing the output into pinned host memory, stream sync; host wall "
+                             "CUDA-graph replay of the fused store + decode, whose kernels read q and the new K/V "
+                             "rows from the caller's tensors over NVLink-C2C (their addresses in a pinned operands "
+                             "array the same call writes) and write the output into pinned host memory, stream "
+                             "sync; host wall "
                              "clock" + ("; the shared-prefix groups derived from the staged block tables "
                                         "inside that call every step" if self.groups is not None else ""))
             return None, None, self.runner.h2d_bytes(st.batch), self.runner.d2h_bytes(st.batch)

@@ -13,8 +13,9 @@
  * pa_store_decode_fp8) and the
  * sampler that turns the step's logits into tokens (pa_sample).  Around them:
  *
- *   pa_decode_ex, pa_store_decode_ex   decode options: split-K plan overrides
- *                     and shared-prefix groups (read each shared page once)
+ *   pa_decode_ex, pa_store_decode_ex   decode options: split-K plan overrides,
+ *                     shared-prefix groups (read each shared page once) and
+ *                     operands read at run time (pa_store_decode_fp8_ex: those)
  *   pa_decode_static_workspace  decode for callers that cannot allocate
  *   pa_prefill_paged_ex  prefill with a cap on its persistent grid
  *   pa_sm_split_*, pa_mixed_step  a mixed step's prefill and decode at once
@@ -422,6 +423,22 @@ PA_API int pa_store_decode_fp8(const void *k, const void *v, int64_t k_row_strid
                         int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, float k_scale,
                         float v_scale, void *out, void *workspace, size_t workspace_bytes, pa_dtype dtype,
                         int32_t *err_flag, void *stream);
+
+/*
+ * pa_store_decode_fp8_ex -- pa_store_decode_fp8 with decode options, of which
+ * an E4M3 pool takes only `operands` (q and the new rows read through three
+ * addresses when the kernels run, as for pa_store_decode_ex); every other field
+ * must be 0 (PA_ERR_INVALID_ARG otherwise), so the workspace is still
+ * pa_decode_fp8_workspace_bytes.  NULL options: pa_store_decode_fp8.
+ */
+PA_API int pa_store_decode_fp8_ex(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                                  const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                                  void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                  float scale, float k_scale, float v_scale, void *out, void *workspace,
+                                  size_t workspace_bytes, const pa_decode_options *options, pa_dtype dtype,
+                                  int32_t *err_flag, void *stream);
 
 /*
  * pa_prefill_paged -- causal varlen prefill over a paged prefix.

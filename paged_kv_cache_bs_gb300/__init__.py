@@ -81,6 +81,9 @@ _lib.pa_decode_fp8.argtypes = [_p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32,
 _lib.pa_store_decode_fp8.restype = ctypes.c_int
 _lib.pa_store_decode_fp8.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
                                      _i32, _i32, _f32, _f32, _f32, _p, _p, _sz, ctypes.c_int, _p, _p]
+_lib.pa_store_decode_fp8_ex.restype = ctypes.c_int
+_lib.pa_store_decode_fp8_ex.argtypes = [_p, _p, _i64, _i64, _p, _p, _i64, _p, _p, _p, _i32, _p, _i32, _i32, _i32,
+                                        _i32, _i32, _i32, _f32, _f32, _f32, _p, _p, _sz, _opt_p, ctypes.c_int, _p, _p]
 _lib.pa_sample.restype = ctypes.c_int
 _lib.pa_sample.argtypes = [_p, _i64, _i32, _i32, ctypes.c_int, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
 _lib.pa_selftest_wait_timeout.restype = ctypes.c_int
@@ -572,9 +575,10 @@ def store_decode_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tenso
                      k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                      context_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                     err_flag: torch.Tensor | None = None) -> torch.Tensor:
+                     err_flag: torch.Tensor | None = None, operands: int = 0) -> torch.Tensor:
     """One decode step over an fp8 pool in one launch: quantise k/v ([B, H_kv, D]) into slot
-    ``slot_mapping`` (each sequence's last context position, or -1) and attend."""
+    ``slot_mapping`` (each sequence's last context position, or -1) and attend.  ``operands``: as
+    :class:`DecodeOptions` (``pa_store_decode_fp8_ex``; the only option an E4M3 pool takes)."""
     _fp8_pool(k_cache, v_cache)
     n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
     B, hq = q.shape[0], q.shape[1]
@@ -587,13 +591,17 @@ def store_decode_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tenso
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=k_cache.device)
     workspace = _fp8_workspace(q, hkv, d, block_tables, bs, workspace, k_cache.device)
-    rc = _lib.pa_store_decode_fp8(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q),
-                                  _rows(q, "q"), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                  block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, n, bs, float(scale),
-                                  float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _dtype(q), _ptr(err_flag),
-                                  _stream(k_cache))
-    _check("pa_store_decode_fp8", rc)
+    args = (_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), _ptr(slot_mapping), _ptr(q), _rows(q, "q"),
+            _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, hq, hkv,
+            d, n, bs, float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size())
+    if operands:
+        rc = _lib.pa_store_decode_fp8_ex(*args, _opts(DecodeOptions(operands=operands)), _dtype(q), _ptr(err_flag),
+                                         _stream(k_cache))
+        _check("pa_store_decode_fp8_ex", rc)
+    else:
+        rc = _lib.pa_store_decode_fp8(*args, _dtype(q), _ptr(err_flag), _stream(k_cache))
+        _check("pa_store_decode_fp8", rc)
     return out
 
 

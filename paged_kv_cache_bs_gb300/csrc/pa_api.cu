@@ -350,6 +350,25 @@ int pa_store_decode_fp8(const void *k, const void *v, int64_t k_row_stride, int6
                         num_blocks, block_size, scale, out, workspace, workspace_bytes, dtype, err_flag, stream, &sc);
 }
 
+int pa_store_decode_fp8_ex(const void *k, const void *v, int64_t k_row_stride, int64_t v_row_stride,
+                           const int32_t *slot_mapping, const void *q, int64_t q_row_stride, void *k_cache,
+                           void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, float k_scale,
+                           float v_scale, void *out, void *workspace, size_t workspace_bytes,
+                           const pa_decode_options *options, pa_dtype dtype, int32_t *err_flag, void *stream) {
+    // an E4M3 pool takes the operands alone: its plan (and so its workspace) has no overrides
+    if (options && (options->partition || options->stages || options->num_groups || options->max_group_size ||
+                    options->max_prefix_len || options->prefix_partition || options->group_offsets ||
+                    options->group_seqs || options->prefix_lens))
+        return fail(PA_ERR_INVALID_ARG, "pa_store_decode_fp8_ex takes options.operands only");
+    const pa::Fp8Scales sc{k_scale, v_scale};
+    return store_decode(k, v, k_row_stride, v_row_stride, slot_mapping, q, q_row_stride, k_cache, v_cache,
+                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                        num_blocks, block_size, scale, out, workspace, workspace_bytes, dtype, err_flag, stream, &sc,
+                        options);
+}
+
 int pa_decode_fp8(const void *q, int64_t q_row_stride, const void *k_cache, const void *v_cache,
                   const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,

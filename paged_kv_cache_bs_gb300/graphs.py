@@ -17,12 +17,9 @@ pinned staging and write the output into pinned memory directly, so the step
 has no copy-engine transfer, whose start-up latency is longer than the
 transfer of these few MB.  q and the new K/V rows come one of two ways, each
 bucket holding a graph for both: when the caller's tensors are page-locked,
-they are read where they are -- over a 16-bit pool by the kernels themselves,
-which take the three addresses from a pinned array (the decode options'
-``operands``) rewritten each step, over an E4M3 pool by a first kernel,
-``pa_copy_segments``, that pulls them with all SMs into device buffers from a
-pinned list of the three copies; otherwise they are copied into the pinned
-staging and the kernels read them there.  With ``zero_copy=False`` the
+the kernels read them where they are, taking the three addresses from a pinned
+array (the decode options' ``operands``) rewritten each step; otherwise they
+are copied into the pinned staging and the kernels read them there.  With ``zero_copy=False`` the
 graph holds a host-to-device copy of the packed inputs, the fused call on
 device buffers and a device-to-host copy of the output.  A step's host side is
 one native call (``pa_stage_decode_step``: metadata rows, padding, shared-prefix
@@ -37,7 +34,7 @@ import ctypes
 
 import torch
 
-from . import (_fp8_pool, _FP8_POOL, _lib, CopySegment, DecodeOptions, DecodeStaging, PagedAttentionError,
+from . import (_fp8_pool, _FP8_POOL, _lib, DecodeOptions, DecodeStaging, PagedAttentionError,
                PrefixGroups, STAGE_DERIVE_GROUPS, STAGE_KEEP_GROUPS, STAGE_NO_GROUPS, decode_fp8_workspace_bytes,
                decode_workspace_bytes, store_decode, store_decode_fp8)
 
@@ -123,23 +120,14 @@ class DecodeGraphRunner:
         out_bytes = max(self.sizes) * num_q_heads * d * esz
         self.host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
         self.host_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
-        # zero_copy: the step's q and new K/V rows are read where the caller left them when they are
-        # page-locked -- over a 16-bit pool by the kernels themselves through a pinned array of
-        # their three addresses (the decode options' operands), over an E4M3 pool (whose calls
-        # take no options) by a first kernel that gathers them into device buffers, from a pinned
-        # list of the three copies (one list per bucket: its destinations are fixed)
+        # zero_copy: when the caller's q and new K/V rows are page-locked, the kernels read them
+        # where they are, through a pinned array of their three addresses (the decode options'
+        # operands) that each step rewrites
         self._qkv_names = ("q", "k_new", "v_new")
         self._operands = None
         if zero_copy:
             self.dev_in = self.dev_out = None
             self._operands = torch.zeros(3, dtype=torch.int64).pin_memory()
-            if self.fp8:
-                lay = self._layout[max(self.sizes)]
-                self._qkv_dev = torch.zeros(sum(lay[n][3] for n in self._qkv_names) + 512, dtype=torch.uint8,
-                                            device=dev)
-                self._seg_buf = torch.zeros(3 * len(self.sizes) * ctypes.sizeof(CopySegment),
-                                            dtype=torch.uint8).pin_memory()
-                self._qkv_views = {}
         else:
             self.dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
             self.dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
@@ -212,35 +200,8 @@ class DecodeGraphRunner:
                                                  members, prefix), operands=operands)
 
     # ----------------------------------------------------------------- capture
-    def _dev_qkv(self, b: int) -> dict:
-        """Device views of bucket b's q, k_new and v_new (zero_copy)."""
-        views = self._qkv_views.get(b)
-        if views is None:
-            lay, off, views = self._layout[b], 0, {}
-            for n in self._qkv_names:
-                _, shape, dt, nbytes = lay[n]
-                views[n] = self._qkv_dev[off:off + nbytes].view(dt).view(shape)
-                off = _align(off + nbytes)
-            self._qkv_views[b] = views
-        return views
-
-    def _segments_ptr(self, b: int) -> int:
-        """Address of bucket b's gather list (three CopySegments in pinned memory)."""
-        return self._seg_buf.data_ptr() + 3 * self.sizes.index(b) * ctypes.sizeof(CopySegment)
-
-    def _point_segments(self, b: int, batch: int, sources) -> None:
-        """Bucket b's gather list: source i (a host tensor's address, or the staging's) to the
-        bucket's device buffer, ``batch`` rows."""
-        dev = self._dev_qkv(b)
-        segs = (CopySegment * 3).from_address(self._segments_ptr(b))
-        for i, (n, src) in enumerate(zip(self._qkv_names, sources)):
-            segs[i].src = src
-            segs[i].dst = dev[n].data_ptr()
-            segs[i].bytes = batch * dev[n][0].numel() * dev[n].element_size()
-
     def _make_staging(self, b: int) -> DecodeStaging:
-        """The pa_decode_staging of bucket b over its pinned views (and its gather list, or the
-        operands array)."""
+        """The pa_decode_staging of bucket b over its pinned views (and the operands array)."""
         h = self._staged(b)
         st = DecodeStaging(rows=b, max_blocks=self.max_blocks, block_size=self.k_cache.shape[1],
                            slot_mapping=h["slot_mapping"].data_ptr(), context_lens=h["context_lens"].data_ptr(),
@@ -250,14 +211,7 @@ class DecodeGraphRunner:
             st.group_offsets = h["group_offsets"].data_ptr()
             st.group_seqs = h["group_seqs"].data_ptr()
             st.prefix_lens = h["prefix_lens"].data_ptr()
-        if self.zero_copy and self.fp8:
-            dev = self._dev_qkv(b)
-            self._point_segments(b, b, [h[n].data_ptr() for n in self._qkv_names])
-            st.segments = self._segments_ptr(b)
-            st.num_segments = 3
-            for i, n in enumerate(self._qkv_names):
-                st.segment_row_bytes[i] = dev[n][0].numel() * dev[n].element_size()
-        elif self.zero_copy:
+        if self.zero_copy:
             st.operands = self._operands.data_ptr()
         return st
 
@@ -266,15 +220,7 @@ class DecodeGraphRunner:
         operands = 0
         if self.zero_copy:
             v = dict(self._views(self.host_in, b))
-            if inplace and self.fp8:
-                # capture with the list pointing at the staging (valid memory); steps rewrite it
-                self._point_segments(b, b, [v[n].data_ptr() for n in self._qkv_names])
-                rc = _lib.pa_copy_segments(ctypes.c_void_p(self._segments_ptr(b)), 3,
-                                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-                if rc != 0:
-                    raise PagedAttentionError("pa_copy_segments", rc)
-                v.update(self._dev_qkv(b))
-            elif inplace:
+            if inplace:
                 # the kernels read q and the new rows through the operands array: captured (and
                 # warmed up) pointing at the staging's own, valid memory; steps rewrite it
                 for i, n in enumerate(self._qkv_names):
@@ -288,7 +234,7 @@ class DecodeGraphRunner:
         if self.fp8:
             store_decode_fp8(v["k_new"], v["v_new"], v["slot_mapping"], v["q"], self.k_cache, self.v_cache,
                              v["block_tables"], v["context_lens"], self.scale, self.k_scale, self.v_scale,
-                             out=out, workspace=self.workspace)
+                             out=out, workspace=self.workspace, operands=operands)
         else:
             store_decode(v["k_new"], v["v_new"], v["slot_mapping"], v["q"], self.k_cache, self.v_cache,
                          v["block_tables"], v["context_lens"], self.scale, out=out, workspace=self.workspace,

@@ -10,6 +10,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    # libpa.so rebuilt before collection when any source is newer (a no-op otherwise), so a test
+    # module that imports the binding at its top never loads a library older than the sources
+    _build_and_import(import_binding=False)
 
 
 @pytest.fixture(scope="session")
@@ -18,13 +21,15 @@ def oracle_lib():
     return oracle.load()
 
 
-def _build_and_import():
+def _build_and_import(import_binding=True):
     import importlib.util
     spec = importlib.util.spec_from_file_location(
         "pa_build", os.path.join(ROOT, "paged_kv_cache_bs_gb300", "build.py"))
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     mod.build()
+    if not import_binding:
+        return None
     import paged_kv_cache_bs_gb300
     return paged_kv_cache_bs_gb300
 

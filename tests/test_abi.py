@@ -291,3 +291,15 @@ def test_headers_compile_as_plain_c(tmp_path):
     r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
                         "-c", str(src), "-o", str(tmp_path / "abi.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_store_decode_fp8_ex_takes_operands_only(lib):
+    import paged_kv_cache_bs_gb300 as pa
+    F = FAKE
+    for field, val in (("partition", 128), ("stages", 2), ("num_groups", 1), ("prefix_partition", 64)):
+        opt = pa._Options()
+        setattr(opt, field, val)
+        rc = lib.pa_store_decode_fp8_ex(F, F, 1024, 1024, F, F, 2048, F, F, F, 4, F, 2, 16, 8, 128, 64, 256, 0.1,
+                                        1.0, 1.0, F, F, 1 << 20, ctypes.byref(opt), 1, None, None)
+        assert rc == -1, field
+        assert b"operands only" in lib.pa_last_error()

@@ -151,3 +151,26 @@ def test_store_decode_operands_read_at_run_time(pa, where, grouped):
                     options=pa.DecodeOptions(groups=groups, operands=ops.data_ptr()))
     torch.cuda.synchronize()
     assert int(flag.item()) & pa.FLAG_BAD_VALUE
+
+
+def test_store_decode_fp8_operands_read_at_run_time(pa):
+    """pa_store_decode_fp8_ex with operands only: output and E4M3 pool bit-identical to the direct
+    call, the operands in page-locked host memory and the call's own q / k / v a zero-filled decoy."""
+    ctx = torch.randint(1, 3000, (29,), generator=torch.Generator().manual_seed(221)).tolist()
+    fs = inputs.make_decode_fp8(ctx, num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=256,
+                                dtype=torch.bfloat16, seed=222)
+    st = fs.step
+    real = {n: t.pin_memory() for n, t in dict(k=st.k_new, v=st.v_new, q=st.q).items()}
+    decoy = {n: torch.zeros_like(t, device="cuda") for n, t in real.items()}
+    sm, bt, cl = st.slot_mapping.cuda(), st.block_tables.cuda(), st.context_lens.cuda()
+    kc_a, vc_a = fs.k_cache.cuda(), fs.v_cache.cuda()
+    ref = pa.store_decode_fp8(real["k"], real["v"], sm, real["q"], kc_a, vc_a, bt, cl, st.scale, fs.k_scale,
+                              fs.v_scale)
+    ops = torch.tensor([real["q"].data_ptr(), real["k"].data_ptr(), real["v"].data_ptr()],
+                       dtype=torch.int64).pin_memory()
+    kc_b, vc_b = fs.k_cache.cuda(), fs.v_cache.cuda()
+    got = pa.store_decode_fp8(decoy["k"], decoy["v"], sm, decoy["q"], kc_b, vc_b, bt, cl, st.scale, fs.k_scale,
+                              fs.v_scale, operands=ops.data_ptr())
+    torch.cuda.synchronize()
+    assert_bit_equal(got, ref, "output through the operands array")
+    assert torch.equal(kc_b.cpu(), kc_a.cpu()) and torch.equal(vc_b.cpu(), vc_a.cpu()), "pool differs"
