@@ -491,24 +491,10 @@ PA_API int pa_prefill_paged(const void *q, const void *k, const void *v, const v
  *             fewer SMs than the device, or to leave SMs to concurrent work.
  *             The results do not depend on it, bit for bit: an item is
  *             computed the same way whichever CTA takes it.
- *   item_counter  NULL: each CTA takes a fixed share of the items.  Otherwise a
- *             DEVICE int32 the caller sets to 0 before the call (and before
- *             any other call that shares it): every CTA takes the next item,
- *             in the same longest-first order, by an atomic add on it, so
- *             several launches given the same counter -- on streams of
- *             different SM partitions, or one queued behind other work --
- *             share one pool of items and a launch whose SMs come free later
- *             takes what is left.  The launches must have identical
- *             arguments; each item is computed once, by whichever CTA takes
- *             it, and the results are the same bit for bit.  (The pages
- *             describe no such scheduling; it keeps SMs busy when the step's
- *             other work finishes early.)
- * PA_ERR_INVALID_ARG for a max_ctas outside that range or an unaligned
- * item_counter.
+ * PA_ERR_INVALID_ARG for a max_ctas outside that range.
  */
 typedef struct pa_prefill_options {
     int32_t max_ctas;
-    int32_t *item_counter;
 } pa_prefill_options;
 PA_API int pa_prefill_paged_ex(const void *q, const void *k, const void *v, const void *k_cache,
                                const void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
@@ -643,8 +629,8 @@ PA_API int pa_selftest_wait_timeout(int64_t max_cycles, int32_t *err_flag, void 
  * at least its minimum partition (8), and leave at least that many SMs;
  * otherwise PA_ERR_INVALID_ARG.  PA_ERR_UNSUPPORTED when the driver lacks
  * green contexts.  It creates driver objects (two green contexts, two
- * streams, three events) and one 256-byte device buffer (the mixed step's
- * prefill item counter): make one per device at start-up and reuse it.  pa_sm_split_info returns the two SM counts and the
+ * streams, three events) and no device buffer: make one per device at
+ * start-up and reuse it.  pa_sm_split_info returns the two SM counts and the
  * two streams (cudaStream_t; the split owns them: do not destroy them).
  * pa_sm_split_destroy waits for the split's streams and releases everything.
  * A split serves one step at a time: steps issued concurrently from several
@@ -679,10 +665,7 @@ PA_API void pa_sm_split_destroy(pa_sm_split *split);
  * With `split` (nullable) the store runs on `stream`, then the prefill on the
  * split's first partition and the decode on its second, at the same time,
  * and `stream` waits for both before anything issued on it later; the split
- * must belong to the current device.  The prefill's items then come from the
- * split's item counter (see pa_prefill_options), and a second prefill launch
- * on the decode's partition, queued behind the decode, takes the items left
- * when the decode is done.  Every argument is checked before
+ * must belong to the current device.  Every argument is checked before
  * anything is launched.  16-bit pools only (dtype PA_F16 or PA_BF16; the
  * E4M3 pool has no prefill and so no mixed step).
  */

@@ -104,7 +104,7 @@ _lib.pa_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, 
 
 
 class _PrefillOptions(ctypes.Structure):
-    _fields_ = [("max_ctas", ctypes.c_int32), ("item_counter", _p)]
+    _fields_ = [("max_ctas", ctypes.c_int32)]
 
 
 _lib.pa_prefill_paged_ex.restype = ctypes.c_int
@@ -368,11 +368,10 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
                   v_cache: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                   max_seqlen_q: int, max_seqlen_k: int, block_tables: torch.Tensor | None, scale: float,
                   out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
-                  max_ctas: int = 0, item_counter: torch.Tensor | None = None) -> torch.Tensor:
+                  max_ctas: int = 0) -> torch.Tensor:
     """Causal varlen prefill over a paged prefix: q [Tq, H_q, D] -> out [Tq, H_q, D].
     ``max_ctas`` > 0 caps the persistent grid (``pa_prefill_paged_ex``), e.g. at the SM count of
-    a green-context partition.  ``item_counter``: a device int32 set to 0 by the caller, from which
-    the CTAs take the items (launches given the same counter share one pool of items)."""
+    a green-context partition."""
     n, bs, hkv, d = _cache_shape(k_cache, v_cache)
     tq, hq = q.shape[0], q.shape[1]
     if not q.is_contiguous():
@@ -391,10 +390,8 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
             cu_seqlens_q.numel() - 1, tq, int(max_seqlen_q), int(max_seqlen_k), _ptr(block_tables),
             block_tables.shape[1] if block_tables is not None else 0, hq, hkv, d, n, bs, float(scale), _ptr(out),
             _dtype(q), _ptr(err_flag))
-    if item_counter is not None and (item_counter.dtype != torch.int32 or not item_counter.is_cuda):
-        raise ValueError("item_counter must be a device int32 tensor")
-    if max_ctas or item_counter is not None:
-        opt = _PrefillOptions(int(max_ctas), _ptr(item_counter))
+    if max_ctas:
+        opt = _PrefillOptions(int(max_ctas))
         rc = _lib.pa_prefill_paged_ex(*args, ctypes.byref(opt), _stream(q))
         _check("pa_prefill_paged_ex", rc)
     else:

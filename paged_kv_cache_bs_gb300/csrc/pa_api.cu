@@ -441,8 +441,6 @@ int pa_prefill_paged_ex(const void *q, const void *k, const void *v, const void 
     const int32_t max_ctas = opt ? opt->max_ctas : 0;
     if (max_ctas < 0 || max_ctas > 65535)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_paged_ex: max_ctas %d is not in [0, 65535]", max_ctas);
-    if (opt && opt->item_counter && !aligned(opt->item_counter, 4))
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_paged_ex: item_counter must be 4-byte aligned");
     bool work = false;
     const int rc = check_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
                                  max_seqlen_q, max_seqlen_k, block_tables, max_blocks_per_seq, num_q_heads,
@@ -456,8 +454,7 @@ int pa_prefill_paged_ex(const void *q, const void *k, const void *v, const void 
     const cudaError_t e = pa::launch_prefill(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, num_seqs,
                                              total_q, max_seqlen_q, block_tables, max_blocks_per_seq, num_q_heads,
                                              num_kv_heads, head_dim, num_blocks, block_size, scale, out, dtype,
-                                             err_flag, max_ctas, opt ? opt->item_counter : nullptr,
-                                             static_cast<cudaStream_t>(stream), &why);
+                                             err_flag, max_ctas, static_cast<cudaStream_t>(stream), &why);
     if (why) return fail(PA_ERR_CUDA, "pa_prefill_paged: %s", why);
     return cuda_status(e, "pa_prefill_paged launch");
 }
@@ -557,34 +554,21 @@ int pa_mixed_step(const void *k, const void *v, int64_t k_row_stride, int64_t v_
                                 num_kv_heads * head_dim, static_cast<int64_t>(num_blocks) * block_size, err_flag,
                                 main);
     const bool both = split && prefill && decode;
-    // with the split, the prefill's items come from the split's counter (zeroed on `stream` before
-    // the partitions fork): its CTAs on the first partition start at once, and a second launch
-    // queued behind the decode takes the items left when the decode's SMs come free
-    int32_t *counter = both ? pa::split_counter(split) : nullptr;
-    if (e == cudaSuccess && both) e = cudaMemsetAsync(counter, 0, sizeof(int32_t), main);
     if (e == cudaSuccess && both) e = pa::split_fork(split, main);
     const cudaStream_t s_prefill = both ? pa::split_stream(split, 0) : main;
     const cudaStream_t s_decode = both ? pa::split_stream(split, 1) : main;
-    auto prefill_on = [&](int32_t sms, cudaStream_t s) -> int {
+    if (e == cudaSuccess && prefill) {
         const char *why = nullptr;
         e = pa::launch_prefill(prefill_q, nullptr, nullptr, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
                                num_prefill_seqs, total_prefill_q, max_seqlen_q, prefill_block_tables,
                                prefill_max_blocks, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
-                               prefill_out, dtype, err_flag, sms, counter, s, &why);
-        return why ? fail(PA_ERR_CUDA, "pa_mixed_step: %s", why) : PA_OK;
-    };
-    if (e == cudaSuccess && prefill) {
-        const int rc = prefill_on(both ? pa::split_sms(split, 0) : 0, s_prefill);
-        if (rc) return rc;
+                               prefill_out, dtype, err_flag, both ? pa::split_sms(split, 0) : 0, s_prefill, &why);
+        if (why) return fail(PA_ERR_CUDA, "pa_mixed_step: %s", why);
     }
     if (e == cudaSuccess && decode)
         e = pa::launch_decode(decode_q, decode_q_row_stride, k_cache, v_cache, decode_block_tables, decode_max_blocks,
                               context_lens, decode_batch, num_q_heads, num_kv_heads, head_dim, num_blocks,
                               block_size, scale, decode_out, workspace, plan, dtype, err_flag, s_decode);
-    if (e == cudaSuccess && both) {
-        const int rc = prefill_on(pa::split_sms(split, 1), s_decode);
-        if (rc) return rc;
-    }
     if (e == cudaSuccess && both) e = pa::split_join(split, main);
     return cuda_status(e, "pa_mixed_step launch");
 }

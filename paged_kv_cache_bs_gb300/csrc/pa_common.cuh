@@ -175,14 +175,12 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
                            int32_t total_q, int32_t max_seqlen_q, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
-                           int32_t *err_flag, int32_t sms, int32_t *item_counter, cudaStream_t stream,
-                           const char **why);
+                           int32_t *err_flag, int32_t sms, cudaStream_t stream, const char **why);
 cudaError_t launch_copy_segments(const pa_copy_segment *segments, int32_t count, int32_t ctas, cudaStream_t stream);
 // The two streams of a pa_sm_split (sm_split.cu): fork makes both wait for `from`'s work so
 // far, join makes `to` wait for everything issued on both.
 cudaStream_t split_stream(const pa_sm_split *s, int i);
 int split_sms(const pa_sm_split *s, int i);
-int32_t *split_counter(const pa_sm_split *s);
 int split_device(const pa_sm_split *s);
 cudaError_t split_fork(const pa_sm_split *s, cudaStream_t from);
 cudaError_t split_join(const pa_sm_split *s, cudaStream_t to);

@@ -88,9 +88,6 @@ struct PrefillArgs {
     float scale_log2;
     void *out;
     int32_t *err_flag;
-    // null: each CTA takes its share of the ranked items (sched_rank); else every CTA -- of this
-    // launch and of any other launch given the same counter -- takes the next rank from it
-    int32_t *item_counter;
 };
 
 // Shared memory, every tile 1024-byte aligned with the 128-byte swizzle and
@@ -107,7 +104,7 @@ template <int D> struct PShape {
     static constexpr int kOffK = 2 * kTile;         // + slot * kTile
     static constexpr int kOffV = 4 * kTile;         // + slot * kTile
     static constexpr int kOffBar = 6 * kTile;
-    static constexpr int kSmem = kOffBar + 512;
+    static constexpr int kSmem = kOffBar + 256;
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -176,20 +173,6 @@ __device__ __forceinline__ bool next_item(const PrefillArgs &a, const int *s_inv
     }
     return false;
 }
-// Items taken from a shared counter instead (PrefillArgs::item_counter): the TMA thread, which
-// needs an item first, takes ranks until one has work (or none is left: -1) and hands it to the
-// MMA thread and the softmax warps through a ring of kRing slots in shared memory, each with a
-// "published" and a "read" mbarrier; this CTA's k-th item sits in slot k % kRing.
-constexpr int kRing = 8;
-__device__ __forceinline__ int take_rank(const PrefillArgs &a, const int *s_inv, bool ranked, int hps, int total,
-                                         Item &it) {
-    for (;;) {
-        const int r = atomicAdd(a.item_counter, 1);
-        if (r >= total) return -1;
-        it = item_at(a, s_inv, ranked, hps, r, true);
-        if (it.nkt > 0) return r;
-    }
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillMaps maps,
@@ -244,11 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem_slot = bar0 + 120;
     volatile int *abort_word = reinterpret_cast<volatile int *>(smem + S::kOffBar + 124);
     const uint32_t bar_drain = bar0 + 128;                            // MMA drain on abort
-    // the item ring (shared counter only): ranks at +256, "published" barriers at +288, "read" at +352
-    volatile int *s_ring = reinterpret_cast<volatile int *>(smem + S::kOffBar + 256);
-    auto bar_pub = [&](int k) { return bar0 + 288 + 8 * (k % kRing); };
-    auto bar_read = [&](int k) { return bar0 + 352 + 8 * (k % kRing); };
-    const bool shared_queue = a.item_counter != nullptr;
 
     if (tid == 0) {
         tc::mbar_init(bar_q(0), 1);
@@ -262,11 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc::mbar_init(bar_o(i), 1);
         }
         tc::mbar_init(bar_drain, 1);
-        if (shared_queue)
-            for (int i = 0; i < kRing; ++i) {
-                tc::mbar_init(bar_pub(i), 1);
-                tc::mbar_init(bar_read(i), 1 + 4 * nwg);  // the MMA thread and every softmax warp
-            }
         tc::mbar_fence_init();
         *abort_word = 0;
     }
@@ -282,24 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     auto tO = [&](int w) { return tmem + 256 * w + 128; };
     auto wait = [&](uint32_t bar, uint32_t phase) {
         return tc::mbar_wait_or_abort(bar, phase, kWaitCycles, abort_word);
-    };
-    // shared counter: the TMA thread publishes this CTA's k-th item (1) or that none is left (0),
-    // once every reader is done with slot k % kRing's previous item; -1: a wait gave up
-    auto publish = [&](int k, Item &it) -> int {
-        if (!wait(bar_read(k), ((k / kRing) & 1) ^ 1)) return -1;
-        const int r = take_rank(a, s_inv, ranked, hps, total, it);
-        s_ring[k % kRing] = r;
-        tc::mbar_arrive(bar_pub(k));
-        return r >= 0 ? 1 : 0;
-    };
-    // ... and the MMA thread and the softmax warps read it (its rank in r); each reader then
-    // arrives on bar_read(k) once (a softmax warp by one lane)
-    auto take = [&](int k, Item &it, int &r) -> int {
-        if (!wait(bar_pub(k), (k / kRing) & 1)) return -1;
-        r = s_ring[k % kRing];
-        if (r < 0) return 0;
-        it = item_at(a, s_inv, ranked, hps, r, false);
-        return 1;
     };
     const bool paged = a.block_tables != nullptr;
 
@@ -355,19 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc::prefetch_tmap(&maps.v);
             int k = 0;
             Item cur;
-            bool ok = true;
-            bool have;
-            if (shared_queue) {
-                const int st = publish(0, cur);
-                ok = st >= 0;
-                have = st > 0;
-            } else {
-                have = next_item(a, s_inv, ranked, hps, total, k, cur, true);
-            }
+            bool have = next_item(a, s_inv, ranked, hps, total, k, cur, true);
             const bool started = have;
             int u = 0, issued = 0;
             int nq[2] = {0, 0};  // stages and Q tiles loaded, for the drain on abort
             int vpage = 0;       // one box per tile: the page of the next V tile (that of the K tile before)
+            bool ok = true;
             if (have) {
                 for (int w = 0; w < nwg; ++w) {
                     load_q(cur, w);
@@ -379,17 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             while (have && ok) {
                 int kn = k + 1;
                 Item nxt;
-                bool more;
-                if (shared_queue) {
-                    const int st = publish(kn, nxt);
-                    if (st < 0) {
-                        ok = false;
-                        break;
-                    }
-                    more = st > 0;
-                } else {
-                    more = next_item(a, s_inv, ranked, hps, total, kn, nxt, true);
-                }
+                const bool more = next_item(a, s_inv, ranked, hps, total, kn, nxt, true);
                 if (more)  // the next item's Q tiles into L2 now; they are loaded at its first tile
                     for (int w = 0; w < nwg; ++w)
                         for (int hf = 0; hf < S::kHalves; ++hf)
@@ -492,17 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // after S(0) of both heads, i = u + 1 after PV(u) and S(u+1) of both heads
             int k = 0, u = 0, j = 0;
             Item cur;
+            bool have = next_item(a, s_inv, ranked, hps, total, k, cur, false);
             bool ok = true;
-            bool have;
-            if (shared_queue) {
-                int r;
-                const int st = take(0, cur, r);
-                tc::mbar_arrive(bar_read(0));
-                ok = st >= 0;
-                have = st > 0;
-            } else {
-                have = next_item(a, s_inv, ranked, hps, total, k, cur, false);
-            }
             if (have) {
                 ok = wait(bar_k0, 0);
                 for (int w = 0; w < nwg && ok; ++w) {
@@ -517,19 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             while (have && ok) {
                 int kn = k + 1;
                 Item nxt;
-                bool more;
-                if (shared_queue) {
-                    int r;
-                    const int st = take(kn, nxt, r);
-                    tc::mbar_arrive(bar_read(kn));
-                    if (st < 0) {
-                        ok = false;
-                        break;
-                    }
-                    more = st > 0;
-                } else {
-                    more = next_item(a, s_inv, ranked, hps, total, kn, nxt, false);
-                }
+                const bool more = next_item(a, s_inv, ranked, hps, total, kn, nxt, false);
                 for (int t = 0; t < cur.nkt && ok; ++t, ++u) {
                     // Per head: O += P V_u as soon as its softmax is done, then S for the next
                     // tile (it overwrites P, which the PV just issued reads first: MMAs run in
@@ -581,19 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (;; ++k, ++j) {
             // only what the tile loop needs stays live across it; the epilogue looks the item up again
             int pq, Lk, nkt;  // prefix + first row of the tile, context length, key tiles
-            int rank;         // the item's rank
             {
                 Item cur;
-                if (shared_queue) {
-                    const int st = take(k, cur, rank);
-                    __syncwarp();
-                    if ((tid & 31) == 0) tc::mbar_arrive(bar_read(k));
-                    ok = __all_sync(0xffffffffu, st >= 0);
-                    if (!ok || st == 0) break;
-                } else {
-                    if (!next_item(a, s_inv, ranked, hps, total, k, cur, false)) break;
-                    rank = sched_rank(k);
-                }
+                if (!next_item(a, s_inv, ranked, hps, total, k, cur, false)) break;
                 pq = cur.P + cur.q0;
                 Lk = cur.Lk;
                 nkt = cur.nkt;
@@ -699,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (!ok) break;
             {
                 tc::fence_after_sync();
-                const Item cur = item_at(a, s_inv, ranked, hps, rank, false);
+                const Item cur = item_at(a, s_inv, ranked, hps, sched_rank(k), false);
                 const int qrow = cur.q0 + row;
                 const float inv_l = 1.f / l_sum;
                 T *dst = static_cast<T *>(a.out) +
@@ -779,8 +686,7 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
                            int32_t total_q, int32_t max_seqlen_q, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t num_blocks, int32_t block_size, float scale, void *out, pa_dtype dtype,
-                           int32_t *err_flag, int32_t sms, int32_t *item_counter, cudaStream_t stream,
-                           const char **why) {
+                           int32_t *err_flag, int32_t sms, cudaStream_t stream, const char **why) {
     *why = nullptr;
     if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return cudaSuccess;
     PrefillMaps maps;
@@ -817,7 +723,6 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const vo
     a.scale_log2 = scale * kLog2e;
     a.out = out;
     a.err_flag = err_flag;
-    a.item_counter = item_counter;
     // persistent: one CTA per SM the kernel may use (it holds a whole SM), at most one per item
     const int64_t items = static_cast<int64_t>(num_seqs) * a.qtiles * (num_q_heads / a.heads_per_cta);
     const int ctas = static_cast<int>(std::min<int64_t>(items, sms > 0 ? sms : device_sms()));

@@ -21,7 +21,6 @@ struct pa_sm_split {
     cudaStream_t stream[2];
     cudaEvent_t fork;
     cudaEvent_t join[2];
-    int32_t *counter;  // device: the prefill's shared item counter of a mixed step
 };
 
 namespace pa {
@@ -97,7 +96,6 @@ void release(pa_sm_split *s) {
         }
     }
     if (s->fork) cudaEventDestroy(s->fork);
-    if (s->counter) cudaFree(s->counter);
     for (int i = 0; i < 2; ++i)
         if (s->ctx[i]) d.ctx_destroy(s->ctx[i]);
     delete s;
@@ -107,7 +105,6 @@ void release(pa_sm_split *s) {
 
 cudaStream_t split_stream(const pa_sm_split *s, int i) { return s->stream[i]; }
 int split_sms(const pa_sm_split *s, int i) { return s->sms[i]; }
-int32_t *split_counter(const pa_sm_split *s) { return s->counter; }
 int split_device(const pa_sm_split *s) { return s->device; }
 
 cudaError_t split_fork(const pa_sm_split *s, cudaStream_t from) {
@@ -186,11 +183,6 @@ PA_API int pa_sm_split_create(int32_t first_sms, pa_sm_split **out) {
     if (e != cudaSuccess) {
         pa::release(s);
         return pa::fail_rt("pa_sm_split_create: cudaEventCreateWithFlags", e);
-    }
-    e = cudaMalloc(reinterpret_cast<void **>(&s->counter), 256);
-    if (e != cudaSuccess) {
-        pa::release(s);
-        return pa::fail_rt("pa_sm_split_create: cudaMalloc of the item counter", e);
     }
     *out = s;
     pa::set_last_error(PA_OK, "");

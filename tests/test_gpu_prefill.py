@@ -190,52 +190,6 @@ def test_prefill_mixed_workload_capped_grid_bit_equal(pa):
     assert_bit_equal(a, b, "40 CTAs vs the full grid")
 
 
-@pytest.mark.parametrize("ctas", [0, 40, 1])
-def test_prefill_shared_item_counter_bit_equal(pa, ctas):
-    # items taken from a counter instead of a fixed share per CTA: the same bits, for the full grid,
-    # a capped one and a single CTA; the counter ends past the last item
-    m = inputs.mixed_chunked_prefill()
-    st = m.prefill
-    p = st.pool
-    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
-    pa.store_kv(m.k_new.cuda(), m.v_new.cuda(), kc, vc, m.slot_mapping.cuda())
-    args = (st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(), st.max_seqlen_q,
-            st.max_seqlen_k, st.block_tables.cuda(), st.scale)
-    ref = pa.prefill_paged(*args)
-    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
-    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    got = pa.prefill_paged(*args, max_ctas=ctas, item_counter=counter, err_flag=flag)
-    torch.cuda.synchronize()
-    assert int(flag.item()) == 0
-    assert_bit_equal(got, ref, f"items from a counter, max_ctas {ctas}")
-    items = (st.cu_seqlens_q.numel() - 1) * ((st.max_seqlen_q + 127) // 128) * (st.q.shape[1] // 2)
-    assert int(counter.item()) >= items
-
-
-def test_prefill_two_launches_share_one_counter(pa):
-    # two launches with the same arguments and counter on two streams at once (3 and 2 CTAs): each
-    # item is computed once, by whichever CTA takes it, and the output equals one launch's bit for
-    # bit.  Neither launch waits on the other: a CTA only takes items until the counter runs out.
-    st, _ = inputs.make_prefill([0, 300, 1200, 40, 700], [300, 129, 200, 1, 256], num_q_heads=8, num_kv_heads=2,
-                                head_dim=128, block_size=64, dtype=torch.bfloat16, seed=231)
-    p = st.pool
-    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
-    pa.store_kv(st.k_new.cuda(), st.v_new.cuda(), kc, vc, st.slot_mapping.cuda())
-    args = (st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(), st.max_seqlen_q,
-            st.max_seqlen_k, st.block_tables.cuda(), st.scale)
-    ref = pa.prefill_paged(*args)
-    out = torch.full_like(ref, float("nan"))
-    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
-    torch.cuda.synchronize()
-    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    with torch.cuda.stream(s1):
-        pa.prefill_paged(*args, out=out, max_ctas=3, item_counter=counter)
-    with torch.cuda.stream(s2):
-        pa.prefill_paged(*args, out=out, max_ctas=2, item_counter=counter)
-    torch.cuda.synchronize()
-    assert_bit_equal(out, ref, "two launches sharing a counter")
-
-
 def test_prefill_bad_metadata_is_flagged_not_fatal(pa):
     st, _ = inputs.make_prefill([40, 40], [30, 30], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
                                 dtype=torch.bfloat16, seed=93)
