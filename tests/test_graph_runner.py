@@ -144,3 +144,32 @@ def test_runner_with_tables_narrower_than_its_width(pa):
                 oracle.store_kv(s.k_new, s.v_new, okc, ovc, s.slot_mapping)
             ref = oracle.decode(s.q, okc, ovc, s.block_tables, s.context_lens, s.scale)
             assert max_err(got, ref) <= TOL[torch.bfloat16], f"step {i} share {share}"
+
+
+@pytest.mark.gpu
+def test_runner_full_shared_prefix_workload_in_place_bit_equal(pa):
+    # the full Qwen3-8B-like shared-prefix step as a caller runs it: page-locked inputs read in
+    # place through the operands array, groups derived by the native staging call, two alternating
+    # steps; each output and the pool bit-identical to the eager fused call with the same groups
+    from paged_kv_cache_bs_gb300.block_manager import prefix_groups
+    from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
+    st = inputs.qwen3_8b_shared_decode()
+    steps = [st, inputs.next_decode_step(st, seed=4242)]
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    runner = DecodeGraphRunner(kc, vc, st.num_q_heads, st.batch, st.block_tables.shape[1], st.scale,
+                               torch.bfloat16, group_caps=(st.batch // 2, 8, 512))
+    kc_e, vc_e = p.k_cache.cuda(), p.v_cache.cuda()
+    for i, s in enumerate(steps):
+        pinned = [t.contiguous().pin_memory() for t in (s.q, s.k_new, s.v_new, s.slot_mapping, s.context_lens,
+                                                         s.block_tables)]
+        got = runner.step(*pinned, share_prefixes=True).clone()
+        g = prefix_groups(s.block_tables, s.context_lens, p.block_size).to("cuda")
+        ref = pa.store_decode(s.k_new.cuda(), s.v_new.cuda(), s.slot_mapping.cuda(), s.q.cuda(), kc_e, vc_e,
+                              s.block_tables.cuda(), s.context_lens.cuda(), s.scale,
+                              options=pa.DecodeOptions(groups=g))
+        torch.cuda.synchronize()
+        assert runner._use_inplace[st.batch], "page-locked inputs take the in-place graph"
+        assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16)), f"step {i}: output differs"
+    assert torch.equal(kc.cpu().view(torch.int16), kc_e.cpu().view(torch.int16)), "k pool differs"
+    assert torch.equal(vc.cpu().view(torch.int16), vc_e.cpu().view(torch.int16)), "v pool differs"
