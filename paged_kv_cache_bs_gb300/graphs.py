@@ -71,6 +71,14 @@ def _graph_launch(graph_exec: int, stream: int) -> None:
         raise RuntimeError(f"cuGraphLaunch failed with CUresult {rc}")
 
 
+def _raw_stream(device_index: int) -> int:
+    """The current stream's handle on a device (torch's direct query where it has one)."""
+    get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if get is not None:
+        return get(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
 def _host_i32(t: torch.Tensor) -> torch.Tensor:
     """t as a contiguous host int32 tensor (itself when it already is one)."""
     if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
@@ -359,8 +367,7 @@ class DecodeGraphRunner:
         """Replay the bucket's graph (inputs from the pinned staging) on the current stream; the
         returned pinned host view of the output is valid once that stream has synchronised."""
         b = self.bucket(batch)
-        _graph_launch(self._execs[(b, self._use_inplace.get(b, False))],
-                      torch._C._cuda_getCurrentRawStream(self._device_index))
+        _graph_launch(self._execs[(b, self._use_inplace.get(b, False))], _raw_stream(self._device_index))
         out = self._staged_out.get(batch)
         if out is None:  # the first `batch` rows of the bucket's output, one view per batch size
             out = self._staged_out[batch] = self._out_view(self.host_out, b)[:batch]
