@@ -91,3 +91,38 @@ def test_decode_random_shared_prefixes(pa, seed):
     assert groups.num_groups >= 1
     opt = pa.DecodeOptions(groups=groups.to("cuda"), partition=rnd.choice([0, 0, 256, 512]))
     check_decode(pa, st, options=opt)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_store_decode_random_operands_in_place(pa, seed):
+    # random shapes, dtypes, block sizes and split plans: q and the new rows read through the operands
+    # array (page-locked or device, the call's own arguments zero-filled decoys) give the output and
+    # pool of the direct call bit for bit
+    rnd = random.Random(7000 + seed)
+    hq, hkv = rnd.choice(HEADS)
+    d = rnd.choice([64, 128])
+    bs = rnd.choice([8, 16, 64, 256])
+    dtype = rnd.choice([torch.float16, torch.bfloat16])
+    b = rnd.randint(1, 33)
+    ctx = [rnd.randint(1, 2500) for _ in range(b)]
+    st = inputs.make_decode(ctx, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs, dtype=dtype,
+                            seed=8000 + seed)
+    options = pa.DecodeOptions(partition=rnd.choice([0, 64, 256, 1024]))
+    where = rnd.choice(["pinned", "device"])
+    real = {n: (t.pin_memory() if where == "pinned" else t.cuda()) for n, t in
+            dict(k=st.k_new, v=st.v_new, q=st.q).items()}
+    decoy = {n: torch.zeros_like(t, device="cuda") for n, t in real.items()}
+    sm, bt, cl = st.slot_mapping.cuda(), st.block_tables.cuda(), st.context_lens.cuda()
+    kc_a, vc_a = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    ref = pa.store_decode(real["k"], real["v"], sm, real["q"], kc_a, vc_a, bt, cl, st.scale, options=options)
+    ops = torch.tensor([real["q"].data_ptr(), real["k"].data_ptr(), real["v"].data_ptr()],
+                       dtype=torch.int64).pin_memory()
+    kc_b, vc_b = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pa.store_decode(decoy["k"], decoy["v"], sm, decoy["q"], kc_b, vc_b, bt, cl, st.scale, err_flag=flag,
+                          options=pa.DecodeOptions(partition=options.partition, operands=ops.data_ptr()))
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"seed {seed}: output differs"
+    assert torch.equal(kc_b.view(torch.int16), kc_a.view(torch.int16)), f"seed {seed}: k pool differs"
+    assert torch.equal(vc_b.view(torch.int16), vc_a.view(torch.int16)), f"seed {seed}: v pool differs"

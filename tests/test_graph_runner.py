@@ -173,3 +173,28 @@ def test_runner_full_shared_prefix_workload_in_place_bit_equal(pa):
         assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16)), f"step {i}: output differs"
     assert torch.equal(kc.cpu().view(torch.int16), kc_e.cpu().view(torch.int16)), "k pool differs"
     assert torch.equal(vc.cpu().view(torch.int16), vc_e.cpu().view(torch.int16)), "v pool differs"
+
+
+@pytest.mark.gpu
+def test_runner_full_fp8_workload_in_place_bit_equal(pa):
+    # the Qwen3-0.6B-like step over its E4M3 pool as a caller runs it: page-locked inputs read in place
+    # through pa_store_decode_fp8_ex's operands, two alternating steps; output and codes bit-identical to
+    # the eager fused call
+    from paged_kv_cache_bs_gb300.graphs import DecodeGraphRunner
+    fs = inputs.qwen3_0p6b_decode_fp8()
+    st = fs.step
+    steps = [st, inputs.next_decode_step(st, seed=4243)]
+    kc, vc = fs.k_cache.cuda(), fs.v_cache.cuda()
+    runner = DecodeGraphRunner(kc, vc, st.num_q_heads, st.batch, st.block_tables.shape[1], st.scale,
+                               torch.bfloat16, k_scale=fs.k_scale, v_scale=fs.v_scale)
+    kc_e, vc_e = fs.k_cache.cuda(), fs.v_cache.cuda()
+    for i, s in enumerate(steps):
+        pinned = [t.contiguous().pin_memory() for t in (s.q, s.k_new, s.v_new, s.slot_mapping, s.context_lens,
+                                                         s.block_tables)]
+        got = runner.step(*pinned).clone()
+        ref = pa.store_decode_fp8(s.k_new.cuda(), s.v_new.cuda(), s.slot_mapping.cuda(), s.q.cuda(), kc_e, vc_e,
+                                  s.block_tables.cuda(), s.context_lens.cuda(), s.scale, fs.k_scale, fs.v_scale)
+        torch.cuda.synchronize()
+        assert runner._use_inplace[runner.bucket(st.batch)], "page-locked inputs take the in-place graph"
+        assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16)), f"step {i}: output differs"
+    assert torch.equal(kc.cpu(), kc_e.cpu()) and torch.equal(vc.cpu(), vc_e.cpu()), "E4M3 pool differs"
