@@ -20,8 +20,10 @@
  *   pa_prefill_paged_ex  prefill with a cap on its persistent grid
  *   pa_sm_split_*, pa_mixed_step  a mixed step's prefill and decode at once
  *                     on disjoint SM partitions
- *   pa_copy_segments, pa_stage_decode_step  the device and host halves of a
- *                     captured decode step fed from the caller's host buffers
+ *   pa_stage_decode_step  the host half of a captured decode step fed from
+ *                     the caller's host buffers (through the operands option)
+ *   pa_copy_segments  several copies in one launch, from a list read when it
+ *                     runs
  *   pa_selftest_wait_timeout  shows the kernels' bounded waits ending
  * and, in pa_block_manager.h, the host-side page directory (pa_bm_*) and the
  * shared-prefix grouping of a decode batch (pa_prefix_groups).
@@ -32,8 +34,10 @@
  *     properties.  Integer size arguments are host values.  Exception: the
  *     per-step operands of pa_store_kv (k, v, slot_mapping), of
  *     pa_store_decode and pa_store_decode_fp8 (k, v, slot_mapping, q,
- *     block_tables, context_lens and out) and of pa_sample (logits,
- *     temperatures, noise, tokens) may instead be
+ *     block_tables, context_lens and out), of pa_sample (logits,
+ *     temperatures, noise, tokens), the output of pa_prefill_paged (out) and
+ *     those of pa_mixed_step (k, v, slot_mapping, decode_q,
+ *     decode_block_tables, context_lens, prefill_out, decode_out) may instead be
  *     page-locked host memory from cudaHostAlloc / cudaMallocHost, which under
  *     unified addressing is device-accessible through its host pointer: the
  *     kernels then read and write it directly over the CPU-GPU link (zero

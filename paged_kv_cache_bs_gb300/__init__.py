@@ -297,6 +297,14 @@ def _step_operands(k_cache: torch.Tensor, **tensors) -> None:
         raise ValueError(f"{name} must be on {k_cache.device} or in pinned host memory")
 
 
+def _device_only(k_cache: torch.Tensor, **tensors) -> None:
+    """Operands a kernel reads by TMA or that the C ABI takes as device memory only: on the device of
+    the call (``k_cache``'s).  A host tensor would reach the kernel as a host pointer."""
+    for name, t in tensors.items():
+        if t is not None and t.device != k_cache.device:
+            raise ValueError(f"{name} must be on {k_cache.device}")
+
+
 def _decode_checks(q, k_cache, v_cache, block_tables, context_lens):
     n, bs, hkv, d = _cache_shape(k_cache, v_cache)
     B = q.shape[0]
@@ -317,6 +325,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     """Paged decode attention: q [B, H_q, D] -> out [B, H_q, D] (``pa_decode``, or
     ``pa_decode_ex`` with ``options``)."""
     n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _device_only(k_cache, q=q, block_tables=block_tables, context_lens=context_lens, out=out)
     B, hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)
@@ -373,6 +382,9 @@ def prefill_paged(q: torch.Tensor, k: torch.Tensor | None, v: torch.Tensor | Non
     ``max_ctas`` > 0 caps the persistent grid (``pa_prefill_paged_ex``), e.g. at the SM count of
     a green-context partition."""
     n, bs, hkv, d = _cache_shape(k_cache, v_cache)
+    _device_only(k_cache, q=q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                 block_tables=block_tables)
+    _step_operands(k_cache, out=out)  # written by plain stores: the device, or page-locked host memory
     tq, hq = q.shape[0], q.shape[1]
     if not q.is_contiguous():
         raise ValueError("q must be contiguous [Tq, H_q, D]")
@@ -483,6 +495,11 @@ def mixed_step(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, pre
     [B, H_q, D]; with ``split`` the prefill and the decode run at once on its two SM partitions.
     Returns (prefill_out, decode_out)."""
     n, bs, hkv, d = _decode_checks(decode_q, k_cache, v_cache, decode_block_tables, context_lens)
+    _device_only(k_cache, prefill_q=prefill_q, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
+                 prefill_block_tables=prefill_block_tables, workspace=workspace)
+    _step_operands(k_cache, k=k, v=v, slot_mapping=slot_mapping, decode_q=decode_q,
+                   decode_block_tables=decode_block_tables, context_lens=context_lens, prefill_out=prefill_out,
+                   decode_out=decode_out)
     B, hq = decode_q.shape[0], decode_q.shape[1]
     tq = prefill_q.shape[0]
     if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous():
@@ -552,6 +569,7 @@ def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     """Paged decode over an fp8 pool (K = code * k_scale, V = code * v_scale): q [B, H_q, D] -> out."""
     _fp8_pool(k_cache, v_cache)
     n, bs, hkv, d = _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _device_only(k_cache, q=q, block_tables=block_tables, context_lens=context_lens, out=out)
     B, hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty(B, hq, d, dtype=q.dtype, device=q.device)

@@ -105,3 +105,29 @@ def test_mixed_step_with_one_side_empty(pa, split):
     torch.cuda.synchronize()
     assert p2.shape[0] == 0
     assert_bit_equal(d2, dout, "decode out without prefill sequences")
+
+
+@pytest.mark.parametrize("use_split", [True, False])
+def test_mixed_step_outputs_in_pinned_host_memory(pa, split, use_split):
+    # both outputs page-locked on the host, written by the kernels over the CPU-GPU link: the same
+    # bits as device outputs; a pageable host output is refused before any launch
+    m = inputs.mixed_chunked_prefill()
+    pf, st = m.prefill, m.decode
+    ref = _mixed(pa, m, split if use_split else None)
+    d = _device(m)
+    kc, vc = pf.pool.k_cache.cuda(), pf.pool.v_cache.cuda()
+    pout = torch.full(tuple(pf.q.shape), float("nan"), dtype=pf.q.dtype).pin_memory()
+    dout = torch.full(tuple(st.q.shape), float("nan"), dtype=st.q.dtype).pin_memory()
+    pa.mixed_step(d["k"], d["v"], d["sm"], d["pq"], d["cuq"], d["cuk"], pf.max_seqlen_q, pf.max_seqlen_k, d["pbt"],
+                  d["dq"], d["dbt"], d["cl"], kc, vc, pf.scale, prefill_out=pout, decode_out=dout,
+                  split=split if use_split else None)
+    torch.cuda.synchronize()
+    assert_bit_equal(pout, ref[0].cpu(), "prefill output in pinned memory")
+    assert_bit_equal(dout, ref[1].cpu(), "decode output in pinned memory")
+    with pytest.raises(ValueError):
+        pa.mixed_step(d["k"], d["v"], d["sm"], d["pq"], d["cuq"], d["cuk"], pf.max_seqlen_q, pf.max_seqlen_k,
+                      d["pbt"], d["dq"], d["dbt"], d["cl"], kc, vc, pf.scale,
+                      prefill_out=torch.empty(tuple(pf.q.shape), dtype=pf.q.dtype), split=None)
+    with pytest.raises(ValueError):  # the prefill's q is read by TMA: device memory only
+        pa.mixed_step(d["k"], d["v"], d["sm"], pf.q.pin_memory(), d["cuq"], d["cuk"], pf.max_seqlen_q,
+                      pf.max_seqlen_k, d["pbt"], d["dq"], d["dbt"], d["cl"], kc, vc, pf.scale, split=None)

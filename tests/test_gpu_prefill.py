@@ -190,6 +190,35 @@ def test_prefill_mixed_workload_capped_grid_bit_equal(pa):
     assert_bit_equal(a, b, "40 CTAs vs the full grid")
 
 
+def test_prefill_output_in_pinned_host_memory(pa):
+    # out page-locked on the host, written by the epilogue's plain stores over the CPU-GPU link: the
+    # same bits as a device out; host inputs (read by TMA) and a pageable out are refused up front
+    st, _ = inputs.make_prefill([0, 300, 1200], [300, 129, 200], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                                block_size=64, dtype=torch.bfloat16, seed=241)
+    p = st.pool
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    pa.store_kv(st.k_new.cuda(), st.v_new.cuda(), kc, vc, st.slot_mapping.cuda())
+    args = (st.q.cuda(), None, None, kc, vc, st.cu_seqlens_q.cuda(), st.cu_seqlens_k.cuda(), st.max_seqlen_q,
+            st.max_seqlen_k, st.block_tables.cuda(), st.scale)
+    ref = pa.prefill_paged(*args)
+    out = torch.full(tuple(st.q.shape), float("nan"), dtype=st.q.dtype).pin_memory()
+    pa.prefill_paged(*args, out=out)
+    torch.cuda.synchronize()
+    assert_bit_equal(out, ref.cpu(), "prefill output in pinned memory")
+    with pytest.raises(ValueError):
+        pa.prefill_paged(*args, out=torch.empty(tuple(st.q.shape), dtype=st.q.dtype))
+    with pytest.raises(ValueError):
+        pa.prefill_paged(st.q.pin_memory(), *args[1:])
+
+
+def test_decode_refuses_host_operands(pa):
+    st = inputs.make_decode([40, 90], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
+                            dtype=torch.bfloat16, seed=242)
+    kc, vc = st.pool.k_cache.cuda(), st.pool.v_cache.cuda()
+    with pytest.raises(ValueError):
+        pa.decode(st.q, kc, vc, st.block_tables.cuda(), st.context_lens.cuda(), st.scale)
+
+
 def test_prefill_bad_metadata_is_flagged_not_fatal(pa):
     st, _ = inputs.make_prefill([40, 40], [30, 30], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
                                 dtype=torch.bfloat16, seed=93)
